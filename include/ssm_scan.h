@@ -1,0 +1,161 @@
+/*
+ * ssm_scan.h -- C ABI of the B300 (sm_103a) Mamba-1 selective scan library
+ * (libssmscan.so).
+ *
+ * Operation (Mamba SSM complete guide (youngju.dev), section 5, "complete Mamba
+ * implementation": MambaBlock.ssm / selective_scan / forward). For every batch
+ * row b, channel d and state n:
+ *     dt_t  = softplus(delta[b,d,t] + delta_bias[d])     (or the raw sum when softplus == 0)
+ *     h_t,n = exp(dt_t * A[d,n]) * h_{t-1,n} + dt_t * B[b,n,t] * u[b,d,t]
+ *     y_t   = sum_n C[b,n,t] * h_t,n + D[d] * u[b,d,t]
+ *     y_t  *= silu(z[b,d,t]) = z / (1 + exp(-z))          (only when z != NULL)
+ * starting from h_{-1} = h0 (zero when h0 == NULL). The input matrix is the
+ * simplified dt*B of the page's selective_scan (not the exact zero-order-hold
+ * form of its section 2 "Discretization"). The d_state == 1 case is the
+ * Scalar Mamba1 (SM1) page's closed form (aitrends.kr, section details);
+ * one-token decode is the same recurrence applied once to a resident state.
+ *
+ * Conventions shared by every entry point:
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller. The library
+ *     allocates no memory, never synchronises the device, and launches only on
+ *     the caller's `stream` (a cudaStream_t passed as void*; NULL = legacy
+ *     default stream).
+ *   - Layouts are dense row-major, last index fastest:
+ *       u, delta, z, y : (batch, dim, seqlen)    seqlen innermost
+ *       B, C           : (batch, dstate, seqlen) seqlen innermost
+ *       A              : (dim, dstate) fp32
+ *       D, delta_bias  : (dim) fp32
+ *       h0, h_last     : (batch, dim, dstate) fp32
+ *   - in_dtype gives the dtype of u, delta, z, B, C; out_dtype the dtype of y.
+ *     A, D, delta_bias and the state are always fp32; all arithmetic is fp32.
+ *   - Optional pointers (D, z, delta_bias, h0, h_last) may be NULL.
+ *   - Argument errors are returned synchronously as a negative ssm_status and
+ *     nothing is launched. Errors raised on the device (a look-back wait that ran
+ *     out of its iteration budget) are written to the workspace status word and
+ *     read back with ssm_query_status().
+ *   - Sizes are int64. Any batch, dim and seqlen >= 0 are accepted (ragged
+ *     seqlen included); supported dstate: 1, 2, 4, 8, 16.
+ *   - Base pointers must be 4-byte aligned (SSM_ERR_ALIGN otherwise); 16-byte
+ *     aligned rows take the vectorised paths.
+ */
+#ifndef SSM_SCAN_H_
+#define SSM_SCAN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SSM_SCAN_ABI_VERSION 1
+
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype_t;
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_NULL = -1,              /* a required pointer is NULL */
+    SSM_ERR_DIM = -2,               /* a negative size, or sizes overflow int64 */
+    SSM_ERR_DTYPE = -3,             /* in_dtype / out_dtype not an ssm_dtype_t */
+    SSM_ERR_ALIGN = -4,             /* a pointer not 4-byte aligned */
+    SSM_ERR_WORKSPACE = -5,         /* workspace NULL or smaller than required */
+    SSM_ERR_LAUNCH = -6,            /* the CUDA launch itself failed */
+    SSM_ERR_LOOKBACK_TIMEOUT = -7,  /* device: a look-back wait exhausted its budget */
+    SSM_ERR_UNSUPPORTED_N = -8,     /* dstate not in {1, 2, 4, 8, 16} */
+    SSM_ERR_ALIAS = -9,             /* an output overlaps an input it must not */
+    SSM_ERR_ALGO = -10              /* unknown algorithm selector */
+} ssm_status_t;
+
+/* Algorithm selectors for ssm_scan_fwd_algo. All compute the same result.
+ *   SSM_ALGO_AUTO         : choose from the shape (what ssm_scan_fwd does).
+ *   SSM_ALGO_THREAD       : one channel's state vector split over 1-4 lanes, each
+ *                           lane walking time sequentially (large batch*dim).
+ *   SSM_ALGO_WARPSCAN     : lanes own consecutive time steps; (a, b) affine pairs
+ *                           composed by a warp-shuffle scan inside each chunk,
+ *                           serial carry across chunks.
+ *   SSM_ALGO_LOOKBACK     : WARPSCAN split along seqlen over many blocks, carries
+ *                           joined by single-pass decoupled look-back (long
+ *                           seqlen at small batch*dim). Needs a workspace. */
+typedef enum {
+    SSM_ALGO_AUTO = 0,
+    SSM_ALGO_THREAD = 1,
+    SSM_ALGO_WARPSCAN = 2,
+    SSM_ALGO_LOOKBACK = 3
+} ssm_algo_t;
+
+/* ABI version of the loaded library (SSM_SCAN_ABI_VERSION at build time). */
+int ssm_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* ssm_status_string(int status);
+
+/* Bytes of device workspace ssm_scan_fwd / ssm_scan_fwd_algo need for these
+ * sizes (0 when the chosen algorithm needs none; always >= 16 so that the
+ * status word fits). The caller allocates it; the library zeroes what it uses,
+ * on `stream`, inside each call. */
+size_t ssm_scan_workspace_size(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate);
+
+/* Selective scan, forward (prefill). See the operation above.
+ *   u, delta   : (batch, dim, seqlen), in_dtype           [required]
+ *   A          : (dim, dstate) fp32                       [required]
+ *   B, C       : (batch, dstate, seqlen), in_dtype        [required]
+ *   D          : (dim) fp32 skip weight                   [optional]
+ *   z          : (batch, dim, seqlen), in_dtype gate      [optional]
+ *   delta_bias : (dim) fp32, added to delta               [optional]
+ *   softplus   : nonzero applies softplus to delta + bias
+ *   h0         : (batch, dim, dstate) fp32 initial state  [optional, zero]
+ *   y          : (batch, dim, seqlen), out_dtype output   [required]
+ *   h_last     : (batch, dim, dstate) fp32 final state    [optional]
+ *   workspace  : device scratch of ssm_scan_workspace_size() bytes; may be NULL
+ *                when that size is 0 or the chosen algorithm needs none.
+ * y must not overlap any input; h_last may equal h0 (in-place resume). */
+int ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
+                 const void* C, const float* D, const void* z, const float* delta_bias,
+                 int softplus, const float* h0, void* y, float* h_last, int64_t batch,
+                 int64_t dim, int64_t seqlen, int64_t dstate, int in_dtype, int out_dtype,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* Same as ssm_scan_fwd with an explicit algorithm (ssm_algo_t). */
+int ssm_scan_fwd_algo(const void* u, const void* delta, const float* A, const void* B,
+                      const void* C, const float* D, const void* z, const float* delta_bias,
+                      int softplus, const float* h0, void* y, float* h_last, int64_t batch,
+                      int64_t dim, int64_t seqlen, int64_t dstate, int in_dtype,
+                      int out_dtype, void* workspace, size_t workspace_bytes, int algo,
+                      void* stream);
+
+/* d_state == 1 scalar scan (Scalar Mamba1 page, section details: with
+ * L = cumprod(exp(dt*A)), h = L * (h0 + cumsum(dt*B*u / L)), y = h * C).
+ * Shapes: A (dim), B and C (batch, seqlen), h0 and h_last (batch, dim); the
+ * rest as ssm_scan_fwd. Computed by the recurrence, which equals the closed
+ * form exactly in exact arithmetic and never divides by the cumulative product. */
+int ssm_scalar_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
+                        const void* C, const float* D, const void* z,
+                        const float* delta_bias, int softplus, const float* h0, void* y,
+                        float* h_last, int64_t batch, int64_t dim, int64_t seqlen,
+                        int in_dtype, int out_dtype, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/* One decode token, updating `state` in place (the per-step body of the same
+ * recurrence; O(1) work and memory per token).
+ *   state : (batch, dim, dstate) fp32, read and written   [required]
+ *   x, delta, z : (batch, dim), in_dtype                  [x, delta required]
+ *   B, C  : (batch, dstate), in_dtype                     [required]
+ *   A (dim, dstate), D (dim), delta_bias (dim) fp32       [A required]
+ *   y     : (batch, dim), out_dtype                       [required]
+ * y must not overlap state or any input. */
+int ssm_state_update(float* state, const void* x, const void* delta, const float* A,
+                     const void* B, const void* C, const float* D, const void* z,
+                     const float* delta_bias, int softplus, void* y, int64_t batch,
+                     int64_t dim, int64_t dstate, int in_dtype, int out_dtype, void* stream);
+
+/* Reads the device status word of `workspace` (written by a previous scan on
+ * the same stream), synchronising `stream` to do so. Returns SSM_OK or the
+ * device-side error (e.g. SSM_ERR_LOOKBACK_TIMEOUT); SSM_ERR_WORKSPACE when the
+ * workspace is NULL or under 16 bytes. */
+int ssm_query_status(const void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_SCAN_H_ */

@@ -1,0 +1,335 @@
+"""Pins of the fp64 oracle: checks against what the pages and the mathematics fix,
+never against the oracle itself. Each check takes an oracle.OracleLib and raises
+AssertionError on a mismatch, so the same checks run on the real oracle and on
+deliberately broken copies of its source (tests/test_oracle_pins.py).
+
+Pages cited:
+  [guide]  Mamba SSM complete guide (youngju.dev): section 2 "Discretization" and
+           "SSM as a convolution kernel"; section 5 "Hardware-Aware Algorithm"
+           (parallel scan) and "complete Mamba implementation" (selective_scan).
+  [SM1]    Scalar Mamba1 (SM1) page (aitrends.kr), section details: the
+           cumprod/cumsum closed form at d_state = 1.
+"""
+from __future__ import annotations
+
+import math
+from fractions import Fraction
+
+import numpy as np
+
+from oracle import forms
+
+
+def _rel(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    scale = max(float(np.sqrt(np.mean(b * b))), 1e-300)
+    return float(np.max(np.abs(a - b))) / scale
+
+
+# ---------------------------------------------------------------------------
+# 1. Brute force: the unrolled sum in exact rational arithmetic, tiny sizes.
+#    h_t = (prod_{s<=t} a_s) h0 + sum_{s<=t} (prod_{s<r<=t} a_r) dt_s B_s u_s,
+#    y_t = sum_n C_tn h_tn + D u_t, times silu(z_t)  ([guide] section 2, the
+#    recurrence unrolled as the page does for the convolution view; section 5
+#    selective_scan for dt*B and the D skip; MambaBlock.forward for the gate).
+# ---------------------------------------------------------------------------
+def _dyadic(rng, shape, den=8, lo=-16, hi=16):
+    return (rng.integers(lo, hi + 1, size=shape) / den).astype(np.float32)
+
+
+def check_bruteforce_rational(orc):
+    rng = np.random.default_rng(7)
+    for case in range(6):
+        bt, dim, L, N = 2, 2, 1 + case % 4, 1 + case % 2
+        u = _dyadic(rng, (bt, dim, L))
+        delta = (rng.integers(1, 9, size=(bt, dim, L)) / 8).astype(np.float32)   # dt in (0, 1]
+        bias = (rng.integers(0, 3, size=(dim,)) / 4).astype(np.float32)
+        A = -(rng.integers(1, 9, size=(dim, N)) / 4).astype(np.float32)
+        B = _dyadic(rng, (bt, N, L))
+        C = _dyadic(rng, (bt, N, L))
+        D = _dyadic(rng, (dim,)) if case % 3 else None
+        z = _dyadic(rng, (bt, dim, L)) if case % 2 else None
+        h0 = _dyadic(rng, (bt, dim, N)).astype(np.float64) if case >= 2 else None
+        y, hl = orc.scan(u, delta, A, B, C, D, z, bias, False, h0)
+        for b in range(bt):
+            for d in range(dim):
+                dt = [Fraction(float(delta[b, d, t])) + Fraction(float(bias[d])) for t in range(L)]
+                a = [[Fraction(math.exp(float(dt[t]) * float(A[d, n]))) for n in range(N)] for t in range(L)]
+                h_end = []
+                for t in range(L):
+                    acc = Fraction(0)
+                    for n in range(N):
+                        h = Fraction(float(h0[b, d, n])) if h0 is not None else Fraction(0)
+                        for s in range(t + 1):
+                            h *= a[s][n]
+                        for s in range(t + 1):
+                            w = Fraction(1)
+                            for r in range(s + 1, t + 1):
+                                w *= a[r][n]
+                            h += w * dt[s] * Fraction(float(B[b, n, s])) * Fraction(float(u[b, d, s]))
+                        acc += Fraction(float(C[b, n, t])) * h
+                        if t == L - 1:
+                            h_end.append(h)
+                    if D is not None:
+                        acc += Fraction(float(D[d])) * Fraction(float(u[b, d, t]))
+                    if z is not None:
+                        zz = float(z[b, d, t])
+                        acc *= Fraction(zz) / (1 + Fraction(math.exp(-zz)))
+                    assert abs(float(acc) - y[b, d, t]) <= 1e-14 * max(1.0, abs(float(acc))), (case, b, d, t)
+                for n in range(N):
+                    assert abs(float(h_end[n]) - hl[b, d, n]) <= 1e-14 * max(1.0, abs(float(h_end[n])))
+
+
+def check_symbolic_two_steps(orc):
+    """L = 2, N = 1 written out: y_2 = C_2 (a_2 (a_1 h0 + dt_1 B_1 u_1) + dt_2 B_2 u_2) + D u_2."""
+    u = np.array([[[3.0, -2.0]]], np.float32)
+    delta = np.array([[[0.5, 0.25]]], np.float32)
+    A = np.array([[-2.0]], np.float32)
+    B = np.array([[[1.5, -4.0]]], np.float32)
+    C = np.array([[[2.0, 0.5]]], np.float32)
+    D = np.array([0.75], np.float32)
+    h0 = np.array([[[1.25]]])
+    y, hl = orc.scan(u, delta, A, B, C, D, None, None, False, h0)
+    a1, a2 = math.exp(-1.0), math.exp(-0.5)
+    h1 = a1 * 1.25 + 0.5 * 1.5 * 3.0
+    h2 = a2 * h1 + 0.25 * -4.0 * -2.0
+    assert abs(y[0, 0, 0] - (2.0 * h1 + 0.75 * 3.0)) < 1e-14
+    assert abs(y[0, 0, 1] - (0.5 * h2 + 0.75 * -2.0)) < 1e-14
+    assert abs(hl[0, 0, 0] - h2) < 1e-14
+
+
+# ---------------------------------------------------------------------------
+# 2. Exact integer case: softplus off, delta = 1, A = 0 => Abar = exp(0) = 1,
+#    so h_t = h0 + cumsum(B u) and y = C.h + D u are exact in floating point.
+# ---------------------------------------------------------------------------
+def check_exact_integer(orc):
+    rng = np.random.default_rng(11)
+    bt, dim, L, N = 3, 5, 37, 4
+    u = rng.integers(-3, 4, size=(bt, dim, L)).astype(np.float32)
+    delta = np.ones((bt, dim, L), np.float32)
+    A = np.zeros((dim, N), np.float32)
+    B = rng.integers(-3, 4, size=(bt, N, L)).astype(np.float32)
+    C = rng.integers(-3, 4, size=(bt, N, L)).astype(np.float32)
+    D = rng.integers(-3, 4, size=(dim,)).astype(np.float32)
+    h0 = rng.integers(-5, 6, size=(bt, dim, N)).astype(np.float64)
+    y, hl = orc.scan(u, delta, A, B, C, D, None, None, False, h0)
+    ui = u.astype(np.int64)
+    Bi = B.astype(np.int64)
+    Ci = C.astype(np.int64)
+    h = h0.astype(np.int64)[:, :, :, None] + np.cumsum(Bi[:, None, :, :] * ui[:, :, None, :], axis=3)
+    yi = (Ci[:, None, :, :] * h).sum(axis=2) + D.astype(np.int64)[None, :, None] * ui
+    assert np.array_equal(y, yi.astype(np.float64))
+    assert np.array_equal(hl, h[:, :, :, -1].astype(np.float64))
+
+
+# ---------------------------------------------------------------------------
+# 3. Scalar functions: identities fixed by the mathematics.
+#    softplus(x) - softplus(-x) = x; softplus(0) = ln 2; identity above 20
+#    (PyTorch's default threshold, the reading taken for F.softplus).
+#    silu(x) - silu(-x) = x; silu(0) = 0.
+# ---------------------------------------------------------------------------
+def check_softplus_silu(orc):
+    for x in [0.1, 0.5, 1.0, 3.0, 7.5, 15.0]:
+        assert abs((orc.softplus(x) - orc.softplus(-x)) - x) <= 4e-16 * max(1.0, x)
+        assert abs((orc.silu(x) - orc.silu(-x)) - x) <= 4e-16 * max(1.0, x)
+    assert abs(orc.softplus(0.0) - math.log(2.0)) <= 2e-16
+    assert orc.softplus(25.0) == 25.0 and orc.softplus(20.5) == 20.5
+    assert abs(orc.softplus(-30.0) / math.exp(-30.0) - 1.0) < 1e-12
+    assert orc.silu(0.0) == 0.0
+    assert abs(orc.silu(40.0) - 40.0) < 1e-12
+    # inside the scan: A = 0, B = u = C = 1 => y_t = sum_{s<=t} softplus(delta_s + bias)
+    rng = np.random.default_rng(3)
+    L = 50
+    delta = rng.standard_normal((1, 1, L)).astype(np.float32) * 3
+    bias = np.array([0.625], np.float32)
+    y, _ = orc.scan(np.ones((1, 1, L), np.float32), delta, np.zeros((1, 1), np.float32),
+                    np.ones((1, 1, L), np.float32), np.ones((1, 1, L), np.float32), None, None,
+                    bias, True, None)
+    sp = np.logaddexp(0.0, delta[0, 0].astype(np.float64) + 0.625)
+    assert _rel(y[0, 0], np.cumsum(sp)) < 1e-14
+
+
+# ---------------------------------------------------------------------------
+# 4. d_state = 1: the SM1 closed form h = Lc (h0 + cumsum(dBx / Lc)), y = h C,
+#    Lc = cumprod(dA) ([SM1]; exact, per the page, at d_state = 1).
+# ---------------------------------------------------------------------------
+def _sm1_case(rng, bt=2, dim=4, L=600):
+    u = rng.standard_normal((bt, dim, L)).astype(np.float32)
+    delta = (rng.standard_normal((bt, dim, L)) * 0.5).astype(np.float32)
+    dt0 = np.exp(rng.uniform(math.log(1e-3), math.log(1e-1), size=dim))
+    bias = (dt0 + np.log(-np.expm1(-dt0))).astype(np.float32)
+    A = (-np.exp(rng.uniform(math.log(0.5), math.log(4.0), size=(dim, 1)))).astype(np.float32)
+    B = rng.standard_normal((bt, 1, L)).astype(np.float32)
+    C = rng.standard_normal((bt, 1, L)).astype(np.float32)
+    h0 = rng.standard_normal((bt, dim, 1))
+    return u, delta, bias, A, B, C, h0
+
+
+def check_sm1_closed_form(orc):
+    rng = np.random.default_rng(21)
+    u, delta, bias, A, B, C, h0 = _sm1_case(rng)
+    y, hl = orc.scan(u, delta, A, B, C, None, None, bias, True, h0)
+    dt = np.logaddexp(0.0, delta.astype(np.float64) + bias[None, :, None])
+    dA = np.exp(dt * A[None, :, :1].astype(np.float64))
+    dBx = dt * B.astype(np.float64) * u
+    h, yc = forms.sm1_closed_form(dA, dBx, h0[..., 0], np.broadcast_to(C.astype(np.float64), u.shape))
+    assert _rel(y, yc) < 1e-12
+    assert _rel(hl[..., 0], h[..., -1]) < 1e-12
+
+
+def check_sm1_literal_clamp_reading(orc):
+    """The page's line with L.clamp(min=1e-6) agrees with the recurrence while the
+    cumulative product stays above 1e-6, and departs from it after."""
+    rng = np.random.default_rng(22)
+    u, delta, bias, A, B, C, h0 = _sm1_case(rng, bt=1, dim=2, L=4000)
+    A = np.full_like(A, -4.0)
+    bias = np.full_like(bias, 0.5)           # dt ~ 1: cumprod falls below 1e-6 quickly
+    y, _ = orc.scan(u, delta, A, B, C, None, None, bias, True, h0)
+    dt = np.logaddexp(0.0, delta.astype(np.float64) + bias[None, :, None])
+    dA = np.exp(dt * -4.0)
+    dBx = dt * B.astype(np.float64) * u
+    Lc = np.cumprod(dA, axis=-1)
+    _, ylit = forms.sm1_literal_clamped(dA, dBx, h0[..., 0], C.astype(np.float64))
+    ok = Lc >= 1e-6
+    assert ok.any() and (~ok).any()
+    scale = np.sqrt(np.mean(y * y))
+    assert np.max(np.abs(ylit[ok] - y[ok])) < 1e-9 * scale
+    assert np.max(np.abs(ylit[~ok] - y[~ok])) > 1e-3 * scale
+
+
+# ---------------------------------------------------------------------------
+# 5. Time-invariant case: dt, B, C constant over t => y = K * u + D u with
+#    K_k = sum_n C_n exp(k dt A_n) dt B_n ([guide] section 2, "SSM as a
+#    convolution kernel").
+# ---------------------------------------------------------------------------
+def check_lti_convolution(orc):
+    rng = np.random.default_rng(5)
+    L, N = 64, 4
+    A = -np.array([[0.5, 1.0, 2.0, 4.0]], np.float32)
+    dt = 0.15625
+    Bn = rng.standard_normal(N).astype(np.float32)
+    Cn = rng.standard_normal(N).astype(np.float32)
+    u = rng.standard_normal((1, 1, L)).astype(np.float32)
+    D = np.array([0.5], np.float32)
+    y, _ = orc.scan(u, np.full((1, 1, L), dt, np.float32), A,
+                    np.repeat(Bn[None, :, None], L, axis=2), np.repeat(Cn[None, :, None], L, axis=2),
+                    D, None, None, False, None)
+    K = forms.lti_kernel(A[0], Bn, Cn, dt, L)
+    ref = forms.causal_conv(K, u[0, 0].astype(np.float64)) + 0.5 * u[0, 0]
+    assert _rel(y[0, 0], ref) < 1e-12
+
+
+# ---------------------------------------------------------------------------
+# 6. Associativity: any bracketing of the affine pairs (g, tok) gives the
+#    sequential result ([guide] section 5, Hardware-Aware Algorithm).
+# ---------------------------------------------------------------------------
+def check_tree_scan(orc):
+    rng = np.random.default_rng(9)
+    T = 48
+    logg = np.log(rng.uniform(0.3, 0.99, size=(T,)))
+    tokens = rng.standard_normal(T).astype(np.float32)
+    # one channel, gate g_t = exp(-dt_t) through a time-varying dt_t = -log g_t and A = -1
+    delta = (-logg).astype(np.float32)
+    gates = np.exp(-delta.astype(np.float64))
+    y, _ = orc.scan(np.ones((1, 1, T), np.float32), delta[None, None], np.array([[-1.0]], np.float32),
+                    (tokens / delta)[None, None].astype(np.float32), np.ones((1, 1, T), np.float32),
+                    None, None, None, False, None)
+    tok = delta.astype(np.float64) * (tokens / delta).astype(np.float32).astype(np.float64)
+    for seed in range(3):
+        xs = forms.tree_scan(gates, tok, np.random.default_rng(seed))
+        assert _rel(y[0, 0], xs) < 1e-13
+
+
+# ---------------------------------------------------------------------------
+# 7. Resume: a run over L1 then a run over L2 started from h_last equals one
+#    run over L1 + L2 (state-based resume; the recurrence only carries h).
+# ---------------------------------------------------------------------------
+def _random_case(rng, bt, dim, L, N, z=True):
+    u = rng.standard_normal((bt, dim, L)).astype(np.float32)
+    delta = (rng.standard_normal((bt, dim, L)) * 0.5).astype(np.float32)
+    dt0 = np.exp(rng.uniform(math.log(1e-3), math.log(1e-1), size=dim))
+    bias = (dt0 + np.log(-np.expm1(-dt0))).astype(np.float32)
+    A = -np.tile(np.arange(1, N + 1, dtype=np.float32), (dim, 1))
+    B = rng.standard_normal((bt, N, L)).astype(np.float32)
+    C = rng.standard_normal((bt, N, L)).astype(np.float32)
+    D = rng.standard_normal(dim).astype(np.float32)
+    zz = rng.standard_normal((bt, dim, L)).astype(np.float32) if z else None
+    return u, delta, A, B, C, D, zz, bias
+
+
+def check_resume(orc):
+    rng = np.random.default_rng(13)
+    u, delta, A, B, C, D, z, bias = _random_case(rng, 2, 3, 256, 16)
+    h0 = rng.standard_normal((2, 3, 16))
+    y, hl = orc.scan(u, delta, A, B, C, D, z, bias, True, h0)
+    L1 = 100
+    y1, h1 = orc.scan(u[..., :L1], delta[..., :L1], A, B[..., :L1], C[..., :L1], D, z[..., :L1], bias, True, h0)
+    y2, h2 = orc.scan(u[..., L1:], delta[..., L1:], A, B[..., L1:], C[..., L1:], D, z[..., L1:], bias, True, h1)
+    assert np.array_equal(np.concatenate([y1, y2], axis=-1), y)
+    assert np.array_equal(h2, hl)
+
+
+# ---------------------------------------------------------------------------
+# 8. Recurrent / parallel duality: L single-token decode updates from h0 equal
+#    the prefill scan over L ([guide] section 1/2: recurrence at inference).
+# ---------------------------------------------------------------------------
+def check_decode_equals_prefill(orc):
+    rng = np.random.default_rng(17)
+    u, delta, A, B, C, D, z, bias = _random_case(rng, 2, 3, 32, 8)
+    h0 = rng.standard_normal((2, 3, 8))
+    y, hl = orc.scan(u, delta, A, B, C, D, z, bias, True, h0)
+    state = h0.copy()
+    for t in range(32):
+        yt = orc.state_update(state, u[..., t], delta[..., t], A, B[..., t], C[..., t], D, z[..., t], bias, True)
+        assert np.array_equal(yt, y[..., t])
+    assert np.array_equal(state, hl)
+
+
+# ---------------------------------------------------------------------------
+# 9. Linearity in (u, h0) for fixed dt, B, C (no gate): the map is linear.
+# ---------------------------------------------------------------------------
+def check_linearity(orc):
+    rng = np.random.default_rng(19)
+    bt, dim, L, N = 2, 3, 40, 4
+    _, delta, A, B, C, D, _, bias = _random_case(rng, bt, dim, L, N, z=False)
+    u1 = rng.integers(-8, 9, size=(bt, dim, L)).astype(np.float32)
+    u2 = rng.integers(-8, 9, size=(bt, dim, L)).astype(np.float32)
+    g1 = rng.integers(-8, 9, size=(bt, dim, N)).astype(np.float64)
+    g2 = rng.integers(-8, 9, size=(bt, dim, N)).astype(np.float64)
+    ya, ha = orc.scan(u1, delta, A, B, C, D, None, bias, True, g1)
+    yb, hb = orc.scan(u2, delta, A, B, C, D, None, bias, True, g2)
+    yc, hc = orc.scan(2 * u1 - 3 * u2, delta, A, B, C, D, None, bias, True, 2 * g1 - 3 * g2)
+    assert _rel(yc, 2 * ya - 3 * yb) < 1e-13
+    assert _rel(hc, 2 * ha - 3 * hb) < 1e-13
+
+
+# ---------------------------------------------------------------------------
+# 10. Limits: C = 0 => y = D u silu(z); dt -> 0 => the state stays at h0.
+# ---------------------------------------------------------------------------
+def check_limits(orc):
+    rng = np.random.default_rng(23)
+    u, delta, A, B, C, D, z, bias = _random_case(rng, 1, 4, 30, 4)
+    y, _ = orc.scan(u, delta, A, B, np.zeros_like(C), D, z, bias, True, None)
+    zz = z.astype(np.float64)
+    ref = D[None, :, None].astype(np.float64) * u * (zz * 0.5 * (1.0 + np.tanh(zz / 2)))
+    assert _rel(y, ref) < 1e-14
+    h0 = rng.standard_normal((1, 4, 4))
+    _, hl = orc.scan(u, np.full_like(delta, -60.0), A, B, C, D, z, None, True, h0)
+    assert np.max(np.abs(hl - h0)) < 1e-20
+
+
+ALL_CHECKS = [
+    check_bruteforce_rational,
+    check_symbolic_two_steps,
+    check_exact_integer,
+    check_softplus_silu,
+    check_sm1_closed_form,
+    check_sm1_literal_clamp_reading,
+    check_lti_convolution,
+    check_tree_scan,
+    check_resume,
+    check_decode_equals_prefill,
+    check_linearity,
+    check_limits,
+]

@@ -1,0 +1,61 @@
+"""Oracle pins (CPU) and a mutation test: every pin runs on the real oracle and must
+pass; each deliberately broken copy of the oracle's C source must fail at least one."""
+import os
+import shutil
+import tempfile
+
+import pytest
+
+import oracle
+from tests import oracle_pins
+
+
+@pytest.mark.parametrize("check", oracle_pins.ALL_CHECKS, ids=lambda f: f.__name__)
+def test_pin(check):
+    check(oracle.default())
+
+
+# (name, exact text in ssm_oracle.c, replacement): plausible mistakes.
+MUTANTS = [
+    ("sign_of_A", "exp(dt * (double)A_d[n])", "exp(-dt * (double)A_d[n])"),
+    ("drop_D", "(D ? (double)D[d] * ut : 0.0)", "0.0"),
+    ("B_for_C", "double bu = dt * (double)B_b[n * seqlen + t] * ut;",
+     "double bu = dt * (double)C_b[n * seqlen + t] * ut;"),
+    ("no_bias", "double x = (double)dl_r[t] + (delta_bias ? (double)delta_bias[d] : 0.0);",
+     "double x = (double)dl_r[t];"),
+    ("y_before_update", "h[n] = a * h[n] + bu;\n                acc += (double)C_b[n * seqlen + t] * h[n];",
+     "acc += (double)C_b[n * seqlen + t] * h[n];\n                h[n] = a * h[n] + bu;"),
+    ("sigmoid_gate", "yv *= oracle_silu((double)z_r[t]);", "yv *= 1.0 / (1.0 + exp(-(double)z_r[t]));"),
+    ("no_softplus", "return x > 20.0 ? x : log1p(exp(x));", "return x;"),
+    ("softplus_threshold", "return x > 20.0 ? x : log1p(exp(x));", "return x > 2.0 ? x : log1p(exp(x));"),
+    ("ignore_h0", "h[n] = h0 ? h0[ch * dstate + n] : 0.0;", "h[n] = 0.0;"),
+    ("B_time_shift", "double bu = dt * (double)B_b[n * seqlen + t] * ut;",
+     "double bu = dt * (double)B_b[n * seqlen + (t > 0 ? t - 1 : 0)] * ut;"),
+    ("zoh_like_Bbar", "double bu = dt * (double)B_b[n * seqlen + t] * ut;",
+     "double bu = (double)B_b[n * seqlen + t] * ut;"),
+    ("decode_drop_dt", "s[n] = a * s[n] + dt * (double)B[b * dstate + n] * xt;",
+     "s[n] = a * s[n] + (double)B[b * dstate + n] * xt;"),
+    ("h_last_zero", "h_last[ch * dstate + n] = h[n];", "h_last[ch * dstate + n] = 0.0;"),
+    ("A_transposed", "const float *A_d = A + d * dstate;", "const float *A_d = A + d;"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(name, old, new):
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique/present"
+    tmp = tempfile.mkdtemp(prefix="oracle_mutant_")
+    try:
+        path = os.path.join(tmp, "mutant.c")
+        with open(path, "w") as f:
+            f.write(src.replace(old, new))
+        lib = oracle.OracleLib(oracle.compile_source(path, os.path.join(tmp, "libmutant.so")))
+        failed = []
+        for check in oracle_pins.ALL_CHECKS:
+            try:
+                check(lib)
+            except AssertionError:
+                failed.append(check.__name__)
+        assert failed, f"no pin catches mutant {name}"
+    finally:
+        shutil.rmtree(tmp)
