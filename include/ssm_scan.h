@@ -28,15 +28,16 @@
  *       h0, h_last     : (batch, dim, dstate) fp32
  *   - in_dtype gives the dtype of u, delta, z, B, C; out_dtype the dtype of y.
  *     A, D, delta_bias and the state are always fp32; all arithmetic is fp32.
- *   - Optional pointers (D, z, delta_bias, h0, h_last) may be NULL.
+ *   - Optional pointers (D, z, delta_bias, h0, h_last) may be NULL. A required
+ *     pointer may be NULL only when its tensor has no elements.
  *   - Argument errors are returned synchronously as a negative ssm_status and
  *     nothing is launched. Errors raised on the device (a look-back wait that ran
  *     out of its iteration budget) are written to the workspace status word and
  *     read back with ssm_query_status().
  *   - Sizes are int64. Any batch, dim and seqlen >= 0 are accepted (ragged
  *     seqlen included); supported dstate: 1, 2, 4, 8, 16.
- *   - Base pointers must be 4-byte aligned (SSM_ERR_ALIGN otherwise); 16-byte
- *     aligned rows take the vectorised paths.
+ *   - Pointers must be aligned to their element size (SSM_ERR_ALIGN otherwise);
+ *     16-byte aligned rows take the vectorised paths.
  */
 #ifndef SSM_SCAN_H_
 #define SSM_SCAN_H_
@@ -50,6 +51,13 @@ extern "C" {
 
 #define SSM_SCAN_ABI_VERSION 1
 
+/* Exported entry points (the library is built with hidden default visibility). */
+#if defined(__GNUC__)
+#define SSM_API __attribute__((visibility("default")))
+#else
+#define SSM_API
+#endif
+
 typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype_t;
 
 typedef enum {
@@ -57,7 +65,7 @@ typedef enum {
     SSM_ERR_NULL = -1,              /* a required pointer is NULL */
     SSM_ERR_DIM = -2,               /* a negative size, or sizes overflow int64 */
     SSM_ERR_DTYPE = -3,             /* in_dtype / out_dtype not an ssm_dtype_t */
-    SSM_ERR_ALIGN = -4,             /* a pointer not 4-byte aligned */
+    SSM_ERR_ALIGN = -4,             /* a pointer not aligned to its element size */
     SSM_ERR_WORKSPACE = -5,         /* workspace NULL or smaller than required */
     SSM_ERR_LAUNCH = -6,            /* the CUDA launch itself failed */
     SSM_ERR_LOOKBACK_TIMEOUT = -7,  /* device: a look-back wait exhausted its budget */
@@ -84,16 +92,16 @@ typedef enum {
 } ssm_algo_t;
 
 /* ABI version of the loaded library (SSM_SCAN_ABI_VERSION at build time). */
-int ssm_abi_version(void);
+SSM_API int ssm_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
-const char* ssm_status_string(int status);
+SSM_API const char* ssm_status_string(int status);
 
 /* Bytes of device workspace ssm_scan_fwd / ssm_scan_fwd_algo need for these
- * sizes (0 when the chosen algorithm needs none; always >= 16 so that the
- * status word fits). The caller allocates it; the library zeroes what it uses,
- * on `stream`, inside each call. */
-size_t ssm_scan_workspace_size(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate);
+ * sizes under any algorithm (always >= 16 so that the status word fits). The
+ * caller allocates it; the library zeroes what it uses, on `stream`, inside
+ * each look-back call. */
+SSM_API size_t ssm_scan_workspace_size(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate);
 
 /* Selective scan, forward (prefill). See the operation above.
  *   u, delta   : (batch, dim, seqlen), in_dtype           [required]
@@ -107,52 +115,67 @@ size_t ssm_scan_workspace_size(int64_t batch, int64_t dim, int64_t seqlen, int64
  *   y          : (batch, dim, seqlen), out_dtype output   [required]
  *   h_last     : (batch, dim, dstate) fp32 final state    [optional]
  *   workspace  : device scratch of ssm_scan_workspace_size() bytes; may be NULL
- *                when that size is 0 or the chosen algorithm needs none.
+ *                when the chosen algorithm needs none (only the look-back does).
  * y must not overlap any input; h_last may equal h0 (in-place resume). */
-int ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
-                 const void* C, const float* D, const void* z, const float* delta_bias,
-                 int softplus, const float* h0, void* y, float* h_last, int64_t batch,
-                 int64_t dim, int64_t seqlen, int64_t dstate, int in_dtype, int out_dtype,
-                 void* workspace, size_t workspace_bytes, void* stream);
+SSM_API int ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
+                         const void* C, const float* D, const void* z, const float* delta_bias,
+                         int softplus, const float* h0, void* y, float* h_last, int64_t batch,
+                         int64_t dim, int64_t seqlen, int64_t dstate, int in_dtype, int out_dtype,
+                         void* workspace, size_t workspace_bytes, void* stream);
 
 /* Same as ssm_scan_fwd with an explicit algorithm (ssm_algo_t). */
-int ssm_scan_fwd_algo(const void* u, const void* delta, const float* A, const void* B,
-                      const void* C, const float* D, const void* z, const float* delta_bias,
-                      int softplus, const float* h0, void* y, float* h_last, int64_t batch,
-                      int64_t dim, int64_t seqlen, int64_t dstate, int in_dtype,
-                      int out_dtype, void* workspace, size_t workspace_bytes, int algo,
-                      void* stream);
+SSM_API int ssm_scan_fwd_algo(const void* u, const void* delta, const float* A, const void* B,
+                              const void* C, const float* D, const void* z,
+                              const float* delta_bias, int softplus, const float* h0, void* y,
+                              float* h_last, int64_t batch, int64_t dim, int64_t seqlen,
+                              int64_t dstate, int in_dtype, int out_dtype, void* workspace,
+                              size_t workspace_bytes, int algo, void* stream);
 
 /* d_state == 1 scalar scan (Scalar Mamba1 page, section details: with
  * L = cumprod(exp(dt*A)), h = L * (h0 + cumsum(dt*B*u / L)), y = h * C).
  * Shapes: A (dim), B and C (batch, seqlen), h0 and h_last (batch, dim); the
  * rest as ssm_scan_fwd. Computed by the recurrence, which equals the closed
  * form exactly in exact arithmetic and never divides by the cumulative product. */
-int ssm_scalar_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
-                        const void* C, const float* D, const void* z,
-                        const float* delta_bias, int softplus, const float* h0, void* y,
-                        float* h_last, int64_t batch, int64_t dim, int64_t seqlen,
-                        int in_dtype, int out_dtype, void* workspace,
-                        size_t workspace_bytes, void* stream);
+SSM_API int ssm_scalar_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
+                                const void* C, const float* D, const void* z,
+                                const float* delta_bias, int softplus, const float* h0, void* y,
+                                float* h_last, int64_t batch, int64_t dim, int64_t seqlen,
+                                int in_dtype, int out_dtype, void* workspace,
+                                size_t workspace_bytes, void* stream);
 
 /* One decode token, updating `state` in place (the per-step body of the same
  * recurrence; O(1) work and memory per token).
- *   state : (batch, dim, dstate) fp32, read and written   [required]
+ *   state : (batch, dim, dstate) fp32, read and written   [required; 16-byte
+ *           aligned when dstate >= 4]
  *   x, delta, z : (batch, dim), in_dtype                  [x, delta required]
  *   B, C  : (batch, dstate), in_dtype                     [required]
  *   A (dim, dstate), D (dim), delta_bias (dim) fp32       [A required]
  *   y     : (batch, dim), out_dtype                       [required]
  * y must not overlap state or any input. */
-int ssm_state_update(float* state, const void* x, const void* delta, const float* A,
-                     const void* B, const void* C, const float* D, const void* z,
-                     const float* delta_bias, int softplus, void* y, int64_t batch,
-                     int64_t dim, int64_t dstate, int in_dtype, int out_dtype, void* stream);
+SSM_API int ssm_state_update(float* state, const void* x, const void* delta, const float* A,
+                             const void* B, const void* C, const float* D, const void* z,
+                             const float* delta_bias, int softplus, void* y, int64_t batch,
+                             int64_t dim, int64_t dstate, int in_dtype, int out_dtype,
+                             void* stream);
 
-/* Reads the device status word of `workspace` (written by a previous scan on
- * the same stream), synchronising `stream` to do so. Returns SSM_OK or the
- * device-side error (e.g. SSM_ERR_LOOKBACK_TIMEOUT); SSM_ERR_WORKSPACE when the
- * workspace is NULL or under 16 bytes. */
-int ssm_query_status(const void* workspace, size_t workspace_bytes, void* stream);
+/* Test hook for the look-back error path. Runs the look-back scan (softplus on,
+ * no D, z, bias or h0; y in in_dtype) with segment `drop_segment` withholding
+ * its publication, so the waits of the next segment run out after `spin_limit`
+ * polls: the kernel then records SSM_ERR_LOOKBACK_TIMEOUT in the workspace
+ * status word and finishes (y is then unspecified). Returns the launch status;
+ * read the device status with ssm_query_status(). */
+SSM_API int ssm_test_lookback_timeout(const void* u, const void* delta, const float* A,
+                                      const void* B, const void* C, void* y, int64_t batch,
+                                      int64_t dim, int64_t seqlen, int64_t dstate, int in_dtype,
+                                      void* workspace, size_t workspace_bytes,
+                                      int64_t drop_segment, uint32_t spin_limit, void* stream);
+
+/* Reads the device status word of `workspace` (reset and written by a previous
+ * look-back scan on the same stream; other algorithms leave it untouched),
+ * synchronising `stream` to do so. Returns SSM_OK or the device-side error
+ * (e.g. SSM_ERR_LOOKBACK_TIMEOUT); SSM_ERR_WORKSPACE when the workspace is
+ * NULL or under 16 bytes. */
+SSM_API int ssm_query_status(const void* workspace, size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,218 @@
+"""B300-native Mamba-1 selective scan: thin Python binding over libssmscan.so.
+
+Every function here only marshals arguments: it checks tensor placement, shape
+and dtype, allocates outputs with torch (device memory is torch's job), and
+calls the C ABI declared in include/ssm_scan.h on torch's current CUDA stream.
+All arithmetic runs in the library's sm_103a kernels; there is no CPU or
+PyTorch fallback. If libssmscan.so is missing, importing this package raises.
+
+Entry points (names follow the C ABI):
+    scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus, h0) -> (y, h_last)
+    scalar_scan_fwd(...)  d_state = 1 (SM1) form of scan_fwd
+    state_update(state, x, delta, A, B, C, D, z, delta_bias, softplus) -> y
+    workspace_size(batch, dim, seqlen, dstate) -> bytes
+    query_status(workspace) -> device status word of a look-back scan
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libssmscan.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python selective_state_space_121_b300/build.py` "
+        "(there is no CPU fallback)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+
+_lib.ssm_abi_version.restype = _I
+_lib.ssm_status_string.argtypes = [_I]
+_lib.ssm_status_string.restype = ctypes.c_char_p
+_lib.ssm_scan_workspace_size.argtypes = [_I64] * 4
+_lib.ssm_scan_workspace_size.restype = _SZ
+_lib.ssm_scan_fwd.argtypes = [_P] * 8 + [_I, _P, _P, _P] + [_I64] * 4 + [_I, _I, _P, _SZ, _P]
+_lib.ssm_scan_fwd.restype = _I
+_lib.ssm_scan_fwd_algo.argtypes = [_P] * 8 + [_I, _P, _P, _P] + [_I64] * 4 + [_I, _I, _P, _SZ, _I, _P]
+_lib.ssm_scan_fwd_algo.restype = _I
+_lib.ssm_scalar_scan_fwd.argtypes = [_P] * 8 + [_I, _P, _P, _P] + [_I64] * 3 + [_I, _I, _P, _SZ, _P]
+_lib.ssm_scalar_scan_fwd.restype = _I
+_lib.ssm_state_update.argtypes = [_P] * 9 + [_I, _P] + [_I64] * 3 + [_I, _I, _P]
+_lib.ssm_state_update.restype = _I
+_lib.ssm_test_lookback_timeout.argtypes = [_P] * 6 + [_I64] * 4 + [_I, _P, _SZ, _I64, ctypes.c_uint32, _P]
+_lib.ssm_test_lookback_timeout.restype = _I
+_lib.ssm_query_status.argtypes = [_P, _SZ, _P]
+_lib.ssm_query_status.restype = _I
+
+SSM_F32, SSM_BF16 = 0, 1
+ALGOS = {"auto": 0, "thread": 1, "warpscan": 2, "lookback": 3}
+SSM_ERR_LOOKBACK_TIMEOUT = -7
+
+# the C ABI entry-point names, as declared in include/ssm_scan.h
+EXPORTS = ("ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_size", "ssm_scan_fwd",
+           "ssm_scan_fwd_algo", "ssm_scalar_scan_fwd", "ssm_state_update",
+           "ssm_test_lookback_timeout", "ssm_query_status")
+
+
+class SSMError(RuntimeError):
+    def __init__(self, status: int):
+        self.status = status
+        super().__init__(_lib.ssm_status_string(status).decode())
+
+
+def _check(status: int):
+    if status != 0:
+        raise SSMError(status)
+
+
+def abi_version() -> int:
+    return _lib.ssm_abi_version()
+
+
+def status_string(status: int) -> str:
+    return _lib.ssm_status_string(status).decode()
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return SSM_F32
+    if t == torch.bfloat16:
+        return SSM_BF16
+    raise TypeError(f"unsupported dtype {t}: use torch.float32 or torch.bfloat16")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr() or None
+
+
+def _f32(t, shape, name):
+    if t is None:
+        return None
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t
+
+
+def _same(ref, named_shapes):
+    for name, t, shp in named_shapes:
+        if t is None:
+            continue
+        if t.dtype != ref.dtype:
+            raise TypeError(f"{name} must have dtype {ref.dtype}")
+        if tuple(t.shape) != tuple(shp):
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shp)}")
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def workspace_size(batch: int, dim: int, seqlen: int, dstate: int) -> int:
+    return int(_lib.ssm_scan_workspace_size(batch, dim, seqlen, dstate))
+
+
+def alloc_workspace(batch: int, dim: int, seqlen: int, dstate: int, device=None) -> torch.Tensor:
+    n = workspace_size(batch, dim, seqlen, dstate)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, h0=None, *,
+             out_dtype=None, return_last_state=True, algo="auto", workspace=None, y=None,
+             h_last=None):
+    """Selective scan forward. u, delta, z: (batch, dim, L); B, C: (batch, N, L);
+    A: (dim, N) fp32; D, delta_bias: (dim,) fp32; h0: (batch, dim, N) fp32.
+    Returns (y (batch, dim, L), h_last (batch, dim, N) fp32 or None)."""
+    bt, dim, L = u.shape
+    N = A.shape[1]
+    in_code = _dtype_code(u.dtype)
+    _same(u, (("delta", delta, u.shape), ("B", B, (bt, N, L)), ("C", C, (bt, N, L)), ("z", z, u.shape)))
+    _f32(A, (dim, N), "A"); _f32(D, (dim,), "D"); _f32(delta_bias, (dim,), "delta_bias")
+    _f32(h0, (bt, dim, N), "h0")
+    if y is None:
+        y = torch.empty((bt, dim, L), dtype=out_dtype or u.dtype, device=u.device)
+    if h_last is None and return_last_state:
+        h_last = torch.empty((bt, dim, N), dtype=torch.float32, device=u.device)
+    if workspace is None and algo in ("auto", "lookback"):
+        workspace = alloc_workspace(bt, dim, L, N, u.device)
+    status = _lib.ssm_scan_fwd_algo(
+        _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+        int(bool(softplus)), _ptr(h0), _ptr(y), _ptr(h_last), bt, dim, L, N, in_code,
+        _dtype_code(y.dtype), _ptr(workspace), _nbytes(workspace), ALGOS[algo], _stream())
+    _check(status)
+    return y, h_last
+
+
+def scalar_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, h0=None, *,
+                    out_dtype=None, return_last_state=True, workspace=None, y=None, h_last=None):
+    """d_state = 1 scan. u, delta, z: (batch, dim, L); A: (dim,) fp32; B, C: (batch, L);
+    h0: (batch, dim) fp32. Returns (y, h_last (batch, dim))."""
+    bt, dim, L = u.shape
+    in_code = _dtype_code(u.dtype)
+    _same(u, (("delta", delta, u.shape), ("B", B, (bt, L)), ("C", C, (bt, L)), ("z", z, u.shape)))
+    _f32(A, (dim,), "A"); _f32(D, (dim,), "D"); _f32(delta_bias, (dim,), "delta_bias")
+    _f32(h0, (bt, dim), "h0")
+    if y is None:
+        y = torch.empty((bt, dim, L), dtype=out_dtype or u.dtype, device=u.device)
+    if h_last is None and return_last_state:
+        h_last = torch.empty((bt, dim), dtype=torch.float32, device=u.device)
+    if workspace is None:
+        workspace = alloc_workspace(bt, dim, L, 1, u.device)
+    status = _lib.ssm_scalar_scan_fwd(
+        _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+        int(bool(softplus)), _ptr(h0), _ptr(y), _ptr(h_last), bt, dim, L, in_code,
+        _dtype_code(y.dtype), _ptr(workspace), _nbytes(workspace), _stream())
+    _check(status)
+    return y, h_last
+
+
+def state_update(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, *,
+                 out_dtype=None, y=None):
+    """One decode token; `state` (batch, dim, N) fp32 is updated in place.
+    x, delta, z: (batch, dim); B, C: (batch, N). Returns y (batch, dim)."""
+    bt, dim, N = state.shape
+    _f32(state, (bt, dim, N), "state")
+    in_code = _dtype_code(x.dtype)
+    _same(x, (("delta", delta, (bt, dim)), ("B", B, (bt, N)), ("C", C, (bt, N)), ("z", z, (bt, dim))))
+    _f32(A, (dim, N), "A"); _f32(D, (dim,), "D"); _f32(delta_bias, (dim,), "delta_bias")
+    if y is None:
+        y = torch.empty((bt, dim), dtype=out_dtype or x.dtype, device=x.device)
+    status = _lib.ssm_state_update(
+        _ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+        _ptr(delta_bias), int(bool(softplus)), _ptr(y), bt, dim, N, in_code, _dtype_code(y.dtype),
+        _stream())
+    _check(status)
+    return y
+
+
+def query_status(workspace) -> int:
+    """Device status word of the last look-back scan that used `workspace` (syncs the stream)."""
+    return int(_lib.ssm_query_status(_ptr(workspace), _nbytes(workspace), _stream()))
+
+
+def run_lookback_timeout_test(u, delta, A, B, C, y, workspace, drop_segment: int, spin_limit: int) -> int:
+    """Runs the look-back error path (see ssm_test_lookback_timeout); returns the launch status."""
+    bt, dim, L = u.shape
+    return int(_lib.ssm_test_lookback_timeout(
+        _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(y), bt, dim, L, A.shape[1],
+        _dtype_code(u.dtype), _ptr(workspace), _nbytes(workspace), drop_segment, spin_limit,
+        _stream()))

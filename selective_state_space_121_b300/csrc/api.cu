@@ -1,0 +1,273 @@
+// api.cu -- the C ABI of libssmscan.so (declared in include/ssm_scan.h): argument
+// validation, algorithm choice and launches on the caller's stream. The library
+// allocates nothing and never synchronises except in ssm_query_status.
+#include <string.h>
+
+#include "launch.h"
+#include "ssm_scan.h"
+
+namespace {
+
+using ssm::DecodeArgs;
+using ssm::ScanArgs;
+
+constexpr uint32_t kSpinLimit = 1u << 20;   // look-back waits: ~0.1-1 s before giving up
+constexpr int64_t kSMs = 148;               // B300
+
+size_t esize(int dtype) { return dtype == SSM_BF16 ? 2 : 4; }
+
+bool valid_dtype(int dt) { return dt == SSM_F32 || dt == SSM_BF16; }
+
+bool valid_n(int64_t n) { return n == 1 || n == 2 || n == 4 || n == 8 || n == 16; }
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// product of non-negative sizes, -1 on overflow past 2^62
+int64_t mul(int64_t a, int64_t b) {
+    if (a < 0 || b < 0) return -1;
+    if (a == 0 || b == 0) return 0;
+    if (a > ((int64_t)1 << 62) / b) return -1;
+    return a * b;
+}
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return x < y + nb && y < x + na;
+}
+
+struct Plan {
+    int algo;
+    int64_t n_seg, seg_len;
+    int lanes_per_channel;
+};
+
+// Channels are the unit of parallel work for the serial-carry algorithms; the
+// look-back cuts time into segments when there are too few channels to fill the
+// B300's 148 SMs.
+Plan plan_scan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int algo) {
+    Plan p{algo, 1, seqlen, 1};
+    const int64_t channels = batch * dim;
+    if (p.algo == SSM_ALGO_AUTO) {
+        if (channels > 0 && channels < kSMs * 8 && seqlen >= 8 * ssm::kWarpScanChunk)
+            p.algo = SSM_ALGO_LOOKBACK;
+        else
+            p.algo = SSM_ALGO_WARPSCAN;
+    }
+    if (p.algo == SSM_ALGO_THREAD) p.lanes_per_channel = dstate >= 4 ? 4 : (int)dstate;
+    if (p.algo == SSM_ALGO_LOOKBACK) {
+        const int64_t groups = dim > 0 ? (dim + 7) / 8 : 1;
+        const int64_t target_ctas = kSMs * 8;
+        const int64_t ctas_per_seg = groups * (batch > 0 ? batch : 1);
+        const int64_t want = (target_ctas + ctas_per_seg - 1) / ctas_per_seg;
+        const int64_t chunk = ssm::kWarpScanChunk;
+        const int64_t min_seg = 8 * chunk;
+        int64_t seg_len = (seqlen + want - 1) / want;
+        seg_len = ((seg_len + chunk - 1) / chunk) * chunk;
+        if (seg_len < min_seg) seg_len = min_seg;
+        p.seg_len = seg_len;
+        p.n_seg = seqlen > 0 ? (seqlen + seg_len - 1) / seg_len : 1;
+    }
+    return p;
+}
+
+size_t workspace_for(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int algo) {
+    Plan p = plan_scan(batch, dim, seqlen, dstate, algo);
+    if (p.algo != SSM_ALGO_LOOKBACK) return 16;
+    return ssm::lookback_workspace_bytes(batch, dim, (int)dstate, p.n_seg);
+}
+
+int scan_impl(const void* u, const void* delta, const float* A, const void* B, const void* C,
+              const float* D, const void* z, const float* delta_bias, int softplus,
+              const float* h0, void* y, float* h_last, int64_t batch, int64_t dim,
+              int64_t seqlen, int64_t dstate, int in_dtype, int out_dtype, void* workspace,
+              size_t workspace_bytes, int algo, void* stream, int64_t drop_segment,
+              uint32_t spin_limit) {
+    if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype)) return SSM_ERR_DTYPE;
+    if (batch < 0 || dim < 0 || seqlen < 0) return SSM_ERR_DIM;
+    if (!valid_n(dstate)) return SSM_ERR_UNSUPPORTED_N;
+    if (algo < SSM_ALGO_AUTO || algo > SSM_ALGO_LOOKBACK) return SSM_ERR_ALGO;
+    const int64_t n_rows = mul(batch, dim);
+    const int64_t n_x = mul(n_rows, seqlen);
+    const int64_t n_bc = mul(mul(batch, dstate), seqlen);
+    const int64_t n_h = mul(n_rows, dstate);
+    if (n_rows < 0 || n_x < 0 || n_bc < 0 || n_h < 0) return SSM_ERR_DIM;
+    if (n_x > 0 && (!u || !delta || !y)) return SSM_ERR_NULL;
+    if (n_bc > 0 && (!B || !C)) return SSM_ERR_NULL;
+    if (dim > 0 && !A) return SSM_ERR_NULL;
+    const size_t ei = esize(in_dtype), eo = esize(out_dtype);
+    const void* in_ptrs[] = {u, delta, z, B, C};
+    for (const void* p : in_ptrs)
+        if (p && !aligned(p, ei)) return SSM_ERR_ALIGN;
+    if (y && !aligned(y, eo)) return SSM_ERR_ALIGN;
+    const void* f32_ptrs[] = {A, D, delta_bias, h0, h_last};
+    for (const void* p : f32_ptrs)
+        if (p && !aligned(p, 4)) return SSM_ERR_ALIGN;
+    // y must not overlap any input; h_last may be h0 exactly, but overlap nothing else
+    const size_t bx = (size_t)n_x * ei, by = (size_t)n_x * eo, bbc = (size_t)n_bc * ei,
+                 bh = (size_t)n_h * 4, bA = (size_t)dim * dstate * 4, bd = (size_t)dim * 4;
+    if (overlap(y, by, u, bx) || overlap(y, by, delta, bx) || overlap(y, by, z, bx) ||
+        overlap(y, by, B, bbc) || overlap(y, by, C, bbc) || overlap(y, by, h0, bh) ||
+        overlap(y, by, h_last, bh) || overlap(y, by, A, bA) || overlap(y, by, D, bd) ||
+        overlap(y, by, delta_bias, bd))
+        return SSM_ERR_ALIAS;
+    if (h_last && h0 && h_last != h0 && overlap(h_last, bh, h0, bh)) return SSM_ERR_ALIAS;
+    if (h_last && (overlap(h_last, bh, u, bx) || overlap(h_last, bh, delta, bx) ||
+                   overlap(h_last, bh, z, bx) || overlap(h_last, bh, B, bbc) ||
+                   overlap(h_last, bh, C, bbc) || overlap(h_last, bh, A, bA) ||
+                   overlap(h_last, bh, D, bd) || overlap(h_last, bh, delta_bias, bd)))
+        return SSM_ERR_ALIAS;
+
+    Plan p = plan_scan(batch, dim, seqlen, dstate, algo);
+    ScanArgs a;
+    memset(&a, 0, sizeof(a));
+    a.u = u; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
+    a.delta_bias = delta_bias; a.h0 = h0; a.y = y; a.h_last = h_last;
+    a.batch = batch; a.dim = dim; a.seqlen = seqlen; a.dstate = (int)dstate;
+    a.softplus = softplus ? 1 : 0; a.in_dtype = in_dtype; a.out_dtype = out_dtype;
+    bool vec = (seqlen * (int64_t)ei) % 16 == 0 && (seqlen * (int64_t)eo) % 16 == 0;
+    for (const void* q : in_ptrs) vec = vec && (!q || aligned(q, 16));
+    vec = vec && (!y || aligned(y, 16));
+    a.vec = vec;
+    a.seg_len = p.seg_len; a.n_seg = p.n_seg;
+    a.drop_segment = drop_segment;
+    a.spin_limit = spin_limit;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (p.algo == SSM_ALGO_LOOKBACK) {
+        const size_t need = ssm::lookback_workspace_bytes(batch, dim, (int)dstate, p.n_seg);
+        if (!workspace || workspace_bytes < need) return SSM_ERR_WORKSPACE;
+        if (!aligned(workspace, 16)) return SSM_ERR_ALIGN;
+        a.workspace = workspace;
+        if (cudaMemsetAsync(workspace, 0, need, s) != cudaSuccess) return SSM_ERR_LAUNCH;
+        return ssm::launch_scan_lookback(a, s) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+    }
+    if (p.algo == SSM_ALGO_THREAD)
+        return ssm::launch_scan_thread(a, p.lanes_per_channel, s) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+    return ssm::launch_scan_warp(a, s) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssm_abi_version(void) { return SSM_SCAN_ABI_VERSION; }
+
+const char* ssm_status_string(int status) {
+    switch (status) {
+        case SSM_OK: return "SSM_OK";
+        case SSM_ERR_NULL: return "SSM_ERR_NULL: a required pointer is NULL";
+        case SSM_ERR_DIM: return "SSM_ERR_DIM: negative or overflowing size";
+        case SSM_ERR_DTYPE: return "SSM_ERR_DTYPE: unknown dtype";
+        case SSM_ERR_ALIGN: return "SSM_ERR_ALIGN: misaligned pointer";
+        case SSM_ERR_WORKSPACE: return "SSM_ERR_WORKSPACE: workspace missing or too small";
+        case SSM_ERR_LAUNCH: return "SSM_ERR_LAUNCH: CUDA launch failed";
+        case SSM_ERR_LOOKBACK_TIMEOUT:
+            return "SSM_ERR_LOOKBACK_TIMEOUT: look-back wait exhausted its budget";
+        case SSM_ERR_UNSUPPORTED_N: return "SSM_ERR_UNSUPPORTED_N: dstate must be 1, 2, 4, 8 or 16";
+        case SSM_ERR_ALIAS: return "SSM_ERR_ALIAS: an output overlaps an input";
+        case SSM_ERR_ALGO: return "SSM_ERR_ALGO: unknown algorithm";
+    }
+    return "unknown ssm status";
+}
+
+size_t ssm_scan_workspace_size(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate) {
+    if (batch < 0 || dim < 0 || seqlen < 0 || !valid_n(dstate)) return 16;
+    if (mul(mul(batch, dim), seqlen) < 0) return 16;
+    size_t a = workspace_for(batch, dim, seqlen, dstate, SSM_ALGO_AUTO);
+    size_t b = workspace_for(batch, dim, seqlen, dstate, SSM_ALGO_LOOKBACK);
+    return a > b ? a : b;
+}
+
+int ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                 const float* D, const void* z, const float* delta_bias, int softplus,
+                 const float* h0, void* y, float* h_last, int64_t batch, int64_t dim,
+                 int64_t seqlen, int64_t dstate, int in_dtype, int out_dtype, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+    return scan_impl(u, delta, A, B, C, D, z, delta_bias, softplus, h0, y, h_last, batch, dim,
+                     seqlen, dstate, in_dtype, out_dtype, workspace, workspace_bytes,
+                     SSM_ALGO_AUTO, stream, -1, kSpinLimit);
+}
+
+int ssm_scan_fwd_algo(const void* u, const void* delta, const float* A, const void* B,
+                      const void* C, const float* D, const void* z, const float* delta_bias,
+                      int softplus, const float* h0, void* y, float* h_last, int64_t batch,
+                      int64_t dim, int64_t seqlen, int64_t dstate, int in_dtype, int out_dtype,
+                      void* workspace, size_t workspace_bytes, int algo, void* stream) {
+    return scan_impl(u, delta, A, B, C, D, z, delta_bias, softplus, h0, y, h_last, batch, dim,
+                     seqlen, dstate, in_dtype, out_dtype, workspace, workspace_bytes, algo,
+                     stream, -1, kSpinLimit);
+}
+
+int ssm_scalar_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
+                        const void* C, const float* D, const void* z, const float* delta_bias,
+                        int softplus, const float* h0, void* y, float* h_last, int64_t batch,
+                        int64_t dim, int64_t seqlen, int in_dtype, int out_dtype,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+    // (dim) A, (batch, seqlen) B/C and (batch, dim) h0/h_last are exactly the
+    // dstate == 1 layouts of the general entry point
+    return scan_impl(u, delta, A, B, C, D, z, delta_bias, softplus, h0, y, h_last, batch, dim,
+                     seqlen, 1, in_dtype, out_dtype, workspace, workspace_bytes, SSM_ALGO_AUTO,
+                     stream, -1, kSpinLimit);
+}
+
+int ssm_test_lookback_timeout(const void* u, const void* delta, const float* A, const void* B,
+                              const void* C, void* y, int64_t batch, int64_t dim,
+                              int64_t seqlen, int64_t dstate, int in_dtype, void* workspace,
+                              size_t workspace_bytes, int64_t drop_segment,
+                              uint32_t spin_limit, void* stream) {
+    return scan_impl(u, delta, A, B, C, nullptr, nullptr, nullptr, 1, nullptr, y, nullptr, batch,
+                     dim, seqlen, dstate, in_dtype, in_dtype, workspace, workspace_bytes,
+                     SSM_ALGO_LOOKBACK, stream, drop_segment, spin_limit);
+}
+
+int ssm_state_update(float* state, const void* x, const void* delta, const float* A,
+                     const void* B, const void* C, const float* D, const void* z,
+                     const float* delta_bias, int softplus, void* y, int64_t batch, int64_t dim,
+                     int64_t dstate, int in_dtype, int out_dtype, void* stream) {
+    if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype)) return SSM_ERR_DTYPE;
+    if (batch < 0 || dim < 0) return SSM_ERR_DIM;
+    if (!valid_n(dstate)) return SSM_ERR_UNSUPPORTED_N;
+    const int64_t n_rows = mul(batch, dim);
+    const int64_t n_h = mul(n_rows, dstate);
+    const int64_t n_bc = mul(batch, dstate);
+    if (n_rows < 0 || n_h < 0 || n_bc < 0) return SSM_ERR_DIM;
+    if (n_rows > 0 && (!state || !x || !delta || !y || !B || !C || !A)) return SSM_ERR_NULL;
+    const size_t ei = esize(in_dtype), eo = esize(out_dtype);
+    const void* in_ptrs[] = {x, delta, z, B, C};
+    for (const void* p : in_ptrs)
+        if (p && !aligned(p, ei)) return SSM_ERR_ALIGN;
+    if (y && !aligned(y, eo)) return SSM_ERR_ALIGN;
+    // the state is streamed with 16-byte vector accesses when dstate >= 4
+    if (state && !aligned(state, dstate >= 4 ? 16 : 4)) return SSM_ERR_ALIGN;
+    const void* f32_ptrs[] = {A, D, delta_bias};
+    for (const void* p : f32_ptrs)
+        if (p && !aligned(p, 4)) return SSM_ERR_ALIGN;
+    const size_t bh = (size_t)n_h * 4, bx = (size_t)n_rows * ei, by = (size_t)n_rows * eo,
+                 bbc = (size_t)n_bc * ei, bA = (size_t)dim * dstate * 4, bd = (size_t)dim * 4;
+    if (overlap(y, by, state, bh) || overlap(y, by, x, bx) || overlap(y, by, delta, bx) ||
+        overlap(y, by, z, bx) || overlap(y, by, B, bbc) || overlap(y, by, C, bbc) ||
+        overlap(y, by, A, bA) || overlap(y, by, D, bd) || overlap(y, by, delta_bias, bd))
+        return SSM_ERR_ALIAS;
+    if (overlap(state, bh, x, bx) || overlap(state, bh, delta, bx) || overlap(state, bh, z, bx) ||
+        overlap(state, bh, B, bbc) || overlap(state, bh, C, bbc) || overlap(state, bh, A, bA) ||
+        overlap(state, bh, D, bd) || overlap(state, bh, delta_bias, bd))
+        return SSM_ERR_ALIAS;
+    DecodeArgs a;
+    memset(&a, 0, sizeof(a));
+    a.state = state; a.x = x; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
+    a.delta_bias = delta_bias; a.y = y; a.batch = batch; a.dim = dim; a.dstate = (int)dstate;
+    a.softplus = softplus ? 1 : 0; a.in_dtype = in_dtype; a.out_dtype = out_dtype;
+    return ssm::launch_state_update(a, (cudaStream_t)stream) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+}
+
+int ssm_query_status(const void* workspace, size_t workspace_bytes, void* stream) {
+    if (!workspace || workspace_bytes < 16) return SSM_ERR_WORKSPACE;
+    int32_t st = 0;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(&st, workspace, sizeof(st), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return SSM_ERR_LAUNCH;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SSM_ERR_LAUNCH;
+    return st;
+}
+
+}  // extern "C"

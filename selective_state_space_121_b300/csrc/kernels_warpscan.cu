@@ -1,0 +1,479 @@
+// kernels_warpscan.cu -- chunked selective scan with a warp-shuffle associative
+// scan inside each chunk, a serial carry across chunks, and a multi-block
+// variant joined by single-pass decoupled look-back.
+//
+// What is computed (Mamba SSM complete guide (youngju.dev), section 5,
+// selective_scan, with MambaBlock.ssm's softplus(dt_proj) and forward's silu(z)
+// gate fused): per (b, d, n)
+//     h_t = a_t h_{t-1} + b_t,   a_t = exp(dt_t A_dn),   b_t = dt_t B_tn u_t
+//     y_t = sum_n C_tn h_t + D_d u_t, then y_t *= silu(z_t).
+// Each step is an affine map h -> a h + b. Maps compose associatively,
+//     (a2, b2) o (a1, b1) = (a2 a1, a2 b1 + b2),
+// which is what lets the time axis be split across lanes and blocks (the
+// parallel scan of the guide's "Hardware-Aware Algorithm" section; the page's
+// printed up-sweep is garbled, this is the composition it stands for).
+//
+// Layout of the work (B300, sm_103a):
+//  * A CTA holds W = 8 warps; warp w owns channel d = 8*blockIdx.x + w of batch
+//    row b. All 8 channels share b, so the B and C tiles of a chunk are staged
+//    once per CTA in shared memory (fp32, [n][t]) and read by all 8 warps.
+//  * A chunk is 256 time steps: lane l owns steps 8l .. 8l+7 of the chunk and
+//    loads its u, delta, z with one 16-byte vector load each (bf16) -- a warp
+//    reads 512 contiguous bytes per tensor, fully coalesced.
+//  * For each state n: the lane computes its 8 (a, b) pairs in registers, folds
+//    them into one lane map (the product of the a's is exp(A * sum dt), one ex2),
+//    the warp composes the 32 lane maps with a 5-step shuffle scan, the lane
+//    takes its exclusive prefix, applies the carry from earlier chunks, and
+//    re-runs its 8 steps to produce h_t and accumulate C_tn h_t into y_t.
+//    Every a_t = exp(dt A) is evaluated exactly once.
+//  * The N-wide carry (state at the chunk boundary) lives in registers; across
+//    chunks it is carried serially by the warp.
+// The look-back variant cuts seqlen into segments handled by different CTAs.
+// A CTA first folds its whole segment into one N-wide map (a pre-pass that
+// needs B but not C and writes nothing), publishes it, looks back over earlier
+// segments' published maps/prefixes until it meets an inclusive prefix, then
+// runs the full pass from the carry it obtained. CTAs take segments in the
+// order of an atomic ticket, so every segment a CTA waits on belongs to a CTA
+// that has already started: the look-back always makes progress. Each wait is
+// also bounded; on expiry the kernel records SSM_ERR_LOOKBACK_TIMEOUT in the
+// workspace status word, publishes what it has and finishes.
+#include "common.cuh"
+#include "launch.h"
+
+namespace ssm {
+namespace {
+
+constexpr int K = kWarpScanItems;     // 8 steps per lane
+constexpr int T = kWarpScanChunk;     // 256 steps per chunk
+constexpr int W = 8;                  // warps (channels) per CTA
+constexpr int kThreads = 32 * W;
+
+constexpr uint32_t kFlagNone = 0, kFlagAgg = 1, kFlagIncl = 2;
+constexpr int kErrLookbackTimeout = -7;
+
+template <int N>
+struct Smem {
+    float B[N][T];
+    float C[N][T];
+};
+
+// Stage B (and C) of batch row b, steps t0 .. t0+T-1, into shared memory as fp32.
+template <int N, typename Tin, bool kVec, bool kWithC>
+__device__ __forceinline__ void stage_bc(const ScanArgs& a, int64_t b, int64_t t0, Smem<N>& sm) {
+    const Tin* Bp = static_cast<const Tin*>(a.B) + b * N * a.seqlen;
+    const Tin* Cp = static_cast<const Tin*>(a.C) + b * N * a.seqlen;
+    const int64_t L = a.seqlen;
+    if constexpr (kVec) {
+        constexpr int V = Vec16<Tin>::kN;
+        constexpr int kVecs = N * T / V;
+        for (int idx = threadIdx.x; idx < kVecs; idx += kThreads) {
+            const int n = idx / (T / V);
+            const int i = (idx % (T / V)) * V;
+            const int64_t t = t0 + i;
+            float vb[V], vc[V];
+            if (t + V <= L) {
+                Vec16<Tin>::load(Bp + n * L + t, vb);
+                if constexpr (kWithC) Vec16<Tin>::load(Cp + n * L + t, vc);
+            } else {
+#pragma unroll
+                for (int k = 0; k < V; k++) {
+                    vb[k] = (t + k < L) ? to_f32(Bp[n * L + t + k]) : 0.f;
+                    if constexpr (kWithC) vc[k] = (t + k < L) ? to_f32(Cp[n * L + t + k]) : 0.f;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < V; k += 4) {
+                *reinterpret_cast<float4*>(&sm.B[n][i + k]) = make_float4(vb[k], vb[k + 1], vb[k + 2], vb[k + 3]);
+                if constexpr (kWithC)
+                    *reinterpret_cast<float4*>(&sm.C[n][i + k]) = make_float4(vc[k], vc[k + 1], vc[k + 2], vc[k + 3]);
+            }
+        }
+    } else {
+        for (int idx = threadIdx.x; idx < N * T; idx += kThreads) {
+            const int n = idx / T, i = idx % T;
+            const int64_t t = t0 + i;
+            sm.B[n][i] = t < L ? to_f32(Bp[n * L + t]) : 0.f;
+            if constexpr (kWithC) sm.C[n][i] = t < L ? to_f32(Cp[n * L + t]) : 0.f;
+        }
+    }
+}
+
+// Load this lane's K steps of one (b, d) row starting at step t (may run past L).
+template <typename Tin, bool kVec>
+__device__ __forceinline__ void load_items(const Tin* row, int64_t t, int64_t L, float* out) {
+    if constexpr (kVec) {
+        constexpr int V = Vec16<Tin>::kN;
+#pragma unroll
+        for (int k = 0; k < K; k += V) {
+            if (t + k + V <= L) {
+                Vec16<Tin>::load(row + t + k, out + k);
+            } else {
+#pragma unroll
+                for (int j = 0; j < V; j++) out[k + j] = (t + k + j < L) ? to_f32(row[t + k + j]) : 0.f;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < K; k++) out[k] = (t + k < L) ? to_f32(row[t + k]) : 0.f;
+    }
+}
+
+template <typename Tout, bool kVec>
+__device__ __forceinline__ void store_items(Tout* row, int64_t t, int64_t L, const float* v) {
+    if constexpr (kVec) {
+        constexpr int V = Vec16<Tout>::kN;
+#pragma unroll
+        for (int k = 0; k < K; k += V) {
+            if (t + k + V <= L) {
+                Vec16<Tout>::store(row + t + k, v + k);
+            } else {
+#pragma unroll
+                for (int j = 0; j < V; j++)
+                    if (t + k + j < L) row[t + k + j] = from_f32<Tout>(v[k + j]);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < K; k++)
+            if (t + k < L) row[t + k] = from_f32<Tout>(v[k]);
+    }
+}
+
+// Per-lane step inputs of one chunk: dtl = dt*log2(e), bu = dt*u (zero past L).
+template <typename Tin, bool kVec>
+__device__ __forceinline__ float prepare_items(const ScanArgs& a, int64_t row_off, int64_t d,
+                                               int64_t t, float* dtl, float* bu, float* u) {
+    const Tin* up = static_cast<const Tin*>(a.u) + row_off;
+    const Tin* dp = static_cast<const Tin*>(a.delta) + row_off;
+    float dl[K];
+    load_items<Tin, kVec>(up, t, a.seqlen, u);
+    load_items<Tin, kVec>(dp, t, a.seqlen, dl);
+    const float bias = a.delta_bias ? a.delta_bias[d] : 0.f;
+    float sdtl = 0.f;
+#pragma unroll
+    for (int k = 0; k < K; k++) {
+        const float x = dl[k] + bias;
+        float dt = a.softplus ? softplus(x) : x;
+        if (t + k >= a.seqlen) dt = 0.f;   // identity map past the end: a = 1, b = 0
+        dtl[k] = dt * kLog2e;
+        bu[k] = dt * u[k];
+        sdtl += dtl[k];
+    }
+    return sdtl;
+}
+
+// Inclusive warp scan of lane maps (P, H): lane l ends with the composition of the
+// maps of lanes 0..l.
+__device__ __forceinline__ void warp_scan_maps(float& P, float& H, int lane) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const float Pp = __shfl_up_sync(0xffffffffu, P, off);
+        const float Hp = __shfl_up_sync(0xffffffffu, H, off);
+        if (lane >= off) {
+            H = fmaf(P, Hp, H);
+            P *= Pp;
+        }
+    }
+}
+
+// Full pass over one chunk: y for the lane's steps from the N-wide carry; carry
+// is advanced to the state at the end of the chunk.
+template <int N, typename Tin, typename Tout, bool kVec>
+__device__ __forceinline__ void chunk_full(const ScanArgs& a, int64_t b, int64_t d, int64_t t0,
+                                           const Smem<N>& sm, const float* Ad, float* carry,
+                                           int lane) {
+    const int64_t row_off = (b * a.dim + d) * a.seqlen;
+    const int64_t t = t0 + lane * K;
+    float dtl[K], bu[K], u[K], y[K];
+    const float sdtl = prepare_items<Tin, kVec>(a, row_off, d, t, dtl, bu, u);
+#pragma unroll
+    for (int k = 0; k < K; k++) y[k] = 0.f;
+#pragma unroll
+    for (int n = 0; n < N; n++) {
+        const float* sb = &sm.B[n][lane * K];
+        const float* sc = &sm.C[n][lane * K];
+        float an[K], bn[K];
+        float H = 0.f;
+#pragma unroll
+        for (int k = 0; k < K; k++) {
+            an[k] = ex2(dtl[k] * Ad[n]);
+            bn[k] = bu[k] * sb[k];
+            H = fmaf(an[k], H, bn[k]);
+        }
+        float P = ex2(sdtl * Ad[n]);
+        warp_scan_maps(P, H, lane);
+        float Pe = __shfl_up_sync(0xffffffffu, P, 1);
+        float He = __shfl_up_sync(0xffffffffu, H, 1);
+        if (lane == 0) { Pe = 1.f; He = 0.f; }
+        float h = fmaf(Pe, carry[n], He);
+#pragma unroll
+        for (int k = 0; k < K; k++) {
+            h = fmaf(an[k], h, bn[k]);
+            y[k] = fmaf(sc[k], h, y[k]);
+        }
+        carry[n] = __shfl_sync(0xffffffffu, fmaf(P, carry[n], H), 31);
+    }
+    const float Dd = a.D ? a.D[d] : 0.f;
+    if (a.z) {
+        float zz[K];
+        load_items<Tin, kVec>(static_cast<const Tin*>(a.z) + row_off, t, a.seqlen, zz);
+#pragma unroll
+        for (int k = 0; k < K; k++) y[k] = fmaf(Dd, u[k], y[k]) * silu(zz[k]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < K; k++) y[k] = fmaf(Dd, u[k], y[k]);
+    }
+    store_items<Tout, kVec>(static_cast<Tout*>(a.y) + row_off, t, a.seqlen, y);
+}
+
+// Aggregate-only pass over one chunk: composes the chunk's map into (aggP, aggH).
+template <int N, typename Tin, bool kVec>
+__device__ __forceinline__ void chunk_aggregate(const ScanArgs& a, int64_t b, int64_t d, int64_t t0,
+                                                const Smem<N>& sm, const float* Ad, float* aggP,
+                                                float* aggH, int lane) {
+    const int64_t row_off = (b * a.dim + d) * a.seqlen;
+    const int64_t t = t0 + lane * K;
+    float dtl[K], bu[K], u[K];
+    const float sdtl = prepare_items<Tin, kVec>(a, row_off, d, t, dtl, bu, u);
+#pragma unroll
+    for (int n = 0; n < N; n++) {
+        const float* sb = &sm.B[n][lane * K];
+        float H = 0.f;
+#pragma unroll
+        for (int k = 0; k < K; k++) H = fmaf(ex2(dtl[k] * Ad[n]), H, bu[k] * sb[k]);
+        float P = ex2(sdtl * Ad[n]);
+        warp_scan_maps(P, H, lane);
+        P = __shfl_sync(0xffffffffu, P, 31);
+        H = __shfl_sync(0xffffffffu, H, 31);
+        aggH[n] = fmaf(P, aggH[n], H);
+        aggP[n] *= P;
+    }
+}
+
+template <int N>
+__device__ __forceinline__ void load_A(const ScanArgs& a, int64_t d, float* Ad) {
+#pragma unroll
+    for (int n = 0; n < N; n++) Ad[n] = a.A[d * N + n];
+}
+
+template <int N>
+__device__ __forceinline__ void load_h0(const ScanArgs& a, int64_t b, int64_t d, float* carry) {
+#pragma unroll
+    for (int n = 0; n < N; n++) carry[n] = a.h0 ? a.h0[(b * a.dim + d) * N + n] : 0.f;
+}
+
+template <int N>
+__device__ __forceinline__ void store_hlast(const ScanArgs& a, int64_t b, int64_t d, const float* carry,
+                                            int lane) {
+    if (!a.h_last) return;
+#pragma unroll
+    for (int n = 0; n < N; n++)
+        if (lane == (n & 31)) a.h_last[(b * a.dim + d) * N + n] = carry[n];
+}
+
+// ---------------------------------------------------------------------------
+// Serial-carry kernel: grid (ceil(dim / 8), batch); each warp walks its
+// channel's whole sequence chunk by chunk.
+// ---------------------------------------------------------------------------
+template <int N, typename Tin, typename Tout, bool kVec>
+__global__ void __launch_bounds__(kThreads) warp_scan_kernel(ScanArgs a) {
+    __shared__ __align__(16) Smem<N> sm;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t b = blockIdx.y;
+    const int64_t d = (int64_t)blockIdx.x * W + warp;
+    const bool active = d < a.dim;
+    float Ad[N], carry[N];
+    if (active) {
+        load_A<N>(a, d, Ad);
+        load_h0<N>(a, b, d, carry);
+    }
+    for (int64_t t0 = 0; t0 < a.seqlen; t0 += T) {
+        stage_bc<N, Tin, kVec, true>(a, b, t0, sm);
+        __syncthreads();
+        if (active) chunk_full<N, Tin, Tout, kVec>(a, b, d, t0, sm, Ad, carry, lane);
+        __syncthreads();
+    }
+    if (active) store_hlast<N>(a, b, d, carry, lane);
+}
+
+// ---------------------------------------------------------------------------
+// Look-back kernel. Workspace layout (zeroed by the host on the stream):
+//   [0] int32 status, [1] uint32 ticket, [2..3] pad;
+//   then per (channel, segment): uint32 flag[N], float P[N], float H[N], float I[N].
+// (P, H) is the segment's own map (published with flag AGG), I the state at the
+// segment's end (published with flag INCL). Published values are never
+// rewritten, so a reader that saw AGG can still read (P, H) after the writer
+// has moved on to INCL. Lane n owns state n of a descriptor: it writes the
+// values and then releases flag[n]; a reader lane n acquires flag[n] before
+// reading the values.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+template <int N>
+struct Desc {
+    uint32_t flag[N];
+    float P[N];
+    float H[N];
+    float I[N];
+};
+
+template <int N, typename Tin, typename Tout, bool kVec>
+__global__ void __launch_bounds__(kThreads) lookback_kernel(ScanArgs a) {
+    __shared__ __align__(16) Smem<N> sm;
+    __shared__ uint32_t s_ticket;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int32_t* status = static_cast<int32_t*>(a.workspace);
+    uint32_t* ticket_ctr = reinterpret_cast<uint32_t*>(status + 1);
+    Desc<N>* desc = reinterpret_cast<Desc<N>*>(static_cast<char*>(a.workspace) + 16);
+
+    if (threadIdx.x == 0) s_ticket = atomicAdd(ticket_ctr, 1u);
+    __syncthreads();
+    const int64_t groups = (a.dim + W - 1) / W;
+    const int64_t per_seg = groups * a.batch;
+    const int64_t tk = s_ticket;
+    const int64_t seg = tk / per_seg;                 // segment-major ticket order
+    const int64_t rem = tk % per_seg;
+    const int64_t b = rem / groups;
+    const int64_t d = (rem % groups) * W + warp;
+    const bool active = d < a.dim;
+    const int64_t ts = seg * a.seg_len;
+    const int64_t te = min(a.seqlen, ts + a.seg_len);
+    const int64_t ch = b * a.dim + d;
+
+    float Ad[N], carry[N], aggP[N], aggH[N];
+    if (active) {
+        load_A<N>(a, d, Ad);
+#pragma unroll
+        for (int n = 0; n < N; n++) { aggP[n] = 1.f; aggH[n] = 0.f; }
+    }
+    const bool last = seg + 1 == a.n_seg;
+    const bool publish = !last && seg != a.drop_segment;
+    // 1) fold the segment into one map; the last segment publishes nothing and skips it
+    if (!last) {
+        for (int64_t t0 = ts; t0 < te; t0 += T) {
+            stage_bc<N, Tin, kVec, false>(a, b, t0, sm);
+            __syncthreads();
+            if (active) chunk_aggregate<N, Tin, kVec>(a, b, d, t0, sm, Ad, aggP, aggH, lane);
+            __syncthreads();
+        }
+    }
+    if (active) {
+        Desc<N>* mine = desc + ch * a.n_seg + seg;
+        if (seg == 0) {
+            load_h0<N>(a, b, d, carry);
+        } else {
+            // 2) publish the segment map (successors may compose it), then 3) look back
+            if (publish) {
+#pragma unroll
+                for (int n = 0; n < N; n++) {
+                    if (lane == n) {
+                        mine->P[n] = aggP[n];
+                        mine->H[n] = aggH[n];
+                        st_release(&mine->flag[n], kFlagAgg);
+                    }
+                }
+            }
+            // lane n < N walks state n back; (accP, accH) is the composed map of the
+            // segments strictly between the one inspected and this one
+            float accP = 1.f, accH = 0.f, cin = 0.f;
+            bool timed_out = false;
+            if (lane < N) {
+                for (int64_t j = seg - 1; j >= 0; j--) {
+                    const Desc<N>* pd = desc + ch * a.n_seg + j;
+                    uint32_t f = ld_acquire(&pd->flag[lane]);
+                    uint32_t spins = 0;
+                    while (f == kFlagNone && spins < a.spin_limit) {
+                        ++spins;
+                        __nanosleep(64);
+                        f = ld_acquire(&pd->flag[lane]);
+                    }
+                    if (f == kFlagNone) { timed_out = true; cin = accH; break; }
+                    if (f == kFlagIncl) { cin = fmaf(accP, __ldcg(&pd->I[lane]), accH); break; }
+                    accH = fmaf(accP, __ldcg(&pd->H[lane]), accH);
+                    accP *= __ldcg(&pd->P[lane]);
+                }
+            }
+            if (timed_out) atomicExch(status, kErrLookbackTimeout);
+#pragma unroll
+            for (int n = 0; n < N; n++) carry[n] = __shfl_sync(0xffffffffu, cin, n);
+        }
+        // 4) publish the inclusive prefix: the state at this segment's end. On a
+        //    timeout this is still published (with the wrong carry) so that later
+        //    segments finish instead of waiting too; the status word has the error.
+        if (publish) {
+#pragma unroll
+            for (int n = 0; n < N; n++) {
+                if (lane == n) {
+                    mine->I[n] = fmaf(aggP[n], carry[n], aggH[n]);
+                    st_release(&mine->flag[n], kFlagIncl);
+                }
+            }
+        }
+    }
+    // 5) full pass over the segment from the carry
+    for (int64_t t0 = ts; t0 < te; t0 += T) {
+        stage_bc<N, Tin, kVec, true>(a, b, t0, sm);
+        __syncthreads();
+        if (active) chunk_full<N, Tin, Tout, kVec>(a, b, d, t0, sm, Ad, carry, lane);
+        __syncthreads();
+    }
+    if (active && last) store_hlast<N>(a, b, d, carry, lane);
+}
+
+template <int N, typename Tin, typename Tout>
+cudaError_t launch_ws_n(const ScanArgs& a, cudaStream_t s) {
+    if (a.batch == 0 || a.dim == 0) return cudaSuccess;
+    dim3 grid((unsigned)((a.dim + W - 1) / W), (unsigned)a.batch);
+    if (a.vec) warp_scan_kernel<N, Tin, Tout, true><<<grid, kThreads, 0, s>>>(a);
+    else warp_scan_kernel<N, Tin, Tout, false><<<grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <int N, typename Tin, typename Tout>
+cudaError_t launch_lb_n(const ScanArgs& a, cudaStream_t s) {
+    if (a.batch == 0 || a.dim == 0) return cudaSuccess;
+    const int64_t ctas = ((a.dim + W - 1) / W) * a.batch * a.n_seg;
+    if (a.vec) lookback_kernel<N, Tin, Tout, true><<<(unsigned)ctas, kThreads, 0, s>>>(a);
+    else lookback_kernel<N, Tin, Tout, false><<<(unsigned)ctas, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <bool kLB, typename Tin, typename Tout>
+cudaError_t dispatch_n(const ScanArgs& a, cudaStream_t s) {
+    switch (a.dstate) {
+        case 1: return kLB ? launch_lb_n<1, Tin, Tout>(a, s) : launch_ws_n<1, Tin, Tout>(a, s);
+        case 2: return kLB ? launch_lb_n<2, Tin, Tout>(a, s) : launch_ws_n<2, Tin, Tout>(a, s);
+        case 4: return kLB ? launch_lb_n<4, Tin, Tout>(a, s) : launch_ws_n<4, Tin, Tout>(a, s);
+        case 8: return kLB ? launch_lb_n<8, Tin, Tout>(a, s) : launch_ws_n<8, Tin, Tout>(a, s);
+        case 16: return kLB ? launch_lb_n<16, Tin, Tout>(a, s) : launch_ws_n<16, Tin, Tout>(a, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <bool kLB>
+cudaError_t dispatch(const ScanArgs& a, cudaStream_t s) {
+    if (a.in_dtype == kBF16)
+        return a.out_dtype == kBF16 ? dispatch_n<kLB, __nv_bfloat16, __nv_bfloat16>(a, s)
+                                    : dispatch_n<kLB, __nv_bfloat16, float>(a, s);
+    return a.out_dtype == kBF16 ? dispatch_n<kLB, float, __nv_bfloat16>(a, s)
+                                : dispatch_n<kLB, float, float>(a, s);
+}
+
+}  // namespace
+
+size_t lookback_workspace_bytes(int64_t batch, int64_t dim, int dstate, int64_t n_seg) {
+    const size_t desc = (size_t)dstate * 16;
+    return 16 + (size_t)batch * (size_t)dim * (size_t)n_seg * desc;
+}
+
+cudaError_t launch_scan_warp(const ScanArgs& a, cudaStream_t s) { return dispatch<false>(a, s); }
+cudaError_t launch_scan_lookback(const ScanArgs& a, cudaStream_t s) { return dispatch<true>(a, s); }
+
+}  // namespace ssm

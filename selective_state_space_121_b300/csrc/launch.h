@@ -1,0 +1,65 @@
+// launch.h -- internal (non-ABI) launch interface between the C ABI in api.cu and
+// the kernel translation units. Host code only.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ssm {
+
+enum DType { kF32 = 0, kBF16 = 1 };
+
+struct ScanArgs {
+    const void* u;
+    const void* delta;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const void* z;
+    const float* delta_bias;
+    const float* h0;
+    void* y;
+    float* h_last;
+    int64_t batch, dim, seqlen;
+    int dstate;
+    int softplus;
+    int in_dtype, out_dtype;
+    bool vec;          // rows of u/delta/z/y/B/C are 16-byte aligned (vector loads allowed)
+    // look-back only
+    void* workspace;
+    int64_t seg_len;   // time steps per look-back segment (multiple of the chunk)
+    int64_t n_seg;
+    uint32_t spin_limit;
+    int64_t drop_segment;   // test hook: this segment withholds its publication (-1: none)
+};
+
+struct DecodeArgs {
+    float* state;
+    const void* x;
+    const void* delta;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const void* z;
+    const float* delta_bias;
+    void* y;
+    int64_t batch, dim;
+    int dstate;
+    int softplus;
+    int in_dtype, out_dtype;
+};
+
+// Each returns cudaSuccess or the launch error.
+cudaError_t launch_state_update(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_scan_warp(const ScanArgs& a, cudaStream_t s);
+cudaError_t launch_scan_lookback(const ScanArgs& a, cudaStream_t s);
+cudaError_t launch_scan_thread(const ScanArgs& a, int lanes_per_channel, cudaStream_t s);
+
+// Look-back workspace geometry (bytes), shared by api.cu and the kernel.
+constexpr int kWarpScanItems = 8;                    // time steps per lane per chunk
+constexpr int kWarpScanChunk = 32 * kWarpScanItems;  // time steps per warp chunk
+size_t lookback_workspace_bytes(int64_t batch, int64_t dim, int dstate, int64_t n_seg);
+
+}  // namespace ssm

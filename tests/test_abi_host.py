@@ -1,0 +1,121 @@
+"""CPU-only checks of the C ABI library: it loads, exports every entry point the
+header declares, and its host-side logic (argument validation, workspace sizing)
+answers without touching a GPU. No kernel is launched here: every call below is
+rejected by validation before any CUDA call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssm_scan.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"^SSM_API\s+[\w\s\*]+?\b(ssm_\w+)\(", src, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def ssm():
+    import selective_state_space_121_b300 as m
+    return m
+
+
+def test_header_declares_entry_points():
+    names = _declared()
+    for need in ("ssm_scan_fwd", "ssm_scalar_scan_fwd", "ssm_state_update", "ssm_scan_workspace_size",
+                 "ssm_query_status"):
+        assert need in names
+
+
+def test_library_exports_every_declared_symbol(ssm):
+    lib = ctypes.CDLL(ssm.LIB_PATH)
+    for name in _declared():
+        assert hasattr(lib, name), f"{name} declared in ssm_scan.h but not exported"
+    assert sorted(ssm.EXPORTS) == _declared()
+
+
+def test_abi_version_matches_header(ssm):
+    v = int(re.search(r"#define SSM_SCAN_ABI_VERSION (\d+)", open(HEADER).read()).group(1))
+    assert ssm.abi_version() == v
+
+
+def test_status_strings(ssm):
+    for code in range(0, -11, -1):
+        assert ssm.status_string(code).startswith("SSM_")
+    assert not ssm.status_string(-99).startswith("SSM_")
+
+
+def test_workspace_size(ssm):
+    # at least the 16-byte status header, and grows with the look-back descriptor count
+    assert ssm.workspace_size(8, 1536, 2048, 16) >= 16
+    small = ssm.workspace_size(1, 16, 1 << 17, 16)
+    big = ssm.workspace_size(1, 64, 1 << 17, 16)
+    assert big > small > 16
+    assert ssm.workspace_size(-1, 4, 4, 16) == 16          # invalid sizes: header only
+    assert ssm.workspace_size(1, 4, 4, 3) == 16
+    assert ssm.workspace_size(2, 0, 16, 16) >= 16          # empty problems do not divide by zero
+    assert ssm.workspace_size(0, 4, 16, 16) >= 16
+
+
+# argument validation, all rejected before any CUDA call ------------------------------
+FAKE = 0x10000          # non-null, 64 KiB aligned: never dereferenced by the host
+
+
+def _scan(ssm, **kw):
+    args = dict(u=FAKE, delta=FAKE * 2, A=FAKE * 3, B=FAKE * 4, C=FAKE * 5, D=None, z=None, bias=None,
+                softplus=1, h0=None, y=FAKE * 6, h_last=None, batch=2, dim=4, L=8, N=16, idt=1, odt=1,
+                ws=None, wsb=0, algo=2)
+    args.update(kw)
+    return ssm._lib.ssm_scan_fwd_algo(args["u"], args["delta"], args["A"], args["B"], args["C"], args["D"],
+                                      args["z"], args["bias"], args["softplus"], args["h0"], args["y"],
+                                      args["h_last"], args["batch"], args["dim"], args["L"], args["N"],
+                                      args["idt"], args["odt"], args["ws"], args["wsb"], args["algo"], None)
+
+
+def test_validation_errors(ssm):
+    assert _scan(ssm, idt=7) == -3
+    assert _scan(ssm, odt=-1) == -3
+    assert _scan(ssm, batch=-1) == -2
+    assert _scan(ssm, L=-5) == -2
+    assert _scan(ssm, N=3) == -8
+    assert _scan(ssm, N=32) == -8
+    assert _scan(ssm, algo=9) == -10
+    assert _scan(ssm, u=None) == -1
+    assert _scan(ssm, A=None) == -1
+    assert _scan(ssm, C=None) == -1
+    assert _scan(ssm, y=FAKE + 1) == -4                     # bf16 output needs 2-byte alignment
+    assert _scan(ssm, D=FAKE * 7 + 2) == -4                 # fp32 needs 4
+    assert _scan(ssm, y=FAKE + 16) == -9                    # y overlaps u
+    assert _scan(ssm, h_last=FAKE * 3) == -9                # h_last over A
+    assert _scan(ssm, h0=FAKE * 8, h_last=FAKE * 8 + 4) == -9   # h_last partly over h0
+    assert _scan(ssm, batch=1 << 40, dim=1 << 30) == -2     # size overflow
+    # the look-back needs a workspace of the advertised size
+    assert _scan(ssm, algo=3, ws=None, wsb=0) == -5
+    need = ssm.workspace_size(2, 4, 8, 16)
+    assert _scan(ssm, algo=3, ws=FAKE * 9, wsb=need - 1) == -5
+
+
+def test_state_update_validation(ssm):
+    f = ssm._lib.ssm_state_update
+
+    def call(**kw):
+        a = dict(state=FAKE, x=FAKE * 2, delta=FAKE * 3, A=FAKE * 4, B=FAKE * 5, C=FAKE * 6, D=None, z=None,
+                 bias=None, sp=1, y=FAKE * 7, batch=2, dim=4, N=16, idt=1, odt=1)
+        a.update(kw)
+        return f(a["state"], a["x"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["bias"], a["sp"],
+                 a["y"], a["batch"], a["dim"], a["N"], a["idt"], a["odt"], None)
+    assert call(idt=5) == -3
+    assert call(N=5) == -8
+    assert call(batch=-2) == -2
+    assert call(state=None) == -1
+    assert call(state=FAKE + 4) == -4          # 16-byte vector state access for N >= 4
+    assert call(y=FAKE + 8) == -9              # y inside the state
+    assert call(x=FAKE + 64) == -9             # state overlaps x
+
+
+def test_query_status_rejects_small_workspace(ssm):
+    assert ssm._lib.ssm_query_status(None, 0, None) == -5
+    assert ssm._lib.ssm_query_status(FAKE, 8, None) == -5
