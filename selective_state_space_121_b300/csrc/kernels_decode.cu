@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(256) state_update_kernel(DecodeArgs a) {
 #pragma unroll
             for (int i = 0; i < NPL; i++) {
                 const int n = j * NPL + i;
-                const float an = ex2(dtl * a.A[d * N + n]);
+                const float an = exp2_dec<sizeof(Tin) == 4>(dtl * a.A[d * N + n]);
                 s[i] = fmaf(an, s[i], dtx * to_f32(Bp[b * N + n]));
                 acc = fmaf(to_f32(Cp[b * N + n]), s[i], acc);
             }

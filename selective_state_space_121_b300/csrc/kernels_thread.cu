@@ -124,6 +124,7 @@ template <int N, int G, typename Tin, typename Tout, bool kVec>
 __global__ void __launch_bounds__(kThreads) thread_scan_kernel(ScanArgs a) {
     using Cfg = TSConfig<N, G, Tin>;
     constexpr int NPL = Cfg::NPL, CPW = Cfg::CPW, T = Cfg::T, V = Cfg::V, PV = Cfg::PV;
+    constexpr bool kAcc = sizeof(Tin) == 4;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     TSSmem<N, G, Tin>& sm = *reinterpret_cast<TSSmem<N, G, Tin>*>(smem_raw);
 
@@ -260,7 +261,7 @@ __global__ void __launch_bounds__(kThreads) thread_scan_kernel(ScanArgs a) {
 #pragma unroll
                     for (int i = 0; i < NPL; i += 2) {
                         const float2 e = mul2(dtl2, make_float2(Al[i], Al[i + 1]));
-                        const float2 an = make_float2(ex2(e.x), ex2(e.y));
+                        const float2 an = make_float2(exp2_dec<kAcc>(e.x), exp2_dec<kAcc>(e.y));
                         const float2 bn = mul2(bu2, make_float2(bq[i], bq[i + 1]));
                         const float2 hh = fma2(an, make_float2(h[i], h[i + 1]), bn);
                         h[i] = hh.x; h[i + 1] = hh.y;
@@ -270,7 +271,7 @@ __global__ void __launch_bounds__(kThreads) thread_scan_kernel(ScanArgs a) {
                 } else {
 #pragma unroll
                     for (int i = 0; i < NPL; i++) {
-                        h[i] = fmaf(ex2(x.x * Al[i]), h[i], x.y * bq[i]);
+                        h[i] = fmaf(exp2_dec<kAcc>(x.x * Al[i]), h[i], x.y * bq[i]);
                         acc = fmaf(cq[i], h[i], acc);
                     }
                 }

@@ -182,6 +182,7 @@ template <int N, typename Tin, typename Tout, bool kVec>
 __device__ __forceinline__ void chunk_full(const ScanArgs& a, int64_t b, int64_t d, int64_t t0,
                                            const Smem<N>& sm, const float* Ad, float* carry,
                                            int lane) {
+    constexpr bool kAcc = sizeof(Tin) == 4;
     const int64_t row_off = (b * a.dim + d) * a.seqlen;
     const int64_t t = t0 + lane * K;
     float dtl[K], bu[K], u[K], y[K];
@@ -196,11 +197,11 @@ __device__ __forceinline__ void chunk_full(const ScanArgs& a, int64_t b, int64_t
         float H = 0.f;
 #pragma unroll
         for (int k = 0; k < K; k++) {
-            an[k] = ex2(dtl[k] * Ad[n]);
+            an[k] = exp2_dec<kAcc>(dtl[k] * Ad[n]);
             bn[k] = bu[k] * sb[k];
             H = fmaf(an[k], H, bn[k]);
         }
-        float P = ex2(sdtl * Ad[n]);
+        float P = exp2_dec<kAcc>(sdtl * Ad[n]);
         warp_scan_maps(P, H, lane);
         float Pe = __shfl_up_sync(0xffffffffu, P, 1);
         float He = __shfl_up_sync(0xffffffffu, H, 1);
@@ -231,6 +232,7 @@ template <int N, typename Tin, bool kVec>
 __device__ __forceinline__ void chunk_aggregate(const ScanArgs& a, int64_t b, int64_t d, int64_t t0,
                                                 const Smem<N>& sm, const float* Ad, float* aggP,
                                                 float* aggH, int lane) {
+    constexpr bool kAcc = sizeof(Tin) == 4;
     const int64_t row_off = (b * a.dim + d) * a.seqlen;
     const int64_t t = t0 + lane * K;
     float dtl[K], bu[K], u[K];
@@ -240,8 +242,8 @@ __device__ __forceinline__ void chunk_aggregate(const ScanArgs& a, int64_t b, in
         const float* sb = &sm.B[n][lane * K];
         float H = 0.f;
 #pragma unroll
-        for (int k = 0; k < K; k++) H = fmaf(ex2(dtl[k] * Ad[n]), H, bu[k] * sb[k]);
-        float P = ex2(sdtl * Ad[n]);
+        for (int k = 0; k < K; k++) H = fmaf(exp2_dec<kAcc>(dtl[k] * Ad[n]), H, bu[k] * sb[k]);
+        float P = exp2_dec<kAcc>(sdtl * Ad[n]);
         warp_scan_maps(P, H, lane);
         P = __shfl_sync(0xffffffffu, P, 31);
         H = __shfl_sync(0xffffffffu, H, 31);

@@ -1,0 +1,88 @@
+"""GPU parity of the single-token decode update (ssm_state_update) against the fp64
+oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from workloads.torch_io import decode_set_to_torch, scan_to_torch, to_torch
+from tests.parity import assert_state_close, assert_y_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ssm():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import selective_state_space_121_b300 as m
+    return m
+
+
+def _decode_run(ssm, inp, steps, rows=None, check_every=None):
+    """Run `steps` decode tokens on the GPU (whole tensor) and the oracle (rows only)."""
+    cfg = inp["cfg"]
+    tol = 2e-3 if cfg.in_dtype == W.BF16 else 1e-5
+    rows = slice(None) if rows is None else rows
+    state = to_torch(inp["state"])
+    A, D, bias = to_torch(inp["A"]), to_torch(inp["D"]), to_torch(inp["delta_bias"])
+    sets = [decode_set_to_torch(s) for s in inp["sets"]]
+    ostate = inp["state"][rows].astype(np.float64).copy()
+    for k in range(steps):
+        s = sets[k % len(sets)]
+        y = ssm.state_update(state, s["x"], s["delta"], A, s["B"], s["C"], D, s["z"], bias, True)
+        hs = inp["sets"][k % len(sets)]
+        yr = oracle.state_update(ostate, hs["x"].f32()[rows], hs["delta"].f32()[rows], inp["A"],
+                                 hs["B"].f32()[rows], hs["C"].f32()[rows], inp["D"], hs["z"].f32()[rows],
+                                 inp["delta_bias"], True)
+        if check_every and ((k + 1) % check_every == 0 or k + 1 == steps):
+            torch.cuda.synchronize()
+            assert_y_close(to_np(y[rows]), yr, tol, y.dtype == torch.bfloat16, f"y step {k + 1}")
+            assert_state_close(to_np(state[rows]), ostate, tol, f"state step {k + 1}")
+    torch.cuda.synchronize()
+    return state, ostate
+
+
+def test_decode_small_many_steps(ssm):
+    inp = W.make_decode_inputs(W.DECODE_CONFIGS["decode"], batch=4, dim=40, token_sets=5)
+    _decode_run(ssm, inp, 37, check_every=1)
+
+
+@pytest.mark.parametrize("N", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_decode_dstate_and_dtype(ssm, N, dt):
+    cfg = W.DecodeConfig("d", 3, 37, N, dt, dt, 5, 5, 7000)
+    inp = W.make_decode_inputs(cfg)
+    _decode_run(ssm, inp, 5, check_every=1)
+
+
+def test_decode_full_size_first_step(ssm):
+    inp = W.make_decode_inputs(W.DECODE_CONFIGS["decode"], token_sets=2)
+    _decode_run(ssm, inp, 1, check_every=1)
+
+
+def test_decode_full_size_1000_steps_rows(ssm):
+    """The full (256, 5120, 16) state for 1000 tokens; the oracle follows batch rows 0-7."""
+    inp = W.make_decode_inputs(W.DECODE_CONFIGS["decode"])
+    _decode_run(ssm, inp, 1000, rows=slice(0, 8), check_every=250)
+
+
+def test_decode_equals_prefill_on_gpu(ssm):
+    """L decode tokens from h0 give the prefill scan's y and h_last (both fp32
+    arithmetic; they round differently -- sequential against tree composition --
+    so they agree to ~1e-5 of the output scale, well inside the 2e-3 bound each
+    meets against the oracle for these bf16 inputs)."""
+    inp = W.make_scan_inputs(W.CONFIGS["mamba130m"], batch=2, dim=24, seqlen=64)
+    t = scan_to_torch(inp)
+    h0 = torch.randn(2, 24, 16, device="cuda", generator=torch.Generator("cuda").manual_seed(3))
+    y, h = ssm.scan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], True,
+                        h0, out_dtype=torch.float32)
+    state = h0.clone()
+    ys = []
+    for k in range(64):
+        ys.append(ssm.state_update(state, t["u"][..., k].contiguous(), t["delta"][..., k].contiguous(), t["A"],
+                                   t["B"][..., k].contiguous(), t["C"][..., k].contiguous(), t["D"],
+                                   t["z"][..., k].contiguous(), t["delta_bias"], True, out_dtype=torch.float32))
+    yd = torch.stack(ys, dim=-1)
+    assert (yd - y).abs().max().item() <= 1e-4 * y.pow(2).mean().sqrt().item()
+    assert (state - h).abs().max().item() <= 1e-4 * h.pow(2).mean().sqrt().item()
