@@ -349,6 +349,29 @@ def _traffic_record(kernel: str):
 
 
 # ------------------------------------------------------------------------------------------
+# multi-process (one process per GPU, independent replicas)
+# ------------------------------------------------------------------------------------------
+def rank_env():
+    """(world, rank, local_rank) from the torchrun environment; (1, 0, 0) without it."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """The slowest rank's time: every rank runs the same per-GPU workload, so the job
+    takes as long as its slowest rank."""
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world: int, tokch_per_rank: int, ms: float) -> float:
+    """Whole-job Gtoken*channel/s: all ranks' units over the slowest rank's step time."""
+    return world * tokch_per_rank / (ms * 1e-3) / 1e9
+
+
+# ------------------------------------------------------------------------------------------
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -359,12 +382,16 @@ def main():
                     help="prefill scan algorithm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--only", choices=["scan", "decode"],
+                    help="time one entry point alone on --config (a kernel case for sweeps and ncu)")
+    ap.add_argument("--config", default="mamba130m",
+                    help="workload of --only: a prefill-scan config name, or 'decode'")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.only:
+        return run_case(args)
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local_rank = rank_env()
 
     if args.impl == "reference":
         return run_reference(args, world, rank)
@@ -405,9 +432,7 @@ def main():
             part_ms[i] += e[i].elapsed_time(e[i + 1])
     part_ms /= args.steps
     if dist:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(ms, dist, device)
         dist.barrier()
 
     # end to end from pinned host buffers through the same public API
@@ -425,9 +450,7 @@ def main():
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
     if dist:
-        t = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e2e_ms, dist, device)
 
     if rank != 0:
         if dist:
@@ -446,7 +469,7 @@ def main():
                            "hbm_frac": nbytes / sec / 1e9 / hbm_peak, "alg_bytes": nbytes, "elements": elems,
                            "roof_us": {"hbm": hbm_t * 1e6, "alu": alu_t * 1e6},
                            "roof_frac": max(hbm_t, alu_t) / sec}
-    value = world * tot_tokch / (ms * 1e-3) / 1e9
+    value = job_value(world, tot_tokch, ms)
 
     # roofline of the dominant kernel (largest share of the step)
     dom_i = int(np.argmax(part_ms))
@@ -484,7 +507,7 @@ def main():
         "parts": parts_out,
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "e2e": {"value": world * tot_tokch / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": e2e_ms,
+        "e2e": {"value": job_value(world, tot_tokch, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": hs.h2d, "d2h_bytes_per_step": hs.d2h, "steps": args.e2e_steps},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks.summary(),
@@ -492,6 +515,71 @@ def main():
     print(json.dumps(out))
     if dist:
         dist.destroy_process_group()
+
+
+def run_case(args):
+    """One entry point alone on one workload: W warm-up launches, then K launches each
+    timed with CUDA events on the launching stream. Prints one JSON line (not the
+    bench contract line): median/mean ms, Gtoken*channel/s, algorithmic GB/s."""
+    import torch
+    import selective_state_space_121_b300 as ssm
+    from workloads.torch_io import decode_set_to_torch, scan_to_torch, to_torch
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    if args.only == "scan":
+        cfg = W.CONFIGS[args.config]
+        inp = W.make_scan_inputs(cfg)
+        t = scan_to_torch(inp, dev)
+        ei = 2 if cfg.in_dtype == W.BF16 else 4
+        eo = 2 if cfg.out_dtype == W.BF16 else 4
+        odt = torch.bfloat16 if cfg.out_dtype == W.BF16 else torch.float32
+        y = torch.empty((cfg.batch, cfg.dim, cfg.seqlen), dtype=odt, device=dev)
+        h = torch.empty((cfg.batch, cfg.dim, cfg.dstate), dtype=torch.float32, device=dev)
+        ws = ssm.alloc_workspace(cfg.batch, cfg.dim, cfg.seqlen, cfg.dstate, dev)
+
+        def launch():
+            ssm.scan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"],
+                         cfg.softplus, t["h0"], y=y, h_last=h, algo=args.algo, workspace=ws)
+        tokch = cfg.tokens_channels
+        nbytes = scan_bytes(cfg.batch, cfg.dim, cfg.seqlen, cfg.dstate, ei, eo, cfg.has_z, t["h0"] is not None)
+        label = f"scan {cfg.name} ({cfg.batch},{cfg.dim},{cfg.seqlen},{cfg.dstate}) algo={args.algo}"
+    else:
+        cfg = W.DECODE_CONFIGS["decode"]
+        inp = W.make_decode_inputs(cfg)
+        # four resident states (4 x 84 MB > the 126 MB L2) taken in turn, so every
+        # launch streams its state from HBM as it would with one state per layer
+        states = [to_torch(inp["state"], dev) for _ in range(4)]
+        A, D, bias = (to_torch(inp[k], dev) for k in ("A", "D", "delta_bias"))
+        sets = [decode_set_to_torch(s, dev) for s in inp["sets"]]
+        yd = torch.empty((cfg.batch, cfg.dim), dtype=torch.bfloat16, device=dev)
+        k = [0]
+
+        def launch():
+            s = sets[k[0] % len(sets)]
+            state = states[k[0] % len(states)]
+            k[0] += 1
+            ssm.state_update(state, s["x"], s["delta"], A, s["B"], s["C"], D, s["z"], bias, True, y=yd)
+        tokch = cfg.batch * cfg.dim
+        nbytes = decode_bytes(cfg.batch, cfg.dim, cfg.dstate, 2, 2)
+        label = f"decode ({cfg.batch},{cfg.dim},{cfg.dstate})"
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for e0, e1 in ev:
+        e0.record(stream)
+        launch()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = np.array([e0.elapsed_time(e1) for e0, e1 in ev])
+    hbm_peak, _, peak_kind = _peaks()
+    med = float(np.median(ms))
+    print(json.dumps({"case": label, "launches": args.steps, "ms_median": med, "ms_mean": float(ms.mean()),
+                      "ms_min": float(ms.min()), "Gtokch_s": tokch / (med * 1e-3) / 1e9,
+                      "alg_bytes": nbytes, "GB_s": nbytes / (med * 1e-3) / 1e9,
+                      "hbm_frac": nbytes / (med * 1e-3) / 1e9 / hbm_peak, "peak_GB_s": hbm_peak,
+                      "peak_kind": peak_kind}))
 
 
 def run_reference(args, world, rank):

@@ -13,6 +13,15 @@ using ssm::ScanArgs;
 
 constexpr uint32_t kSpinLimit = 1u << 20;   // look-back waits: ~0.1-1 s before giving up
 constexpr int64_t kSMs = 148;               // B300
+// lanes per channel of the time-serial kernel at dstate >= 4 (a build option; 2 is
+// also built for dstate 16)
+#ifndef SSM_SERIAL_LANES
+#define SSM_SERIAL_LANES 4
+#endif
+constexpr int kSerialLanes = SSM_SERIAL_LANES;
+// channels from which the time-serial kernels have >= ~4 warps per SM (4 lanes per
+// channel at dstate >= 4; 8 lanes per channel at dstate 1)
+constexpr int64_t kSerialMinChannels = kSMs * 32;
 
 size_t esize(int dtype) { return dtype == SSM_BF16 ? 2 : 4; }
 
@@ -49,12 +58,17 @@ Plan plan_scan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int a
     Plan p{algo, 1, seqlen, 1};
     const int64_t channels = batch * dim;
     if (p.algo == SSM_ALGO_AUTO) {
-        if (channels > 0 && channels < kSMs * 8 && seqlen >= 8 * ssm::kWarpScanChunk)
+        // Time-serial lanes when the channels alone fill the GPU (the fewest
+        // instructions per element); otherwise split time: across CTAs for long
+        // sequences, across a warp's lanes for short ones.
+        if (channels >= kSerialMinChannels)
+            p.algo = SSM_ALGO_THREAD;
+        else if (channels > 0 && channels < kSMs * 8 && seqlen >= 8 * ssm::kWarpScanChunk)
             p.algo = SSM_ALGO_LOOKBACK;
         else
             p.algo = SSM_ALGO_WARPSCAN;
     }
-    if (p.algo == SSM_ALGO_THREAD) p.lanes_per_channel = dstate >= 4 ? 4 : (int)dstate;
+    if (p.algo == SSM_ALGO_THREAD) p.lanes_per_channel = dstate >= 4 ? kSerialLanes : (int)dstate;
     if (p.algo == SSM_ALGO_LOOKBACK) {
         const int64_t groups = dim > 0 ? (dim + 7) / 8 : 1;
         const int64_t target_ctas = kSMs * 8;
@@ -141,8 +155,11 @@ int scan_impl(const void* u, const void* delta, const float* A, const void* B, c
         if (cudaMemsetAsync(workspace, 0, need, s) != cudaSuccess) return SSM_ERR_LAUNCH;
         return ssm::launch_scan_lookback(a, s) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
     }
-    if (p.algo == SSM_ALGO_THREAD)
-        return ssm::launch_scan_thread(a, p.lanes_per_channel, s) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+    if (p.algo == SSM_ALGO_THREAD) {
+        const cudaError_t e = dstate == 1 ? ssm::launch_scan_scalar(a, s)
+                                          : ssm::launch_scan_thread(a, p.lanes_per_channel, s);
+        return e == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+    }
     return ssm::launch_scan_warp(a, s) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
 
@@ -257,6 +274,7 @@ int ssm_state_update(float* state, const void* x, const void* delta, const float
     a.state = state; a.x = x; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
     a.delta_bias = delta_bias; a.y = y; a.batch = batch; a.dim = dim; a.dstate = (int)dstate;
     a.softplus = softplus ? 1 : 0; a.in_dtype = in_dtype; a.out_dtype = out_dtype;
+    a.vec = dstate >= 4 && aligned(A, 16) && aligned(B, 4 * ei) && aligned(C, 4 * ei);
     return ssm::launch_state_update(a, (cudaStream_t)stream) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
 

@@ -1,0 +1,195 @@
+// kernels_scalar.cu -- the d_state = 1 scan (SM1, "Scalar Mamba1").
+//
+// What is computed (SM1 (Scalar Mamba1) page, section details: with one state per
+// channel the selective scan has the closed form h = L * (h0 + cumsum(dBx / L)),
+// L = cumprod(dA); the kernel evaluates the same recurrence without dividing by the
+// cumulative product):
+//     h_t = exp(dt_t A_d) h_{t-1} + dt_t B_t u_t,   y_t = C_t h_t (+ D_d u_t) (* silu(z_t))
+// with dt_t = softplus(delta_t + bias_d).
+//
+// The scan moves 12 bytes (fp32 u, delta, y) per token*channel against one exp,
+// one softplus and a handful of FP32 ops: it is HBM-bound, and the design goal is
+// enough independent work in flight. With one state per channel a lane holding a
+// whole channel would leave the GPU nearly idle (batch*dim lanes), so time is
+// split inside the warp:
+//  * a warp holds 4 channels (consecutive rows of the flattened (batch, dim)),
+//    8 lanes per channel; time goes in chunks of 64 steps, lane s of a channel
+//    owns steps 8s .. 8s+7 of the chunk and loads them with 16-byte vectors (a
+//    warp reads 4 x 256 contiguous bytes per tensor); the next chunk's inputs
+//    are loaded while the current one computes;
+//  * each lane folds its 8 steps into one affine map (a, b) (the associative
+//    composition (a2, b2) o (a1, b1) = (a2 a1, a2 b1 + b2), the parallel scan idea
+//    of the Mamba SSM complete guide's "Hardware-Aware Algorithm" section), a
+//    3-round shuffle scan over the channel's 8 lanes gives each lane the map of
+//    the steps before it, and the lane re-runs its 8 steps from the carry;
+//  * the carry (the state at the chunk boundary) comes from the channel's last
+//    lane. The decay factors and the state follow the same precision scheme as
+//    the N-state kernels: for fp32 inputs decays are carried as expm1 and the
+//    state as an anchored pair, so a slowly decaying large state is rounded once
+//    per output; for bf16 inputs the plain SFU form.
+#include "common.cuh"
+#include "launch.h"
+
+namespace ssm {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kSeg = 8;             // lanes per channel
+constexpr int kK = 8;               // steps per lane per chunk
+constexpr int kChunk = kSeg * kK;   // 64 steps
+constexpr int kChPerWarp = 32 / kSeg;
+
+// kK consecutive values of row[t ..] widened to fp32 (zero past L or when !ok).
+template <typename T, bool kVec>
+__device__ __forceinline__ void load_k(const T* row, int64_t t, int64_t L, bool ok, float* out) {
+    if (!ok) {
+#pragma unroll
+        for (int k = 0; k < kK; k++) out[k] = 0.f;
+        return;
+    }
+    if constexpr (kVec) {
+        constexpr int V = Vec16<T>::kN;
+        if (t + kK <= L) {
+#pragma unroll
+            for (int k = 0; k < kK; k += V) Vec16<T>::load(row + t + k, out + k);
+            return;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kK; k++) out[k] = (t + k < L) ? to_f32(row[t + k]) : 0.f;
+}
+
+template <typename T, bool kVec>
+__device__ __forceinline__ void store_k(T* row, int64_t t, int64_t L, const float* v) {
+    if constexpr (kVec) {
+        constexpr int V = Vec16<T>::kN;
+        if (t + kK <= L) {
+#pragma unroll
+            for (int k = 0; k < kK; k += V) Vec16<T>::store(row + t + k, v + k);
+            return;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kK; k++)
+        if (t + k < L) row[t + k] = from_f32<T>(v[k]);
+}
+
+template <typename Tin, typename Tout, bool kVec>
+__global__ void __launch_bounds__(kThreads) scalar_scan_kernel(ScanArgs a) {
+    constexpr bool kAcc = sizeof(Tin) == 4;
+    using Dec = Decay<kAcc>;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int c = lane / kSeg, s = lane % kSeg;
+    const int64_t rows = a.batch * a.dim;
+    const int64_t row = ((int64_t)blockIdx.x * kWarps + warp) * kChPerWarp + c;
+    const bool ok = row < rows;
+    const int64_t b = ok ? row / a.dim : 0, d = ok ? row % a.dim : 0;
+    const int64_t L = a.seqlen;
+    const Tin* up = static_cast<const Tin*>(a.u) + row * L;
+    const Tin* dp = static_cast<const Tin*>(a.delta) + row * L;
+    const Tin* zp = a.z ? static_cast<const Tin*>(a.z) + row * L : nullptr;
+    const Tin* Bp = static_cast<const Tin*>(a.B) + b * L;
+    const Tin* Cp = static_cast<const Tin*>(a.C) + b * L;
+    Tout* yp = static_cast<Tout*>(a.y) + row * L;
+    const float Ad = ok ? a.A[d] * Dec::scale : 0.f;
+    const float bias = (ok && a.delta_bias) ? a.delta_bias[d] : 0.f;
+    const float Dd = (ok && a.D) ? a.D[d] : 0.f;
+    float carry = (ok && a.h0) ? a.h0[row] : 0.f, carry_lo = 0.f;
+
+    float nu[kK], nd[kK], nz[kK], nB[kK], nC[kK];
+    auto prefetch = [&](int64_t t) {
+        load_k<Tin, kVec>(up, t, L, ok, nu);
+        load_k<Tin, kVec>(dp, t, L, ok, nd);
+        load_k<Tin, kVec>(zp, t, L, ok && zp, nz);
+        load_k<Tin, kVec>(Bp, t, L, ok, nB);
+        load_k<Tin, kVec>(Cp, t, L, ok, nC);
+    };
+    if (L > 0) prefetch((int64_t)s * kK);
+    for (int64_t t0 = 0; t0 < L; t0 += kChunk) {
+        const int64_t t = t0 + (int64_t)s * kK;
+        float u[kK], p[kK], bb[kK], zz[kK], C[kK];
+#pragma unroll
+        for (int k = 0; k < kK; k++) {
+            const float x = nd[k] + bias;
+            float dt = a.softplus ? softplus_acc<kAcc>(x) : x;
+            if (t + k >= L) dt = 0.f;                 // identity step past the end
+            u[k] = nu[k];
+            zz[k] = nz[k];
+            C[k] = nC[k];
+            p[k] = Dec::make(dt * Ad);
+            bb[k] = dt * nu[k] * nB[k];
+        }
+        if (t0 + kChunk < L) prefetch(t + kChunk);
+        // fold the lane's steps into one map (P, H), then scan the 8 lane maps
+        float P = Dec::one(), H = 0.f;
+#pragma unroll
+        for (int k = 0; k < kK; k++) {
+            H = Dec::step(p[k], H, bb[k]);
+            P = Dec::mul(p[k], P);
+        }
+#pragma unroll
+        for (int off = 1; off < kSeg; off <<= 1) {
+            const float Pp = __shfl_up_sync(0xffffffffu, P, off, kSeg);
+            const float Hp = __shfl_up_sync(0xffffffffu, H, off, kSeg);
+            if (s >= off) {
+                H = Dec::step(P, Hp, H);
+                P = Dec::mul(P, Pp);
+            }
+        }
+        float Pe = __shfl_up_sync(0xffffffffu, P, 1, kSeg);
+        float He = __shfl_up_sync(0xffffffffu, H, 1, kSeg);
+        if (s == 0) { Pe = Dec::one(); He = 0.f; }
+        const float Pt = __shfl_sync(0xffffffffu, P, kSeg - 1, kSeg);
+        const float Ht = __shfl_sync(0xffffffffu, H, kSeg - 1, kSeg);
+        float y[kK];
+        if constexpr (kAcc) {
+            float dlt = fmaf(Pe, carry, He) + carry_lo;
+            float h = carry + dlt;
+#pragma unroll
+            for (int k = 0; k < kK; k++) {
+                dlt += fmaf(p[k], h, bb[k]);
+                h = carry + dlt;
+                y[k] = C[k] * h;
+            }
+            two_sum(carry, fmaf(Pt, carry, Ht) + carry_lo, carry, carry_lo);
+        } else {
+            float h = Dec::step(Pe, carry, He);
+#pragma unroll
+            for (int k = 0; k < kK; k++) {
+                h = Dec::step(p[k], h, bb[k]);
+                y[k] = C[k] * h;
+            }
+            carry = Dec::step(Pt, carry, Ht);
+        }
+#pragma unroll
+        for (int k = 0; k < kK; k++) {
+            y[k] = fmaf(Dd, u[k], y[k]);
+            if (zp) y[k] *= silu_acc<kAcc>(zz[k]);
+        }
+        if (ok) store_k<Tout, kVec>(yp, t, L, y);
+    }
+    if (ok && s == 0 && a.h_last) a.h_last[row] = carry + carry_lo;
+}
+
+template <typename Tin, typename Tout>
+cudaError_t launch(const ScanArgs& a, cudaStream_t s) {
+    const int64_t rows = a.batch * a.dim;
+    if (rows == 0) return cudaSuccess;
+    const int64_t per_cta = (int64_t)kWarps * kChPerWarp;
+    const int64_t ctas = (rows + per_cta - 1) / per_cta;
+    if (ctas > ((int64_t)1 << 31) - 1) return cudaErrorInvalidValue;
+    if (a.vec) scalar_scan_kernel<Tin, Tout, true><<<(unsigned)ctas, kThreads, 0, s>>>(a);
+    else scalar_scan_kernel<Tin, Tout, false><<<(unsigned)ctas, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_scan_scalar(const ScanArgs& a, cudaStream_t s) {
+    if (a.in_dtype == kBF16)
+        return a.out_dtype == kBF16 ? launch<__nv_bfloat16, __nv_bfloat16>(a, s) : launch<__nv_bfloat16, float>(a, s);
+    return a.out_dtype == kBF16 ? launch<float, __nv_bfloat16>(a, s) : launch<float, float>(a, s);
+}
+
+}  // namespace ssm

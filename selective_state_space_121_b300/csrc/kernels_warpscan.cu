@@ -155,7 +155,7 @@ __device__ __forceinline__ float prepare_items(const ScanArgs& a, int64_t row_of
         const float x = dl[k] + bias;
         float dt = a.softplus ? softplus(x) : x;
         if (t + k >= a.seqlen) dt = 0.f;   // identity map past the end: a = 1, b = 0
-        dtl[k] = dt * kLog2e;
+        dtl[k] = dt * Decay<sizeof(Tin) == 4>::scale;
         bu[k] = dt * u[k];
         sdtl += dtl[k];
     }
@@ -164,25 +164,33 @@ __device__ __forceinline__ float prepare_items(const ScanArgs& a, int64_t row_of
 
 // Inclusive warp scan of lane maps (P, H): lane l ends with the composition of the
 // maps of lanes 0..l.
+template <class Dec>
 __device__ __forceinline__ void warp_scan_maps(float& P, float& H, int lane) {
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
         const float Pp = __shfl_up_sync(0xffffffffu, P, off);
         const float Hp = __shfl_up_sync(0xffffffffu, H, off);
         if (lane >= off) {
-            H = fmaf(P, Hp, H);
-            P *= Pp;
+            H = Dec::step(P, Hp, H);
+            P = Dec::mul(P, Pp);
         }
     }
 }
 
 // Full pass over one chunk: y for the lane's steps from the N-wide carry; carry
 // is advanced to the state at the end of the chunk.
+// With fp32 inputs (Decay<true>) the carry is an unevaluated pair (carry, carry_lo)
+// and every state inside the chunk is formed as carry + delta, where delta (the
+// change since the chunk start) is accumulated on its own: a slowly decaying
+// large state is then rounded once per output instead of once per step, which
+// keeps the fp32 result within ~1e-6 of its scale over thousands of steps. With
+// bf16 inputs carry_lo stays zero and the plain recurrence runs.
 template <int N, typename Tin, typename Tout, bool kVec>
 __device__ __forceinline__ void chunk_full(const ScanArgs& a, int64_t b, int64_t d, int64_t t0,
                                            const Smem<N>& sm, const float* Ad, float* carry,
-                                           int lane) {
-    constexpr bool kAcc = sizeof(Tin) == 4;
+                                           float* carry_lo, int lane) {
+    constexpr bool kAnchored = sizeof(Tin) == 4;
+    using Dec = Decay<kAnchored>;
     const int64_t row_off = (b * a.dim + d) * a.seqlen;
     const int64_t t = t0 + lane * K;
     float dtl[K], bu[K], u[K], y[K];
@@ -197,22 +205,36 @@ __device__ __forceinline__ void chunk_full(const ScanArgs& a, int64_t b, int64_t
         float H = 0.f;
 #pragma unroll
         for (int k = 0; k < K; k++) {
-            an[k] = exp2_dec<kAcc>(dtl[k] * Ad[n]);
+            an[k] = Dec::make(dtl[k] * Ad[n]);
             bn[k] = bu[k] * sb[k];
-            H = fmaf(an[k], H, bn[k]);
+            H = Dec::step(an[k], H, bn[k]);
         }
-        float P = exp2_dec<kAcc>(sdtl * Ad[n]);
-        warp_scan_maps(P, H, lane);
+        float P = Dec::make(sdtl * Ad[n]);
+        warp_scan_maps<Dec>(P, H, lane);
         float Pe = __shfl_up_sync(0xffffffffu, P, 1);
         float He = __shfl_up_sync(0xffffffffu, H, 1);
-        if (lane == 0) { Pe = 1.f; He = 0.f; }
-        float h = fmaf(Pe, carry[n], He);
+        if (lane == 0) { Pe = Dec::one(); He = 0.f; }
+        const float Pt = __shfl_sync(0xffffffffu, P, 31);
+        const float Ht = __shfl_sync(0xffffffffu, H, 31);
+        if constexpr (kAnchored) {
+            float dlt = fmaf(Pe, carry[n], He) + carry_lo[n];
+            float h = carry[n] + dlt;
 #pragma unroll
-        for (int k = 0; k < K; k++) {
-            h = fmaf(an[k], h, bn[k]);
-            y[k] = fmaf(sc[k], h, y[k]);
+            for (int k = 0; k < K; k++) {
+                dlt += fmaf(an[k], h, bn[k]);
+                h = carry[n] + dlt;
+                y[k] = fmaf(sc[k], h, y[k]);
+            }
+            two_sum(carry[n], fmaf(Pt, carry[n], Ht) + carry_lo[n], carry[n], carry_lo[n]);
+        } else {
+            float h = Dec::step(Pe, carry[n], He);
+#pragma unroll
+            for (int k = 0; k < K; k++) {
+                h = Dec::step(an[k], h, bn[k]);
+                y[k] = fmaf(sc[k], h, y[k]);
+            }
+            carry[n] = Dec::step(Pt, carry[n], Ht);
         }
-        carry[n] = __shfl_sync(0xffffffffu, fmaf(P, carry[n], H), 31);
     }
     const float Dd = a.D ? a.D[d] : 0.f;
     if (a.z) {
@@ -232,7 +254,7 @@ template <int N, typename Tin, bool kVec>
 __device__ __forceinline__ void chunk_aggregate(const ScanArgs& a, int64_t b, int64_t d, int64_t t0,
                                                 const Smem<N>& sm, const float* Ad, float* aggP,
                                                 float* aggH, int lane) {
-    constexpr bool kAcc = sizeof(Tin) == 4;
+    using Dec = Decay<sizeof(Tin) == 4>;
     const int64_t row_off = (b * a.dim + d) * a.seqlen;
     const int64_t t = t0 + lane * K;
     float dtl[K], bu[K], u[K];
@@ -242,13 +264,13 @@ __device__ __forceinline__ void chunk_aggregate(const ScanArgs& a, int64_t b, in
         const float* sb = &sm.B[n][lane * K];
         float H = 0.f;
 #pragma unroll
-        for (int k = 0; k < K; k++) H = fmaf(exp2_dec<kAcc>(dtl[k] * Ad[n]), H, bu[k] * sb[k]);
-        float P = exp2_dec<kAcc>(sdtl * Ad[n]);
-        warp_scan_maps(P, H, lane);
+        for (int k = 0; k < K; k++) H = Dec::step(Dec::make(dtl[k] * Ad[n]), H, bu[k] * sb[k]);
+        float P = Dec::make(sdtl * Ad[n]);
+        warp_scan_maps<Dec>(P, H, lane);
         P = __shfl_sync(0xffffffffu, P, 31);
         H = __shfl_sync(0xffffffffu, H, 31);
-        aggH[n] = fmaf(P, aggH[n], H);
-        aggP[n] *= P;
+        aggH[n] = Dec::step(P, aggH[n], H);
+        aggP[n] = Dec::mul(P, aggP[n]);
     }
 }
 
@@ -259,18 +281,21 @@ __device__ __forceinline__ void load_A(const ScanArgs& a, int64_t d, float* Ad) 
 }
 
 template <int N>
-__device__ __forceinline__ void load_h0(const ScanArgs& a, int64_t b, int64_t d, float* carry) {
+__device__ __forceinline__ void load_h0(const ScanArgs& a, int64_t b, int64_t d, float* carry, float* carry_lo) {
 #pragma unroll
-    for (int n = 0; n < N; n++) carry[n] = a.h0 ? a.h0[(b * a.dim + d) * N + n] : 0.f;
+    for (int n = 0; n < N; n++) {
+        carry[n] = a.h0 ? a.h0[(b * a.dim + d) * N + n] : 0.f;
+        carry_lo[n] = 0.f;
+    }
 }
 
 template <int N>
 __device__ __forceinline__ void store_hlast(const ScanArgs& a, int64_t b, int64_t d, const float* carry,
-                                            int lane) {
+                                            const float* carry_lo, int lane) {
     if (!a.h_last) return;
 #pragma unroll
     for (int n = 0; n < N; n++)
-        if (lane == (n & 31)) a.h_last[(b * a.dim + d) * N + n] = carry[n];
+        if (lane == (n & 31)) a.h_last[(b * a.dim + d) * N + n] = carry[n] + carry_lo[n];
 }
 
 // ---------------------------------------------------------------------------
@@ -284,25 +309,26 @@ __global__ void __launch_bounds__(kThreads) warp_scan_kernel(ScanArgs a) {
     const int64_t b = blockIdx.y;
     const int64_t d = (int64_t)blockIdx.x * W + warp;
     const bool active = d < a.dim;
-    float Ad[N], carry[N];
+    float Ad[N], carry[N], carry_lo[N];
     if (active) {
         load_A<N>(a, d, Ad);
-        load_h0<N>(a, b, d, carry);
+        load_h0<N>(a, b, d, carry, carry_lo);
     }
     for (int64_t t0 = 0; t0 < a.seqlen; t0 += T) {
         stage_bc<N, Tin, kVec, true>(a, b, t0, sm);
         __syncthreads();
-        if (active) chunk_full<N, Tin, Tout, kVec>(a, b, d, t0, sm, Ad, carry, lane);
+        if (active) chunk_full<N, Tin, Tout, kVec>(a, b, d, t0, sm, Ad, carry, carry_lo, lane);
         __syncthreads();
     }
-    if (active) store_hlast<N>(a, b, d, carry, lane);
+    if (active) store_hlast<N>(a, b, d, carry, carry_lo, lane);
 }
 
 // ---------------------------------------------------------------------------
 // Look-back kernel. Workspace layout (zeroed by the host on the stream):
 //   [0] int32 status, [1] uint32 ticket, [2..3] pad;
 //   then per (channel, segment): uint32 flag[N], float P[N], float H[N], float I[N].
-// (P, H) is the segment's own map (published with flag AGG), I the state at the
+// (P, H) is the segment's own map (published with flag AGG; P in the kernel's
+// Decay representation: the factor itself, or factor - 1 for fp32 inputs), I the state at the
 // segment's end (published with flag INCL). Published values are never
 // rewritten, so a reader that saw AGG can still read (P, H) after the writer
 // has moved on to INCL. Lane n owns state n of a descriptor: it writes the
@@ -330,6 +356,7 @@ template <int N, typename Tin, typename Tout, bool kVec>
 __global__ void __launch_bounds__(kThreads) lookback_kernel(ScanArgs a) {
     __shared__ __align__(16) Smem<N> sm;
     __shared__ uint32_t s_ticket;
+    using Dec = Decay<sizeof(Tin) == 4>;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int32_t* status = static_cast<int32_t*>(a.workspace);
     uint32_t* ticket_ctr = reinterpret_cast<uint32_t*>(status + 1);
@@ -349,11 +376,11 @@ __global__ void __launch_bounds__(kThreads) lookback_kernel(ScanArgs a) {
     const int64_t te = min(a.seqlen, ts + a.seg_len);
     const int64_t ch = b * a.dim + d;
 
-    float Ad[N], carry[N], aggP[N], aggH[N];
+    float Ad[N], carry[N], carry_lo[N], aggP[N], aggH[N];
     if (active) {
         load_A<N>(a, d, Ad);
 #pragma unroll
-        for (int n = 0; n < N; n++) { aggP[n] = 1.f; aggH[n] = 0.f; }
+        for (int n = 0; n < N; n++) { aggP[n] = Dec::one(); aggH[n] = 0.f; }
     }
     const bool last = seg + 1 == a.n_seg;
     const bool publish = !last && seg != a.drop_segment;
@@ -369,7 +396,7 @@ __global__ void __launch_bounds__(kThreads) lookback_kernel(ScanArgs a) {
     if (active) {
         Desc<N>* mine = desc + ch * a.n_seg + seg;
         if (seg == 0) {
-            load_h0<N>(a, b, d, carry);
+            load_h0<N>(a, b, d, carry, carry_lo);
         } else {
             // 2) publish the segment map (successors may compose it), then 3) look back
             if (publish) {
@@ -384,7 +411,7 @@ __global__ void __launch_bounds__(kThreads) lookback_kernel(ScanArgs a) {
             }
             // lane n < N walks state n back; (accP, accH) is the composed map of the
             // segments strictly between the one inspected and this one
-            float accP = 1.f, accH = 0.f, cin = 0.f;
+            float accP = Dec::one(), accH = 0.f, cin = 0.f;
             bool timed_out = false;
             if (lane < N) {
                 for (int64_t j = seg - 1; j >= 0; j--) {
@@ -397,14 +424,17 @@ __global__ void __launch_bounds__(kThreads) lookback_kernel(ScanArgs a) {
                         f = ld_acquire(&pd->flag[lane]);
                     }
                     if (f == kFlagNone) { timed_out = true; cin = accH; break; }
-                    if (f == kFlagIncl) { cin = fmaf(accP, __ldcg(&pd->I[lane]), accH); break; }
-                    accH = fmaf(accP, __ldcg(&pd->H[lane]), accH);
-                    accP *= __ldcg(&pd->P[lane]);
+                    if (f == kFlagIncl) { cin = Dec::step(accP, __ldcg(&pd->I[lane]), accH); break; }
+                    accH = Dec::step(accP, __ldcg(&pd->H[lane]), accH);
+                    accP = Dec::mul(accP, __ldcg(&pd->P[lane]));
                 }
             }
             if (timed_out) atomicExch(status, kErrLookbackTimeout);
 #pragma unroll
-            for (int n = 0; n < N; n++) carry[n] = __shfl_sync(0xffffffffu, cin, n);
+            for (int n = 0; n < N; n++) {
+                carry[n] = __shfl_sync(0xffffffffu, cin, n);
+                carry_lo[n] = 0.f;
+            }
         }
         // 4) publish the inclusive prefix: the state at this segment's end. On a
         //    timeout this is still published (with the wrong carry) so that later
@@ -413,7 +443,7 @@ __global__ void __launch_bounds__(kThreads) lookback_kernel(ScanArgs a) {
 #pragma unroll
             for (int n = 0; n < N; n++) {
                 if (lane == n) {
-                    mine->I[n] = fmaf(aggP[n], carry[n], aggH[n]);
+                    mine->I[n] = Dec::step(aggP[n], carry[n], aggH[n]) + carry_lo[n];
                     st_release(&mine->flag[n], kFlagIncl);
                 }
             }
@@ -423,10 +453,10 @@ __global__ void __launch_bounds__(kThreads) lookback_kernel(ScanArgs a) {
     for (int64_t t0 = ts; t0 < te; t0 += T) {
         stage_bc<N, Tin, kVec, true>(a, b, t0, sm);
         __syncthreads();
-        if (active) chunk_full<N, Tin, Tout, kVec>(a, b, d, t0, sm, Ad, carry, lane);
+        if (active) chunk_full<N, Tin, Tout, kVec>(a, b, d, t0, sm, Ad, carry, carry_lo, lane);
         __syncthreads();
     }
-    if (active && last) store_hlast<N>(a, b, d, carry, lane);
+    if (active && last) store_hlast<N>(a, b, d, carry, carry_lo, lane);
 }
 
 template <int N, typename Tin, typename Tout>

@@ -49,6 +49,7 @@ struct DecodeArgs {
     int dstate;
     int softplus;
     int in_dtype, out_dtype;
+    bool vec;          // A 16-byte and B, C (4 * element size)-byte aligned: vector loads
 };
 
 // Each returns cudaSuccess or the launch error.
@@ -56,6 +57,7 @@ cudaError_t launch_state_update(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_scan_warp(const ScanArgs& a, cudaStream_t s);
 cudaError_t launch_scan_lookback(const ScanArgs& a, cudaStream_t s);
 cudaError_t launch_scan_thread(const ScanArgs& a, int lanes_per_channel, cudaStream_t s);
+cudaError_t launch_scan_scalar(const ScanArgs& a, cudaStream_t s);
 
 // Look-back workspace geometry (bytes), shared by api.cu and the kernel.
 constexpr int kWarpScanItems = 8;                    // time steps per lane per chunk
