@@ -259,66 +259,90 @@ __global__ void __launch_bounds__(kThreads) serial_scan_kernel(ScanArgs a) {
         if (c + 1 < n_chunks) prefetch(t0 + kT);
         __syncthreads();
 
-        // B. recurrence, in groups of 4 steps: the loads and exps of a group do
-        // not depend on the state, only the 4 chained state updates do
+        // B. recurrence, in groups of 4 steps. Only the chained state updates of a
+        // group depend on the state; its loads and exps do not. The bf16 path is
+        // software-pipelined by hand: the loads and exps of group g+1 are issued
+        // before the chained updates of group g, so an in-order warp has the
+        // SFU/shared-memory latency of one group covered by the other's FMAs.
         const float4* db = reinterpret_cast<const float4*>(s_db[warp][g]);   // 2 steps per load
+        // B and C of this lane's states at step t, in pairs
+        auto load_bc = [&](int t, float2* bq, float2* cq) {
+            const float* bc = s_bc[buf][t];
+            if constexpr (NPL % 4 == 0) {
 #pragma unroll
-        for (int tg = 0; tg < kT; tg += 4) {
-            float2 x[4];
-            {
-                const float4 x01 = db[tg / 2], x23 = db[tg / 2 + 1];
-                x[0] = make_float2(x01.x, x01.y); x[1] = make_float2(x01.z, x01.w);
-                x[2] = make_float2(x23.x, x23.y); x[3] = make_float2(x23.z, x23.w);
-            }
-            float2 bq[4][NP2], cq[4][NP2];   // B, C of this lane's states, in pairs
-#pragma unroll
-            for (int st = 0; st < 4; st++) {
-                const float* bc = s_bc[buf][tg + st];
-                if constexpr (NPL % 4 == 0) {
-#pragma unroll
-                    for (int i = 0; i < NPL; i += 4) {
-                        const float4 vb = *reinterpret_cast<const float4*>(bc + j * NPL + i);
-                        const float4 vc = *reinterpret_cast<const float4*>(bc + N + j * NPL + i);
-                        bq[st][i / 2] = make_float2(vb.x, vb.y); bq[st][i / 2 + 1] = make_float2(vb.z, vb.w);
-                        cq[st][i / 2] = make_float2(vc.x, vc.y); cq[st][i / 2 + 1] = make_float2(vc.z, vc.w);
-                    }
-                } else if constexpr (NPL == 2) {
-                    bq[st][0] = *reinterpret_cast<const float2*>(bc + j * 2);
-                    cq[st][0] = *reinterpret_cast<const float2*>(bc + N + j * 2);
-                } else {
-                    bq[st][0] = make_float2(bc[j], 0.f);
-                    cq[st][0] = make_float2(bc[N + j], 0.f);
+                for (int i = 0; i < NPL; i += 4) {
+                    const float4 vb = *reinterpret_cast<const float4*>(bc + j * NPL + i);
+                    const float4 vc = *reinterpret_cast<const float4*>(bc + N + j * NPL + i);
+                    bq[i / 2] = make_float2(vb.x, vb.y); bq[i / 2 + 1] = make_float2(vb.z, vb.w);
+                    cq[i / 2] = make_float2(vc.x, vc.y); cq[i / 2 + 1] = make_float2(vc.z, vc.w);
                 }
+            } else if constexpr (NPL == 2) {
+                bq[0] = *reinterpret_cast<const float2*>(bc + j * 2);
+                cq[0] = *reinterpret_cast<const float2*>(bc + N + j * 2);
+            } else {
+                bq[0] = make_float2(bc[j], 0.f);
+                cq[0] = make_float2(bc[N + j], 0.f);
             }
-            float acc[4];
-            if constexpr (!kAcc && NPL % 2 == 0) {
-                float2 an[4][NP2], bn[4][NP2];
+        };
+        auto load_x = [&](int tg, float2* x) {
+            const float4 x01 = db[tg / 2], x23 = db[tg / 2 + 1];
+            x[0] = make_float2(x01.x, x01.y); x[1] = make_float2(x01.z, x01.w);
+            x[2] = make_float2(x23.x, x23.y); x[3] = make_float2(x23.z, x23.w);
+        };
+        if constexpr (!kAcc && NPL % 2 == 0) {
+            // operands of one group, ready for its chained updates
+            struct Stage {
+                float2 an[4][NP2], bn[4][NP2], cq[4][NP2];
+            };
+            auto stage = [&](int tg, Stage& S) {
+                float2 x[4];
+                load_x(tg, x);
 #pragma unroll
                 for (int st = 0; st < 4; st++) {
+                    float2 bq[NP2];
+                    load_bc(tg + st, bq, S.cq[st]);
                     const float2 dtl2 = make_float2(x[st].x, x[st].x), bu2 = make_float2(x[st].y, x[st].y);
 #pragma unroll
                     for (int i = 0; i < NP2; i++) {
                         const float2 e = mul2(dtl2, A2[i]);
-                        an[st][i] = make_float2(ex2(e.x), ex2(e.y));
-                        bn[st][i] = mul2(bu2, bq[st][i]);
+                        S.an[st][i] = make_float2(ex2(e.x), ex2(e.y));
+                        S.bn[st][i] = mul2(bu2, bq[i]);
                     }
                 }
+            };
+            Stage cur, nxt;
+            stage(0, cur);
+#pragma unroll
+            for (int tg = 0; tg < kT; tg += 4) {
+                if (tg + 4 < kT) stage(tg + 4, nxt);
+                float acc[4];
 #pragma unroll
                 for (int st = 0; st < 4; st++) {
                     float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
                     for (int i = 0; i < NP2; i++) {
-                        h2[i] = fma2(an[st][i], h2[i], bn[st][i]);
-                        acc2 = fma2(cq[st][i], h2[i], acc2);
+                        h2[i] = fma2(cur.an[st][i], h2[i], cur.bn[st][i]);
+                        acc2 = fma2(cur.cq[st][i], h2[i], acc2);
                     }
                     acc[st] = acc2.x + acc2.y;
                 }
-            } else {
+                s_p[warp][tg / 4][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                if (tg + 4 < kT) cur = nxt;
+            }
+        } else {
+#pragma unroll
+            for (int tg = 0; tg < kT; tg += 4) {
+                float2 x[4];
+                load_x(tg, x);
+                float2 bq[4][NP2], cq[4][NP2];
+#pragma unroll
+                for (int st = 0; st < 4; st++) load_bc(tg + st, bq[st], cq[st]);
                 float an[4][NPL];
 #pragma unroll
                 for (int st = 0; st < 4; st++)
 #pragma unroll
                     for (int i = 0; i < NPL; i++) an[st][i] = Dec::make(x[st].x * lo_hi(A2[i / 2], i));
+                float acc[4];
 #pragma unroll
                 for (int st = 0; st < 4; st++) {
                     acc[st] = 0.f;
@@ -335,8 +359,8 @@ __global__ void __launch_bounds__(kThreads) serial_scan_kernel(ScanArgs a) {
                         acc[st] = fmaf(lo_hi(cq[st][i / 2], i), hi, acc[st]);
                     }
                 }
+                s_p[warp][tg / 4][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
             }
-            s_p[warp][tg / 4][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
         }
         if constexpr (kAcc) {
             // re-anchor: (hhi, hlo) <- the exact sum of the pair and dlt
