@@ -71,7 +71,8 @@ typedef enum {
     SSM_ERR_LOOKBACK_TIMEOUT = -7,  /* device: a look-back wait exhausted its budget */
     SSM_ERR_UNSUPPORTED_N = -8,     /* dstate not in {1, 2, 4, 8, 16} */
     SSM_ERR_ALIAS = -9,             /* an output overlaps an input it must not */
-    SSM_ERR_ALGO = -10              /* unknown algorithm selector */
+    SSM_ERR_ALGO = -10,             /* unknown algorithm selector */
+    SSM_ERR_SCRATCH_LIMIT = -11     /* problem needs more than SSM_STATIC_SCRATCH_BYTES of scratch */
 } ssm_status_t;
 
 /* Algorithm selectors for ssm_scan_fwd_algo. All compute the same result.
@@ -169,6 +170,46 @@ SSM_API int ssm_test_lookback_timeout(const void* u, const void* delta, const fl
                                       int64_t dim, int64_t seqlen, int64_t dstate, int in_dtype,
                                       void* workspace, size_t workspace_bytes,
                                       int64_t drop_segment, uint32_t spin_limit, void* stream);
+
+/* Size of the library's own device scratch area used by
+ * ssm_scan_fwd_lookback_static (4 MiB). */
+#define SSM_STATIC_SCRATCH_BYTES ((size_t)4 << 20)
+
+/* The look-back scan (SSM_ALGO_LOOKBACK of ssm_scan_fwd_algo) without a caller
+ * workspace: the pages have no counterpart to this entry point; it exists for
+ * callers that cannot allocate device memory or hand the library a workspace --
+ * for instance a plugin or callback running inside a host application that owns
+ * all device memory and exposes no allocator to it, or a latency-critical path
+ * that must not call cudaMalloc, which can synchronise the device and stall
+ * every other stream.
+ *   Arguments and results are those of ssm_scan_fwd (the caller still passes the
+ *   inputs and outputs as device pointers); the scratch is a 4 MiB device array
+ *   owned by the library. The library allocates nothing: no cudaMalloc or
+ *   cudaFree, no allocating library routine.
+ *   Limit: sizes whose look-back scratch, ssm_scan_workspace_size(batch, dim,
+ *   seqlen, dstate), exceeds SSM_STATIC_SCRATCH_BYTES return SSM_ERR_SCRATCH_LIMIT
+ *   with nothing launched (at dstate 16 that is about 16,000 channel-segments,
+ *   e.g. batch*dim = 1536 at seqlen 131072).
+ *   Memory: every GPU that loads the library holds the 4 MiB array until the
+ *   process exits.
+ *   First call on a device: it looks up the array's device address on the
+ *   current device (cudaGetSymbolAddress) and caches it, so make that first
+ *   call before any stream capture.
+ *   Sharing: all calls on a device use the same array, which keeps what the last
+ *   call left there; each call zeroes the part it needs, on `stream`, before its
+ *   kernel. Calls whose executions overlap on the GPU (issued on different
+ *   streams with no ordering between them) race on the array and give undefined
+ *   results: serialise them, e.g. on one stream.
+ *   Device-side errors: the look-back waits stay bounded, but the status word
+ *   lives in the library's array, so a wait that runs out of budget is not
+ *   reported to the caller (the output is then unspecified); use ssm_scan_fwd_algo
+ *   with a workspace when that report is needed. */
+SSM_API int ssm_scan_fwd_lookback_static(const void* u, const void* delta, const float* A,
+                                         const void* B, const void* C, const float* D,
+                                         const void* z, const float* delta_bias, int softplus,
+                                         const float* h0, void* y, float* h_last, int64_t batch,
+                                         int64_t dim, int64_t seqlen, int64_t dstate,
+                                         int in_dtype, int out_dtype, void* stream);
 
 /* Reads the device status word of `workspace` (reset and written by a previous
  * look-back scan on the same stream; other algorithms leave it untouched),

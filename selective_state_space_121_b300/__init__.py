@@ -51,15 +51,19 @@ _lib.ssm_test_lookback_timeout.argtypes = [_P] * 6 + [_I64] * 4 + [_I, _P, _SZ, 
 _lib.ssm_test_lookback_timeout.restype = _I
 _lib.ssm_query_status.argtypes = [_P, _SZ, _P]
 _lib.ssm_query_status.restype = _I
+_lib.ssm_scan_fwd_lookback_static.argtypes = [_P] * 8 + [_I, _P, _P, _P] + [_I64] * 4 + [_I, _I, _P]
+_lib.ssm_scan_fwd_lookback_static.restype = _I
 
 SSM_F32, SSM_BF16 = 0, 1
 ALGOS = {"auto": 0, "thread": 1, "warpscan": 2, "lookback": 3}
 SSM_ERR_LOOKBACK_TIMEOUT = -7
+SSM_ERR_SCRATCH_LIMIT = -11
+STATIC_SCRATCH_BYTES = 4 << 20   # SSM_STATIC_SCRATCH_BYTES
 
 # the C ABI entry-point names, as declared in include/ssm_scan.h
 EXPORTS = ("ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_size", "ssm_scan_fwd",
            "ssm_scan_fwd_algo", "ssm_scalar_scan_fwd", "ssm_state_update",
-           "ssm_test_lookback_timeout", "ssm_query_status")
+           "ssm_test_lookback_timeout", "ssm_query_status", "ssm_scan_fwd_lookback_static")
 
 
 class SSMError(RuntimeError):
@@ -202,6 +206,25 @@ def state_update(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, soft
         _stream())
     _check(status)
     return y
+
+
+def scan_fwd_lookback_static(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, h0=None, *,
+                             y, h_last=None) -> int:
+    """The look-back scan on the library's own fixed scratch area
+    (ssm_scan_fwd_lookback_static): for callers that cannot allocate device memory or
+    pass a workspace. The caller provides y (and h_last) preallocated; this function
+    allocates nothing. Returns the ABI status (0 on success, SSM_ERR_SCRATCH_LIMIT
+    when the sizes need more than STATIC_SCRATCH_BYTES of scratch)."""
+    bt, dim, L = u.shape
+    N = A.shape[1]
+    in_code = _dtype_code(u.dtype)
+    _same(u, (("delta", delta, u.shape), ("B", B, (bt, N, L)), ("C", C, (bt, N, L)), ("z", z, u.shape)))
+    _f32(A, (dim, N), "A"); _f32(D, (dim,), "D"); _f32(delta_bias, (dim,), "delta_bias")
+    _f32(h0, (bt, dim, N), "h0"); _f32(h_last, (bt, dim, N), "h_last")
+    return int(_lib.ssm_scan_fwd_lookback_static(
+        _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+        int(bool(softplus)), _ptr(h0), _ptr(y), _ptr(h_last), bt, dim, L, N, in_code, _dtype_code(y.dtype),
+        _stream()))
 
 
 def query_status(workspace) -> int:

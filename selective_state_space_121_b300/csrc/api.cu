@@ -183,6 +183,8 @@ const char* ssm_status_string(int status) {
         case SSM_ERR_UNSUPPORTED_N: return "SSM_ERR_UNSUPPORTED_N: dstate must be 1, 2, 4, 8 or 16";
         case SSM_ERR_ALIAS: return "SSM_ERR_ALIAS: an output overlaps an input";
         case SSM_ERR_ALGO: return "SSM_ERR_ALGO: unknown algorithm";
+        case SSM_ERR_SCRATCH_LIMIT:
+            return "SSM_ERR_SCRATCH_LIMIT: problem needs more scratch than the library's fixed 4 MiB area";
     }
     return "unknown ssm status";
 }

@@ -43,7 +43,7 @@ def test_abi_version_matches_header(ssm):
 
 
 def test_status_strings(ssm):
-    for code in range(0, -11, -1):
+    for code in range(0, -12, -1):
         assert ssm.status_string(code).startswith("SSM_")
     assert not ssm.status_string(-99).startswith("SSM_")
 
