@@ -40,7 +40,7 @@ WORKLOAD = "mamba130m_layer_step"
 N_SM = 148
 SM_MAX_MHZ_NOMINAL = 2032.0
 FP32_LANES_PER_CLK_SM = 128       # FMA pipe
-SFU_EX2_PER_CLK_SM = 32           # measured on B300 (about twice B200's)
+SFU_EX2_PER_CLK_SM = 32           # ex2 lanes per clock per SM, measured on B300
 
 
 def _peaks():
@@ -68,12 +68,17 @@ def decode_bytes(bt, dim, N, ei, eo):
     return bt * dim * N * 4 * 2 + bt * dim * (3 * ei + eo) + 2 * bt * N * ei + dim * (N + 2) * 4
 
 
+SFU_HALF_RATE_SLOTS = 2           # lg2 and rcp issue at half the ex2 rate (16/clk/SM measured)
+
+
 def alu_roof_seconds(elements, tokch, has_z, mhz):
-    """Time the SFU/FP32 pipes need at the given clock: per (t, n) element one ex2 and
-    4 FP32 FMA-pipe ops; per (b, d, t) two SFU ops for softplus (+2 for silu) and ~10 FP32
-    ops of the fused prologue/epilogue."""
+    """Time the SFU and FP32 pipes need at the given clock (the larger of the two):
+    per (t, n) element one ex2 and 4 FP32 FMA-pipe ops; per (b, d, t) softplus = ex2 + lg2
+    and silu = ex2 + rcp (lg2/rcp at half rate, 2 slots each) and ~10 FP32 ops of the
+    fused prologue/epilogue."""
     f = mhz * 1e6 * N_SM
-    sfu = elements + tokch * (2 + (2 if has_z else 0))
+    per_tok = (1 + SFU_HALF_RATE_SLOTS) * (2 if has_z else 1)
+    sfu = elements + tokch * per_tok
     fp = 4 * elements + 10 * tokch
     return max(sfu / (SFU_EX2_PER_CLK_SM * f), fp / (FP32_LANES_PER_CLK_SM * f))
 
@@ -482,8 +487,9 @@ def main():
         peak = 6.0 * elems / alu_t / 1e12
         roofline = {"bound": "alu", "kernel": name, "achieved": flops / sec / 1e12, "peak": peak,
                     "unit": "TFLOP/s", "frac": (flops / sec / 1e12) / peak,
-                    "peak_kind": "derived: 148 SMs x 2032 MHz, per (t,n) element 1 ex2 (32/clk/SM) + 4 FP32 "
-                                 "FMA-pipe ops (128/clk/SM), per (b,d,t) 4 SFU + 10 FP32 ops; 6 flops/element",
+                    "peak_kind": "derived: 148 SMs x 2032 MHz; per (t,n) element 1 ex2 (32/clk/SM, measured) + "
+                                 "4 FP32 FMA-pipe ops (128/clk/SM); per (b,d,t) softplus+silu = 6 SFU slots "
+                                 "(lg2, rcp at half rate) + 10 FP32 ops; 6 flops/element",
                     "hbm_GB_s": nbytes / sec / 1e9, "hbm_frac_of_measured": nbytes / sec / 1e9 / hbm_peak,
                     "traffic": _traffic_record(name)}
     else:

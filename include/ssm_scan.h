@@ -188,8 +188,9 @@ SSM_API int ssm_test_lookback_timeout(const void* u, const void* delta, const fl
  *   cudaFree, no allocating library routine.
  *   Limit: sizes whose look-back scratch, ssm_scan_workspace_size(batch, dim,
  *   seqlen, dstate), exceeds SSM_STATIC_SCRATCH_BYTES return SSM_ERR_SCRATCH_LIMIT
- *   with nothing launched (at dstate 16 that is about 16,000 channel-segments,
- *   e.g. batch*dim = 1536 at seqlen 131072).
+ *   with nothing launched (at dstate 16 that is about 16,000 channel-segments:
+ *   batch*dim = 1536 fits up to seqlen of about 20K; longer sequences need a
+ *   caller workspace).
  *   Memory: every GPU that loads the library holds the 4 MiB array until the
  *   process exits.
  *   First call on a device: it looks up the array's device address on the

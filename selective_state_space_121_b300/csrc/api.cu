@@ -13,6 +13,15 @@ using ssm::ScanArgs;
 
 constexpr uint32_t kSpinLimit = 1u << 20;   // look-back waits: ~0.1-1 s before giving up
 constexpr int64_t kSMs = 148;               // B300
+// look-back geometry (build options): CTAs per SM aimed at, shortest segment
+#ifndef SSM_LB_CTAS_PER_SM
+#define SSM_LB_CTAS_PER_SM 3
+#endif
+#ifndef SSM_LB_MIN_SEG
+#define SSM_LB_MIN_SEG 2048
+#endif
+constexpr int64_t kLookbackCtasPerSM = SSM_LB_CTAS_PER_SM;
+constexpr int64_t kLookbackMinSeg = SSM_LB_MIN_SEG;
 // lanes per channel of the time-serial kernel at dstate >= 4 (a build option; 2 is
 // also built for dstate 16)
 #ifndef SSM_SERIAL_LANES
@@ -54,7 +63,7 @@ struct Plan {
 // Channels are the unit of parallel work for the serial-carry algorithms; the
 // look-back cuts time into segments when there are too few channels to fill the
 // B300's 148 SMs.
-Plan plan_scan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int algo) {
+Plan plan_scan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int algo, int in_dtype) {
     Plan p{algo, 1, seqlen, 1};
     const int64_t channels = batch * dim;
     if (p.algo == SSM_ALGO_AUTO) {
@@ -70,14 +79,20 @@ Plan plan_scan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int a
     }
     if (p.algo == SSM_ALGO_THREAD) p.lanes_per_channel = dstate >= 4 ? kSerialLanes : (int)dstate;
     if (p.algo == SSM_ALGO_LOOKBACK) {
-        const int64_t groups = dim > 0 ? (dim + 7) / 8 : 1;
-        const int64_t target_ctas = kSMs * 8;
+        // segments of the serial look-back: one CTA per (channel group, segment);
+        // about 3 CTAs per SM of the B300 in total, segments a multiple of 256
+        // steps (a whole number of chunks) and at least 2048 steps long
+        const int G = dstate >= 4 ? kSerialLanes : (int)dstate;
+        p.lanes_per_channel = G;
+        const int64_t ch_per_cta = ssm::lookback_channels_per_cta((int)dstate, G, in_dtype);
+        const int64_t groups = dim > 0 ? (dim + ch_per_cta - 1) / ch_per_cta : 1;
         const int64_t ctas_per_seg = groups * (batch > 0 ? batch : 1);
+        const int64_t target_ctas = kSMs * kLookbackCtasPerSM;
         const int64_t want = (target_ctas + ctas_per_seg - 1) / ctas_per_seg;
-        const int64_t chunk = ssm::kWarpScanChunk;
-        const int64_t min_seg = 8 * chunk;
+        const int64_t gran = ssm::kWarpScanChunk;
+        const int64_t min_seg = kLookbackMinSeg;
         int64_t seg_len = (seqlen + want - 1) / want;
-        seg_len = ((seg_len + chunk - 1) / chunk) * chunk;
+        seg_len = ((seg_len + gran - 1) / gran) * gran;
         if (seg_len < min_seg) seg_len = min_seg;
         p.seg_len = seg_len;
         p.n_seg = seqlen > 0 ? (seqlen + seg_len - 1) / seg_len : 1;
@@ -85,8 +100,8 @@ Plan plan_scan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int a
     return p;
 }
 
-size_t workspace_for(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int algo) {
-    Plan p = plan_scan(batch, dim, seqlen, dstate, algo);
+size_t workspace_for(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int algo, int in_dtype) {
+    Plan p = plan_scan(batch, dim, seqlen, dstate, algo, in_dtype);
     if (p.algo != SSM_ALGO_LOOKBACK) return 16;
     return ssm::lookback_workspace_bytes(batch, dim, (int)dstate, p.n_seg);
 }
@@ -132,7 +147,7 @@ int scan_impl(const void* u, const void* delta, const float* A, const void* B, c
                    overlap(h_last, bh, D, bd) || overlap(h_last, bh, delta_bias, bd)))
         return SSM_ERR_ALIAS;
 
-    Plan p = plan_scan(batch, dim, seqlen, dstate, algo);
+    Plan p = plan_scan(batch, dim, seqlen, dstate, algo, in_dtype);
     ScanArgs a;
     memset(&a, 0, sizeof(a));
     a.u = u; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z;
@@ -153,7 +168,8 @@ int scan_impl(const void* u, const void* delta, const float* A, const void* B, c
         if (!aligned(workspace, 16)) return SSM_ERR_ALIGN;
         a.workspace = workspace;
         if (cudaMemsetAsync(workspace, 0, need, s) != cudaSuccess) return SSM_ERR_LAUNCH;
-        return ssm::launch_scan_lookback(a, s) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+        return ssm::launch_scan_serial_lookback(a, p.lanes_per_channel, s) == cudaSuccess ? SSM_OK
+                                                                                       : SSM_ERR_LAUNCH;
     }
     if (p.algo == SSM_ALGO_THREAD) {
         const cudaError_t e = dstate == 1 ? ssm::launch_scan_scalar(a, s)
@@ -192,9 +208,15 @@ const char* ssm_status_string(int status) {
 size_t ssm_scan_workspace_size(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate) {
     if (batch < 0 || dim < 0 || seqlen < 0 || !valid_n(dstate)) return 16;
     if (mul(mul(batch, dim), seqlen) < 0) return 16;
-    size_t a = workspace_for(batch, dim, seqlen, dstate, SSM_ALGO_AUTO);
-    size_t b = workspace_for(batch, dim, seqlen, dstate, SSM_ALGO_LOOKBACK);
-    return a > b ? a : b;
+    // the largest need over the algorithms and input dtypes (the look-back's
+    // segments depend on how many channels one CTA holds, which depends on dtype)
+    size_t need = 16;
+    for (int dt : {(int)SSM_F32, (int)SSM_BF16})
+        for (int algo : {(int)SSM_ALGO_AUTO, (int)SSM_ALGO_LOOKBACK}) {
+            const size_t w = workspace_for(batch, dim, seqlen, dstate, algo, dt);
+            if (w > need) need = w;
+        }
+    return need;
 }
 
 int ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
@@ -277,6 +299,11 @@ int ssm_state_update(float* state, const void* x, const void* delta, const float
     a.delta_bias = delta_bias; a.y = y; a.batch = batch; a.dim = dim; a.dstate = (int)dstate;
     a.softplus = softplus ? 1 : 0; a.in_dtype = in_dtype; a.out_dtype = out_dtype;
     a.vec = dstate >= 4 && aligned(A, 16) && aligned(B, 4 * ei) && aligned(C, 4 * ei);
+    // bulk copies need 16-byte aligned addresses and sizes: the per-row vectors
+    // (dim values of x, delta, z; dstate values of B, C) must be whole 16-byte units
+    a.tma = dstate >= 8 && a.vec && aligned(state, 16) && aligned(x, 16) && aligned(delta, 16) &&
+            (!z || aligned(z, 16)) && aligned(B, 16) && aligned(C, 16) && (dim * (int64_t)ei) % 16 == 0 &&
+            (dstate * (int64_t)ei) % 16 == 0;
     return ssm::launch_state_update(a, (cudaStream_t)stream) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
 

@@ -131,10 +131,202 @@ __global__ void __launch_bounds__(kThreads) state_update_kernel(DecodeArgs a) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Streaming variant (dstate 8 or 16, bf16/fp32 inputs with 16-byte aligned rows):
+// a persistent CTA owns kTileCh channels and walks batch rows (its A, bias and D
+// stay in registers); per row, the tile's
+// state (kTileCh x N fp32, contiguous), its x, delta, z (kTileCh values each) and
+// the row's B and C are fetched into a kStages-deep shared-memory ring with bulk
+// asynchronous copies (cp.async.bulk, completion counted on an mbarrier), so the
+// bytes in flight are set by the ring, not by registers: with 4 stages and ~4 CTAs
+// per SM about 70 KB per SM are outstanding, enough to cover HBM latency.
+// Threads read their 4 states from shared memory, update them and store them
+// straight back to global memory with 16-byte stores. Every mbarrier wait is
+// bounded; on expiry the CTA records the failure in g_decode_status, waits (again
+// bounded) for its own copies in flight and returns.
+// ---------------------------------------------------------------------------
+constexpr int kTmaThreads = 256;
+constexpr int kStages = 4;
+constexpr uint32_t kWaitLimit = 1u << 24;
+
+__device__ int g_decode_status;   // 0, or the line of a wait that ran out of budget
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+// true once the phase with this parity has completed
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kWaitLimit; i++)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+// global -> shared bulk copy of `bytes` (a multiple of 16, both addresses 16-byte
+// aligned), completion counted on `bar`
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+template <int N, typename Tin>
+struct TmaTile {
+    static constexpr int G = N / 4;                    // lanes per channel (4 states each)
+    static constexpr int kTileCh = kTmaThreads / G;    // channels per tile
+    float state[kTileCh * N];
+    Tin x[kTileCh], dl[kTileCh], z[kTileCh];
+    Tin B[N], C[N];
+};
+
+template <int N, typename Tin, typename Tout>
+__global__ void __launch_bounds__(kTmaThreads) state_update_tma_kernel(DecodeArgs a) {
+    using Tile = TmaTile<N, Tin>;
+    constexpr int G = Tile::G, kTileCh = Tile::kTileCh;
+    using Dec = Decay<sizeof(Tin) == 4>;
+    __shared__ __align__(128) Tile s_tile[kStages];
+    __shared__ __align__(8) uint64_t s_full[kStages];
+
+    // CTA (range r, row offset q) owns channels [r*kTileCh, (r+1)*kTileCh) of batch
+    // rows q, q + R, q + 2R, ... (gridDim.x = ranges * R): its A, bias and D stay in
+    // registers for the whole walk
+    const int64_t ranges = (a.dim + kTileCh - 1) / kTileCh;
+    const int64_t R = gridDim.x / ranges;
+    const int64_t r = blockIdx.x % ranges, q = blockIdx.x / ranges;
+    const int64_t d0 = r * kTileCh;
+    const int64_t nch = min((int64_t)kTileCh, a.dim - d0);
+    const int64_t n_rows = q < a.batch ? (a.batch - 1 - q) / R + 1 : 0;   // rows of this CTA
+    const int c = threadIdx.x / G, j = threadIdx.x % G;
+    const int64_t d = d0 + c;
+    const bool ok = c < nch;
+    const Tin* zp = static_cast<const Tin*>(a.z);
+    Tout* y = static_cast<Tout*>(a.y);
+    float Av[4] = {0.f, 0.f, 0.f, 0.f};
+    float bias = 0.f, Dd = 0.f;
+    if (ok) {
+        const float4 A4 = *reinterpret_cast<const float4*>(a.A + d * N + j * 4);
+        Av[0] = A4.x; Av[1] = A4.y; Av[2] = A4.z; Av[3] = A4.w;
+        bias = a.delta_bias ? a.delta_bias[d] : 0.f;
+        Dd = a.D ? a.D[d] : 0.f;
+    }
+
+    // the copies of this CTA's k-th row (thread 0 only)
+    auto issue = [&](int64_t k) {
+        if (k >= n_rows) return;
+        const int st = (int)(k % kStages);
+        const int64_t b = q + k * R;
+        const uint32_t sb = (uint32_t)(nch * N * 4), xb = (uint32_t)(nch * sizeof(Tin)),
+                       bb = (uint32_t)(N * sizeof(Tin));
+        const uint32_t total = sb + xb * (zp ? 3u : 2u) + 2u * bb;
+        Tile& t = s_tile[st];
+        mbar_expect_tx(&s_full[st], total);
+        bulk_g2s(t.state, a.state + (b * a.dim + d0) * N, sb, &s_full[st]);
+        bulk_g2s(t.x, static_cast<const Tin*>(a.x) + b * a.dim + d0, xb, &s_full[st]);
+        bulk_g2s(t.dl, static_cast<const Tin*>(a.delta) + b * a.dim + d0, xb, &s_full[st]);
+        if (zp) bulk_g2s(t.z, zp + b * a.dim + d0, xb, &s_full[st]);
+        bulk_g2s(t.B, static_cast<const Tin*>(a.B) + b * N, bb, &s_full[st]);
+        bulk_g2s(t.C, static_cast<const Tin*>(a.C) + b * N, bb, &s_full[st]);
+    };
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < kStages; st++) mbar_init(&s_full[st], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        for (int k = 0; k < kStages; k++) issue(k);
+
+    bool failed = false;
+    int64_t k = 0;
+    for (; k < n_rows; k++) {
+        const int st = (int)(k % kStages);
+        const uint32_t parity = (uint32_t)((k / kStages) & 1);
+        // a wait that runs out of budget in any thread stops the whole CTA (the
+        // decision has to be uniform: the loop holds __syncthreads)
+        const bool got = mbar_wait(&s_full[st], parity);
+        if (__syncthreads_or(!got)) {
+            failed = true;
+            break;
+        }
+        const Tile& t = s_tile[st];
+        const int64_t b = q + k * R;
+        float acc = 0.f, xt = 0.f, zt = 0.f;
+        if (ok) {
+            const float4 s4 = *reinterpret_cast<const float4*>(&t.state[c * N + j * 4]);
+            float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+            xt = to_f32(t.x[c]);
+            const float v = to_f32(t.dl[c]) + bias;
+            const float dt = a.softplus ? softplus(v) : v;
+            const float dts = dt * Dec::scale, dtx = dt * xt;
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const float Bv = to_f32(t.B[j * 4 + i]), Cv = to_f32(t.C[j * 4 + i]);
+                sv[i] = Dec::step(Dec::make(dts * Av[i]), sv[i], dtx * Bv);
+                acc = fmaf(Cv, sv[i], acc);
+            }
+            *reinterpret_cast<float4*>(a.state + (b * a.dim + d) * N + j * 4) =
+                make_float4(sv[0], sv[1], sv[2], sv[3]);
+            if (zp) zt = to_f32(t.z[c]);
+        }
+#pragma unroll
+        for (int off = 1; off < G; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (ok && j == 0) {
+            float yv = fmaf(Dd, xt, acc);
+            if (zp) yv *= silu(zt);
+            y[b * a.dim + d] = from_f32<Tout>(yv);
+        }
+        __syncthreads();   // every thread is done with stage st
+        if (threadIdx.x == 0) issue(k + kStages);
+    }
+    if (failed) {
+        // record, then drain this CTA's copies still in flight before leaving
+        if (threadIdx.x == 0) atomicExch(&g_decode_status, __LINE__);
+        for (int64_t kk = k; kk < k + kStages && kk < n_rows; kk++)
+            (void)mbar_wait(&s_full[kk % kStages], (uint32_t)((kk / kStages) & 1));
+    }
+}
+
 template <int N, typename Tin, typename Tout>
 cudaError_t launch_n(const DecodeArgs& a, cudaStream_t s) {
     constexpr int G = N < 4 ? 1 : N / 4;
     if (a.batch == 0 || a.dim == 0) return cudaSuccess;
+    if constexpr (N >= 8) {
+        if (a.tma) {
+            // persistent: one wave of CTAs
+            static const int64_t wave = [] {
+                int dev = 0, sms = 148, per_sm = 1;
+                if (cudaGetDevice(&dev) == cudaSuccess)
+                    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, state_update_tma_kernel<N, Tin, Tout>,
+                                                              kTmaThreads, 0);
+                return (int64_t)(sms > 0 ? sms : 148) * (per_sm > 0 ? per_sm : 1);
+            }();
+            // ranges x R CTAs: R row offsets per channel range, about one wave in all
+            const int64_t ranges = (a.dim + TmaTile<N, Tin>::kTileCh - 1) / TmaTile<N, Tin>::kTileCh;
+            int64_t R = wave / ranges;
+            if (R < 1) R = 1;
+            if (R > a.batch) R = a.batch;
+            const int64_t grid = ranges * R;
+            if (grid > ((int64_t)1 << 31) - 1) return cudaErrorInvalidValue;
+            state_update_tma_kernel<N, Tin, Tout><<<(unsigned)grid, kTmaThreads, 0, s>>>(a);
+            return cudaGetLastError();
+        }
+    }
     const int64_t bx = (a.dim * G + kThreads - 1) / kThreads;
     // enough CTAs to fill the GPU several times over, each thread kRows rows deep
     int64_t by = (a.batch + kRows - 1) / kRows;

@@ -1,32 +1,39 @@
-// kernels_serial.cu -- time-serial selective scan for many channels: each channel's
-// N-wide state is split over G lanes (G = 1, 2 or 4) and every lane walks time
-// step by step.
+// kernels_serial.cu -- time-serial selective scan for many channels: each lane owns
+// a few states of K channels (K = 1 or 2) and walks time step by step; plus the
+// look-back variant that splits time into segments for long sequences.
 //
 // Operation (Mamba SSM complete guide (youngju.dev), section 5: selective_scan,
 // with MambaBlock.ssm's softplus(dt_proj) and MambaBlock.forward's silu(z) gate):
 //     h_t = exp(dt_t A) h_{t-1} + dt_t B_t u_t,  y_t = C_t . h_t + D u_t,  y_t *= silu(z_t)
 //
-// Why time-serial: on B300 the N = 16 bf16 scan is bound by the SFU (ex2, 32 per
-// clock per SM) and by instruction issue (4 warp-instructions per clock per SM),
-// not by HBM: every (t, n) element needs one exp and four FP32 operations, two
-// bytes of HBM traffic per element feed it. With batch * dim in the tens of
+// Why time-serial: on B300 the N = 16 bf16 scan is bound by the SM, not by HBM:
+// every (t, n) element needs one exp (SFU ex2, 32 per clock per SM) and four FP32
+// operations, and two bytes of HBM traffic feed it. With batch * dim in the tens of
 // thousands there is enough independent work without splitting time, and walking
 // time serially is the formulation with the fewest instructions per element:
 //     e = dt*A (packed mul), a = ex2(e), bB = (dt*u)*B (packed mul),
 //     h = a*h + bB (packed fma), acc += C*h (packed fma)
-// -- 2 packed FP32 instructions, 1 SFU instruction and 1/2 shared-memory load per
-// element, no shuffle scan, no second pass.
+// -- 2 packed FP32 instructions and 1 SFU instruction per element, no shuffle
+// scan, no second pass.
 //
-// Work layout. A CTA holds W = 4 warps; warp w owns CPW = 32/G consecutive
-// channels of batch row b; lane (g, j) owns channel g's states
-// [j*NPL, (j+1)*NPL), NPL = N/G. Time goes in chunks of T = 32 steps:
+// The operands B_tn and C_tn are the same for every channel of a batch row and
+// come from shared memory. A 16-byte shared load is served in four quarter-warp
+// phases, so one wavefront of shared-memory bandwidth delivers 4 values to 8
+// lanes; at one state-channel per lane that bandwidth, not the SFU, limits the
+// scan (measured: removing the B/C loads made the kernel 1.5x faster while
+// removing every exp changed nothing). Each lane therefore owns the same states
+// of K = 2 channels on the bf16 path: one B/C load feeds 2K elements.
+//
+// Work layout. A CTA holds W = 4 warps; warp w owns CPW = 32 K / G consecutive
+// channels of batch row b; lane (p, j) owns states [j*NPL, (j+1)*NPL), NPL = N/G,
+// of channels K*p .. K*p + K-1. Time goes in chunks of T steps:
 //   A. prologue, one lane per (channel, 16 bytes of consecutive steps): the
 //      per-step scalars of the chunk (loaded one chunk ahead into registers) give
-//      dt = softplus(delta + bias) and dt*u, written to shared memory DB[ch][t];
-//   B. recurrence, lane (g, j): per step reads DB[g][t] (a broadcast within the
-//      channel's lanes) and the B and C values of its states from the chunk's
-//      B/C tile (fp32, [t][n], one tile per CTA: all warps share the batch row),
-//      updates its states and writes its partial C.h to P[t][lane];
+//      dt = softplus(delta + bias) and dt*u, written to shared memory; the K
+//      channels of a lane are adjacent there, so one load gives a step for all K;
+//   B. recurrence, lane (p, j): per step the (dt, dt*u) of its K channels and the
+//      B and C values of its states (fp32 [t][n] tile, one per CTA: all warps
+//      share the batch row); writes its partial C.h sums, 4 steps per store;
 //   C. epilogue, same ownership as A: y = sum of the G partials + D*u, times
 //      silu(z), stored with 16-byte stores.
 // The B/C tile is double-buffered and filled from registers loaded one chunk
@@ -35,9 +42,9 @@
 // Precision. bf16 inputs (tolerance 2e-3): decay factors on the SFU (Decay<false>),
 // dt via softplus(x) = ln2 * log2(1 + 2^(x*log2 e)) with SFU ex2/lg2 -- the kernel
 // keeps dtl = dt*log2(e) (the ex2 argument scale) and folds ln2 into the staged B
-// tile. fp32 inputs (tolerance 1e-5): accurate softplus (expf, log1pf), decays as
-// expm1 (Decay<true>), and the state anchored at each chunk start: h = (hhi + hlo)
-// + dlt, where the anchor is an unevaluated fp32 pair and dlt the change since the
+// tile. fp32 inputs (tolerance 1e-5): accurate softplus, decays as expm1
+// (Decay<true>), and the state anchored at each chunk start: h = (hhi + hlo) +
+// dlt, where the anchor is an unevaluated fp32 pair and dlt the change since the
 // chunk start, so a slowly decaying large state is rounded once per output, not
 // once per step.
 #include <string.h>
@@ -48,7 +55,11 @@
 namespace ssm {
 namespace {
 
-constexpr int kWarps = 4;
+// warps per CTA (a build option; all warps of a CTA share one batch row's B/C tile)
+#ifndef SSM_SERIAL_WARPS
+#define SSM_SERIAL_WARPS 4
+#endif
+constexpr int kWarps = SSM_SERIAL_WARPS;
 constexpr int kThreads = 32 * kWarps;
 
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
@@ -67,22 +78,34 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
     return d;
 }
 
+// Channels per lane a kernel may use: 2 on the bf16 path when a lane holds 2 to 4
+// states (more would not fit the registers), else 1. The serial kernel keeps 1: at
+// Mamba-130M sizes (12,288 channels) it needs every warp it can get to hide
+// latency, and 2 channels per lane halves the warps (measured slower); the
+// look-back kernel, whose segments supply the parallelism, takes 2.
 template <int N, int G, typename Tin>
+constexpr int max_k() { return (sizeof(Tin) == 2 && N / G >= 2 && N / G <= 4) ? 2 : 1; }
+
+template <int N, int G, typename Tin, int K_>
 struct SerialCfg {
-    // time steps per chunk; with one lane per channel (G = 1) a warp owns 32
-    // channels and a short chunk keeps the prologue's register footprint small
-    static constexpr int kT = G == 1 ? 8 : 32;
+    static constexpr int K = K_;
+    static_assert(K == 1 || K == max_k<N, G, Tin>(), "unsupported channels per lane");
+    // time steps per chunk: short enough that the prologue's registers and the
+    // tiles (static shared memory, at most 48 KB) stay small -- a warp owns 32
+    // channels at G = 1 and 32 K / G at G >= 2
+    static constexpr int kT = G == 1 ? 8 : (K == 2 ? 16 : 32);
     static constexpr int NPL = N / G;                 // states per lane
-    static constexpr int CPW = 32 / G;                // channels per warp
+    static constexpr int CPW = 32 * K / G;            // channels per warp
     static constexpr int V = 16 / (int)sizeof(Tin);   // steps per 16-byte vector
     static constexpr int VPR = kT / V;                // vectors per (channel, chunk) row
     static constexpr int PV = CPW * VPR / 32;         // prologue vectors per lane per tensor
     static constexpr int BCV = 2 * N * VPR;           // vectors per B+C tile
-    static constexpr int BCPT = (BCV + kThreads - 1) / kThreads;
-    static constexpr int DBS = kT + 2;                // row (float2) of the DB tile: 16-byte rows
+    // row of the (dt, dt*u) tile in floats: kT steps x K channels x 2, padded by
+    // 16 bytes to keep rows 16-byte aligned and spread a warp's rows over the banks
+    static constexpr int DBS = 2 * K * kT + 4;
     static constexpr int PS = 32 + 1;                 // row (float4) of the partials tile
     static_assert(PV >= 1 && CPW * VPR % 32 == 0, "chunk must cover the warp's channels");
-    static_assert(kT % V == 0, "chunk must be whole vectors");
+    static_assert(kT % V == 0 && kT % 4 == 0, "chunk must be whole vectors and step groups");
 };
 
 // element i % 2 of a pair
@@ -133,29 +156,61 @@ __device__ __forceinline__ void store_steps(Tout* p, const float* v) {
     }
 }
 
-template <int N, int G, typename Tin, typename Tout, bool kVec>
-__global__ void __launch_bounds__(kThreads) serial_scan_kernel(ScanArgs a) {
-    using Cfg = SerialCfg<N, G, Tin>;
-    constexpr int NPL = Cfg::NPL, CPW = Cfg::CPW, V = Cfg::V, VPR = Cfg::VPR, PV = Cfg::PV, kT = Cfg::kT;
-    constexpr bool kAcc = sizeof(Tin) == 4;
-    using Dec = Decay<kAcc>;
-    // separate arrays (not one struct) so the compiler sees that the partial-sum
-    // stores cannot alias the operand loads of later steps
-    __shared__ __align__(16) float s_bc[2][kT][2 * N];              // [buf][t][B n.. | C n..]
-    __shared__ __align__(16) float2 s_db[kWarps][CPW][Cfg::DBS];    // (dt*scale, dt*scale*u)
-    __shared__ __align__(16) float4 s_p[kWarps][kT / 4][Cfg::PS];   // partial C.h of 4 steps per lane
+// Per-lane recurrence state of the serial kernels, for K channels: the lane's NPL
+// states in pairs (the packed f32x2 operands); on the fp32 path also the chunk
+// anchor (hhi, hlo) and dlt, the change since the chunk start; for the aggregate
+// pass the sum of dt*scale over the pass (Kahan-compensated on the fp32 path).
+template <int K, int NPL>
+struct LaneState {
+    static constexpr int NP2 = (NPL + 1) / 2;
+    float2 h2[K][NP2];
+    float hhi[K][NPL], hlo[K][NPL], dlt[K][NPL];
+    float sdt[K], sdt_c[K];
+};
 
+// The chunk tiles of a CTA (separate arrays, not one struct, so the compiler sees
+// that the partial-sum stores cannot alias the operand loads of later steps).
+template <int N, int G, typename Tin, int K>
+struct Tiles {
+    using Cfg = SerialCfg<N, G, Tin, K>;
+    float (*bc)[Cfg::kT][2 * N];                  // [buf][t][B n.. | C n..]
+    float (*db)[Cfg::CPW / Cfg::K][Cfg::DBS];     // [warp][lane group][t][K][dt, dt*u]
+    float4 (*p)[Cfg::K][Cfg::kT / 4][Cfg::PS];    // [warp][k][t/4][lane]: partial C.h
+};
+
+template <int N, int G, int K>
+using A2Arr = float2[K][LaneState<1, N / G>::NP2];
+template <int N, int G, int K>
+using LaneStateT = LaneState<K, N / G>;
+
+// One pass of the serial scan over steps [tb, te) of batch row b, for the warp's
+// channels d_warp0 .. d_warp0 + CPW - 1, continuing the lane state S.
+//   kFull:  the whole operation; y is written for steps [tb, te).
+//   !kFull: the aggregate pass of the look-back: the state recurrence only (B
+//           staged, no C, no y) plus the sum of dt*scale, so the caller can form
+//           the map of the segment: decay exp(A * sum dt), offset = S.
+// Every thread of the CTA must call it with the same (tb, te).
+template <int N, int G, int K, typename Tin, typename Tout, bool kVec, bool kFull>
+__device__ __forceinline__ void serial_pass(const ScanArgs& a, int64_t b, int64_t d_warp0, int64_t tb,
+                                            int64_t te, const A2Arr<N, G, K>& A2, LaneStateT<N, G, K>& S,
+                                            const Tiles<N, G, Tin, K>& tl) {
+    using Cfg = SerialCfg<N, G, Tin, K>;
+    constexpr int NPL = Cfg::NPL, V = Cfg::V, VPR = Cfg::VPR, PV = Cfg::PV, kT = Cfg::kT;
+    constexpr int NP2 = LaneState<K, NPL>::NP2;
+    constexpr bool kAcc = sizeof(Tin) == 4;
+    constexpr int BCV = kFull ? Cfg::BCV : Cfg::BCV / 2;   // the aggregate pass stages B only
+    constexpr int BCPT = (BCV + kThreads - 1) / kThreads;
+    using Dec = Decay<kAcc>;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t b = blockIdx.y;
     const int64_t L = a.seqlen;
-    const int64_t d_warp0 = ((int64_t)blockIdx.x * kWarps + warp) * CPW;
     const Tin* u_base = static_cast<const Tin*>(a.u);
     const Tin* dl_base = static_cast<const Tin*>(a.delta);
     const Tin* z_base = static_cast<const Tin*>(a.z);
     const Tin* B_b = static_cast<const Tin*>(a.B) + b * N * L;
     const Tin* C_b = static_cast<const Tin*>(a.C) + b * N * L;
     Tout* y_base = static_cast<Tout*>(a.y);
-    const bool has_z = a.z != nullptr;
+    const bool has_z = kFull && a.z != nullptr;
+    const int p = lane / G, j = lane % G;
 
     // prologue/epilogue ownership: vector q of this lane covers channel pc[q],
     // steps pt[q] .. pt[q]+V of the chunk
@@ -171,31 +226,11 @@ __global__ void __launch_bounds__(kThreads) serial_scan_kernel(ScanArgs a) {
         chan_ok[q] = d < a.dim;
         bias[q] = (chan_ok[q] && a.delta_bias) ? a.delta_bias[d] : 0.f;
         if constexpr (!kAcc) bias[q] *= kLog2e;
-        Dd[q] = (chan_ok[q] && a.D) ? a.D[d] : 0.f;
-    }
-    // recurrence ownership
-    const int g = lane / G, j = lane % G;
-    const int64_t dR = d_warp0 + g;
-    const bool okR = dR < a.dim;
-    // A and the state in pairs (the packed f32x2 operands); the anchored form of
-    // the fp32 path also keeps (hhi, hlo, dlt) per state
-    constexpr int NP2 = (NPL + 1) / 2;
-    float2 A2[NP2], h2[NP2];
-    float hhi[NPL], hlo[NPL], dlt[NPL];
-#pragma unroll
-    for (int i = 0; i < NP2; i++) { A2[i] = make_float2(0.f, 0.f); h2[i] = make_float2(0.f, 0.f); }
-#pragma unroll
-    for (int i = 0; i < NPL; i++) {
-        lo_hi_ref(A2[i / 2], i) = okR ? a.A[dR * N + j * NPL + i] : 0.f;
-        const float h0 = (okR && a.h0) ? a.h0[(b * a.dim + dR) * N + j * NPL + i] : 0.f;
-        lo_hi_ref(h2[i / 2], i) = h0;
-        hhi[i] = h0;
-        hlo[i] = 0.f;
-        dlt[i] = 0.f;
+        Dd[q] = (kFull && chan_ok[q] && a.D) ? a.D[d] : 0.f;
     }
 
     // one chunk of raw inputs, loaded a chunk ahead
-    uint4 ru[PV], rd[PV], rz[PV], rbc[Cfg::BCPT];
+    uint4 ru[PV], rd[PV], rz[PV], rbc[BCPT];
     auto prefetch = [&](int64_t t0) {
 #pragma unroll
         for (int q = 0; q < PV; q++) {
@@ -205,31 +240,31 @@ __global__ void __launch_bounds__(kThreads) serial_scan_kernel(ScanArgs a) {
             rz[q] = load_raw<Tin, kVec>(has_z ? z_base + row : u_base, t0 + pt[q], L, chan_ok[q] && has_z);
         }
 #pragma unroll
-        for (int r = 0; r < Cfg::BCPT; r++) {
+        for (int r = 0; r < BCPT; r++) {
             const int v = r * kThreads + threadIdx.x;
             const int which = v / (N * VPR), rem = v % (N * VPR);
             const int n = rem / VPR, tt = (rem % VPR) * V;
-            rbc[r] = load_raw<Tin, kVec>((which ? C_b : B_b) + (int64_t)n * L, t0 + tt, L, v < Cfg::BCV);
+            rbc[r] = load_raw<Tin, kVec>((which ? C_b : B_b) + (int64_t)n * L, t0 + tt, L, v < BCV);
         }
     };
 
-    const int64_t n_chunks = (L + kT - 1) / kT;
-    if (n_chunks > 0) prefetch(0);
+    const int64_t n_chunks = te > tb ? (te - tb + kT - 1) / kT : 0;
+    if (n_chunks > 0) prefetch(tb);
     for (int64_t c = 0; c < n_chunks; c++) {
-        const int64_t t0 = c * kT;
+        const int64_t t0 = tb + c * kT;
         const int buf = (int)(c & 1);
         // B/C tile of this chunk: fp32, [t][n]; B carries ln2 on the bf16 path
 #pragma unroll
-        for (int r = 0; r < Cfg::BCPT; r++) {
+        for (int r = 0; r < BCPT; r++) {
             const int v = r * kThreads + threadIdx.x;
-            if (v < Cfg::BCV) {
+            if (v < BCV) {
                 const int which = v / (N * VPR), rem = v % (N * VPR);
                 const int n = rem / VPR, tt = (rem % VPR) * V;
                 float f[V];
                 unpack<Tin>(rbc[r], f);
-                const float s = (!kAcc && which == 0) ? kLn2 : 1.f;
+                const float sc = (!kAcc && which == 0) ? kLn2 : 1.f;
 #pragma unroll
-                for (int k = 0; k < V; k++) s_bc[buf][tt + k][which * N + n] = f[k] * s;
+                for (int k = 0; k < V; k++) tl.bc[buf][tt + k][which * N + n] = f[k] * sc;
             }
         }
         // A. prologue
@@ -241,6 +276,7 @@ __global__ void __launch_bounds__(kThreads) serial_scan_kernel(ScanArgs a) {
             unpack<Tin>(rd[q], fd);
             ku[q] = ru[q];
             kz[q] = rz[q];
+            float* dbrow = tl.db[warp][pc[q] / K] + (pc[q] % K) * 2;
 #pragma unroll
             for (int k = 0; k < V; k++) {
                 float dts;   // dt * Dec::scale
@@ -252,170 +288,441 @@ __global__ void __launch_bounds__(kThreads) serial_scan_kernel(ScanArgs a) {
                     const float xl = fmaf(fd[k], kLog2e, bias[q]);
                     dts = a.softplus ? (xl > 24.f ? xl : lg2(1.f + ex2(xl))) : xl;
                 }
-                if (t0 + pt[q] + k >= L || !chan_ok[q]) dts = 0.f;   // identity step past the end
-                s_db[warp][pc[q]][pt[q] + k] = make_float2(dts, dts * fu[k]);
+                if (t0 + pt[q] + k >= te || !chan_ok[q]) dts = 0.f;   // identity step past the end
+                *reinterpret_cast<float2*>(dbrow + (pt[q] + k) * 2 * K) = make_float2(dts, dts * fu[k]);
             }
         }
         if (c + 1 < n_chunks) prefetch(t0 + kT);
         __syncthreads();
 
-        // B. recurrence, in groups of 4 steps. Only the chained state updates of a
-        // group depend on the state; its loads and exps do not. The bf16 path is
-        // software-pipelined by hand: the loads and exps of group g+1 are issued
-        // before the chained updates of group g, so an in-order warp has the
-        // SFU/shared-memory latency of one group covered by the other's FMAs.
-        const float4* db = reinterpret_cast<const float4*>(s_db[warp][g]);   // 2 steps per load
+        // B. recurrence, in groups of 4 steps: the loads and exps of a group do not
+        // depend on the state, only its chained state updates do
+        const float* dbg = tl.db[warp][p];
+        // (dt*scale, dt*scale*u) of the lane's K channels for 4 steps
+        auto load_x = [&](int tg, float2 (&x)[4][K]) {
+            if constexpr (K == 2) {
+#pragma unroll
+                for (int st = 0; st < 4; st++) {
+                    const float4 v = *reinterpret_cast<const float4*>(dbg + (tg + st) * 4);
+                    x[st][0] = make_float2(v.x, v.y);
+                    x[st][K - 1] = make_float2(v.z, v.w);
+                }
+            } else {
+                const float4 x01 = *reinterpret_cast<const float4*>(dbg + tg * 2);
+                const float4 x23 = *reinterpret_cast<const float4*>(dbg + tg * 2 + 4);
+                x[0][0] = make_float2(x01.x, x01.y); x[1][0] = make_float2(x01.z, x01.w);
+                x[2][0] = make_float2(x23.x, x23.y); x[3][0] = make_float2(x23.z, x23.w);
+            }
+        };
         // B and C of this lane's states at step t, in pairs
         auto load_bc = [&](int t, float2* bq, float2* cq) {
-            const float* bc = s_bc[buf][t];
+            const float* bc = tl.bc[buf][t];
             if constexpr (NPL % 4 == 0) {
 #pragma unroll
                 for (int i = 0; i < NPL; i += 4) {
                     const float4 vb = *reinterpret_cast<const float4*>(bc + j * NPL + i);
-                    const float4 vc = *reinterpret_cast<const float4*>(bc + N + j * NPL + i);
                     bq[i / 2] = make_float2(vb.x, vb.y); bq[i / 2 + 1] = make_float2(vb.z, vb.w);
-                    cq[i / 2] = make_float2(vc.x, vc.y); cq[i / 2 + 1] = make_float2(vc.z, vc.w);
+                    if constexpr (kFull) {
+                        const float4 vc = *reinterpret_cast<const float4*>(bc + N + j * NPL + i);
+                        cq[i / 2] = make_float2(vc.x, vc.y); cq[i / 2 + 1] = make_float2(vc.z, vc.w);
+                    }
                 }
             } else if constexpr (NPL == 2) {
                 bq[0] = *reinterpret_cast<const float2*>(bc + j * 2);
-                cq[0] = *reinterpret_cast<const float2*>(bc + N + j * 2);
+                if constexpr (kFull) cq[0] = *reinterpret_cast<const float2*>(bc + N + j * 2);
             } else {
                 bq[0] = make_float2(bc[j], 0.f);
-                cq[0] = make_float2(bc[N + j], 0.f);
+                if constexpr (kFull) cq[0] = make_float2(bc[N + j], 0.f);
             }
         };
-        auto load_x = [&](int tg, float2* x) {
-            const float4 x01 = db[tg / 2], x23 = db[tg / 2 + 1];
-            x[0] = make_float2(x01.x, x01.y); x[1] = make_float2(x01.z, x01.w);
-            x[2] = make_float2(x23.x, x23.y); x[3] = make_float2(x23.z, x23.w);
-        };
-        if constexpr (!kAcc && NPL % 2 == 0) {
-            // operands of one group, ready for its chained updates
-            struct Stage {
-                float2 an[4][NP2], bn[4][NP2], cq[4][NP2];
-            };
-            auto stage = [&](int tg, Stage& S) {
-                float2 x[4];
-                load_x(tg, x);
-#pragma unroll
-                for (int st = 0; st < 4; st++) {
-                    float2 bq[NP2];
-                    load_bc(tg + st, bq, S.cq[st]);
-                    const float2 dtl2 = make_float2(x[st].x, x[st].x), bu2 = make_float2(x[st].y, x[st].y);
-#pragma unroll
-                    for (int i = 0; i < NP2; i++) {
-                        const float2 e = mul2(dtl2, A2[i]);
-                        S.an[st][i] = make_float2(ex2(e.x), ex2(e.y));
-                        S.bn[st][i] = mul2(bu2, bq[i]);
-                    }
-                }
-            };
-            Stage cur, nxt;
-            stage(0, cur);
-#pragma unroll
-            for (int tg = 0; tg < kT; tg += 4) {
-                if (tg + 4 < kT) stage(tg + 4, nxt);
-                float acc[4];
-#pragma unroll
-                for (int st = 0; st < 4; st++) {
-                    float2 acc2 = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int i = 0; i < NP2; i++) {
-                        h2[i] = fma2(cur.an[st][i], h2[i], cur.bn[st][i]);
-                        acc2 = fma2(cur.cq[st][i], h2[i], acc2);
-                    }
-                    acc[st] = acc2.x + acc2.y;
-                }
-                s_p[warp][tg / 4][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                if (tg + 4 < kT) cur = nxt;
+        // sum of dt*scale for the aggregate decay (Kahan on the fp32 path)
+        auto add_dt = [&](int k, float v) {
+            if constexpr (kAcc) {
+                const float yk = v - S.sdt_c[k];
+                const float tk = S.sdt[k] + yk;
+                S.sdt_c[k] = (tk - S.sdt[k]) - yk;
+                S.sdt[k] = tk;
+            } else {
+                S.sdt[k] += v;
             }
-        } else {
+        };
 #pragma unroll
-            for (int tg = 0; tg < kT; tg += 4) {
-                float2 x[4];
-                load_x(tg, x);
-                float2 bq[4][NP2], cq[4][NP2];
+        for (int tg = 0; tg < kT; tg += 4) {
+            float2 x[4][K];
+            load_x(tg, x);
+            float2 bq[4][NP2], cq[4][NP2];
 #pragma unroll
-                for (int st = 0; st < 4; st++) load_bc(tg + st, bq[st], cq[st]);
-                float an[4][NPL];
+            for (int st = 0; st < 4; st++) load_bc(tg + st, bq[st], cq[st]);
+            if constexpr (!kFull) {
 #pragma unroll
                 for (int st = 0; st < 4; st++)
 #pragma unroll
-                    for (int i = 0; i < NPL; i++) an[st][i] = Dec::make(x[st].x * lo_hi(A2[i / 2], i));
-                float acc[4];
+                    for (int k = 0; k < K; k++) add_dt(k, x[st][k].x);
+            }
+            float acc[K][4];
+            if constexpr (!kAcc && NPL % 2 == 0) {
+                float2 an[4][K][NP2], bn[4][K][NP2];
 #pragma unroll
-                for (int st = 0; st < 4; st++) {
-                    acc[st] = 0.f;
+                for (int st = 0; st < 4; st++)
 #pragma unroll
-                    for (int i = 0; i < NPL; i++) {
-                        const float bv = x[st].y * lo_hi(bq[st][i / 2], i);
-                        float& hi = lo_hi_ref(h2[i / 2], i);
-                        if constexpr (kAcc) {
-                            dlt[i] += fmaf(an[st][i], hi, bv);
-                            hi = hhi[i] + (dlt[i] + hlo[i]);
-                        } else {
-                            hi = Dec::step(an[st][i], hi, bv);
+                    for (int k = 0; k < K; k++) {
+                        const float2 dtl2 = make_float2(x[st][k].x, x[st][k].x);
+                        const float2 bu2 = make_float2(x[st][k].y, x[st][k].y);
+#pragma unroll
+                        for (int i = 0; i < NP2; i++) {
+                            const float2 e = mul2(dtl2, A2[k][i]);
+                            an[st][k][i] = make_float2(ex2(e.x), ex2(e.y));
+                            bn[st][k][i] = mul2(bu2, bq[st][i]);
                         }
-                        acc[st] = fmaf(lo_hi(cq[st][i / 2], i), hi, acc[st]);
                     }
-                }
-                s_p[warp][tg / 4][lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+#pragma unroll
+                for (int st = 0; st < 4; st++)
+#pragma unroll
+                    for (int k = 0; k < K; k++) {
+                        float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int i = 0; i < NP2; i++) {
+                            S.h2[k][i] = fma2(an[st][k][i], S.h2[k][i], bn[st][k][i]);
+                            if constexpr (kFull) acc2 = fma2(cq[st][i], S.h2[k][i], acc2);
+                        }
+                        acc[k][st] = acc2.x + acc2.y;
+                    }
+            } else {
+#pragma unroll
+                for (int st = 0; st < 4; st++)
+#pragma unroll
+                    for (int k = 0; k < K; k++) {
+                        acc[k][st] = 0.f;
+#pragma unroll
+                        for (int i = 0; i < NPL; i++) {
+                            const float an = Dec::make(x[st][k].x * lo_hi(A2[k][i / 2], i));
+                            const float bv = x[st][k].y * lo_hi(bq[st][i / 2], i);
+                            float& hi = lo_hi_ref(S.h2[k][i / 2], i);
+                            if constexpr (kAcc) {
+                                S.dlt[k][i] += fmaf(an, hi, bv);
+                                hi = S.hhi[k][i] + (S.dlt[k][i] + S.hlo[k][i]);
+                            } else {
+                                hi = Dec::step(an, hi, bv);
+                            }
+                            if constexpr (kFull) acc[k][st] = fmaf(lo_hi(cq[st][i / 2], i), hi, acc[k][st]);
+                        }
+                    }
+            }
+            if constexpr (kFull) {
+#pragma unroll
+                for (int k = 0; k < K; k++)
+                    tl.p[warp][k][tg / 4][lane] = make_float4(acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
             }
         }
         if constexpr (kAcc) {
             // re-anchor: (hhi, hlo) <- the exact sum of the pair and dlt
 #pragma unroll
-            for (int i = 0; i < NPL; i++) {
-                two_sum(hhi[i], dlt[i] + hlo[i], hhi[i], hlo[i]);
-                dlt[i] = 0.f;
-            }
+            for (int k = 0; k < K; k++)
+#pragma unroll
+                for (int i = 0; i < NPL; i++) {
+                    two_sum(S.hhi[k][i], S.dlt[k][i] + S.hlo[k][i], S.hhi[k][i], S.hlo[k][i]);
+                    S.dlt[k][i] = 0.f;
+                }
         }
-        __syncwarp();
-
-        // C. epilogue: y = (sum of the G partials + D*u) * silu(z)
+        if constexpr (kFull) {
+            __syncwarp();
+            // C. epilogue: y = (sum of the G partials + D*u) * silu(z)
 #pragma unroll
-        for (int q = 0; q < PV; q++) {
-            float fu[V], yv[V];
-            unpack<Tin>(ku[q], fu);
+            for (int q = 0; q < PV; q++) {
+                float fu[V], yv[V];
+                unpack<Tin>(ku[q], fu);
 #pragma unroll
-            for (int k = 0; k < V; k++) yv[k] = fu[k] * Dd[q];
+                for (int k = 0; k < V; k++) yv[k] = fu[k] * Dd[q];
+                const int pk = pc[q] % K, pl = (pc[q] / K) * G;
 #pragma unroll
-            for (int jj = 0; jj < G; jj++) {
+                for (int jj = 0; jj < G; jj++) {
 #pragma unroll
-                for (int k = 0; k < V; k += 4) {
-                    const float4 p4 = s_p[warp][(pt[q] + k) / 4][pc[q] * G + jj];
-                    yv[k] += p4.x; yv[k + 1] += p4.y; yv[k + 2] += p4.z; yv[k + 3] += p4.w;
+                    for (int k = 0; k < V; k += 4) {
+                        const float4 p4 = tl.p[warp][pk][(pt[q] + k) / 4][pl + jj];
+                        yv[k] += p4.x; yv[k + 1] += p4.y; yv[k + 2] += p4.z; yv[k + 3] += p4.w;
+                    }
+                }
+                if (has_z) {
+                    float fz[V];
+                    unpack<Tin>(kz[q], fz);
+#pragma unroll
+                    for (int k = 0; k < V; k++) yv[k] *= silu_acc<kAcc>(fz[k]);
+                }
+                if (chan_ok[q]) {
+                    Tout* yrow = y_base + (b * a.dim + d_warp0 + pc[q]) * L;
+                    const int64_t tt = t0 + pt[q];
+                    if (kVec && tt + V <= te) {
+                        store_steps<Tout, V>(yrow + tt, yv);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < V; k++)
+                            if (tt + k < te) yrow[tt + k] = from_f32<Tout>(yv[k]);
+                    }
                 }
             }
-            if (has_z) {
-                float fz[V];
-                unpack<Tin>(kz[q], fz);
-#pragma unroll
-                for (int k = 0; k < V; k++) yv[k] *= silu_acc<kAcc>(fz[k]);
-            }
-            if (chan_ok[q]) {
-                Tout* yrow = y_base + (b * a.dim + d_warp0 + pc[q]) * L;
-                const int64_t tt = t0 + pt[q];
-                if (kVec && tt + V <= L) {
-                    store_steps<Tout, V>(yrow + tt, yv);
-                } else {
-#pragma unroll
-                    for (int k = 0; k < V; k++)
-                        if (tt + k < L) yrow[tt + k] = from_f32<Tout>(yv[k]);
-                }
-            }
         }
+        (void)ku; (void)kz;
     }
-    if (okR && a.h_last) {
+    // the next pass (or caller) reuses the tiles: all warps must be done with them
+    __syncthreads();
+}
+
+// The lane's A values (pairs) and states initialised to h[k] (anchor h, nothing
+// since), for its K channels dR[k] (valid while okR[k]).
+template <int N, int G, int K>
+__device__ __forceinline__ void lane_init(const ScanArgs& a, const int64_t* dR, const bool* okR, int j,
+                                          A2Arr<N, G, K>& A2, LaneStateT<N, G, K>& S, const float (*h)[N / G]) {
+    constexpr int NPL = N / G;
+#pragma unroll
+    for (int k = 0; k < K; k++) {
+#pragma unroll
+        for (int i = 0; i < LaneState<K, NPL>::NP2; i++) {
+            A2[k][i] = make_float2(0.f, 0.f);
+            S.h2[k][i] = make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < NPL; i++) {
+            lo_hi_ref(A2[k][i / 2], i) = okR[k] ? a.A[dR[k] * N + j * NPL + i] : 0.f;
+            const float h0 = h ? h[k][i] : 0.f;
+            lo_hi_ref(S.h2[k][i / 2], i) = h0;
+            S.hhi[k][i] = h0;
+            S.hlo[k][i] = 0.f;
+            S.dlt[k][i] = 0.f;
+        }
+        S.sdt[k] = 0.f;
+        S.sdt_c[k] = 0.f;
+    }
+}
+
+// State i of channel k of the lane (the anchored pair's sum on the fp32 path).
+template <int N, int G, int K, typename Tin>
+__device__ __forceinline__ float lane_state(const LaneStateT<N, G, K>& S, int k, int i) {
+    if constexpr (sizeof(Tin) == 4) return S.hhi[k][i] + S.hlo[k][i];
+    else return lo_hi(S.h2[k][i / 2], i);
+}
+
+template <int N, int G, typename Tin, typename Tout, bool kVec>
+__global__ void __launch_bounds__(kThreads) serial_scan_kernel(ScanArgs a) {
+    constexpr int K = 1;
+    using Cfg = SerialCfg<N, G, Tin, K>;
+    constexpr int NPL = Cfg::NPL, CPW = Cfg::CPW, kT = Cfg::kT;
+    __shared__ __align__(16) float s_bc[2][kT][2 * N];
+    __shared__ __align__(16) float s_db[kWarps][CPW / K][Cfg::DBS];
+    __shared__ __align__(16) float4 s_p[kWarps][K][kT / 4][Cfg::PS];
+    const Tiles<N, G, Tin, K> tl{s_bc, s_db, s_p};
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t b = blockIdx.y;
+    const int64_t d_warp0 = ((int64_t)blockIdx.x * kWarps + warp) * CPW;
+    const int p = lane / G, j = lane % G;
+    int64_t dR[K];
+    bool okR[K];
+    float h0[K][NPL];
+#pragma unroll
+    for (int k = 0; k < K; k++) {
+        dR[k] = d_warp0 + p * K + k;
+        okR[k] = dR[k] < a.dim;
 #pragma unroll
         for (int i = 0; i < NPL; i++)
-            a.h_last[(b * a.dim + dR) * N + j * NPL + i] = kAcc ? hhi[i] + hlo[i] : lo_hi(h2[i / 2], i);
+            h0[k][i] = (okR[k] && a.h0) ? a.h0[(b * a.dim + dR[k]) * N + j * NPL + i] : 0.f;
+    }
+    A2Arr<N, G, K> A2;
+    LaneStateT<N, G, K> S;
+    lane_init<N, G, K>(a, dR, okR, j, A2, S, h0);
+    serial_pass<N, G, K, Tin, Tout, kVec, true>(a, b, d_warp0, 0, a.seqlen, A2, S, tl);
+    if (a.h_last) {
+#pragma unroll
+        for (int k = 0; k < K; k++)
+            if (okR[k]) {
+#pragma unroll
+                for (int i = 0; i < NPL; i++)
+                    a.h_last[(b * a.dim + dR[k]) * N + j * NPL + i] = lane_state<N, G, K, Tin>(S, k, i);
+            }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Look-back kernel: time cut into segments of seg_len steps; one CTA per
+// (channel group, segment), taken in the order of an atomic ticket, segment-major,
+// so every segment a CTA waits on belongs to a CTA that has already started.
+// A CTA (1) runs the aggregate pass over its segment from a zero state, giving
+// each state's map over the segment: decay P = exp(A * sum dt) and offset H;
+// (2) publishes (P, H) with flag AGG; (3) walks back over earlier segments,
+// composing their maps until it meets a published inclusive prefix I (the state
+// at that segment's end), which gives its carry; (4) publishes its own inclusive
+// prefix with flag INCL; (5) runs the full pass from the carry. The last segment
+// publishes nothing and skips (1). Every wait is bounded: on expiry the kernel
+// records SSM_ERR_LOOKBACK_TIMEOUT in the workspace status word, continues with
+// what it has (publishing so that later segments finish too) and the output is
+// then unspecified.
+// Workspace (zeroed by the host on the stream): [0] int32 status, [1] uint32
+// ticket, [2..3] pad; then per (channel, segment) a descriptor: uint32 flag[N]
+// (flag[j] covers the states of lane j of the channel's lane group), float P[N],
+// H[N], I[N] (P in the Decay representation: the factor, or factor - 1 for fp32
+// inputs). Published values are never rewritten.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kFlagAgg = 1, kFlagIncl = 2;
+constexpr int kErrLookbackTimeout = -7;
+
+template <int N>
+struct LbDesc {
+    uint32_t flag[N];
+    float P[N];
+    float H[N];
+    float I[N];
+};
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+template <int N, int G, typename Tin, typename Tout, bool kVec>
+__global__ void __launch_bounds__(kThreads) serial_lookback_kernel(ScanArgs a) {
+    constexpr int K = max_k<N, G, Tin>();
+    using Cfg = SerialCfg<N, G, Tin, K>;
+    constexpr int NPL = Cfg::NPL, CPW = Cfg::CPW, kT = Cfg::kT;
+    constexpr bool kAcc = sizeof(Tin) == 4;
+    using Dec = Decay<kAcc>;
+    __shared__ __align__(16) float s_bc[2][kT][2 * N];
+    __shared__ __align__(16) float s_db[kWarps][CPW / K][Cfg::DBS];
+    __shared__ __align__(16) float4 s_p[kWarps][K][kT / 4][Cfg::PS];
+    __shared__ uint32_t s_ticket;
+    const Tiles<N, G, Tin, K> tl{s_bc, s_db, s_p};
+
+    int32_t* status = static_cast<int32_t*>(a.workspace);
+    uint32_t* ticket_ctr = reinterpret_cast<uint32_t*>(status + 1);
+    LbDesc<N>* desc = reinterpret_cast<LbDesc<N>*>(static_cast<char*>(a.workspace) + 16);
+
+    if (threadIdx.x == 0) s_ticket = atomicAdd(ticket_ctr, 1u);
+    __syncthreads();
+    const int64_t ch_per_cta = (int64_t)kWarps * CPW;
+    const int64_t groups = (a.dim + ch_per_cta - 1) / ch_per_cta;
+    const int64_t per_seg = groups * a.batch;
+    const int64_t tk = s_ticket;
+    const int64_t seg = tk / per_seg;
+    const int64_t rem = tk % per_seg;
+    const int64_t b = rem / groups;
+    const int64_t grp = rem % groups;
+    const int64_t ts = seg * a.seg_len;
+    const int64_t te = min(a.seqlen, ts + a.seg_len);
+    const bool last = seg + 1 == a.n_seg;
+    const bool publish = !last && seg != a.drop_segment;
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t d_warp0 = (grp * kWarps + warp) * CPW;
+    const int p = lane / G, j = lane % G;
+    int64_t dR[K], ch[K];
+    bool okR[K];
+#pragma unroll
+    for (int k = 0; k < K; k++) {
+        dR[k] = d_warp0 + p * K + k;
+        okR[k] = dR[k] < a.dim;
+        ch[k] = b * a.dim + dR[k];
+    }
+    A2Arr<N, G, K> A2;
+    LaneStateT<N, G, K> S;
+
+    // (1) the segment's map from a zero state
+    lane_init<N, G, K>(a, dR, okR, j, A2, S, nullptr);
+    float aggP[K][NPL], aggH[K][NPL];
+#pragma unroll
+    for (int k = 0; k < K; k++)
+#pragma unroll
+        for (int i = 0; i < NPL; i++) { aggP[k][i] = Dec::one(); aggH[k][i] = 0.f; }
+    if (!last) {
+        serial_pass<N, G, K, Tin, Tout, kVec, false>(a, b, d_warp0, ts, te, A2, S, tl);
+#pragma unroll
+        for (int k = 0; k < K; k++)
+#pragma unroll
+            for (int i = 0; i < NPL; i++) {
+                aggP[k][i] = Dec::make(S.sdt[k] * lo_hi(A2[k][i / 2], i));
+                aggH[k][i] = lane_state<N, G, K, Tin>(S, k, i);
+            }
+    }
+    // (2)-(4) per lane, for each of its channels' states
+    float carry[K][NPL];
+#pragma unroll
+    for (int k = 0; k < K; k++) {
+#pragma unroll
+        for (int i = 0; i < NPL; i++) carry[k][i] = 0.f;
+        if (!okR[k]) continue;
+        LbDesc<N>* mine = desc + ch[k] * a.n_seg + seg;
+        if (seg == 0) {
+#pragma unroll
+            for (int i = 0; i < NPL; i++) carry[k][i] = a.h0 ? a.h0[ch[k] * N + j * NPL + i] : 0.f;
+        } else {
+            if (publish) {
+#pragma unroll
+                for (int i = 0; i < NPL; i++) {
+                    mine->P[j * NPL + i] = aggP[k][i];
+                    mine->H[j * NPL + i] = aggH[k][i];
+                }
+                st_release(&mine->flag[j], kFlagAgg);
+            }
+            // (accP, accH): composed map of the segments strictly between the one
+            // inspected and this one
+            float accP[NPL], accH[NPL];
+#pragma unroll
+            for (int i = 0; i < NPL; i++) { accP[i] = Dec::one(); accH[i] = 0.f; }
+            bool timed_out = false;
+            for (int64_t s = seg - 1; s >= 0; s--) {
+                const LbDesc<N>* pd = desc + ch[k] * a.n_seg + s;
+                uint32_t f = ld_acquire(&pd->flag[j]);
+                uint32_t spins = 0;
+                while (f == 0 && spins < a.spin_limit) {
+                    ++spins;
+                    __nanosleep(64);
+                    f = ld_acquire(&pd->flag[j]);
+                }
+                if (f == 0) {
+#pragma unroll
+                    for (int i = 0; i < NPL; i++) carry[k][i] = accH[i];
+                    timed_out = true;
+                    break;
+                }
+                if (f == kFlagIncl) {
+#pragma unroll
+                    for (int i = 0; i < NPL; i++)
+                        carry[k][i] = Dec::step(accP[i], __ldcg(&pd->I[j * NPL + i]), accH[i]);
+                    break;
+                }
+#pragma unroll
+                for (int i = 0; i < NPL; i++) {
+                    accH[i] = Dec::step(accP[i], __ldcg(&pd->H[j * NPL + i]), accH[i]);
+                    accP[i] = Dec::mul(accP[i], __ldcg(&pd->P[j * NPL + i]));
+                }
+            }
+            if (timed_out) atomicExch(status, kErrLookbackTimeout);
+        }
+        // (4) the inclusive prefix: the state at this segment's end. On a timeout it
+        // is still published (with the wrong carry) so that later segments finish.
+        if (publish) {
+#pragma unroll
+            for (int i = 0; i < NPL; i++) mine->I[j * NPL + i] = Dec::step(aggP[k][i], carry[k][i], aggH[k][i]);
+            st_release(&mine->flag[j], kFlagIncl);
+        }
+    }
+    // (5) the full pass from the carry
+    lane_init<N, G, K>(a, dR, okR, j, A2, S, carry);
+    serial_pass<N, G, K, Tin, Tout, kVec, true>(a, b, d_warp0, ts, te, A2, S, tl);
+    if (last && a.h_last) {
+#pragma unroll
+        for (int k = 0; k < K; k++)
+            if (okR[k]) {
+#pragma unroll
+                for (int i = 0; i < NPL; i++) a.h_last[ch[k] * N + j * NPL + i] = lane_state<N, G, K, Tin>(S, k, i);
+            }
     }
 }
 
 template <int N, int G, typename Tin, typename Tout>
 cudaError_t launch_serial(const ScanArgs& a, cudaStream_t s) {
-    using Cfg = SerialCfg<N, G, Tin>;
+    using Cfg = SerialCfg<N, G, Tin, 1>;
     if (a.batch == 0 || a.dim == 0) return cudaSuccess;
     const int64_t ch_per_cta = (int64_t)kWarps * Cfg::CPW;
     dim3 grid((unsigned)((a.dim + ch_per_cta - 1) / ch_per_cta), (unsigned)a.batch);
@@ -424,39 +731,70 @@ cudaError_t launch_serial(const ScanArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+template <int N, int G, typename Tin, typename Tout>
+cudaError_t launch_lookback(const ScanArgs& a, cudaStream_t s) {
+    using Cfg = SerialCfg<N, G, Tin, max_k<N, G, Tin>()>;
+    if (a.batch == 0 || a.dim == 0) return cudaSuccess;
+    const int64_t ch_per_cta = (int64_t)kWarps * Cfg::CPW;
+    const int64_t ctas = ((a.dim + ch_per_cta - 1) / ch_per_cta) * a.batch * a.n_seg;
+    if (ctas > ((int64_t)1 << 31) - 1) return cudaErrorInvalidValue;
+    if (a.vec) serial_lookback_kernel<N, G, Tin, Tout, true><<<(unsigned)ctas, kThreads, 0, s>>>(a);
+    else serial_lookback_kernel<N, G, Tin, Tout, false><<<(unsigned)ctas, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
 // lanes per channel: 4 for N >= 4 (2 also built for N = 16), else N
-template <int N, typename Tin, typename Tout>
+template <int N, typename Tin, typename Tout, bool kLB>
 cudaError_t launch_g(const ScanArgs& a, int G, cudaStream_t s) {
     if constexpr (N >= 4) {
         if constexpr (N == 16) {
-            if (G == 2) return launch_serial<N, 2, Tin, Tout>(a, s);
+            if (G == 2) return kLB ? launch_lookback<N, 2, Tin, Tout>(a, s) : launch_serial<N, 2, Tin, Tout>(a, s);
         }
-        return launch_serial<N, 4, Tin, Tout>(a, s);
+        return kLB ? launch_lookback<N, 4, Tin, Tout>(a, s) : launch_serial<N, 4, Tin, Tout>(a, s);
     } else {
-        return launch_serial<N, N, Tin, Tout>(a, s);
+        return kLB ? launch_lookback<N, N, Tin, Tout>(a, s) : launch_serial<N, N, Tin, Tout>(a, s);
     }
 }
 
-template <typename Tin, typename Tout>
+template <typename Tin, typename Tout, bool kLB>
 cudaError_t launch_n(const ScanArgs& a, int G, cudaStream_t s) {
     switch (a.dstate) {
-        case 1: return launch_g<1, Tin, Tout>(a, G, s);
-        case 2: return launch_g<2, Tin, Tout>(a, G, s);
-        case 4: return launch_g<4, Tin, Tout>(a, G, s);
-        case 8: return launch_g<8, Tin, Tout>(a, G, s);
-        case 16: return launch_g<16, Tin, Tout>(a, G, s);
+        case 1: return launch_g<1, Tin, Tout, kLB>(a, G, s);
+        case 2: return launch_g<2, Tin, Tout, kLB>(a, G, s);
+        case 4: return launch_g<4, Tin, Tout, kLB>(a, G, s);
+        case 8: return launch_g<8, Tin, Tout, kLB>(a, G, s);
+        case 16: return launch_g<16, Tin, Tout, kLB>(a, G, s);
     }
     return cudaErrorInvalidValue;
 }
 
+template <bool kLB>
+cudaError_t dispatch(const ScanArgs& a, int G, cudaStream_t s) {
+    if (a.in_dtype == kBF16)
+        return a.out_dtype == kBF16 ? launch_n<__nv_bfloat16, __nv_bfloat16, kLB>(a, G, s)
+                                    : launch_n<__nv_bfloat16, float, kLB>(a, G, s);
+    return a.out_dtype == kBF16 ? launch_n<float, __nv_bfloat16, kLB>(a, G, s)
+                                : launch_n<float, float, kLB>(a, G, s);
+}
+
 }  // namespace
 
+int lookback_channels_per_cta(int dstate, int lanes_per_channel, int in_dtype) {
+    const int npl = dstate / lanes_per_channel;
+    const int k = (in_dtype == kBF16 && npl >= 2 && npl <= 4) ? 2 : 1;   // max_k()
+    return kWarps * 32 * k / lanes_per_channel;
+}
+
 cudaError_t launch_scan_thread(const ScanArgs& a, int lanes_per_channel, cudaStream_t s) {
-    if (a.in_dtype == kBF16)
-        return a.out_dtype == kBF16 ? launch_n<__nv_bfloat16, __nv_bfloat16>(a, lanes_per_channel, s)
-                                    : launch_n<__nv_bfloat16, float>(a, lanes_per_channel, s);
-    return a.out_dtype == kBF16 ? launch_n<float, __nv_bfloat16>(a, lanes_per_channel, s)
-                                : launch_n<float, float>(a, lanes_per_channel, s);
+    return dispatch<false>(a, lanes_per_channel, s);
+}
+
+cudaError_t launch_scan_serial_lookback(const ScanArgs& a, int lanes_per_channel, cudaStream_t s) {
+    return dispatch<true>(a, lanes_per_channel, s);
+}
+
+size_t lookback_workspace_bytes(int64_t batch, int64_t dim, int dstate, int64_t n_seg) {
+    return 16 + (size_t)batch * (size_t)dim * (size_t)n_seg * sizeof(LbDesc<1>) * (size_t)dstate;
 }
 
 }  // namespace ssm

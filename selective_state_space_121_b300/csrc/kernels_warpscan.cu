@@ -1,6 +1,7 @@
 // kernels_warpscan.cu -- chunked selective scan with a warp-shuffle associative
-// scan inside each chunk, a serial carry across chunks, and a multi-block
-// variant joined by single-pass decoupled look-back.
+// scan inside each chunk and a serial carry across chunks (lanes split time, so
+// it keeps a whole warp busy per channel: the algorithm for few channels and
+// short sequences).
 //
 // What is computed (Mamba SSM complete guide (youngju.dev), section 5,
 // selective_scan, with MambaBlock.ssm's softplus(dt_proj) and forward's silu(z)
@@ -28,15 +29,6 @@
 //    Every a_t = exp(dt A) is evaluated exactly once.
 //  * The N-wide carry (state at the chunk boundary) lives in registers; across
 //    chunks it is carried serially by the warp.
-// The look-back variant cuts seqlen into segments handled by different CTAs.
-// A CTA first folds its whole segment into one N-wide map (a pre-pass that
-// needs B but not C and writes nothing), publishes it, looks back over earlier
-// segments' published maps/prefixes until it meets an inclusive prefix, then
-// runs the full pass from the carry it obtained. CTAs take segments in the
-// order of an atomic ticket, so every segment a CTA waits on belongs to a CTA
-// that has already started: the look-back always makes progress. Each wait is
-// also bounded; on expiry the kernel records SSM_ERR_LOOKBACK_TIMEOUT in the
-// workspace status word, publishes what it has and finishes.
 #include "common.cuh"
 #include "launch.h"
 
@@ -47,9 +39,6 @@ constexpr int K = kWarpScanItems;     // 8 steps per lane
 constexpr int T = kWarpScanChunk;     // 256 steps per chunk
 constexpr int W = 8;                  // warps (channels) per CTA
 constexpr int kThreads = 32 * W;
-
-constexpr uint32_t kFlagNone = 0, kFlagAgg = 1, kFlagIncl = 2;
-constexpr int kErrLookbackTimeout = -7;
 
 template <int N>
 struct Smem {
@@ -249,31 +238,6 @@ __device__ __forceinline__ void chunk_full(const ScanArgs& a, int64_t b, int64_t
     store_items<Tout, kVec>(static_cast<Tout*>(a.y) + row_off, t, a.seqlen, y);
 }
 
-// Aggregate-only pass over one chunk: composes the chunk's map into (aggP, aggH).
-template <int N, typename Tin, bool kVec>
-__device__ __forceinline__ void chunk_aggregate(const ScanArgs& a, int64_t b, int64_t d, int64_t t0,
-                                                const Smem<N>& sm, const float* Ad, float* aggP,
-                                                float* aggH, int lane) {
-    using Dec = Decay<sizeof(Tin) == 4>;
-    const int64_t row_off = (b * a.dim + d) * a.seqlen;
-    const int64_t t = t0 + lane * K;
-    float dtl[K], bu[K], u[K];
-    const float sdtl = prepare_items<Tin, kVec>(a, row_off, d, t, dtl, bu, u);
-#pragma unroll
-    for (int n = 0; n < N; n++) {
-        const float* sb = &sm.B[n][lane * K];
-        float H = 0.f;
-#pragma unroll
-        for (int k = 0; k < K; k++) H = Dec::step(Dec::make(dtl[k] * Ad[n]), H, bu[k] * sb[k]);
-        float P = Dec::make(sdtl * Ad[n]);
-        warp_scan_maps<Dec>(P, H, lane);
-        P = __shfl_sync(0xffffffffu, P, 31);
-        H = __shfl_sync(0xffffffffu, H, 31);
-        aggH[n] = Dec::step(P, aggH[n], H);
-        aggP[n] = Dec::mul(P, aggP[n]);
-    }
-}
-
 template <int N>
 __device__ __forceinline__ void load_A(const ScanArgs& a, int64_t d, float* Ad) {
 #pragma unroll
@@ -323,142 +287,6 @@ __global__ void __launch_bounds__(kThreads) warp_scan_kernel(ScanArgs a) {
     if (active) store_hlast<N>(a, b, d, carry, carry_lo, lane);
 }
 
-// ---------------------------------------------------------------------------
-// Look-back kernel. Workspace layout (zeroed by the host on the stream):
-//   [0] int32 status, [1] uint32 ticket, [2..3] pad;
-//   then per (channel, segment): uint32 flag[N], float P[N], float H[N], float I[N].
-// (P, H) is the segment's own map (published with flag AGG; P in the kernel's
-// Decay representation: the factor itself, or factor - 1 for fp32 inputs), I the state at the
-// segment's end (published with flag INCL). Published values are never
-// rewritten, so a reader that saw AGG can still read (P, H) after the writer
-// has moved on to INCL. Lane n owns state n of a descriptor: it writes the
-// values and then releases flag[n]; a reader lane n acquires flag[n] before
-// reading the values.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-template <int N>
-struct Desc {
-    uint32_t flag[N];
-    float P[N];
-    float H[N];
-    float I[N];
-};
-
-template <int N, typename Tin, typename Tout, bool kVec>
-__global__ void __launch_bounds__(kThreads) lookback_kernel(ScanArgs a) {
-    __shared__ __align__(16) Smem<N> sm;
-    __shared__ uint32_t s_ticket;
-    using Dec = Decay<sizeof(Tin) == 4>;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int32_t* status = static_cast<int32_t*>(a.workspace);
-    uint32_t* ticket_ctr = reinterpret_cast<uint32_t*>(status + 1);
-    Desc<N>* desc = reinterpret_cast<Desc<N>*>(static_cast<char*>(a.workspace) + 16);
-
-    if (threadIdx.x == 0) s_ticket = atomicAdd(ticket_ctr, 1u);
-    __syncthreads();
-    const int64_t groups = (a.dim + W - 1) / W;
-    const int64_t per_seg = groups * a.batch;
-    const int64_t tk = s_ticket;
-    const int64_t seg = tk / per_seg;                 // segment-major ticket order
-    const int64_t rem = tk % per_seg;
-    const int64_t b = rem / groups;
-    const int64_t d = (rem % groups) * W + warp;
-    const bool active = d < a.dim;
-    const int64_t ts = seg * a.seg_len;
-    const int64_t te = min(a.seqlen, ts + a.seg_len);
-    const int64_t ch = b * a.dim + d;
-
-    float Ad[N], carry[N], carry_lo[N], aggP[N], aggH[N];
-    if (active) {
-        load_A<N>(a, d, Ad);
-#pragma unroll
-        for (int n = 0; n < N; n++) { aggP[n] = Dec::one(); aggH[n] = 0.f; }
-    }
-    const bool last = seg + 1 == a.n_seg;
-    const bool publish = !last && seg != a.drop_segment;
-    // 1) fold the segment into one map; the last segment publishes nothing and skips it
-    if (!last) {
-        for (int64_t t0 = ts; t0 < te; t0 += T) {
-            stage_bc<N, Tin, kVec, false>(a, b, t0, sm);
-            __syncthreads();
-            if (active) chunk_aggregate<N, Tin, kVec>(a, b, d, t0, sm, Ad, aggP, aggH, lane);
-            __syncthreads();
-        }
-    }
-    if (active) {
-        Desc<N>* mine = desc + ch * a.n_seg + seg;
-        if (seg == 0) {
-            load_h0<N>(a, b, d, carry, carry_lo);
-        } else {
-            // 2) publish the segment map (successors may compose it), then 3) look back
-            if (publish) {
-#pragma unroll
-                for (int n = 0; n < N; n++) {
-                    if (lane == n) {
-                        mine->P[n] = aggP[n];
-                        mine->H[n] = aggH[n];
-                        st_release(&mine->flag[n], kFlagAgg);
-                    }
-                }
-            }
-            // lane n < N walks state n back; (accP, accH) is the composed map of the
-            // segments strictly between the one inspected and this one
-            float accP = Dec::one(), accH = 0.f, cin = 0.f;
-            bool timed_out = false;
-            if (lane < N) {
-                for (int64_t j = seg - 1; j >= 0; j--) {
-                    const Desc<N>* pd = desc + ch * a.n_seg + j;
-                    uint32_t f = ld_acquire(&pd->flag[lane]);
-                    uint32_t spins = 0;
-                    while (f == kFlagNone && spins < a.spin_limit) {
-                        ++spins;
-                        __nanosleep(64);
-                        f = ld_acquire(&pd->flag[lane]);
-                    }
-                    if (f == kFlagNone) { timed_out = true; cin = accH; break; }
-                    if (f == kFlagIncl) { cin = Dec::step(accP, __ldcg(&pd->I[lane]), accH); break; }
-                    accH = Dec::step(accP, __ldcg(&pd->H[lane]), accH);
-                    accP = Dec::mul(accP, __ldcg(&pd->P[lane]));
-                }
-            }
-            if (timed_out) atomicExch(status, kErrLookbackTimeout);
-#pragma unroll
-            for (int n = 0; n < N; n++) {
-                carry[n] = __shfl_sync(0xffffffffu, cin, n);
-                carry_lo[n] = 0.f;
-            }
-        }
-        // 4) publish the inclusive prefix: the state at this segment's end. On a
-        //    timeout this is still published (with the wrong carry) so that later
-        //    segments finish instead of waiting too; the status word has the error.
-        if (publish) {
-#pragma unroll
-            for (int n = 0; n < N; n++) {
-                if (lane == n) {
-                    mine->I[n] = Dec::step(aggP[n], carry[n], aggH[n]) + carry_lo[n];
-                    st_release(&mine->flag[n], kFlagIncl);
-                }
-            }
-        }
-    }
-    // 5) full pass over the segment from the carry
-    for (int64_t t0 = ts; t0 < te; t0 += T) {
-        stage_bc<N, Tin, kVec, true>(a, b, t0, sm);
-        __syncthreads();
-        if (active) chunk_full<N, Tin, Tout, kVec>(a, b, d, t0, sm, Ad, carry, carry_lo, lane);
-        __syncthreads();
-    }
-    if (active && last) store_hlast<N>(a, b, d, carry, carry_lo, lane);
-}
-
 template <int N, typename Tin, typename Tout>
 cudaError_t launch_ws_n(const ScanArgs& a, cudaStream_t s) {
     if (a.batch == 0 || a.dim == 0) return cudaSuccess;
@@ -468,44 +296,25 @@ cudaError_t launch_ws_n(const ScanArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <int N, typename Tin, typename Tout>
-cudaError_t launch_lb_n(const ScanArgs& a, cudaStream_t s) {
-    if (a.batch == 0 || a.dim == 0) return cudaSuccess;
-    const int64_t ctas = ((a.dim + W - 1) / W) * a.batch * a.n_seg;
-    if (a.vec) lookback_kernel<N, Tin, Tout, true><<<(unsigned)ctas, kThreads, 0, s>>>(a);
-    else lookback_kernel<N, Tin, Tout, false><<<(unsigned)ctas, kThreads, 0, s>>>(a);
-    return cudaGetLastError();
-}
-
-template <bool kLB, typename Tin, typename Tout>
+template <typename Tin, typename Tout>
 cudaError_t dispatch_n(const ScanArgs& a, cudaStream_t s) {
     switch (a.dstate) {
-        case 1: return kLB ? launch_lb_n<1, Tin, Tout>(a, s) : launch_ws_n<1, Tin, Tout>(a, s);
-        case 2: return kLB ? launch_lb_n<2, Tin, Tout>(a, s) : launch_ws_n<2, Tin, Tout>(a, s);
-        case 4: return kLB ? launch_lb_n<4, Tin, Tout>(a, s) : launch_ws_n<4, Tin, Tout>(a, s);
-        case 8: return kLB ? launch_lb_n<8, Tin, Tout>(a, s) : launch_ws_n<8, Tin, Tout>(a, s);
-        case 16: return kLB ? launch_lb_n<16, Tin, Tout>(a, s) : launch_ws_n<16, Tin, Tout>(a, s);
+        case 1: return launch_ws_n<1, Tin, Tout>(a, s);
+        case 2: return launch_ws_n<2, Tin, Tout>(a, s);
+        case 4: return launch_ws_n<4, Tin, Tout>(a, s);
+        case 8: return launch_ws_n<8, Tin, Tout>(a, s);
+        case 16: return launch_ws_n<16, Tin, Tout>(a, s);
     }
     return cudaErrorInvalidValue;
 }
 
-template <bool kLB>
-cudaError_t dispatch(const ScanArgs& a, cudaStream_t s) {
-    if (a.in_dtype == kBF16)
-        return a.out_dtype == kBF16 ? dispatch_n<kLB, __nv_bfloat16, __nv_bfloat16>(a, s)
-                                    : dispatch_n<kLB, __nv_bfloat16, float>(a, s);
-    return a.out_dtype == kBF16 ? dispatch_n<kLB, float, __nv_bfloat16>(a, s)
-                                : dispatch_n<kLB, float, float>(a, s);
-}
-
 }  // namespace
 
-size_t lookback_workspace_bytes(int64_t batch, int64_t dim, int dstate, int64_t n_seg) {
-    const size_t desc = (size_t)dstate * 16;
-    return 16 + (size_t)batch * (size_t)dim * (size_t)n_seg * desc;
+cudaError_t launch_scan_warp(const ScanArgs& a, cudaStream_t s) {
+    if (a.in_dtype == kBF16)
+        return a.out_dtype == kBF16 ? dispatch_n<__nv_bfloat16, __nv_bfloat16>(a, s)
+                                    : dispatch_n<__nv_bfloat16, float>(a, s);
+    return a.out_dtype == kBF16 ? dispatch_n<float, __nv_bfloat16>(a, s) : dispatch_n<float, float>(a, s);
 }
-
-cudaError_t launch_scan_warp(const ScanArgs& a, cudaStream_t s) { return dispatch<false>(a, s); }
-cudaError_t launch_scan_lookback(const ScanArgs& a, cudaStream_t s) { return dispatch<true>(a, s); }
 
 }  // namespace ssm

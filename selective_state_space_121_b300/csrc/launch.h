@@ -50,16 +50,21 @@ struct DecodeArgs {
     int softplus;
     int in_dtype, out_dtype;
     bool vec;          // A 16-byte and B, C (4 * element size)-byte aligned: vector loads
+    bool tma;          // state, x, delta, z, B, C rows all 16-byte aligned: bulk-copy streaming
 };
 
 // Each returns cudaSuccess or the launch error.
 cudaError_t launch_state_update(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_scan_warp(const ScanArgs& a, cudaStream_t s);
-cudaError_t launch_scan_lookback(const ScanArgs& a, cudaStream_t s);
+cudaError_t launch_scan_serial_lookback(const ScanArgs& a, int lanes_per_channel, cudaStream_t s);
+// channels one CTA of the look-back kernel covers (its segments are planned with it)
+int lookback_channels_per_cta(int dstate, int lanes_per_channel, int in_dtype);
 cudaError_t launch_scan_thread(const ScanArgs& a, int lanes_per_channel, cudaStream_t s);
 cudaError_t launch_scan_scalar(const ScanArgs& a, cudaStream_t s);
 
-// Look-back workspace geometry (bytes), shared by api.cu and the kernel.
+// Look-back workspace geometry (bytes), shared by api.cu and the look-back kernel
+// (kernels_serial.cu): a 16-byte header and one descriptor of 16*dstate bytes per
+// (channel, segment).
 constexpr int kWarpScanItems = 8;                    // time steps per lane per chunk
 constexpr int kWarpScanChunk = 32 * kWarpScanItems;  // time steps per warp chunk
 size_t lookback_workspace_bytes(int64_t batch, int64_t dim, int dstate, int64_t n_seg);
