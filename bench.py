@@ -338,17 +338,21 @@ def base_config(extra=None):
 
 
 def _traffic_record(kernel: str):
-    """ncu DRAM bytes per launch recorded under profiles/, valid only for the kernel source it was taken on."""
+    """ncu DRAM bytes (read + write) per launch recorded in profiles/traffic.json, valid
+    only while the kernel's sources hash to what they were when the counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     rec = json.load(open(path)).get(kernel)
     if not rec:
         return None
-    src = os.path.join(ROOT, rec["source"])
-    if not os.path.exists(src):
-        return None
-    if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != rec["source_sha"]:
+    h = hashlib.sha256()
+    for src in rec["sources"]:
+        p = os.path.join(ROOT, src)
+        if not os.path.exists(p):
+            return None
+        h.update(open(p, "rb").read())
+    if h.hexdigest()[:16] != rec["sources_sha"]:
         return None
     return rec["bytes_per_launch"]
 
@@ -387,6 +391,7 @@ def main():
                     help="prefill scan algorithm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-configs", action="store_true", help="skip timing the other prefill configs")
     ap.add_argument("--only", choices=["scan", "decode"],
                     help="time one entry point alone on --config (a kernel case for sweeps and ncu)")
     ap.add_argument("--config", default="mamba130m",
@@ -462,10 +467,23 @@ def main():
             dist.destroy_process_group()
         return
 
+    # every prefill config of the hot path on its own (auto algorithm; inputs > L2)
+    configs_measured = {}
+    step_parts = st.parts()
+    step_inputs = (st.pre_in, st.sm1_in, st.dec_in)
+    h2d, d2h = hs.h2d, hs.d2h
+    if not args.no_configs:
+        del st, hs
+        torch.cuda.empty_cache()
+        for name, steps in (("tiny", 50), ("mamba2p8b", 10), ("long", 5)):
+            rec = time_case("scan", name, "auto", steps, 3, device)
+            configs_measured[name] = {k: rec[k] for k in ("case", "ms_median", "Gtokch_s", "GB_s", "hbm_frac")}
+            torch.cuda.empty_cache()
+
     hbm_peak, _, peak_kind = _peaks()
     parts_out = {}
     tot_tokch = 0
-    for (name, tokch, elems, nbytes, has_z), pm in zip(st.parts(), part_ms):
+    for (name, tokch, elems, nbytes, has_z), pm in zip(step_parts, part_ms):
         tot_tokch += tokch
         sec = pm * 1e-3
         hbm_t = nbytes / (hbm_peak * 1e9)
@@ -478,7 +496,7 @@ def main():
 
     # roofline of the dominant kernel (largest share of the step)
     dom_i = int(np.argmax(part_ms))
-    name, tokch, elems, nbytes, has_z = st.parts()[dom_i]
+    name, tokch, elems, nbytes, has_z = step_parts[dom_i]
     sec = part_ms[dom_i] * 1e-3
     hbm_t = nbytes / (hbm_peak * 1e9)
     alu_t = alu_roof_seconds(elems, tokch, has_z, SM_MAX_MHZ_NOMINAL)
@@ -499,7 +517,7 @@ def main():
 
     cpu = None
     if not args.no_cpu_baseline:
-        rates, cores, sample = oracle_sample(st.pre_in, st.sm1_in, st.dec_in, 12.0)
+        rates, cores, sample = oracle_sample(*step_inputs, 12.0)
         cpu = {"value": cpu_value(rates), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
                "parts_Gtokch_s": {k: v / 1e9 for k, v in rates.items()}}
 
@@ -514,7 +532,8 @@ def main():
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": job_value(world, tot_tokch, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": hs.h2d, "d2h_bytes_per_step": hs.d2h, "steps": args.e2e_steps},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
+        "configs_measured": configs_measured,
         "gpu_launches": 3 * args.steps,
         "clocks": clocks.summary(),
     }
@@ -528,13 +547,18 @@ def run_case(args):
     timed with CUDA events on the launching stream. Prints one JSON line (not the
     bench contract line): median/mean ms, Gtoken*channel/s, algorithmic GB/s."""
     import torch
+    torch.cuda.set_device(0)
+    print(json.dumps(time_case(args.only, args.config, args.algo, args.steps, args.warmup, torch.device("cuda", 0))))
+
+
+def time_case(only, config, algo, steps, warmup, dev):
+    """Times one entry point alone on one workload (see run_case); returns the record."""
+    import torch
     import selective_state_space_121_b300 as ssm
     from workloads.torch_io import decode_set_to_torch, scan_to_torch, to_torch
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream()
-    if args.only == "scan":
-        cfg = W.CONFIGS[args.config]
+    if only == "scan":
+        cfg = W.CONFIGS[config]
         inp = W.make_scan_inputs(cfg)
         t = scan_to_torch(inp, dev)
         ei = 2 if cfg.in_dtype == W.BF16 else 4
@@ -546,10 +570,10 @@ def run_case(args):
 
         def launch():
             ssm.scan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"],
-                         cfg.softplus, t["h0"], y=y, h_last=h, algo=args.algo, workspace=ws)
+                         cfg.softplus, t["h0"], y=y, h_last=h, algo=algo, workspace=ws)
         tokch = cfg.tokens_channels
         nbytes = scan_bytes(cfg.batch, cfg.dim, cfg.seqlen, cfg.dstate, ei, eo, cfg.has_z, t["h0"] is not None)
-        label = f"scan {cfg.name} ({cfg.batch},{cfg.dim},{cfg.seqlen},{cfg.dstate}) algo={args.algo}"
+        label = f"scan {cfg.name} ({cfg.batch},{cfg.dim},{cfg.seqlen},{cfg.dstate}) algo={algo}"
     else:
         cfg = W.DECODE_CONFIGS["decode"]
         inp = W.make_decode_inputs(cfg)
@@ -569,10 +593,10 @@ def run_case(args):
         tokch = cfg.batch * cfg.dim
         nbytes = decode_bytes(cfg.batch, cfg.dim, cfg.dstate, 2, 2)
         label = f"decode ({cfg.batch},{cfg.dim},{cfg.dstate})"
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         launch()
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for e0, e1 in ev:
         e0.record(stream)
         launch()
@@ -581,11 +605,10 @@ def run_case(args):
     ms = np.array([e0.elapsed_time(e1) for e0, e1 in ev])
     hbm_peak, _, peak_kind = _peaks()
     med = float(np.median(ms))
-    print(json.dumps({"case": label, "launches": args.steps, "ms_median": med, "ms_mean": float(ms.mean()),
-                      "ms_min": float(ms.min()), "Gtokch_s": tokch / (med * 1e-3) / 1e9,
-                      "alg_bytes": nbytes, "GB_s": nbytes / (med * 1e-3) / 1e9,
-                      "hbm_frac": nbytes / (med * 1e-3) / 1e9 / hbm_peak, "peak_GB_s": hbm_peak,
-                      "peak_kind": peak_kind}))
+    return {"case": label, "launches": steps, "ms_median": med, "ms_mean": float(ms.mean()),
+            "ms_min": float(ms.min()), "Gtokch_s": tokch / (med * 1e-3) / 1e9,
+            "alg_bytes": nbytes, "GB_s": nbytes / (med * 1e-3) / 1e9,
+            "hbm_frac": nbytes / (med * 1e-3) / 1e9 / hbm_peak, "peak_GB_s": hbm_peak, "peak_kind": peak_kind}
 
 
 def run_reference(args, world, rank):

@@ -67,6 +67,10 @@ class OracleLib:
         lib.oracle_silu.argtypes = [ctypes.c_double]
         lib.oracle_silu.restype = ctypes.c_double
         lib.oracle_max_threads.restype = ctypes.c_int
+        lib.oracle_causal_conv1d.argtypes = [P] * 4 + [ctypes.c_int, P, P, I64, I64, I64, I64, ctypes.c_int]
+        lib.oracle_causal_conv1d.restype = ctypes.c_int
+        lib.oracle_conv_update.argtypes = [P] * 4 + [ctypes.c_int, P, I64, I64, I64, ctypes.c_int]
+        lib.oracle_conv_update.restype = ctypes.c_int
         self.lib = lib
         self.path = path
 
@@ -124,6 +128,43 @@ class OracleLib:
         return y
 
 
+    def causal_conv1d(self, x, w, bias=None, conv_state=None, silu=True, threads: int = 0):
+        """Causal depthwise conv1d (+ silu) in fp64.
+
+        x: (batch, dim, L); w: (dim, width); bias: (dim,); conv_state: (batch, dim,
+        width-1) fp64, the inputs before x (zeros when None). Returns (out (batch, dim,
+        L) fp64, conv_state_out (batch, dim, width-1) fp64).
+        """
+        x = _f32(x); w = _f32(w); bias = _f32(bias)
+        bt, dim, L = x.shape
+        width = w.shape[1]
+        assert w.shape == (dim, width) and width >= 1
+        st = None if conv_state is None else _f64(conv_state)
+        assert st is None or st.shape == (bt, dim, width - 1)
+        out = np.empty((bt, dim, L), dtype=np.float64)
+        so = np.empty((bt, dim, width - 1), dtype=np.float64)
+        rc = self.lib.oracle_causal_conv1d(_p(x), _p(w), _p(bias), _p(st), int(bool(silu)), _p(out),
+                                           _p(so), bt, dim, L, width, int(threads))
+        if rc != 0:
+            raise ValueError("oracle_causal_conv1d rejected the sizes")
+        return out, so
+
+    def conv_update(self, conv_state, x, w, bias=None, silu=True, threads: int = 0):
+        """One decode token of the convolution; conv_state (batch, dim, width-1) fp64 is
+        updated IN PLACE. x: (batch, dim). Returns out (batch, dim) fp64."""
+        assert conv_state.dtype == np.float64 and conv_state.flags.c_contiguous
+        x = _f32(x); w = _f32(w); bias = _f32(bias)
+        bt, dim = x.shape
+        width = w.shape[1]
+        assert conv_state.shape == (bt, dim, width - 1) and w.shape == (dim, width)
+        out = np.empty((bt, dim), dtype=np.float64)
+        rc = self.lib.oracle_conv_update(_p(conv_state), _p(x), _p(w), _p(bias), int(bool(silu)),
+                                         _p(out), bt, dim, width, int(threads))
+        if rc != 0:
+            raise ValueError("oracle_conv_update rejected the sizes")
+        return out
+
+
 _default = None
 
 
@@ -152,6 +193,14 @@ def scan(*args, **kw):
 
 def state_update(*args, **kw):
     return default().state_update(*args, **kw)
+
+
+def causal_conv1d(*args, **kw):
+    return default().causal_conv1d(*args, **kw)
+
+
+def conv_update(*args, **kw):
+    return default().conv_update(*args, **kw)
 
 
 def scan_inputs(inp: dict, channels=None, threads: int = 0):

@@ -118,6 +118,79 @@ int oracle_state_update(double *state, const float *x, const float *delta, const
     return 0;
 }
 
+/* Causal depthwise 1-D convolution and SiLU: the step before the scan in the
+ * same page's MambaBlock (section 5, "complete Mamba implementation"): __init__
+ * builds nn.Conv1d(d_inner, d_inner, kernel_size=d_conv, groups=d_inner,
+ * padding=d_conv - 1, bias=True) and forward keeps the first seqlen outputs of
+ * the convolution and applies silu. PyTorch's Conv1d is a cross-correlation over
+ * the input padded with width-1 zeros on the left, so with xp the padded input
+ * (xp[j] = x[j - (width-1)], zero for j < width-1):
+ *     out[t] = bias[d] + sum_{k=0}^{width-1} w[d][k] * xp[t + k]
+ * w[d][width-1] multiplies the current input x[t]. Reading for the state the
+ * page leaves open (chunked prefill, decode): the zero padding is replaced by
+ * the width-1 inputs that preceded this call, oldest first (conv_state_in;
+ * zeros when NULL), and conv_state_out receives the last width-1 entries of the
+ * padded input, i.e. the state a following call continues from.
+ *   x, out : (batch, dim, seqlen)     w : (dim, width)     bias : (dim) or NULL
+ *   conv_state_in, conv_state_out : (batch, dim, width - 1) or NULL
+ */
+int oracle_causal_conv1d(const float *x, const float *w, const float *bias,
+                         const double *conv_state_in, int silu, double *out,
+                         double *conv_state_out, int64_t batch, int64_t dim, int64_t seqlen,
+                         int64_t width, int nthreads) {
+    if (batch < 0 || dim < 0 || seqlen < 0 || width < 1) return -1;
+    int64_t nch = batch * dim, hw = width - 1;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t ch = 0; ch < nch; ch++) {
+        int64_t d = ch % dim;
+        /* the padded input of this channel: width-1 state entries, then x */
+        double *xp = (double *)malloc(sizeof(double) * (size_t)(hw + seqlen + 1));
+        for (int64_t j = 0; j < hw; j++) xp[j] = conv_state_in ? conv_state_in[ch * hw + j] : 0.0;
+        for (int64_t t = 0; t < seqlen; t++) xp[hw + t] = (double)x[ch * seqlen + t];
+        for (int64_t t = 0; t < seqlen; t++) {
+            double acc = bias ? (double)bias[d] : 0.0;
+            for (int64_t k = 0; k < width; k++) acc += (double)w[d * width + k] * xp[t + k];
+            out[ch * seqlen + t] = silu ? oracle_silu(acc) : acc;
+        }
+        if (conv_state_out)
+            for (int64_t j = 0; j < hw; j++) conv_state_out[ch * hw + j] = xp[seqlen + j];
+        free(xp);
+    }
+    return 0;
+}
+
+/* One decode token of the same convolution, in place on the state (the width-1
+ * most recent inputs, oldest first): out = bias + sum_{k<width-1} w[k] state[k]
+ * + w[width-1] x, optionally silu; then the state drops its oldest entry and
+ * appends x.
+ *   conv_state : (batch, dim, width - 1) in/out   x, out : (batch, dim)
+ */
+int oracle_conv_update(double *conv_state, const float *x, const float *w, const float *bias,
+                       int silu, double *out, int64_t batch, int64_t dim, int64_t width,
+                       int nthreads) {
+    if (batch < 0 || dim < 0 || width < 1) return -1;
+    int64_t nch = batch * dim, hw = width - 1;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t ch = 0; ch < nch; ch++) {
+        int64_t d = ch % dim;
+        double *s = conv_state + ch * hw;
+        double xt = (double)x[ch];
+        double acc = bias ? (double)bias[d] : 0.0;
+        for (int64_t k = 0; k < hw; k++) acc += (double)w[d * width + k] * s[k];
+        acc += (double)w[d * width + hw] * xt;
+        out[ch] = silu ? oracle_silu(acc) : acc;
+        for (int64_t k = 0; k + 1 < hw; k++) s[k] = s[k + 1];
+        if (hw > 0) s[hw - 1] = xt;
+    }
+    return 0;
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -33,7 +33,9 @@
 namespace ssm {
 namespace {
 
-constexpr int kWarps = 4;
+// one warp per CTA: the finest unit of residency, so that the register budget
+// below, not the CTA shape, sets how many warps an SM holds
+constexpr int kWarps = 1;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kSeg = 8;             // lanes per channel
 constexpr int kK = 8;               // steps per lane per chunk
@@ -75,8 +77,16 @@ __device__ __forceinline__ void store_k(T* row, int64_t t, int64_t L, const floa
         if (t + k < L) row[t + k] = from_f32<T>(v[k]);
 }
 
-template <typename Tin, typename Tout, bool kVec>
-__global__ void __launch_bounds__(kThreads) scalar_scan_kernel(ScanArgs a) {
+// Register budget: 96 per thread without z and D lets an SM hold 21 warps, so the
+// Mamba-shaped SM1 workload (12,288 channels, 3,072 warps) runs in one wave; at
+// the unconstrained ~110 it needs 1.3 waves, and each warp walks the whole
+// sequence, so the partial second wave costs nearly a full one. With z or D the
+// kernel takes up to 128.
+#ifndef SSM_SCALAR_MAXNREG
+#define SSM_SCALAR_MAXNREG 96
+#endif
+template <typename Tin, typename Tout, bool kVec, bool kZ, bool kD>
+__global__ void __maxnreg__((kZ || kD) ? 128 : SSM_SCALAR_MAXNREG) scalar_scan_kernel(ScanArgs a) {
     constexpr bool kAcc = sizeof(Tin) == 4;
     using Dec = Decay<kAcc>;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -88,34 +98,35 @@ __global__ void __launch_bounds__(kThreads) scalar_scan_kernel(ScanArgs a) {
     const int64_t L = a.seqlen;
     const Tin* up = static_cast<const Tin*>(a.u) + row * L;
     const Tin* dp = static_cast<const Tin*>(a.delta) + row * L;
-    const Tin* zp = a.z ? static_cast<const Tin*>(a.z) + row * L : nullptr;
+    const Tin* zp = kZ ? static_cast<const Tin*>(a.z) + row * L : nullptr;
     const Tin* Bp = static_cast<const Tin*>(a.B) + b * L;
     const Tin* Cp = static_cast<const Tin*>(a.C) + b * L;
     Tout* yp = static_cast<Tout*>(a.y) + row * L;
     const float Ad = ok ? a.A[d] * Dec::scale : 0.f;
     const float bias = (ok && a.delta_bias) ? a.delta_bias[d] : 0.f;
-    const float Dd = (ok && a.D) ? a.D[d] : 0.f;
+    const float Dd = (kD && ok) ? a.D[d] : 0.f;
     float carry = (ok && a.h0) ? a.h0[row] : 0.f, carry_lo = 0.f;
 
-    float nu[kK], nd[kK], nz[kK], nB[kK], nC[kK];
+    // the next chunk's inputs are loaded while the current one computes
+    float nu[kK], nd[kK], nB[kK], nC[kK], nz[kK];
     auto prefetch = [&](int64_t t) {
         load_k<Tin, kVec>(up, t, L, ok, nu);
         load_k<Tin, kVec>(dp, t, L, ok, nd);
-        load_k<Tin, kVec>(zp, t, L, ok && zp, nz);
         load_k<Tin, kVec>(Bp, t, L, ok, nB);
         load_k<Tin, kVec>(Cp, t, L, ok, nC);
+        if constexpr (kZ) load_k<Tin, kVec>(zp, t, L, ok, nz);
     };
     if (L > 0) prefetch((int64_t)s * kK);
     for (int64_t t0 = 0; t0 < L; t0 += kChunk) {
         const int64_t t = t0 + (int64_t)s * kK;
-        float u[kK], p[kK], bb[kK], zz[kK], C[kK];
+        float du[kK], p[kK], bb[kK], zz[kK], C[kK];
 #pragma unroll
         for (int k = 0; k < kK; k++) {
             const float x = nd[k] + bias;
             float dt = a.softplus ? softplus_acc<kAcc>(x) : x;
             if (t + k >= L) dt = 0.f;                 // identity step past the end
-            u[k] = nu[k];
-            zz[k] = nz[k];
+            if constexpr (kD) du[k] = Dd * nu[k];
+            if constexpr (kZ) zz[k] = nz[k];
             C[k] = nC[k];
             p[k] = Dec::make(dt * Ad);
             bb[k] = dt * nu[k] * nB[k];
@@ -164,8 +175,8 @@ __global__ void __launch_bounds__(kThreads) scalar_scan_kernel(ScanArgs a) {
         }
 #pragma unroll
         for (int k = 0; k < kK; k++) {
-            y[k] = fmaf(Dd, u[k], y[k]);
-            if (zp) y[k] *= silu_acc<kAcc>(zz[k]);
+            if constexpr (kD) y[k] += du[k];
+            if constexpr (kZ) y[k] *= silu_acc<kAcc>(zz[k]);
         }
         if (ok) store_k<Tout, kVec>(yp, t, L, y);
     }
@@ -179,8 +190,20 @@ cudaError_t launch(const ScanArgs& a, cudaStream_t s) {
     const int64_t per_cta = (int64_t)kWarps * kChPerWarp;
     const int64_t ctas = (rows + per_cta - 1) / per_cta;
     if (ctas > ((int64_t)1 << 31) - 1) return cudaErrorInvalidValue;
-    if (a.vec) scalar_scan_kernel<Tin, Tout, true><<<(unsigned)ctas, kThreads, 0, s>>>(a);
-    else scalar_scan_kernel<Tin, Tout, false><<<(unsigned)ctas, kThreads, 0, s>>>(a);
+    // z (the gate) and D (the skip) are template switches: without them the kernel
+    // holds no registers for them
+    const int sel = (a.vec ? 4 : 0) | (a.z ? 2 : 0) | (a.D ? 1 : 0);
+    const unsigned g = (unsigned)ctas;
+    switch (sel) {
+        case 0: scalar_scan_kernel<Tin, Tout, false, false, false><<<g, kThreads, 0, s>>>(a); break;
+        case 1: scalar_scan_kernel<Tin, Tout, false, false, true><<<g, kThreads, 0, s>>>(a); break;
+        case 2: scalar_scan_kernel<Tin, Tout, false, true, false><<<g, kThreads, 0, s>>>(a); break;
+        case 3: scalar_scan_kernel<Tin, Tout, false, true, true><<<g, kThreads, 0, s>>>(a); break;
+        case 4: scalar_scan_kernel<Tin, Tout, true, false, false><<<g, kThreads, 0, s>>>(a); break;
+        case 5: scalar_scan_kernel<Tin, Tout, true, false, true><<<g, kThreads, 0, s>>>(a); break;
+        case 6: scalar_scan_kernel<Tin, Tout, true, true, false><<<g, kThreads, 0, s>>>(a); break;
+        default: scalar_scan_kernel<Tin, Tout, true, true, true><<<g, kThreads, 0, s>>>(a); break;
+    }
     return cudaGetLastError();
 }
 

@@ -319,6 +319,79 @@ def check_limits(orc):
     assert np.max(np.abs(hl - h0)) < 1e-20
 
 
+# ---------------------------------------------------------------------------
+# 11-13. The causal depthwise conv1d + silu before the scan ([guide] section 5,
+#        "complete Mamba implementation": MambaBlock.__init__'s nn.Conv1d with
+#        groups = d_inner, kernel d_conv, padding d_conv - 1, and forward's
+#        trim to the first seqlen outputs and silu).
+# ---------------------------------------------------------------------------
+def check_conv_impulse(orc):
+    """A unit impulse at t0 returns the kernel reversed (the current input meets the
+    last weight: PyTorch's Conv1d is a cross-correlation), plus the bias everywhere;
+    exact in fp64 for small integers."""
+    dim, L, t0 = 3, 12, 4
+    for width in (1, 2, 3, 4):
+        w = (np.arange(dim * width, dtype=np.float32).reshape(dim, width) + 1)
+        bias = np.array([0.5, -1.0, 2.0], np.float32)
+        x = np.zeros((1, dim, L), np.float32)
+        x[0, :, t0] = 1.0
+        out, st = orc.causal_conv1d(x, w, bias, None, silu=False)
+        ref = np.broadcast_to(bias[None, :, None].astype(np.float64), (1, dim, L)).copy()
+        for j in range(width):
+            ref[0, :, t0 + j] += w[:, width - 1 - j]
+        assert np.array_equal(out, ref), (width, out, ref)
+        assert np.array_equal(st, x[..., L - (width - 1):].astype(np.float64)) or width == 1
+
+
+def check_conv_library(orc):
+    """Equal to the library routine the page calls (torch.nn.functional.conv1d, fp64,
+    padding width-1, groups = channels, first L outputs) followed by silu; with a
+    state, equal to the same routine over [state | x] without padding."""
+    import torch
+    import torch.nn.functional as F
+    rng = np.random.default_rng(29)
+    for width in (2, 3, 4):
+        bt, dim, L = 2, 5, 37
+        x = rng.standard_normal((bt, dim, L)).astype(np.float32)
+        w = rng.standard_normal((dim, width)).astype(np.float32)
+        bias = rng.standard_normal((dim,)).astype(np.float32)
+        xt = torch.from_numpy(x.astype(np.float64))
+        wt = torch.from_numpy(w.astype(np.float64))[:, None, :]
+        bt_ = torch.from_numpy(bias.astype(np.float64))
+        ref = F.silu(F.conv1d(xt, wt, bt_, padding=width - 1, groups=dim)[..., :L]).numpy()
+        out, _ = orc.causal_conv1d(x, w, bias, None, silu=True)
+        assert _rel(out, ref) < 1e-14
+        st = rng.standard_normal((bt, dim, width - 1))
+        full = torch.cat([torch.from_numpy(st), xt], dim=-1)
+        ref2 = F.conv1d(full, wt, bt_, padding=0, groups=dim).numpy()
+        out2, so = orc.causal_conv1d(x, w, bias, st, silu=False)
+        assert _rel(out2, ref2) < 1e-14
+        assert np.array_equal(so, x[..., L - (width - 1):].astype(np.float64))
+
+
+def check_conv_resume_and_decode(orc):
+    """conv(x1 ++ x2) = conv(x1) ++ conv(x2 from x1's final state); and L decode
+    updates from a state equal one prefill call from it (same values, same state)."""
+    rng = np.random.default_rng(31)
+    bt, dim, L1, L2, width = 2, 3, 9, 14, 4
+    x = rng.standard_normal((bt, dim, L1 + L2)).astype(np.float32)
+    w = rng.standard_normal((dim, width)).astype(np.float32)
+    bias = rng.standard_normal((dim,)).astype(np.float32)
+    st0 = rng.standard_normal((bt, dim, width - 1))
+    full, sf = orc.causal_conv1d(x, w, bias, st0, silu=True)
+    a, sa = orc.causal_conv1d(x[..., :L1], w, bias, st0, silu=True)
+    b, sb = orc.causal_conv1d(x[..., L1:], w, bias, sa, silu=True)
+    assert np.array_equal(np.concatenate([a, b], -1), full) and np.array_equal(sb, sf)
+    state = st0.copy()
+    for t in range(L1 + L2):
+        ot = orc.conv_update(state, x[..., t], w, bias, silu=True)
+        assert np.array_equal(ot, full[..., t])
+    assert np.array_equal(state, sf)
+    # a call shorter than the state keeps the older state entries in order
+    short, ss = orc.causal_conv1d(x[..., :1], w, bias, st0, silu=False)
+    assert np.array_equal(ss, np.concatenate([st0[..., 1:], x[..., :1].astype(np.float64)], -1))
+
+
 ALL_CHECKS = [
     check_bruteforce_rational,
     check_symbolic_two_steps,
@@ -332,4 +405,7 @@ ALL_CHECKS = [
     check_decode_equals_prefill,
     check_linearity,
     check_limits,
+    check_conv_impulse,
+    check_conv_library,
+    check_conv_resume_and_decode,
 ]

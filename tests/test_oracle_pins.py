@@ -37,6 +37,16 @@ MUTANTS = [
      "s[n] = a * s[n] + (double)B[b * dstate + n] * xt;"),
     ("h_last_zero", "h_last[ch * dstate + n] = h[n];", "h_last[ch * dstate + n] = 0.0;"),
     ("A_transposed", "const float *A_d = A + d * dstate;", "const float *A_d = A + d;"),
+    ("conv_flipped", "acc += (double)w[d * width + k] * xp[t + k];",
+     "acc += (double)w[d * width + (width - 1 - k)] * xp[t + k];"),
+    ("conv_no_bias", "double acc = bias ? (double)bias[d] : 0.0;\n            for (int64_t k = 0; k < width; k++)",
+     "double acc = 0.0;\n            for (int64_t k = 0; k < width; k++)"),
+    ("conv_state_ignored", "xp[j] = conv_state_in ? conv_state_in[ch * hw + j] : 0.0;", "xp[j] = 0.0;"),
+    ("conv_state_out_shift", "conv_state_out[ch * hw + j] = xp[seqlen + j];",
+     "conv_state_out[ch * hw + j] = xp[seqlen + j - (j > 0)];"),
+    ("conv_no_silu", "out[ch * seqlen + t] = silu ? oracle_silu(acc) : acc;", "out[ch * seqlen + t] = acc;"),
+    ("conv_update_no_shift", "for (int64_t k = 0; k + 1 < hw; k++) s[k] = s[k + 1];", ""),
+    ("conv_update_wrong_weight", "acc += (double)w[d * width + hw] * xt;", "acc += (double)w[d * width] * xt;"),
 ]
 
 
