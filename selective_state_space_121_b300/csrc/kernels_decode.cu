@@ -146,7 +146,11 @@ __global__ void __launch_bounds__(kThreads) state_update_kernel(DecodeArgs a) {
 // bounded) for its own copies in flight and returns.
 // ---------------------------------------------------------------------------
 constexpr int kTmaThreads = 256;
-constexpr int kStages = 4;
+// ring depth (a build option; static shared memory keeps it under 48 KB per CTA)
+#ifndef SSM_DECODE_STAGES
+#define SSM_DECODE_STAGES 4
+#endif
+constexpr int kStages = SSM_DECODE_STAGES;
 constexpr uint32_t kWaitLimit = 1u << 24;
 
 __device__ int g_decode_status;   // 0, or the line of a wait that ran out of budget

@@ -17,22 +17,26 @@
 // scan, no second pass.
 //
 // The operands B_tn and C_tn are the same for every channel of a batch row and
-// come from shared memory. A 16-byte shared load is served in four quarter-warp
-// phases, so one wavefront of shared-memory bandwidth delivers 4 values to 8
-// lanes; at one state-channel per lane that bandwidth, not the SFU, limits the
-// scan (measured: removing the B/C loads made the kernel 1.5x faster while
-// removing every exp changed nothing). Each lane therefore owns the same states
-// of K = 2 channels on the bf16 path: one B/C load feeds 2K elements.
+// come from shared memory, and that bandwidth first limited the scan (measured:
+// removing the B/C loads made the kernel 1.5x faster while removing every exp
+// changed nothing). Three things cut the traffic: in the serial kernel the lanes
+// reading one state group form a quarter-warp, so a 16-byte B/C load is a
+// broadcast within each quarter (2 passes instead of 4), and on the bf16 path
+// B and C stay bf16 there (one 16-byte load gives a lane-step its 4 B and 4 C);
+// the look-back kernel gives each lane the same states of K = 2 channels, so one
+// load feeds 2K elements. What is left bounding the serial kernel at Mamba-130M
+// sizes is issue and latency: about 10 warps per SM.
 //
 // Work layout. A CTA holds W = 4 warps; warp w owns CPW = 32 K / G consecutive
-// channels of batch row b; lane (p, j) owns states [j*NPL, (j+1)*NPL), NPL = N/G,
-// of channels K*p .. K*p + K-1. Time goes in chunks of T steps:
+// channels of batch row b; lane (p, j) (see lane_grp) owns states
+// [j*NPL, (j+1)*NPL), NPL = N/G, of channels K*p .. K*p + K-1. Time goes in
+// chunks of T steps:
 //   A. prologue, one lane per (channel, 16 bytes of consecutive steps): the
 //      per-step scalars of the chunk (loaded one chunk ahead into registers) give
 //      dt = softplus(delta + bias) and dt*u, written to shared memory; the K
 //      channels of a lane are adjacent there, so one load gives a step for all K;
 //   B. recurrence, lane (p, j): per step the (dt, dt*u) of its K channels and the
-//      B and C values of its states (fp32 [t][n] tile, one per CTA: all warps
+//      B and C values of its states ([t][...] tile, one per CTA: all warps
 //      share the batch row); writes its partial C.h sums, 4 steps per store;
 //   C. epilogue, same ownership as A: y = sum of the G partials + D*u, times
 //      silu(z), stored with 16-byte stores.
@@ -107,6 +111,25 @@ struct SerialCfg {
     static_assert(PV >= 1 && CPW * VPR % 32 == 0, "chunk must cover the warp's channels");
     static_assert(kT % V == 0 && kT % 4 == 0, "chunk must be whole vectors and step groups");
 };
+
+// Lane (p, j) of a warp: lane group p (channels K p .. K p + K - 1 of the warp)
+// and state group j (states j NPL .. j NPL + NPL - 1). At K = 1 the 32/G lanes of
+// one state group are consecutive -- at G = 4 a quarter-warp -- so the 8 lanes of
+// a quarter read the same B/C address and a 16-byte shared load takes 2 passes
+// instead of 4 (measured on B300: 2.2 against 4.0 cycles per warp load; the
+// Mamba-130M scan runs 7% faster). At K = 2 the G lanes of a channel group are
+// adjacent instead: there each step's (dt, dt*u) load is a 16-byte one too, and
+// this order measured 7% faster in the look-back. A channel's partial C.h sums
+// meet in shared memory, so its G lanes need not be adjacent.
+template <int G, int K> __device__ __forceinline__ int lane_grp(int lane) {
+    return K == 1 ? lane % (32 / G) : lane / G;
+}
+template <int G, int K> __device__ __forceinline__ int lane_sgrp(int lane) {
+    return K == 1 ? lane / (32 / G) : lane % G;
+}
+template <int G, int K> __device__ __forceinline__ int lane_of(int p, int j) {
+    return K == 1 ? j * (32 / G) + p : p * G + j;
+}
 
 // element i % 2 of a pair
 __device__ __forceinline__ float lo_hi(const float2& v, int i) { return (i & 1) ? v.y : v.x; }
@@ -195,11 +218,25 @@ __device__ __forceinline__ void serial_pass(const ScanArgs& a, int64_t b, int64_
                                             int64_t te, const A2Arr<N, G, K>& A2, LaneStateT<N, G, K>& S,
                                             const Tiles<N, G, Tin, K>& tl) {
     using Cfg = SerialCfg<N, G, Tin, K>;
-    constexpr int NPL = Cfg::NPL, V = Cfg::V, VPR = Cfg::VPR, PV = Cfg::PV, kT = Cfg::kT;
+    constexpr int NPL = Cfg::NPL, V = Cfg::V, VPR = Cfg::VPR, PV = Cfg::PV, kT = Cfg::kT, CPW = Cfg::CPW;
     constexpr int NP2 = LaneState<K, NPL>::NP2;
     constexpr bool kAcc = sizeof(Tin) == 4;
     constexpr int BCV = kFull ? Cfg::BCV : Cfg::BCV / 2;   // the aggregate pass stages B only
     constexpr int BCPT = (BCV + kThreads - 1) / kThreads;
+    // Serial kernel, bf16 inputs, 4 states per lane: B and C stay bf16 in shared
+    // memory, a lane's 4 B and 4 C values of a step side by side in one 16-byte
+    // slot, so one quarter-warp broadcast load serves a lane-step: half the
+    // shared-memory wavefronts of fp32 operands for one integer unpacking op per
+    // value. Measured: 10% faster at Mamba-2.8B sizes (4-5 CTAs per SM, where
+    // shared memory is the limit), 1% slower at Mamba-130M sizes (2.6 CTAs per
+    // SM, latency-bound), slower in the look-back (K = 2 reads each slot for two
+    // channels already), where it is off.
+    constexpr bool kRawBC = !kAcc && NPL == 4 && K == 1;
+    // A raw tile row (one step) has N/2 16-byte slots, state group g in slot
+    // g ^ ((2 (t / 8)) mod N/2): the lanes staging 8-step vectors of one tensor
+    // then write to 16 different banks (unswizzled, the rows t, t+8, t+16, t+24
+    // they fill at once share banks); reads stay one slot per quarter-warp.
+    auto raw_slot = [](int g, int t) { return g ^ ((2 * (t / 8)) & (N / 2 - 1)); };
     using Dec = Decay<kAcc>;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t L = a.seqlen;
@@ -210,7 +247,7 @@ __device__ __forceinline__ void serial_pass(const ScanArgs& a, int64_t b, int64_
     const Tin* C_b = static_cast<const Tin*>(a.C) + b * N * L;
     Tout* y_base = static_cast<Tout*>(a.y);
     const bool has_z = kFull && a.z != nullptr;
-    const int p = lane / G, j = lane % G;
+    const int p = lane_grp<G, K>(lane), j = lane_sgrp<G, K>(lane);
 
     // prologue/epilogue ownership: vector q of this lane covers channel pc[q],
     // steps pt[q] .. pt[q]+V of the chunk
@@ -220,8 +257,13 @@ __device__ __forceinline__ void serial_pass(const ScanArgs& a, int64_t b, int64_
 #pragma unroll
     for (int q = 0; q < PV; q++) {
         const int v = q * 32 + lane;
-        pc[q] = v / VPR;
-        pt[q] = (v % VPR) * V;
+        // K = 1: a quarter-warp's lanes take 8 channels at the same steps (their
+        // (dt, dt*u) stores and partial-sum reads are conflict-free). K = 2: a lane's
+        // neighbours take the next vector of the same channel (with the K = 2
+        // partial-sum layout the K = 1 order makes the epilogue's reads 4-way
+        // bank conflicts; measured 23% slower in the look-back).
+        pc[q] = K == 1 ? v % CPW : v / VPR;
+        pt[q] = K == 1 ? (v / CPW) * V : (v % VPR) * V;
         const int64_t d = d_warp0 + pc[q];
         chan_ok[q] = d < a.dim;
         bias[q] = (chan_ok[q] && a.delta_bias) ? a.delta_bias[d] : 0.f;
@@ -253,18 +295,27 @@ __device__ __forceinline__ void serial_pass(const ScanArgs& a, int64_t b, int64_
     for (int64_t c = 0; c < n_chunks; c++) {
         const int64_t t0 = tb + c * kT;
         const int buf = (int)(c & 1);
-        // B/C tile of this chunk: fp32, [t][n]; B carries ln2 on the bf16 path
+        // B/C tile of this chunk, [t][...]: fp32 [n], B then C (B carries ln2 on
+        // the bf16 path), or the raw bf16 slots above (ln2 then goes into dt*u)
 #pragma unroll
         for (int r = 0; r < BCPT; r++) {
             const int v = r * kThreads + threadIdx.x;
             if (v < BCV) {
                 const int which = v / (N * VPR), rem = v % (N * VPR);
                 const int n = rem / VPR, tt = (rem % VPR) * V;
-                float f[V];
-                unpack<Tin>(rbc[r], f);
-                const float sc = (!kAcc && which == 0) ? kLn2 : 1.f;
+                if constexpr (kRawBC) {
+                    const uint16_t* raw = reinterpret_cast<const uint16_t*>(&rbc[r]);
+                    const int slot = raw_slot(n / NPL, tt) * 2 * NPL + which * NPL + n % NPL;
 #pragma unroll
-                for (int k = 0; k < V; k++) tl.bc[buf][tt + k][which * N + n] = f[k] * sc;
+                    for (int k = 0; k < V; k++)
+                        reinterpret_cast<uint16_t*>(tl.bc[buf][tt + k])[slot] = raw[k];
+                } else {
+                    float f[V];
+                    unpack<Tin>(rbc[r], f);
+                    const float sc = (!kAcc && which == 0) ? kLn2 : 1.f;
+#pragma unroll
+                    for (int k = 0; k < V; k++) tl.bc[buf][tt + k][which * N + n] = f[k] * sc;
+                }
             }
         }
         // A. prologue
@@ -286,10 +337,11 @@ __device__ __forceinline__ void serial_pass(const ScanArgs& a, int64_t b, int64_
                 } else {
                     // x*log2(e); log2(1 + 2^xl) equals xl in fp32 once xl > 24
                     const float xl = fmaf(fd[k], kLog2e, bias[q]);
-                    dts = a.softplus ? (xl > 24.f ? xl : lg2(1.f + ex2(xl))) : xl;
+                    dts = a.softplus ? softplus_log2(xl) : xl;
                 }
                 if (t0 + pt[q] + k >= te || !chan_ok[q]) dts = 0.f;   // identity step past the end
-                *reinterpret_cast<float2*>(dbrow + (pt[q] + k) * 2 * K) = make_float2(dts, dts * fu[k]);
+                const float bu = kRawBC ? dts * (fu[k] * kLn2) : dts * fu[k];
+                *reinterpret_cast<float2*>(dbrow + (pt[q] + k) * 2 * K) = make_float2(dts, bu);
             }
         }
         if (c + 1 < n_chunks) prefetch(t0 + kT);
@@ -317,7 +369,15 @@ __device__ __forceinline__ void serial_pass(const ScanArgs& a, int64_t b, int64_
         // B and C of this lane's states at step t, in pairs
         auto load_bc = [&](int t, float2* bq, float2* cq) {
             const float* bc = tl.bc[buf][t];
-            if constexpr (NPL % 4 == 0) {
+            if constexpr (kRawBC) {
+                const uint4 w = reinterpret_cast<const uint4*>(bc)[raw_slot(j, t)];
+                bq[0] = make_float2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
+                bq[1] = make_float2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+                if constexpr (kFull) {
+                    cq[0] = make_float2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u));
+                    cq[1] = make_float2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u));
+                }
+            } else if constexpr (NPL % 4 == 0) {
 #pragma unroll
                 for (int i = 0; i < NPL; i += 4) {
                     const float4 vb = *reinterpret_cast<const float4*>(bc + j * NPL + i);
@@ -433,12 +493,12 @@ __device__ __forceinline__ void serial_pass(const ScanArgs& a, int64_t b, int64_
                 unpack<Tin>(ku[q], fu);
 #pragma unroll
                 for (int k = 0; k < V; k++) yv[k] = fu[k] * Dd[q];
-                const int pk = pc[q] % K, pl = (pc[q] / K) * G;
+                const int pk = pc[q] % K, pg = pc[q] / K;
 #pragma unroll
                 for (int jj = 0; jj < G; jj++) {
 #pragma unroll
                     for (int k = 0; k < V; k += 4) {
-                        const float4 p4 = tl.p[warp][pk][(pt[q] + k) / 4][pl + jj];
+                        const float4 p4 = tl.p[warp][pk][(pt[q] + k) / 4][lane_of<G, K>(pg, jj)];
                         yv[k] += p4.x; yv[k + 1] += p4.y; yv[k + 2] += p4.z; yv[k + 3] += p4.w;
                     }
                 }
@@ -514,7 +574,7 @@ __global__ void __launch_bounds__(kThreads) serial_scan_kernel(ScanArgs a) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t b = blockIdx.y;
     const int64_t d_warp0 = ((int64_t)blockIdx.x * kWarps + warp) * CPW;
-    const int p = lane / G, j = lane % G;
+    const int p = lane_grp<G, K>(lane), j = lane_sgrp<G, K>(lane);
     int64_t dR[K];
     bool okR[K];
     float h0[K][NPL];
@@ -615,7 +675,7 @@ __global__ void __launch_bounds__(kThreads) serial_lookback_kernel(ScanArgs a) {
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t d_warp0 = (grp * kWarps + warp) * CPW;
-    const int p = lane / G, j = lane % G;
+    const int p = lane_grp<G, K>(lane), j = lane_sgrp<G, K>(lane);
     int64_t dR[K], ch[K];
     bool okR[K];
 #pragma unroll
