@@ -19,6 +19,7 @@ weak scaling); the step time is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -66,6 +67,16 @@ def scan_bytes(bt, dim, L, N, ei, eo, has_z, has_h0):
 def decode_bytes(bt, dim, N, ei, eo):
     """State read + write, x/delta/z in, y out, B and C, A/D/bias."""
     return bt * dim * N * 4 * 2 + bt * dim * (3 * ei + eo) + 2 * bt * N * ei + dim * (N + 2) * 4
+
+
+def conv_bytes(bt, dim, L, width, ei, eo):
+    """Causal conv1d: x in and u out once, the conv state in and out, weights and bias."""
+    return bt * dim * L * (ei + eo) + 2 * bt * dim * (width - 1) * 4 + dim * (width + 1) * 4
+
+
+def conv_update_bytes(bt, dim, width, ei, eo):
+    """Conv decode update: x in, u out, the state read and written, weights and bias."""
+    return bt * dim * (ei + eo + 2 * (width - 1) * 4) + dim * (width + 1) * 4
 
 
 SFU_HALF_RATE_SLOTS = 2           # lg2 and rcp issue at half the ex2 rate (16/clk/SM measured)
@@ -392,7 +403,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-configs", action="store_true", help="skip timing the other prefill configs")
-    ap.add_argument("--only", choices=["scan", "decode"],
+    ap.add_argument("--only", choices=["scan", "decode", "conv", "conv_update"],
                     help="time one entry point alone on --config (a kernel case for sweeps and ncu)")
     ap.add_argument("--config", default="mamba130m",
                     help="workload of --only: a prefill-scan config name, or 'decode'")
@@ -478,6 +489,11 @@ def main():
         for name, steps in (("tiny", 50), ("mamba2p8b", 10), ("long", 5)):
             rec = time_case("scan", name, "auto", steps, 3, device)
             configs_measured[name] = {k: rec[k] for k in ("case", "ms_median", "Gtokch_s", "GB_s", "hbm_frac")}
+            torch.cuda.empty_cache()
+        # the conv that feeds the scan, prefill and decode update (HBM-bound rows)
+        for only, steps in (("conv", 50), ("conv_update", 100)):
+            rec = time_case(only, None, "auto", steps, 5, device)
+            configs_measured[only] = {k: rec[k] for k in ("case", "ms_median", "Gtokch_s", "GB_s", "hbm_frac")}
             torch.cuda.empty_cache()
 
     hbm_peak, _, peak_kind = _peaks()
@@ -574,6 +590,39 @@ def time_case(only, config, algo, steps, warmup, dev):
         tokch = cfg.tokens_channels
         nbytes = scan_bytes(cfg.batch, cfg.dim, cfg.seqlen, cfg.dstate, ei, eo, cfg.has_z, t["h0"] is not None)
         label = f"scan {cfg.name} ({cfg.batch},{cfg.dim},{cfg.seqlen},{cfg.dstate}) algo={algo}"
+    elif only == "conv":
+        cfg = W.CONV_CONFIGS["conv_mamba130m"]
+        inp = W.make_conv_inputs(cfg)
+        x, w, bias, st = (to_torch(inp[k], dev) for k in ("x", "weight", "bias", "conv_state"))
+        odt = torch.bfloat16 if cfg.out_dtype == W.BF16 else torch.float32
+        out = torch.empty(x.shape, dtype=odt, device=dev)
+        so = torch.empty_like(st)
+
+        def launch():
+            ssm.causal_conv1d_fwd(x, w, bias, st, True, out=out, conv_state_out=so)
+        ei = 2 if cfg.in_dtype == W.BF16 else 4
+        eo = 2 if cfg.out_dtype == W.BF16 else 4
+        tokch = cfg.batch * cfg.dim * cfg.seqlen
+        nbytes = conv_bytes(cfg.batch, cfg.dim, cfg.seqlen, cfg.width, ei, eo)
+        label = f"causal_conv1d {cfg.name} ({cfg.batch},{cfg.dim},{cfg.seqlen}) width={cfg.width}"
+    elif only == "conv_update":
+        cfg = W.CONV_CONFIGS["conv_decode"]
+        # 12 state/input/output sets (12 x 16 MB > the 126 MB L2) taken in turn
+        sets = []
+        for k in range(12):
+            inp = W.make_conv_inputs(dataclasses.replace(cfg, seed_base=cfg.seed_base + 10 * k))
+            sets.append((to_torch(inp["conv_state"], dev), to_torch(inp["x"], dev)[..., 0].contiguous(),
+                         torch.empty((cfg.batch, cfg.dim), dtype=torch.bfloat16, device=dev)))
+        w, bias = to_torch(inp["weight"], dev), to_torch(inp["bias"], dev)
+        k = [0]
+
+        def launch():
+            st, xt, o = sets[k[0] % len(sets)]
+            k[0] += 1
+            ssm.causal_conv1d_update(st, xt, w, bias, True, out=o)
+        tokch = cfg.batch * cfg.dim
+        nbytes = conv_update_bytes(cfg.batch, cfg.dim, cfg.width, 2, 2)
+        label = f"causal_conv1d_update ({cfg.batch},{cfg.dim}) width={cfg.width}"
     else:
         cfg = W.DECODE_CONFIGS["decode"]
         inp = W.make_decode_inputs(cfg)

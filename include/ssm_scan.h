@@ -72,7 +72,8 @@ typedef enum {
     SSM_ERR_UNSUPPORTED_N = -8,     /* dstate not in {1, 2, 4, 8, 16} */
     SSM_ERR_ALIAS = -9,             /* an output overlaps an input it must not */
     SSM_ERR_ALGO = -10,             /* unknown algorithm selector */
-    SSM_ERR_SCRATCH_LIMIT = -11     /* problem needs more than SSM_STATIC_SCRATCH_BYTES of scratch */
+    SSM_ERR_SCRATCH_LIMIT = -11,    /* problem needs more than SSM_STATIC_SCRATCH_BYTES of scratch */
+    SSM_ERR_WIDTH = -12             /* conv width not in 1..4 */
 } ssm_status_t;
 
 /* Algorithm selectors for ssm_scan_fwd_algo. All compute the same result.
@@ -158,6 +159,44 @@ SSM_API int ssm_state_update(float* state, const void* x, const void* delta, con
                              const float* delta_bias, int softplus, void* y, int64_t batch,
                              int64_t dim, int64_t dstate, int in_dtype, int out_dtype,
                              void* stream);
+
+/* Causal depthwise conv1d (+ silu), the step that produces the scan's input u
+ * in the Mamba block (Mamba SSM complete guide (youngju.dev), section 5,
+ * "complete Mamba implementation": MambaBlock.__init__'s depthwise nn.Conv1d
+ * with kernel d_conv = width and padding width - 1, and forward's trim to the
+ * first seqlen outputs followed by silu). PyTorch's Conv1d is a cross-correlation
+ * over the left-padded input, so with xp the input preceded by width-1 earlier
+ * values:
+ *     out[b,d,t] = silu( bias[d] + sum_{k<width} weight[d,k] * xp[b,d,t+k] )
+ * (weight[d,width-1] multiplies x[b,d,t]; no silu when silu == 0).
+ *   x              : (batch, dim, seqlen), in_dtype                [required]
+ *   weight         : (dim, width) fp32, width in 1..4              [required]
+ *   bias           : (dim) fp32                                    [optional]
+ *   conv_state_in  : (batch, dim, width-1) fp32, the width-1 inputs before x,
+ *                    oldest first                         [optional, zeros]
+ *   conv_state_out : (batch, dim, width-1) fp32, receives the last width-1
+ *                    entries of xp (what a following call or the decode update
+ *                    continues from); may be conv_state_in itself  [optional]
+ *   out            : (batch, dim, seqlen), out_dtype               [required]
+ * out overlaps no input. Errors as ssm_scan_fwd, plus SSM_ERR_WIDTH. */
+SSM_API int ssm_causal_conv1d_fwd(const void* x, const float* weight, const float* bias,
+                                  const float* conv_state_in, float* conv_state_out, void* out,
+                                  int64_t batch, int64_t dim, int64_t seqlen, int64_t width,
+                                  int silu, int in_dtype, int out_dtype, void* stream);
+
+/* One decode token of the same convolution, in place on the state:
+ *     out[b,d] = silu( bias[d] + sum_{k<width-1} weight[d,k] * conv_state[b,d,k]
+ *                      + weight[d,width-1] * x[b,d] )
+ * then conv_state[b,d] drops its oldest entry and appends x[b,d].
+ *   conv_state : (batch, dim, width-1) fp32, read and written  [required if width > 1]
+ *   x          : (batch, dim), in_dtype                        [required]
+ *   weight     : (dim, width) fp32; bias (dim) fp32 optional
+ *   out        : (batch, dim), out_dtype                       [required]
+ * out overlaps no input and not the state. */
+SSM_API int ssm_causal_conv1d_update(float* conv_state, const void* x, const float* weight,
+                                     const float* bias, void* out, int64_t batch, int64_t dim,
+                                     int64_t width, int silu, int in_dtype, int out_dtype,
+                                     void* stream);
 
 /* Test hook for the look-back error path. Runs the look-back scan (softplus on,
  * no D, z, bias or h0; y in in_dtype) with segment `drop_segment` withholding

@@ -10,6 +10,8 @@ Entry points (names follow the C ABI):
     scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus, h0) -> (y, h_last)
     scalar_scan_fwd(...)  d_state = 1 (SM1) form of scan_fwd
     state_update(state, x, delta, A, B, C, D, z, delta_bias, softplus) -> y
+    causal_conv1d_fwd(x, weight, bias, conv_state, silu) -> (u, conv_state_out)
+    causal_conv1d_update(conv_state, x, weight, bias, silu) -> u_t
     workspace_size(batch, dim, seqlen, dstate) -> bytes
     query_status(workspace) -> device status word of a look-back scan
 """
@@ -53,17 +55,23 @@ _lib.ssm_query_status.argtypes = [_P, _SZ, _P]
 _lib.ssm_query_status.restype = _I
 _lib.ssm_scan_fwd_lookback_static.argtypes = [_P] * 8 + [_I, _P, _P, _P] + [_I64] * 4 + [_I, _I, _P]
 _lib.ssm_scan_fwd_lookback_static.restype = _I
+_lib.ssm_causal_conv1d_fwd.argtypes = [_P] * 6 + [_I64] * 4 + [_I, _I, _I, _P]
+_lib.ssm_causal_conv1d_fwd.restype = _I
+_lib.ssm_causal_conv1d_update.argtypes = [_P] * 5 + [_I64] * 3 + [_I, _I, _I, _P]
+_lib.ssm_causal_conv1d_update.restype = _I
 
 SSM_F32, SSM_BF16 = 0, 1
 ALGOS = {"auto": 0, "thread": 1, "warpscan": 2, "lookback": 3}
 SSM_ERR_LOOKBACK_TIMEOUT = -7
 SSM_ERR_SCRATCH_LIMIT = -11
+SSM_ERR_WIDTH = -12
 STATIC_SCRATCH_BYTES = 4 << 20   # SSM_STATIC_SCRATCH_BYTES
 
 # the C ABI entry-point names, as declared in include/ssm_scan.h
 EXPORTS = ("ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_size", "ssm_scan_fwd",
            "ssm_scan_fwd_algo", "ssm_scalar_scan_fwd", "ssm_state_update",
-           "ssm_test_lookback_timeout", "ssm_query_status", "ssm_scan_fwd_lookback_static")
+           "ssm_test_lookback_timeout", "ssm_query_status", "ssm_scan_fwd_lookback_static",
+           "ssm_causal_conv1d_fwd", "ssm_causal_conv1d_update")
 
 
 class SSMError(RuntimeError):
@@ -225,6 +233,44 @@ def scan_fwd_lookback_static(u, delta, A, B, C, D=None, z=None, delta_bias=None,
         _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
         int(bool(softplus)), _ptr(h0), _ptr(y), _ptr(h_last), bt, dim, L, N, in_code, _dtype_code(y.dtype),
         _stream()))
+
+
+def causal_conv1d_fwd(x, weight, bias=None, conv_state=None, silu=True, *, out_dtype=None, out=None,
+                      conv_state_out=None, return_state=True):
+    """Causal depthwise conv1d (+ silu) over x (batch, dim, L): weight (dim, width) fp32,
+    bias (dim,), conv_state (batch, dim, width-1) fp32 = the inputs before x (zeros when
+    None). Returns (out (batch, dim, L), conv_state_out (batch, dim, width-1) fp32, or
+    None when return_state is False and no conv_state_out is given)."""
+    bt, dim, L = x.shape
+    width = weight.shape[1]
+    _f32(weight, (dim, width), "weight"); _f32(bias, (dim,), "bias")
+    _f32(conv_state, (bt, dim, width - 1), "conv_state")
+    if out is None:
+        out = torch.empty((bt, dim, L), dtype=out_dtype or x.dtype, device=x.device)
+    if conv_state_out is None and return_state:
+        conv_state_out = torch.empty((bt, dim, width - 1), dtype=torch.float32, device=x.device)
+    _f32(conv_state_out, (bt, dim, width - 1), "conv_state_out")
+    status = _lib.ssm_causal_conv1d_fwd(
+        _ptr(x), _ptr(weight), _ptr(bias), _ptr(conv_state), _ptr(conv_state_out), _ptr(out), bt, dim, L,
+        width, int(bool(silu)), _dtype_code(x.dtype), _dtype_code(out.dtype), _stream())
+    _check(status)
+    return out, conv_state_out
+
+
+def causal_conv1d_update(conv_state, x, weight, bias=None, silu=True, *, out_dtype=None, out=None):
+    """One decode token of the conv: conv_state (batch, dim, width-1) fp32 is updated in
+    place; x (batch, dim). Returns out (batch, dim)."""
+    bt, dim = x.shape
+    width = weight.shape[1]
+    _f32(weight, (dim, width), "weight"); _f32(bias, (dim,), "bias")
+    _f32(conv_state, (bt, dim, width - 1), "conv_state")
+    if out is None:
+        out = torch.empty((bt, dim), dtype=out_dtype or x.dtype, device=x.device)
+    status = _lib.ssm_causal_conv1d_update(
+        _ptr(conv_state), _ptr(x), _ptr(weight), _ptr(bias), _ptr(out), bt, dim, width, int(bool(silu)),
+        _dtype_code(x.dtype), _dtype_code(out.dtype), _stream())
+    _check(status)
+    return out
 
 
 def query_status(workspace) -> int:

@@ -9,6 +9,7 @@
 namespace {
 
 using ssm::DecodeArgs;
+using ssm::ConvArgs;
 using ssm::ScanArgs;
 
 constexpr uint32_t kSpinLimit = 1u << 20;   // look-back waits: ~0.1-1 s before giving up
@@ -209,6 +210,7 @@ const char* ssm_status_string(int status) {
         case SSM_ERR_UNSUPPORTED_N: return "SSM_ERR_UNSUPPORTED_N: dstate must be 1, 2, 4, 8 or 16";
         case SSM_ERR_ALIAS: return "SSM_ERR_ALIAS: an output overlaps an input";
         case SSM_ERR_ALGO: return "SSM_ERR_ALGO: unknown algorithm";
+        case SSM_ERR_WIDTH: return "SSM_ERR_WIDTH: conv width must be 1, 2, 3 or 4";
         case SSM_ERR_SCRATCH_LIMIT:
             return "SSM_ERR_SCRATCH_LIMIT: problem needs more scratch than the library's fixed 4 MiB area";
     }
@@ -315,6 +317,84 @@ int ssm_state_update(float* state, const void* x, const void* delta, const float
             (!z || aligned(z, 16)) && aligned(B, 16) && aligned(C, 16) && (dim * (int64_t)ei) % 16 == 0 &&
             (dstate * (int64_t)ei) % 16 == 0;
     return ssm::launch_state_update(a, (cudaStream_t)stream) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+}
+
+int ssm_causal_conv1d_fwd(const void* x, const float* weight, const float* bias,
+                          const float* conv_state_in, float* conv_state_out, void* out, int64_t batch,
+                          int64_t dim, int64_t seqlen, int64_t width, int silu, int in_dtype,
+                          int out_dtype, void* stream) {
+    if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype)) return SSM_ERR_DTYPE;
+    if (batch < 0 || dim < 0 || seqlen < 0) return SSM_ERR_DIM;
+    if (width < 1 || width > 4) return SSM_ERR_WIDTH;
+    const int64_t n_rows = mul(batch, dim);
+    const int64_t n_x = mul(n_rows, seqlen);
+    const int64_t n_s = mul(n_rows, width - 1);
+    if (n_rows < 0 || n_x < 0 || n_s < 0) return SSM_ERR_DIM;
+    if (n_x > 0 && (!x || !out)) return SSM_ERR_NULL;
+    if (n_rows > 0 && !weight) return SSM_ERR_NULL;
+    const size_t ei = esize(in_dtype), eo = esize(out_dtype);
+    if ((x && !aligned(x, ei)) || (out && !aligned(out, eo))) return SSM_ERR_ALIGN;
+    const void* f32_ptrs[] = {weight, bias, conv_state_in, conv_state_out};
+    for (const void* p : f32_ptrs)
+        if (p && !aligned(p, 4)) return SSM_ERR_ALIGN;
+    const size_t bx = (size_t)n_x * ei, bo = (size_t)n_x * eo, bs = (size_t)n_s * 4,
+                 bw = (size_t)dim * width * 4, bb = (size_t)dim * 4;
+    // out overlaps no input; the outgoing state may be the incoming one exactly
+    if (overlap(out, bo, x, bx) || overlap(out, bo, weight, bw) || overlap(out, bo, bias, bb) ||
+        overlap(out, bo, conv_state_in, bs) || overlap(out, bo, conv_state_out, bs))
+        return SSM_ERR_ALIAS;
+    if (overlap(conv_state_out, bs, x, bx) || overlap(conv_state_out, bs, weight, bw) ||
+        overlap(conv_state_out, bs, bias, bb) ||
+        (conv_state_out != conv_state_in && overlap(conv_state_out, bs, conv_state_in, bs)))
+        return SSM_ERR_ALIAS;
+    ConvArgs a;
+    memset(&a, 0, sizeof(a));
+    a.x = x; a.w = weight; a.bias = bias; a.state_in = conv_state_in; a.state_out = conv_state_out;
+    a.out = out; a.batch = batch; a.dim = dim; a.seqlen = seqlen; a.width = (int)width;
+    a.silu = silu ? 1 : 0; a.in_dtype = in_dtype; a.out_dtype = out_dtype;
+    a.vec = (seqlen * (int64_t)ei) % 16 == 0 && (seqlen * (int64_t)eo) % 16 == 0 && (!x || aligned(x, 16)) &&
+            (!out || aligned(out, 16));
+    // one warp per row unless that leaves the GPU short of warps (about 48 per SM
+    // keep enough loads in flight for HBM): then rows are cut into segments of
+    // whole 32-vector blocks
+    const int64_t blk = ssm::conv_block_steps(in_dtype);
+    const int64_t blocks = (seqlen + blk - 1) / blk;
+    int64_t n_seg = n_rows > 0 ? (kSMs * 48 + n_rows - 1) / n_rows : 1;
+    if (n_seg > blocks) n_seg = blocks;
+    if (n_seg < 1) n_seg = 1;
+    a.seg_len = ((blocks + n_seg - 1) / n_seg) * blk;
+    a.n_seg = seqlen > 0 ? (seqlen + a.seg_len - 1) / a.seg_len : 1;
+    return ssm::launch_causal_conv1d(a, (cudaStream_t)stream) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+}
+
+int ssm_causal_conv1d_update(float* conv_state, const void* x, const float* weight, const float* bias,
+                             void* out, int64_t batch, int64_t dim, int64_t width, int silu, int in_dtype,
+                             int out_dtype, void* stream) {
+    if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype)) return SSM_ERR_DTYPE;
+    if (batch < 0 || dim < 0) return SSM_ERR_DIM;
+    if (width < 1 || width > 4) return SSM_ERR_WIDTH;
+    const int64_t n_rows = mul(batch, dim);
+    const int64_t n_s = mul(n_rows, width - 1);
+    if (n_rows < 0 || n_s < 0) return SSM_ERR_DIM;
+    if (n_rows > 0 && (!x || !out || !weight || (width > 1 && !conv_state))) return SSM_ERR_NULL;
+    const size_t ei = esize(in_dtype), eo = esize(out_dtype);
+    if ((x && !aligned(x, ei)) || (out && !aligned(out, eo))) return SSM_ERR_ALIGN;
+    const void* f32_ptrs[] = {weight, bias, conv_state};
+    for (const void* p : f32_ptrs)
+        if (p && !aligned(p, 4)) return SSM_ERR_ALIGN;
+    const size_t bx = (size_t)n_rows * ei, bo = (size_t)n_rows * eo, bs = (size_t)n_s * 4,
+                 bw = (size_t)dim * width * 4, bb = (size_t)dim * 4;
+    if (overlap(out, bo, x, bx) || overlap(out, bo, weight, bw) || overlap(out, bo, bias, bb) ||
+        overlap(out, bo, conv_state, bs))
+        return SSM_ERR_ALIAS;
+    if (overlap(conv_state, bs, x, bx) || overlap(conv_state, bs, weight, bw) || overlap(conv_state, bs, bias, bb))
+        return SSM_ERR_ALIAS;
+    ConvArgs a;
+    memset(&a, 0, sizeof(a));
+    a.x = x; a.w = weight; a.bias = bias; a.state_out = conv_state; a.out = out;
+    a.batch = batch; a.dim = dim; a.width = (int)width; a.silu = silu ? 1 : 0;
+    a.in_dtype = in_dtype; a.out_dtype = out_dtype;
+    return ssm::launch_conv_update(a, (cudaStream_t)stream) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
 
 int ssm_query_status(const void* workspace, size_t workspace_bytes, void* stream) {

@@ -53,7 +53,28 @@ struct DecodeArgs {
     bool tma;          // state, x, delta, z, B, C rows all 16-byte aligned: bulk-copy streaming
 };
 
+// Causal depthwise conv1d (+ silu), prefill and single-token update.
+struct ConvArgs {
+    const void* x;          // prefill (batch, dim, seqlen); update (batch, dim)
+    const float* w;         // (dim, width)
+    const float* bias;      // (dim) or null
+    const float* state_in;  // prefill: (batch, dim, width-1) or null (zeros)
+    float* state_out;       // prefill: (batch, dim, width-1) or null; update: the state, in/out
+    void* out;              // same shape as x
+    int64_t batch, dim, seqlen;
+    int width;              // 1..4
+    int silu;
+    int in_dtype, out_dtype;
+    bool vec;               // x and out rows 16-byte aligned (prefill vector path)
+    int64_t seg_len;        // prefill: steps per warp segment (a multiple of conv_block_steps)
+    int64_t n_seg;
+};
+
 // Each returns cudaSuccess or the launch error.
+cudaError_t launch_causal_conv1d(const ConvArgs& a, cudaStream_t s);
+cudaError_t launch_conv_update(const ConvArgs& a, cudaStream_t s);
+// steps one warp covers per block of the prefill conv (32 16-byte vectors)
+int conv_block_steps(int in_dtype);
 cudaError_t launch_state_update(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_scan_warp(const ScanArgs& a, cudaStream_t s);
 cudaError_t launch_scan_serial_lookback(const ScanArgs& a, int lanes_per_channel, cudaStream_t s);

@@ -43,7 +43,7 @@ def test_abi_version_matches_header(ssm):
 
 
 def test_status_strings(ssm):
-    for code in range(0, -12, -1):
+    for code in range(0, -13, -1):
         assert ssm.status_string(code).startswith("SSM_")
     assert not ssm.status_string(-99).startswith("SSM_")
 
@@ -119,3 +119,40 @@ def test_state_update_validation(ssm):
 def test_query_status_rejects_small_workspace(ssm):
     assert ssm._lib.ssm_query_status(None, 0, None) == -5
     assert ssm._lib.ssm_query_status(FAKE, 8, None) == -5
+
+
+def test_conv_validation(ssm):
+    f = ssm._lib.ssm_causal_conv1d_fwd
+
+    def call(**kw):
+        a = dict(x=FAKE, w=FAKE * 2, bias=None, sin=None, sout=None, out=FAKE * 3, batch=2, dim=4, L=8, width=4,
+                 silu=1, idt=1, odt=1)
+        a.update(kw)
+        return f(a["x"], a["w"], a["bias"], a["sin"], a["sout"], a["out"], a["batch"], a["dim"], a["L"],
+                 a["width"], a["silu"], a["idt"], a["odt"], None)
+    assert call(idt=3) == -3
+    assert call(width=0) == -12
+    assert call(width=5) == -12
+    assert call(L=-1) == -2
+    assert call(x=None) == -1
+    assert call(w=None) == -1
+    assert call(out=FAKE + 1) == -4                   # bf16 output needs 2-byte alignment
+    assert call(sin=FAKE * 4 + 2) == -4               # fp32 state needs 4
+    assert call(out=FAKE + 32) == -9                  # out overlaps x
+    assert call(sout=FAKE * 2) == -9                  # state out over the weights
+    assert call(sin=FAKE * 4, sout=FAKE * 4 + 4) == -9  # partly over the incoming state
+    assert call(batch=1 << 40, dim=1 << 30) == -2
+
+    g = ssm._lib.ssm_causal_conv1d_update
+
+    def upd(**kw):
+        a = dict(st=FAKE, x=FAKE * 2, w=FAKE * 3, bias=None, out=FAKE * 4, batch=2, dim=4, width=4, silu=1,
+                 idt=1, odt=1)
+        a.update(kw)
+        return g(a["st"], a["x"], a["w"], a["bias"], a["out"], a["batch"], a["dim"], a["width"], a["silu"],
+                 a["idt"], a["odt"], None)
+    assert upd(width=9) == -12
+    assert upd(st=None) == -1
+    assert upd(out=FAKE + 8) == -9                    # out inside the state
+    assert upd(x=FAKE + 16) == -9                     # state overlaps x
+    assert upd(st=FAKE + 2) == -4

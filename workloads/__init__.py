@@ -97,6 +97,28 @@ DECODE_CONFIGS = {
 }
 
 
+@dataclasses.dataclass(frozen=True)
+class ConvConfig:
+    """Causal depthwise conv1d (+ silu) workload: the block's input x before the scan
+    (batch, dim, seqlen), kernel width, and the decode batch for the update."""
+    name: str
+    batch: int
+    dim: int
+    seqlen: int
+    width: int
+    in_dtype: str
+    out_dtype: str
+    seed_base: int
+
+
+CONV_CONFIGS = {
+    # the conv feeding the Mamba-130M-shaped scan (d_conv = 4, the page's default)
+    "conv_mamba130m": ConvConfig("conv_mamba130m", 8, 1536, 2048, 4, BF16, BF16, 6000),
+    # one decode token on the decode workload's (256, 5120) channels
+    "conv_decode": ConvConfig("conv_decode", 256, 5120, 1, 4, BF16, BF16, 7000),
+}
+
+
 def _rng(seed: int) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64(seed))
 
@@ -230,3 +252,26 @@ def make_decode_inputs(cfg: DecodeConfig, batch: Optional[int] = None,
         "softplus": True,
         "sets": sets,
     }
+
+
+def make_conv_inputs(cfg: ConvConfig, batch: Optional[int] = None, dim: Optional[int] = None,
+                     seqlen: Optional[int] = None, width: Optional[int] = None,
+                     with_state: bool = True) -> dict:
+    """Seeded inputs of the causal conv1d: x ~ N(0, 1) in cfg.in_dtype (batch, dim, L);
+    weight (dim, width) and bias (dim) ~ U(-1/sqrt(width), 1/sqrt(width)) fp32 (the
+    bound of PyTorch's default Conv1d init for a depthwise kernel, fan-in = width);
+    conv_state (batch, dim, width-1) = earlier inputs, N(0, 1) rounded like x, held
+    in fp32. Seeds base + {x: 1, weight: 2, bias: 3, state: 4}."""
+    Bt = batch or cfg.batch
+    Dm = dim or cfg.dim
+    L = cfg.seqlen if seqlen is None else seqlen
+    W_ = width or cfg.width
+    sb = cfg.seed_base
+    bound = 1.0 / math.sqrt(W_)
+    out = {"batch": Bt, "dim": Dm, "seqlen": L, "width": W_, "cfg": cfg}
+    out["x"] = Tensor(_normal(sb + 1, (Bt, Dm, L)), cfg.in_dtype)
+    out["weight"] = _rng(sb + 2).uniform(-bound, bound, size=(Dm, W_)).astype(np.float32)
+    out["bias"] = _rng(sb + 3).uniform(-bound, bound, size=(Dm,)).astype(np.float32)
+    st = Tensor(_normal(sb + 4, (Bt, Dm, W_ - 1)), cfg.in_dtype).f32() if with_state else None
+    out["conv_state"] = None if st is None else np.ascontiguousarray(st, dtype=np.float32)
+    return out
