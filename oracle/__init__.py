@@ -67,6 +67,8 @@ class OracleLib:
         lib.oracle_silu.argtypes = [ctypes.c_double]
         lib.oracle_silu.restype = ctypes.c_double
         lib.oracle_max_threads.restype = ctypes.c_int
+        lib.oracle_scan_bwd.argtypes = [P] * 8 + [ctypes.c_int] + [P] * 12 + [I64] * 4 + [ctypes.c_int]
+        lib.oracle_scan_bwd.restype = ctypes.c_int
         lib.oracle_causal_conv1d.argtypes = [P] * 4 + [ctypes.c_int, P, P, I64, I64, I64, I64, ctypes.c_int]
         lib.oracle_causal_conv1d.restype = ctypes.c_int
         lib.oracle_conv_update.argtypes = [P] * 4 + [ctypes.c_int, P, I64, I64, I64, ctypes.c_int]
@@ -127,6 +129,31 @@ class OracleLib:
             raise ValueError("oracle_state_update rejected the sizes")
         return y
 
+
+    def scan_bwd(self, u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, h0=None,
+                 dout=None, dh_last=None, threads: int = 0):
+        """fp64 gradients of the scan for dout = dl/d(out) (batch, dim, L) and dh_last =
+        dl/d(h_last) (batch, dim, N) or None. Returns a dict with du, ddelta, dz (None
+        without z), dA, dB, dC, dD, ddelta_bias, dh0 (fp64)."""
+        u = _f32(u); delta = _f32(delta); A = _f32(A); B = _f32(B); C = _f32(C)
+        D = _f32(D); z = _f32(z); delta_bias = _f32(delta_bias); h0 = _f64(h0)
+        dout = _f64(dout); dh_last = _f64(dh_last)
+        bt, dim, L = u.shape
+        N = A.shape[1]
+        assert dout.shape == u.shape and B.shape == (bt, N, L) and C.shape == (bt, N, L)
+        assert dh_last is None or dh_last.shape == (bt, dim, N)
+        out = {k: np.empty(s_, dtype=np.float64) for k, s_ in (
+            ("du", (bt, dim, L)), ("ddelta", (bt, dim, L)), ("dA", (dim, N)), ("dB", (bt, N, L)),
+            ("dC", (bt, N, L)), ("dD", (dim,)), ("ddelta_bias", (dim,)), ("dh0", (bt, dim, N)))}
+        out["dz"] = np.empty((bt, dim, L), dtype=np.float64) if z is not None else None
+        rc = self.lib.oracle_scan_bwd(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
+                                      int(bool(softplus)), _p(h0), _p(dout), _p(dh_last), _p(out["du"]),
+                                      _p(out["ddelta"]), _p(out["dA"]), _p(out["dB"]), _p(out["dC"]),
+                                      _p(out["dD"]), _p(out["dz"]), _p(out["ddelta_bias"]), _p(out["dh0"]),
+                                      bt, dim, L, N, int(threads))
+        if rc != 0:
+            raise ValueError("oracle_scan_bwd failed")
+        return out
 
     def causal_conv1d(self, x, w, bias=None, conv_state=None, silu=True, threads: int = 0):
         """Causal depthwise conv1d (+ silu) in fp64.
@@ -193,6 +220,10 @@ def scan(*args, **kw):
 
 def state_update(*args, **kw):
     return default().state_update(*args, **kw)
+
+
+def scan_bwd(*args, **kw):
+    return default().scan_bwd(*args, **kw)
 
 
 def causal_conv1d(*args, **kw):

@@ -118,6 +118,132 @@ int oracle_state_update(double *state, const float *x, const float *delta, const
     return 0;
 }
 
+/* Backward of oracle_scan: the gradients of a loss l(out, h_last) given
+ * dout = dl/dout (batch, dim, seqlen) and dh_last = dl/dh_last (or NULL), by the
+ * chain rule through the same operations in reverse (the pages print no
+ * backward; this is the derivative of the forward above, step by step):
+ *   out_t = y_t silu(z_t),  y_t = sum_n C_tn h_tn + D u_t,
+ *   h_tn = a_tn h_{t-1,n} + dt_t B_tn u_t,  a_tn = exp(dt_t A_n),
+ *   dt_t = softplus(delta_t + bias) (or the raw sum).
+ * With g_n = dl/dh_tn accumulated backwards (g starts at dh_last):
+ *   dy = dout silu(z); dz = dout y silu'(z), silu'(z) = s (1 + z (1 - s)), s = sigmoid(z)
+ *   g_n += C_tn dy;  dC_tn += dy h_tn;  dD += dy u;  du += D dy
+ *   d(dt) += sum_n g_n (h_{t-1,n} a_tn A_n + B_tn u);  dA_n += g_n h_{t-1,n} a_tn dt
+ *   dB_tn += g_n dt u;  du += sum_n g_n dt B_tn;  then g_n *= a_tn
+ *   ddelta = d(dt) sigmoid(delta + bias) (softplus' ; 1 without softplus, and the
+ *   identity branch above 20); dbias += ddelta;  finally dh0 = g.
+ * Sums over channels (dB, dC) and over batch rows (dA, dD, dbias) run in a fixed
+ * sequential order after the parallel per-channel loop.
+ *   du, ddelta, dz : (batch, dim, seqlen)   dB, dC : (batch, dstate, seqlen)
+ *   dA : (dim, dstate)   dD, dbias : (dim)   dh0 : (batch, dim, dstate)
+ * dz may be NULL when z is; the others are required. */
+int oracle_scan_bwd(const float *u, const float *delta, const float *A, const float *B,
+                    const float *C, const float *D, const float *z, const float *delta_bias,
+                    int softplus, const double *h0, const double *dout, const double *dh_last,
+                    double *du, double *ddelta, double *dA, double *dB, double *dC, double *dD,
+                    double *dz, double *dbias, double *dh0, int64_t batch, int64_t dim,
+                    int64_t seqlen, int64_t dstate, int nthreads) {
+    if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 1) return -1;
+    int64_t nch = batch * dim, N = dstate, L = seqlen;
+    /* per-channel partials of the cross-channel sums, reduced afterwards */
+    double *pA = (double *)calloc((size_t)(nch * N) + 1, sizeof(double));
+    double *pD = (double *)calloc((size_t)nch + 1, sizeof(double));
+    double *pbias = (double *)calloc((size_t)nch + 1, sizeof(double));
+    double *pB = (double *)calloc((size_t)(nch * N * L) + 1, sizeof(double));
+    double *pC = (double *)calloc((size_t)(nch * N * L) + 1, sizeof(double));
+    if (!pA || !pD || !pbias || !pB || !pC) return -2;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 4)
+#endif
+    for (int64_t ch = 0; ch < nch; ch++) {
+        int64_t b = ch / dim, d = ch % dim;
+        const float *u_r = u + ch * L, *dl_r = delta + ch * L;
+        const float *z_r = z ? z + ch * L : NULL;
+        const float *B_b = B + b * N * L, *C_b = C + b * N * L;
+        const float *A_d = A + d * N;
+        double bias = delta_bias ? (double)delta_bias[d] : 0.0;
+        double Dd = D ? (double)D[d] : 0.0;
+        /* forward, keeping every state: hs[(t + 1) * N + n] = h_tn, hs[n] = h0 */
+        double *hs = (double *)malloc(sizeof(double) * (size_t)((L + 1) * N));
+        double *g = (double *)malloc(sizeof(double) * (size_t)N);
+        for (int64_t n = 0; n < N; n++) hs[n] = h0 ? h0[ch * N + n] : 0.0;
+        for (int64_t t = 0; t < L; t++) {
+            double x = (double)dl_r[t] + bias;
+            double dt = softplus ? oracle_softplus(x) : x;
+            for (int64_t n = 0; n < N; n++)
+                hs[(t + 1) * N + n] = exp(dt * (double)A_d[n]) * hs[t * N + n] +
+                                      dt * (double)B_b[n * L + t] * (double)u_r[t];
+        }
+        for (int64_t n = 0; n < N; n++) g[n] = dh_last ? dh_last[ch * N + n] : 0.0;
+        for (int64_t t = L - 1; t >= 0; t--) {
+            double ut = (double)u_r[t];
+            double x = (double)dl_r[t] + bias;
+            double dt = softplus ? oracle_softplus(x) : x;
+            double yv = Dd * ut;
+            for (int64_t n = 0; n < N; n++) yv += (double)C_b[n * L + t] * hs[(t + 1) * N + n];
+            double dy = dout[ch * L + t];
+            if (z_r) {
+                double zz = (double)z_r[t];
+                double sg = 1.0 / (1.0 + exp(-zz));
+                dz[ch * L + t] = dy * yv * sg * (1.0 + zz * (1.0 - sg));
+                dy *= zz * sg;
+            } else if (dz) {
+                dz[ch * L + t] = 0.0;
+            }
+            pD[ch] += dy * ut;
+            double dut = Dd * dy, ddt = 0.0;
+            for (int64_t n = 0; n < N; n++) {
+                double Cn = (double)C_b[n * L + t], Bn = (double)B_b[n * L + t];
+                double an = exp(dt * (double)A_d[n]);
+                double hprev = hs[t * N + n];
+                g[n] += Cn * dy;
+                pC[(ch * N + n) * L + t] = dy * hs[(t + 1) * N + n];
+                ddt += g[n] * (hprev * an * (double)A_d[n] + Bn * ut);
+                pA[ch * N + n] += g[n] * hprev * an * dt;
+                pB[(ch * N + n) * L + t] = g[n] * dt * ut;
+                dut += g[n] * dt * Bn;
+                g[n] *= an;
+            }
+            double dx = ddt;
+            if (softplus) dx = x > 20.0 ? ddt : ddt / (1.0 + exp(-x));
+            du[ch * L + t] = dut;
+            ddelta[ch * L + t] = dx;
+            pbias[ch] += dx;
+        }
+        for (int64_t n = 0; n < N; n++) dh0[ch * N + n] = g[n];
+        free(hs);
+        free(g);
+    }
+    for (int64_t d = 0; d < dim; d++) {
+        double sD = 0.0, sb = 0.0;
+        for (int64_t b = 0; b < batch; b++) {
+            sD += pD[b * dim + d];
+            sb += pbias[b * dim + d];
+        }
+        dD[d] = sD;
+        dbias[d] = sb;
+        for (int64_t n = 0; n < N; n++) {
+            double sA = 0.0;
+            for (int64_t b = 0; b < batch; b++) sA += pA[(b * dim + d) * N + n];
+            dA[d * N + n] = sA;
+        }
+    }
+    for (int64_t b = 0; b < batch; b++)
+        for (int64_t n = 0; n < N; n++)
+            for (int64_t t = 0; t < L; t++) {
+                double sB = 0.0, sC = 0.0;
+                for (int64_t d = 0; d < dim; d++) {
+                    sB += pB[((b * dim + d) * N + n) * L + t];
+                    sC += pC[((b * dim + d) * N + n) * L + t];
+                }
+                dB[(b * N + n) * L + t] = sB;
+                dC[(b * N + n) * L + t] = sC;
+            }
+    free(pA); free(pD); free(pbias); free(pB); free(pC);
+    return 0;
+}
+
 /* Causal depthwise 1-D convolution and SiLU: the step before the scan in the
  * same page's MambaBlock (section 5, "complete Mamba implementation"): __init__
  * builds nn.Conv1d(d_inner, d_inner, kernel_size=d_conv, groups=d_inner,

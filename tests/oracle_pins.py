@@ -392,6 +392,56 @@ def check_conv_resume_and_decode(orc):
     assert np.array_equal(ss, np.concatenate([st0[..., 1:], x[..., :1].astype(np.float64)], -1))
 
 
+# ---------------------------------------------------------------------------
+# 14. Backward: every gradient equals a central finite difference of the forward
+#     oracle (pinned above) for the loss l = <dout, out> + <dh_last, h_last>, on
+#     dyadic inputs where x +- 2^-10 is exact in fp32.
+# ---------------------------------------------------------------------------
+def check_bwd_finite_differences(orc):
+    rng = np.random.default_rng(37)
+    bt, dim, L, N = 2, 2, 5, 3
+    eps = 2.0 ** -10
+
+    def dy(shape, den=64, lo=-96, hi=96):
+        return (rng.integers(lo, hi + 1, size=shape) / den).astype(np.float32)
+    for with_z, sp in ((True, True), (False, False)):
+        u, delta = dy((bt, dim, L)), dy((bt, dim, L), lo=-64, hi=32)
+        z = dy((bt, dim, L)) if with_z else None
+        B, C = dy((bt, N, L)), dy((bt, N, L))
+        A = -(rng.integers(16, 128, size=(dim, N)) / 64).astype(np.float32)
+        D = dy((dim,))
+        bias = dy((dim,), lo=-32, hi=0)
+        if not sp:       # raw dt must stay positive and modest
+            delta = (rng.integers(4, 48, size=(bt, dim, L)) / 64).astype(np.float32)
+            bias = np.zeros((dim,), np.float32)
+        h0 = rng.standard_normal((bt, dim, N))
+        dout = rng.standard_normal((bt, dim, L))
+        dhl = rng.standard_normal((bt, dim, N))
+
+        def loss(**kw):
+            args = dict(u=u, delta=delta, A=A, B=B, C=C, D=D, z=z, bias=bias, h0=h0)
+            args.update(kw)
+            y, hl = orc.scan(args["u"], args["delta"], args["A"], args["B"], args["C"], args["D"], args["z"],
+                             args["bias"], sp, args["h0"])
+            return float(np.sum(dout * y) + np.sum(dhl * hl))
+        g = orc.scan_bwd(u, delta, A, B, C, D, z, bias, sp, h0, dout, dhl)
+        pairs = [("u", u, "du"), ("delta", delta, "ddelta"), ("B", B, "dB"), ("C", C, "dC"), ("A", A, "dA"),
+                 ("D", D, "dD"), ("bias", bias, "ddelta_bias"), ("h0", h0, "dh0")]
+        if with_z:
+            pairs.append(("z", z, "dz"))
+        for name, arr, gname in pairs:
+            if name == "bias" and not sp:
+                continue
+            fd = np.zeros(arr.shape)
+            for idx in np.ndindex(arr.shape):
+                p_, m_ = arr.copy(), arr.copy()
+                p_[idx] += eps
+                m_[idx] -= eps
+                fd[idx] = (loss(**{name: p_}) - loss(**{name: m_})) / (2 * eps)
+            err = np.max(np.abs(fd - g[gname])) / max(1.0, float(np.max(np.abs(fd))))
+            assert err < 2e-5, (name, with_z, err)
+
+
 ALL_CHECKS = [
     check_bruteforce_rational,
     check_symbolic_two_steps,
@@ -408,4 +458,5 @@ ALL_CHECKS = [
     check_conv_impulse,
     check_conv_library,
     check_conv_resume_and_decode,
+    check_bwd_finite_differences,
 ]

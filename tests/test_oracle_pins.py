@@ -17,7 +17,7 @@ def test_pin(check):
 
 # (name, exact text in ssm_oracle.c, replacement): plausible mistakes.
 MUTANTS = [
-    ("sign_of_A", "exp(dt * (double)A_d[n])", "exp(-dt * (double)A_d[n])"),
+    ("sign_of_A", "double a = exp(dt * (double)A_d[n]);", "double a = exp(-dt * (double)A_d[n]);"),
     ("drop_D", "(D ? (double)D[d] * ut : 0.0)", "0.0"),
     ("B_for_C", "double bu = dt * (double)B_b[n * seqlen + t] * ut;",
      "double bu = dt * (double)C_b[n * seqlen + t] * ut;"),
@@ -46,6 +46,14 @@ MUTANTS = [
      "conv_state_out[ch * hw + j] = xp[seqlen + j - (j > 0)];"),
     ("conv_no_silu", "out[ch * seqlen + t] = silu ? oracle_silu(acc) : acc;", "out[ch * seqlen + t] = acc;"),
     ("conv_update_no_shift", "for (int64_t k = 0; k + 1 < hw; k++) s[k] = s[k + 1];", ""),
+    ("bwd_no_softplus_grad", "if (softplus) dx = x > 20.0 ? ddt : ddt / (1.0 + exp(-x));", ""),
+    ("bwd_no_decay_propagation", "g[n] *= an;", ""),
+    ("bwd_dC_uses_prev_state", "pC[(ch * N + n) * L + t] = dy * hs[(t + 1) * N + n];",
+     "pC[(ch * N + n) * L + t] = dy * hs[t * N + n];"),
+    ("bwd_gate_derivative", "dz[ch * L + t] = dy * yv * sg * (1.0 + zz * (1.0 - sg));",
+     "dz[ch * L + t] = dy * yv * sg;"),
+    ("bwd_dA_missing_dt", "pA[ch * N + n] += g[n] * hprev * an * dt;", "pA[ch * N + n] += g[n] * hprev * an;"),
+    ("bwd_du_missing_skip", "double dut = Dd * dy, ddt = 0.0;", "double dut = 0.0, ddt = 0.0;"),
     ("conv_update_wrong_weight", "acc += (double)w[d * width + hw] * xt;", "acc += (double)w[d * width] * xt;"),
 ]
 
