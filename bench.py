@@ -403,7 +403,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-configs", action="store_true", help="skip timing the other prefill configs")
-    ap.add_argument("--only", choices=["scan", "decode", "conv", "conv_update"],
+    ap.add_argument("--only", choices=["scan", "decode", "conv", "conv_update", "scan_bwd"],
                     help="time one entry point alone on --config (a kernel case for sweeps and ncu)")
     ap.add_argument("--config", default="mamba130m",
                     help="workload of --only: a prefill-scan config name, or 'decode'")
@@ -590,6 +590,26 @@ def time_case(only, config, algo, steps, warmup, dev):
         tokch = cfg.tokens_channels
         nbytes = scan_bytes(cfg.batch, cfg.dim, cfg.seqlen, cfg.dstate, ei, eo, cfg.has_z, t["h0"] is not None)
         label = f"scan {cfg.name} ({cfg.batch},{cfg.dim},{cfg.seqlen},{cfg.dstate}) algo={algo}"
+    elif only == "scan_bwd":
+        cfg = W.CONFIGS[config]
+        inp = W.make_scan_inputs(cfg)
+        t = scan_to_torch(inp, dev)
+        odt = torch.bfloat16 if cfg.out_dtype == W.BF16 else torch.float32
+        dout = torch.randn((cfg.batch, cfg.dim, cfg.seqlen), generator=torch.Generator(dev).manual_seed(1),
+                           device=dev).to(odt)
+        wsb = torch.empty(max(ssm.scan_bwd_workspace_size(cfg.batch, cfg.dim, cfg.seqlen, cfg.dstate), 16),
+                          dtype=torch.uint8, device=dev)
+
+        def launch():
+            ssm.scan_bwd(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], cfg.softplus,
+                         t["h0"], dout=dout, workspace=wsb, want_dh0=False)
+        ei = 2 if cfg.in_dtype == W.BF16 else 4
+        eo = 2 if cfg.out_dtype == W.BF16 else 4
+        tokch = cfg.tokens_channels
+        x = cfg.batch * cfg.dim * cfg.seqlen
+        # inputs u, delta, z, dout, B, C read; du, ddelta, dz written; dB, dC fp32 written
+        nbytes = x * (3 * ei + eo + 3 * ei) + 2 * cfg.batch * cfg.dstate * cfg.seqlen * (ei + 4)
+        label = f"scan_bwd {cfg.name} ({cfg.batch},{cfg.dim},{cfg.seqlen},{cfg.dstate})"
     elif only == "conv":
         cfg = W.CONV_CONFIGS["conv_mamba130m"]
         inp = W.make_conv_inputs(cfg)

@@ -160,6 +160,42 @@ SSM_API int ssm_state_update(float* state, const void* x, const void* delta, con
                              int64_t dim, int64_t dstate, int in_dtype, int out_dtype,
                              void* stream);
 
+/* Bytes of device workspace ssm_scan_bwd needs: the state at every 8-step chunk
+ * start, (batch, dim, ceil(seqlen/8), dstate) fp32. 0 for invalid sizes. */
+SSM_API size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate);
+
+/* Backward of ssm_scan_fwd: the gradients of a loss l given dout = dl/d(y)
+ * (the gated output) and dh_last = dl/d(h_last), by the chain rule through the
+ * forward's steps in reverse time (the pages print no backward). With g =
+ * dl/dh_t carried from the end:
+ *   dy = dout silu(z),  dz = dout y silu'(z),  g += C_t dy,  dC_t += dy h_t,
+ *   dD += dy u_t,  du_t = D dy + sum_n g dt B_t,
+ *   d(dt) = sum_n g (h_{t-1} a A + B_t u_t),  dA += g h_{t-1} a dt,
+ *   dB_t += g dt u_t,  ddelta_t = d(dt) softplus'(delta_t + bias),  dbias += ddelta_t,
+ *   g *= a;  dh0 = g at t = 0.
+ * Inputs as ssm_scan_fwd (same u, delta, A, B, C, D, z, delta_bias, softplus,
+ * h0), plus
+ *   dout    : (batch, dim, seqlen), dout_dtype                       [required]
+ *   dh_last : (batch, dim, dstate) fp32                    [optional, zero]
+ * Outputs (all overwritten):
+ *   du, ddelta : (batch, dim, seqlen), in_dtype                     [required]
+ *   dz         : (batch, dim, seqlen), in_dtype                     [required iff z]
+ *   dA         : (dim, dstate) fp32 (summed over batch rows)        [required]
+ *   dB, dC     : (batch, dstate, seqlen) fp32 (summed over channels) [required]
+ *   dD, ddelta_bias : (dim) fp32                [dD required iff D; optional]
+ *   dh0        : (batch, dim, dstate) fp32                          [optional]
+ *   workspace  : ssm_scan_bwd_workspace_size() bytes, 16-byte aligned
+ * The summed gradients are zeroed on `stream` and accumulated with atomic adds,
+ * so their low bits vary between runs. Outputs overlap no input, the workspace
+ * or each other. */
+SSM_API int ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                         const float* D, const void* z, const float* delta_bias, int softplus,
+                         const float* h0, const void* dout, const float* dh_last, void* du, void* ddelta,
+                         float* dA, float* dB, float* dC, float* dD, void* dz, float* ddelta_bias,
+                         float* dh0, int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                         int in_dtype, int dout_dtype, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
 /* Causal depthwise conv1d (+ silu), the step that produces the scan's input u
  * in the Mamba block (Mamba SSM complete guide (youngju.dev), section 5,
  * "complete Mamba implementation": MambaBlock.__init__'s depthwise nn.Conv1d

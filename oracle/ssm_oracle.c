@@ -132,8 +132,8 @@ int oracle_state_update(double *state, const float *x, const float *delta, const
  *   dB_tn += g_n dt u;  du += sum_n g_n dt B_tn;  then g_n *= a_tn
  *   ddelta = d(dt) sigmoid(delta + bias) (softplus' ; 1 without softplus, and the
  *   identity branch above 20); dbias += ddelta;  finally dh0 = g.
- * Sums over channels (dB, dC) and over batch rows (dA, dD, dbias) run in a fixed
- * sequential order after the parallel per-channel loop.
+ * Sums over channels (dB, dC) run in channel order inside each batch row (rows
+ * in parallel); sums over batch rows (dA, dD, dbias) in a fixed order after.
  *   du, ddelta, dz : (batch, dim, seqlen)   dB, dC : (batch, dstate, seqlen)
  *   dA : (dim, dstate)   dD, dbias : (dim)   dh0 : (batch, dim, dstate)
  * dz may be NULL when z is; the others are required. */
@@ -145,73 +145,77 @@ int oracle_scan_bwd(const float *u, const float *delta, const float *A, const fl
                     int64_t seqlen, int64_t dstate, int nthreads) {
     if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 1) return -1;
     int64_t nch = batch * dim, N = dstate, L = seqlen;
-    /* per-channel partials of the cross-channel sums, reduced afterwards */
+    /* per-channel partials of the sums over batch rows, reduced afterwards */
     double *pA = (double *)calloc((size_t)(nch * N) + 1, sizeof(double));
     double *pD = (double *)calloc((size_t)nch + 1, sizeof(double));
     double *pbias = (double *)calloc((size_t)nch + 1, sizeof(double));
-    double *pB = (double *)calloc((size_t)(nch * N * L) + 1, sizeof(double));
-    double *pC = (double *)calloc((size_t)(nch * N * L) + 1, sizeof(double));
-    if (!pA || !pD || !pbias || !pB || !pC) return -2;
+    if (!pA || !pD || !pbias) return -2;
+    for (int64_t k = 0; k < batch * N * L; k++) { dB[k] = 0.0; dC[k] = 0.0; }
+    /* batch rows in parallel; inside a row the channels run in order d = 0, 1, ...
+     * and add their dB, dC contributions directly (the sum over channels) */
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
-#pragma omp parallel for schedule(dynamic, 4)
+#pragma omp parallel for schedule(dynamic, 1)
 #endif
-    for (int64_t ch = 0; ch < nch; ch++) {
-        int64_t b = ch / dim, d = ch % dim;
-        const float *u_r = u + ch * L, *dl_r = delta + ch * L;
-        const float *z_r = z ? z + ch * L : NULL;
-        const float *B_b = B + b * N * L, *C_b = C + b * N * L;
-        const float *A_d = A + d * N;
-        double bias = delta_bias ? (double)delta_bias[d] : 0.0;
-        double Dd = D ? (double)D[d] : 0.0;
-        /* forward, keeping every state: hs[(t + 1) * N + n] = h_tn, hs[n] = h0 */
+    for (int64_t b = 0; b < batch; b++) {
         double *hs = (double *)malloc(sizeof(double) * (size_t)((L + 1) * N));
         double *g = (double *)malloc(sizeof(double) * (size_t)N);
-        for (int64_t n = 0; n < N; n++) hs[n] = h0 ? h0[ch * N + n] : 0.0;
-        for (int64_t t = 0; t < L; t++) {
-            double x = (double)dl_r[t] + bias;
-            double dt = softplus ? oracle_softplus(x) : x;
-            for (int64_t n = 0; n < N; n++)
-                hs[(t + 1) * N + n] = exp(dt * (double)A_d[n]) * hs[t * N + n] +
-                                      dt * (double)B_b[n * L + t] * (double)u_r[t];
-        }
-        for (int64_t n = 0; n < N; n++) g[n] = dh_last ? dh_last[ch * N + n] : 0.0;
-        for (int64_t t = L - 1; t >= 0; t--) {
-            double ut = (double)u_r[t];
-            double x = (double)dl_r[t] + bias;
-            double dt = softplus ? oracle_softplus(x) : x;
-            double yv = Dd * ut;
-            for (int64_t n = 0; n < N; n++) yv += (double)C_b[n * L + t] * hs[(t + 1) * N + n];
-            double dy = dout[ch * L + t];
-            if (z_r) {
-                double zz = (double)z_r[t];
-                double sg = 1.0 / (1.0 + exp(-zz));
-                dz[ch * L + t] = dy * yv * sg * (1.0 + zz * (1.0 - sg));
-                dy *= zz * sg;
-            } else if (dz) {
-                dz[ch * L + t] = 0.0;
+        const float *B_b = B + b * N * L, *C_b = C + b * N * L;
+        double *dB_b = dB + b * N * L, *dC_b = dC + b * N * L;
+        for (int64_t d = 0; d < dim; d++) {
+            int64_t ch = b * dim + d;
+            const float *u_r = u + ch * L, *dl_r = delta + ch * L;
+            const float *z_r = z ? z + ch * L : NULL;
+            const float *A_d = A + d * N;
+            double bias = delta_bias ? (double)delta_bias[d] : 0.0;
+            double Dd = D ? (double)D[d] : 0.0;
+            /* forward, keeping every state: hs[(t + 1) * N + n] = h_tn, hs[n] = h0 */
+            for (int64_t n = 0; n < N; n++) hs[n] = h0 ? h0[ch * N + n] : 0.0;
+            for (int64_t t = 0; t < L; t++) {
+                double x = (double)dl_r[t] + bias;
+                double dt = softplus ? oracle_softplus(x) : x;
+                for (int64_t n = 0; n < N; n++)
+                    hs[(t + 1) * N + n] = exp(dt * (double)A_d[n]) * hs[t * N + n] +
+                                          dt * (double)B_b[n * L + t] * (double)u_r[t];
             }
-            pD[ch] += dy * ut;
-            double dut = Dd * dy, ddt = 0.0;
-            for (int64_t n = 0; n < N; n++) {
-                double Cn = (double)C_b[n * L + t], Bn = (double)B_b[n * L + t];
-                double an = exp(dt * (double)A_d[n]);
-                double hprev = hs[t * N + n];
-                g[n] += Cn * dy;
-                pC[(ch * N + n) * L + t] = dy * hs[(t + 1) * N + n];
-                ddt += g[n] * (hprev * an * (double)A_d[n] + Bn * ut);
-                pA[ch * N + n] += g[n] * hprev * an * dt;
-                pB[(ch * N + n) * L + t] = g[n] * dt * ut;
-                dut += g[n] * dt * Bn;
-                g[n] *= an;
+            for (int64_t n = 0; n < N; n++) g[n] = dh_last ? dh_last[ch * N + n] : 0.0;
+            for (int64_t t = L - 1; t >= 0; t--) {
+                double ut = (double)u_r[t];
+                double x = (double)dl_r[t] + bias;
+                double dt = softplus ? oracle_softplus(x) : x;
+                double yv = Dd * ut;
+                for (int64_t n = 0; n < N; n++) yv += (double)C_b[n * L + t] * hs[(t + 1) * N + n];
+                double dy = dout[ch * L + t];
+                if (z_r) {
+                    double zz = (double)z_r[t];
+                    double sg = 1.0 / (1.0 + exp(-zz));
+                    dz[ch * L + t] = dy * yv * sg * (1.0 + zz * (1.0 - sg));
+                    dy *= zz * sg;
+                } else if (dz) {
+                    dz[ch * L + t] = 0.0;
+                }
+                pD[ch] += dy * ut;
+                double dut = Dd * dy, ddt = 0.0;
+                for (int64_t n = 0; n < N; n++) {
+                    double Cn = (double)C_b[n * L + t], Bn = (double)B_b[n * L + t];
+                    double an = exp(dt * (double)A_d[n]);
+                    double hprev = hs[t * N + n];
+                    g[n] += Cn * dy;
+                    dC_b[n * L + t] += dy * hs[(t + 1) * N + n];
+                    ddt += g[n] * (hprev * an * (double)A_d[n] + Bn * ut);
+                    pA[ch * N + n] += g[n] * hprev * an * dt;
+                    dB_b[n * L + t] += g[n] * dt * ut;
+                    dut += g[n] * dt * Bn;
+                    g[n] *= an;
+                }
+                double dx = ddt;
+                if (softplus) dx = x > 20.0 ? ddt : ddt / (1.0 + exp(-x));
+                du[ch * L + t] = dut;
+                ddelta[ch * L + t] = dx;
+                pbias[ch] += dx;
             }
-            double dx = ddt;
-            if (softplus) dx = x > 20.0 ? ddt : ddt / (1.0 + exp(-x));
-            du[ch * L + t] = dut;
-            ddelta[ch * L + t] = dx;
-            pbias[ch] += dx;
+            for (int64_t n = 0; n < N; n++) dh0[ch * N + n] = g[n];
         }
-        for (int64_t n = 0; n < N; n++) dh0[ch * N + n] = g[n];
         free(hs);
         free(g);
     }
@@ -229,18 +233,7 @@ int oracle_scan_bwd(const float *u, const float *delta, const float *A, const fl
             dA[d * N + n] = sA;
         }
     }
-    for (int64_t b = 0; b < batch; b++)
-        for (int64_t n = 0; n < N; n++)
-            for (int64_t t = 0; t < L; t++) {
-                double sB = 0.0, sC = 0.0;
-                for (int64_t d = 0; d < dim; d++) {
-                    sB += pB[((b * dim + d) * N + n) * L + t];
-                    sC += pC[((b * dim + d) * N + n) * L + t];
-                }
-                dB[(b * N + n) * L + t] = sB;
-                dC[(b * N + n) * L + t] = sC;
-            }
-    free(pA); free(pD); free(pbias); free(pB); free(pC);
+    free(pA); free(pD); free(pbias);
     return 0;
 }
 

@@ -10,6 +10,7 @@ Entry points (names follow the C ABI):
     scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus, h0) -> (y, h_last)
     scalar_scan_fwd(...)  d_state = 1 (SM1) form of scan_fwd
     state_update(state, x, delta, A, B, C, D, z, delta_bias, softplus) -> y
+    scan_bwd(u, delta, A, B, C, D, z, delta_bias, softplus, h0, dout, dh_last) -> gradients
     causal_conv1d_fwd(x, weight, bias, conv_state, silu) -> (u, conv_state_out)
     causal_conv1d_update(conv_state, x, weight, bias, silu) -> u_t
     workspace_size(batch, dim, seqlen, dstate) -> bytes
@@ -55,6 +56,10 @@ _lib.ssm_query_status.argtypes = [_P, _SZ, _P]
 _lib.ssm_query_status.restype = _I
 _lib.ssm_scan_fwd_lookback_static.argtypes = [_P] * 8 + [_I, _P, _P, _P] + [_I64] * 4 + [_I, _I, _P]
 _lib.ssm_scan_fwd_lookback_static.restype = _I
+_lib.ssm_scan_bwd_workspace_size.argtypes = [_I64] * 4
+_lib.ssm_scan_bwd_workspace_size.restype = _SZ
+_lib.ssm_scan_bwd.argtypes = [_P] * 8 + [_I] + [_P] * 12 + [_I64] * 4 + [_I, _I, _P, _SZ, _P]
+_lib.ssm_scan_bwd.restype = _I
 _lib.ssm_causal_conv1d_fwd.argtypes = [_P] * 6 + [_I64] * 4 + [_I, _I, _I, _P]
 _lib.ssm_causal_conv1d_fwd.restype = _I
 _lib.ssm_causal_conv1d_update.argtypes = [_P] * 5 + [_I64] * 3 + [_I, _I, _I, _P]
@@ -71,7 +76,8 @@ STATIC_SCRATCH_BYTES = 4 << 20   # SSM_STATIC_SCRATCH_BYTES
 EXPORTS = ("ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_size", "ssm_scan_fwd",
            "ssm_scan_fwd_algo", "ssm_scalar_scan_fwd", "ssm_state_update",
            "ssm_test_lookback_timeout", "ssm_query_status", "ssm_scan_fwd_lookback_static",
-           "ssm_causal_conv1d_fwd", "ssm_causal_conv1d_update")
+           "ssm_causal_conv1d_fwd", "ssm_causal_conv1d_update", "ssm_scan_bwd_workspace_size",
+           "ssm_scan_bwd")
 
 
 class SSMError(RuntimeError):
@@ -233,6 +239,44 @@ def scan_fwd_lookback_static(u, delta, A, B, C, D=None, z=None, delta_bias=None,
         _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
         int(bool(softplus)), _ptr(h0), _ptr(y), _ptr(h_last), bt, dim, L, N, in_code, _dtype_code(y.dtype),
         _stream()))
+
+
+def scan_bwd_workspace_size(batch: int, dim: int, seqlen: int, dstate: int) -> int:
+    return int(_lib.ssm_scan_bwd_workspace_size(batch, dim, seqlen, dstate))
+
+
+def scan_bwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, h0=None, *, dout,
+             dh_last=None, workspace=None, want_dh0=True):
+    """Backward of scan_fwd for dout = dl/dy (batch, dim, L) and dh_last = dl/dh_last.
+    Returns a dict: du, ddelta, dz (None without z) in u's dtype; dA, dB, dC, dD (None
+    without D), ddelta_bias (None without delta_bias), dh0 (None unless want_dh0) fp32."""
+    bt, dim, L = u.shape
+    N = A.shape[1]
+    in_code = _dtype_code(u.dtype)
+    _same(u, (("delta", delta, u.shape), ("B", B, (bt, N, L)), ("C", C, (bt, N, L)), ("z", z, u.shape)))
+    _f32(A, (dim, N), "A"); _f32(D, (dim,), "D"); _f32(delta_bias, (dim,), "delta_bias")
+    _f32(h0, (bt, dim, N), "h0"); _f32(dh_last, (bt, dim, N), "dh_last")
+    if tuple(dout.shape) != (bt, dim, L):
+        raise ValueError("dout must have u's shape")
+    dev = u.device
+    f32 = torch.float32
+    g = {"du": torch.empty_like(u), "ddelta": torch.empty_like(u),
+         "dz": torch.empty_like(u) if z is not None else None,
+         "dA": torch.empty((dim, N), dtype=f32, device=dev), "dB": torch.empty((bt, N, L), dtype=f32, device=dev),
+         "dC": torch.empty((bt, N, L), dtype=f32, device=dev),
+         "dD": torch.empty((dim,), dtype=f32, device=dev) if D is not None else None,
+         "ddelta_bias": torch.empty((dim,), dtype=f32, device=dev) if delta_bias is not None else None,
+         "dh0": torch.empty((bt, dim, N), dtype=f32, device=dev) if want_dh0 else None}
+    if workspace is None:
+        need = scan_bwd_workspace_size(bt, dim, L, N)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    status = _lib.ssm_scan_bwd(
+        _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(softplus)),
+        _ptr(h0), _ptr(dout), _ptr(dh_last), _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]),
+        _ptr(g["dC"]), _ptr(g["dD"]), _ptr(g["dz"]), _ptr(g["ddelta_bias"]), _ptr(g["dh0"]), bt, dim, L, N,
+        in_code, _dtype_code(dout.dtype), _ptr(workspace), _nbytes(workspace), _stream())
+    _check(status)
+    return g
 
 
 def causal_conv1d_fwd(x, weight, bias=None, conv_state=None, silu=True, *, out_dtype=None, out=None,

@@ -9,6 +9,7 @@
 namespace {
 
 using ssm::DecodeArgs;
+using ssm::BwdArgs;
 using ssm::ConvArgs;
 using ssm::ScanArgs;
 
@@ -394,7 +395,78 @@ int ssm_causal_conv1d_update(float* conv_state, const void* x, const float* weig
     a.x = x; a.w = weight; a.bias = bias; a.state_out = conv_state; a.out = out;
     a.batch = batch; a.dim = dim; a.width = (int)width; a.silu = silu ? 1 : 0;
     a.in_dtype = in_dtype; a.out_dtype = out_dtype;
+
     return ssm::launch_conv_update(a, (cudaStream_t)stream) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+}
+
+size_t ssm_scan_bwd_workspace_size(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate) {
+    if (batch < 0 || dim < 0 || seqlen < 0 || !valid_n(dstate)) return 0;
+    const int64_t n = mul(mul(mul(batch, dim), (seqlen + 7) / 8), dstate);
+    if (n < 0) return 0;
+    return ssm::scan_bwd_workspace_bytes(batch, dim, seqlen, (int)dstate);
+}
+
+int ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                 const float* D, const void* z, const float* delta_bias, int softplus, const float* h0,
+                 const void* dout, const float* dh_last, void* du, void* ddelta, float* dA, float* dB,
+                 float* dC, float* dD, void* dz, float* ddelta_bias, float* dh0, int64_t batch, int64_t dim,
+                 int64_t seqlen, int64_t dstate, int in_dtype, int dout_dtype, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+    if (!valid_dtype(in_dtype) || !valid_dtype(dout_dtype)) return SSM_ERR_DTYPE;
+    if (batch < 0 || dim < 0 || seqlen < 0) return SSM_ERR_DIM;
+    if (!valid_n(dstate)) return SSM_ERR_UNSUPPORTED_N;
+    const int64_t n_rows = mul(batch, dim);
+    const int64_t n_x = mul(n_rows, seqlen);
+    const int64_t n_bc = mul(mul(batch, dstate), seqlen);
+    const int64_t n_h = mul(n_rows, dstate);
+    if (n_rows < 0 || n_x < 0 || n_bc < 0 || n_h < 0) return SSM_ERR_DIM;
+    if (n_x > 0 && (!u || !delta || !dout || !du || !ddelta || !B || !C || !dB || !dC)) return SSM_ERR_NULL;
+    if (dim > 0 && (!A || !dA)) return SSM_ERR_NULL;
+    if (n_x > 0 && z && !dz) return SSM_ERR_NULL;
+    if (dim > 0 && D && !dD) return SSM_ERR_NULL;
+    const size_t ei = esize(in_dtype), eo = esize(dout_dtype);
+    const void* in_ptrs[] = {u, delta, z, B, C, du, ddelta, dz};
+    for (const void* q : in_ptrs)
+        if (q && !aligned(q, ei)) return SSM_ERR_ALIGN;
+    if (dout && !aligned(dout, eo)) return SSM_ERR_ALIGN;
+    const void* f32_ptrs[] = {A, D, delta_bias, h0, dh_last, dA, dB, dC, dD, ddelta_bias, dh0};
+    for (const void* q : f32_ptrs)
+        if (q && !aligned(q, 4)) return SSM_ERR_ALIGN;
+    // checkpoints are read and written as 16-byte vectors
+    if (workspace && !aligned(workspace, 16)) return SSM_ERR_ALIGN;
+    const size_t need = ssm::scan_bwd_workspace_bytes(batch, dim, seqlen, (int)dstate);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return SSM_ERR_WORKSPACE;
+    // outputs overlap no input and no other output
+    const size_t bx = (size_t)n_x * ei, bo = (size_t)n_x * eo, bbc = (size_t)n_bc * ei, bbc4 = (size_t)n_bc * 4,
+                 bh = (size_t)n_h * 4, bA = (size_t)dim * dstate * 4, bd = (size_t)dim * 4;
+    const struct { const void* p; size_t n; } ins[] = {{u, bx}, {delta, bx}, {z, bx}, {B, bbc}, {C, bbc},
+                                                        {A, bA}, {D, bd}, {delta_bias, bd}, {h0, bh},
+                                                        {dout, bo}, {dh_last, bh}, {workspace, need}};
+    const struct { const void* p; size_t n; } outs[] = {{du, bx}, {ddelta, bx}, {dz, bx}, {dA, bA}, {dB, bbc4},
+                                                         {dC, bbc4}, {dD, bd}, {ddelta_bias, bd}, {dh0, bh}};
+    for (const auto& o : outs) {
+        for (const auto& i : ins)
+            if (overlap(o.p, o.n, i.p, i.n)) return SSM_ERR_ALIAS;
+        for (const auto& o2 : outs)
+            if (&o2 != &o && overlap(o.p, o.n, o2.p, o2.n)) return SSM_ERR_ALIAS;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    // the accumulated gradients start at zero
+    const struct { void* p; size_t n; } acc[] = {{dA, bA}, {dB, bbc4}, {dC, bbc4}, {dD, bd}, {ddelta_bias, bd}};
+    for (const auto& z0 : acc)
+        if (z0.p && z0.n && cudaMemsetAsync(z0.p, 0, z0.n, s) != cudaSuccess) return SSM_ERR_LAUNCH;
+    BwdArgs a;
+    memset(&a, 0, sizeof(a));
+    a.u = u; a.delta = delta; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.delta_bias = delta_bias;
+    a.h0 = h0; a.dout = dout; a.dh_last = dh_last; a.du = du; a.ddelta = ddelta; a.dz = dz; a.dA = dA;
+    a.dB = dB; a.dC = dC; a.dD = dD; a.ddelta_bias = ddelta_bias; a.dh0 = dh0; a.workspace = workspace;
+    a.batch = batch; a.dim = dim; a.seqlen = seqlen; a.dstate = (int)dstate; a.softplus = softplus ? 1 : 0;
+    a.in_dtype = in_dtype; a.dout_dtype = dout_dtype;
+    bool vec = (seqlen * (int64_t)ei) % 16 == 0 && (seqlen * (int64_t)eo) % 16 == 0;
+    const void* vec_ptrs[] = {u, delta, z, dout, du, ddelta, dz};
+    for (const void* q : vec_ptrs) vec = vec && (!q || aligned(q, 16));
+    a.vec = vec;
+    return ssm::launch_scan_bwd(a, s) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
 
 int ssm_query_status(const void* workspace, size_t workspace_bytes, void* stream) {

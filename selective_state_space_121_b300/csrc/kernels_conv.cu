@@ -22,9 +22,11 @@
 // block, so each load and store instruction moves 512 contiguous bytes. The W-1
 // inputs before a lane's vector come from lane i-1 by shuffle; lane 0 takes the
 // previous block's last inputs (carried in registers) or, at the segment start,
-// reads them from x (or the conv state). The next block is loaded while the
-// current one computes. Rows are cut into segments only when there are too few
-// rows to fill the GPU.
+// reads them from x (or the conv state). Each lane keeps its next four vectors
+// in flight. Rows are cut into segments only when there are too few rows to
+// fill the GPU.
+#include <string.h>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -33,18 +35,6 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
-
-// V consecutive inputs at row[t ..] widened to fp32; zero past L.
-template <typename T, bool kVec>
-__device__ __forceinline__ void load_v(const T* row, int64_t t, int64_t L, float* out) {
-    constexpr int V = Vec16<T>::kN;
-    if (kVec && t + V <= L) {
-        Vec16<T>::load(row + t, out);
-        return;
-    }
-#pragma unroll
-    for (int k = 0; k < V; k++) out[k] = (t + k < L) ? to_f32(row[t + k]) : 0.f;
-}
 
 // V outputs at row[t ..], those before te only.
 template <typename Tout, int V, bool kVec>
@@ -76,6 +66,42 @@ __device__ __forceinline__ float padded(const Tin* xr, const float* st, int hw, 
     return st ? st[hw + tau] : 0.f;
 }
 
+// raw 16-byte vector at row[t ..] (zero past L; element loads when not whole)
+template <typename T, bool kVec>
+__device__ __forceinline__ uint4 load_raw(const T* row, int64_t t, int64_t L) {
+    constexpr int V = Vec16<T>::kN;
+    if (kVec && t + V <= L) return __ldg(reinterpret_cast<const uint4*>(row + t));
+    float f[V];
+#pragma unroll
+    for (int k = 0; k < V; k++) f[k] = (t + k < L) ? to_f32(row[t + k]) : 0.f;
+    T tmp[V];
+#pragma unroll
+    for (int k = 0; k < V; k++) tmp[k] = from_f32<T>(f[k]);
+    uint4 r;
+    memcpy(&r, tmp, 16);
+    return r;
+}
+
+template <typename T>
+__device__ __forceinline__ void widen(const uint4& r, float* out) {
+    if constexpr (sizeof(T) == 2) {
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            out[2 * i] = __uint_as_float(w[i] << 16);
+            out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    } else {
+        out[0] = __uint_as_float(r.x); out[1] = __uint_as_float(r.y);
+        out[2] = __uint_as_float(r.z); out[3] = __uint_as_float(r.w);
+    }
+}
+
+// blocks of 32 vectors each lane keeps in flight: 4 x 512 bytes per warp, so the
+// ~32 resident warps of an SM hold ~64 KB of loads in flight (HBM latency x the
+// SM's share of the bandwidth)
+constexpr int kDepth = 4;
+
 template <typename Tin, typename Tout, int W, bool kVec>
 __global__ void __launch_bounds__(kThreads) causal_conv1d_kernel(ConvArgs a) {
     constexpr bool kAcc = sizeof(Tin) == 4;
@@ -97,6 +123,13 @@ __global__ void __launch_bounds__(kThreads) causal_conv1d_kernel(ConvArgs a) {
     for (int k = 0; k < W; k++) w[k] = a.w[d * W + k];
     const float bias = a.bias ? a.bias[d] : 0.f;
 
+    // the first blocks' loads go out before anything else
+    const int64_t nblk = te > tb ? (te - tb + 32 * V - 1) / (32 * V) : 0;
+    uint4 ring[kDepth];
+#pragma unroll
+    for (int u = 0; u < kDepth; u++)
+        if (u < nblk) ring[u] = load_raw<Tin, kVec>(xr, tb + (int64_t)(u * 32 + lane) * V, L);
+
     // inputs before the segment (every lane holds them; lane 0 uses them)
     float h[HA];
 #pragma unroll
@@ -113,61 +146,90 @@ __global__ void __launch_bounds__(kThreads) causal_conv1d_kernel(ConvArgs a) {
         for (int j = 0; j < HW; j++) a.state_out[row * HW + j] = so[j];
     }
 
-    float nv[V];
-    if (tb < te) load_v<Tin, kVec>(xr, tb + (int64_t)lane * V, L, nv);
-    for (int64_t blk = tb; blk < te; blk += 32 * V) {
-        const int64_t t = blk + (int64_t)lane * V;
-        float v[V];
+    for (int64_t b0 = 0; b0 < nblk; b0 += kDepth) {
 #pragma unroll
-        for (int k = 0; k < V; k++) v[k] = nv[k];
-        if (blk + 32 * V < te) load_v<Tin, kVec>(xr, t + 32 * V, L, nv);
-        // the W-1 inputs before this lane's vector
-        float prev[HA];
+        for (int u = 0; u < kDepth; u++) {
+            const int64_t bk = b0 + u;
+            if (bk >= nblk) break;                   // warp-uniform
+            const int64_t t = tb + (bk * 32 + lane) * V;
+            float v[V];
+            widen<Tin>(ring[u], v);
+            if (bk + kDepth < nblk) ring[u] = load_raw<Tin, kVec>(xr, t + (int64_t)kDepth * 32 * V, L);
+            // the W-1 inputs before this lane's vector
+            float prev[HA];
 #pragma unroll
-        for (int j = 0; j < HW; j++) {
-            const float up = __shfl_up_sync(0xffffffffu, v[V - HW + j], 1);
-            prev[j] = lane == 0 ? h[j] : up;
-        }
-#pragma unroll
-        for (int j = 0; j < HW; j++) h[j] = __shfl_sync(0xffffffffu, v[V - HW + j], 31);
-        float o[V];
-#pragma unroll
-        for (int k = 0; k < V; k++) {
-            float acc = bias;
-#pragma unroll
-            for (int i = 0; i < W; i++) {
-                const int e = k + i;   // index into prev ++ v
-                acc = fmaf(w[i], e < HW ? prev[e] : v[e - HW], acc);
+            for (int j = 0; j < HW; j++) {
+                const float up = __shfl_up_sync(0xffffffffu, v[V - HW + j], 1);
+                prev[j] = lane == 0 ? h[j] : up;
             }
-            o[k] = a.silu ? silu_acc<kAcc>(acc) : acc;
+#pragma unroll
+            for (int j = 0; j < HW; j++) h[j] = __shfl_sync(0xffffffffu, v[V - HW + j], 31);
+            float o[V];
+#pragma unroll
+            for (int k = 0; k < V; k++) {
+                float acc = bias;
+#pragma unroll
+                for (int i = 0; i < W; i++) {
+                    const int e = k + i;   // index into prev ++ v
+                    acc = fmaf(w[i], e < HW ? prev[e] : v[e - HW], acc);
+                }
+                o[k] = a.silu ? silu_acc<kAcc>(acc) : acc;
+            }
+            if (t < te) store_v<Tout, V, kVec>(orow, t, te, o);
         }
-        if (t < te) store_v<Tout, V, kVec>(orow, t, te, o);
     }
 }
 
-// One decode token per (b, d) thread: the state row (W-1 fp32 inputs, oldest
-// first) and x give the output; the state drops its oldest entry and takes x.
+// One decode token of the conv. A thread takes kUpdCh = 4 channels spaced by the
+// grid's thread count, so each load instruction of a warp reads consecutive
+// channels (coalesced), and issues all their loads before any arithmetic: 4W
+// loads in flight per thread. (One channel per thread leaves the kernel waiting
+// on HBM latency; 4 or 8 consecutive channels per thread with 16-byte state
+// vectors measured slower: a warp's vector loads then stride over 4-8 times the
+// bytes per instruction.) Each channel's output uses (state, x); its state drops
+// the oldest entry and takes x.
+constexpr int kUpdCh = 4;
+
+template <int W>
+__device__ __forceinline__ float conv_token(const ConvArgs& a, int64_t d, const float* s, float xt) {
+    float acc = a.bias ? a.bias[d] : 0.f;
+#pragma unroll
+    for (int j = 0; j < W - 1; j++) acc = fmaf(a.w[d * W + j], s[j], acc);
+    return fmaf(a.w[d * W + W - 1], xt, acc);
+}
+
 template <typename Tin, typename Tout, int W>
 __global__ void __launch_bounds__(256) conv_update_kernel(ConvArgs a) {
     constexpr bool kAcc = sizeof(Tin) == 4;
     constexpr int HW = W - 1;
     constexpr int HA = HW > 0 ? HW : 1;
-    const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
-    if (i >= a.batch * a.dim) return;
-    const int64_t d = i % a.dim;
-    float* st = a.state_out + i * HW;
-    float s[HA];
+    const int64_t n = a.batch * a.dim;
+    const int64_t stride = (int64_t)gridDim.x * 256;
+    const int64_t i0 = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    const Tin* xp = static_cast<const Tin*>(a.x);
+    Tout* op = static_cast<Tout*>(a.out);
+    float s[kUpdCh][HA], xt[kUpdCh];
 #pragma unroll
-    for (int j = 0; j < HW; j++) s[j] = st[j];
-    const float xt = to_f32(static_cast<const Tin*>(a.x)[i]);
-    float acc = a.bias ? a.bias[d] : 0.f;
+    for (int c = 0; c < kUpdCh; c++) {
+        const int64_t i = i0 + c * stride;
+        if (i < n) {
 #pragma unroll
-    for (int j = 0; j < HW; j++) acc = fmaf(a.w[d * W + j], s[j], acc);
-    acc = fmaf(a.w[d * W + HW], xt, acc);
-    static_cast<Tout*>(a.out)[i] = from_f32<Tout>(a.silu ? silu_acc<kAcc>(acc) : acc);
+            for (int j = 0; j < HW; j++) s[c][j] = a.state_out[i * HW + j];
+            xt[c] = to_f32(xp[i]);
+        }
+    }
 #pragma unroll
-    for (int j = 0; j + 1 < HW; j++) st[j] = s[j + 1];
-    if constexpr (HW > 0) st[HW - 1] = xt;
+    for (int c = 0; c < kUpdCh; c++) {
+        const int64_t i = i0 + c * stride;
+        if (i < n) {
+            const float acc = conv_token<W>(a, i % a.dim, s[c], xt[c]);
+            op[i] = from_f32<Tout>(a.silu ? silu_acc<kAcc>(acc) : acc);
+            float* st = a.state_out + i * HW;
+#pragma unroll
+            for (int j = 0; j + 1 < HW; j++) st[j] = s[c][j + 1];
+            if constexpr (HW > 0) st[HW - 1] = xt[c];
+        }
+    }
 }
 
 template <typename Tin, typename Tout, int W>
@@ -185,7 +247,9 @@ template <typename Tin, typename Tout, int W>
 cudaError_t launch_upd(const ConvArgs& a, cudaStream_t s) {
     const int64_t n = a.batch * a.dim;
     if (n == 0) return cudaSuccess;
-    conv_update_kernel<Tin, Tout, W><<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a);
+    const int64_t ctas = ((n + kUpdCh - 1) / kUpdCh + 255) / 256;
+    if (ctas > ((int64_t)1 << 31) - 1) return cudaErrorInvalidValue;
+    conv_update_kernel<Tin, Tout, W><<<(unsigned)ctas, 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 

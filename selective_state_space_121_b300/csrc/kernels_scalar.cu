@@ -27,6 +27,8 @@
 //    the N-state kernels: for fp32 inputs decays are carried as expm1 and the
 //    state as an anchored pair, so a slowly decaying large state is rounded once
 //    per output; for bf16 inputs the plain SFU form.
+#include <type_traits>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -107,31 +109,58 @@ __global__ void __maxnreg__((kZ || kD) ? 128 : SSM_SCALAR_MAXNREG) scalar_scan_k
     const float Dd = (kD && ok) ? a.D[d] : 0.f;
     float carry = (ok && a.h0) ? a.h0[row] : 0.f, carry_lo = 0.f;
 
-    // the next chunk's inputs are loaded while the current one computes
+    // The next chunk's inputs are loaded while the current one computes: u, delta
+    // and B once the current ones are consumed (after the first pass), C and z
+    // after the last use of the current ones (after the second pass), so no
+    // register copies are needed. Whole chunks (all but the last) skip every
+    // bounds check: one warp-uniform test per chunk.
     float nu[kK], nd[kK], nB[kK], nC[kK], nz[kK];
-    auto prefetch = [&](int64_t t) {
-        load_k<Tin, kVec>(up, t, L, ok, nu);
-        load_k<Tin, kVec>(dp, t, L, ok, nd);
-        load_k<Tin, kVec>(Bp, t, L, ok, nB);
-        load_k<Tin, kVec>(Cp, t, L, ok, nC);
-        if constexpr (kZ) load_k<Tin, kVec>(zp, t, L, ok, nz);
-    };
-    if (L > 0) prefetch((int64_t)s * kK);
-    for (int64_t t0 = 0; t0 < L; t0 += kChunk) {
-        const int64_t t = t0 + (int64_t)s * kK;
-        float du[kK], p[kK], bb[kK], zz[kK], C[kK];
+    const int64_t t_l = (int64_t)s * kK;   // the lane's first step within a chunk
+    auto load_run = [&](const Tin* row, int64_t t, bool full, float* out) {
+        if (kVec && full && ok) {
+            constexpr int V = Vec16<Tin>::kN;
 #pragma unroll
-        for (int k = 0; k < kK; k++) {
-            const float x = nd[k] + bias;
-            float dt = a.softplus ? softplus_acc<kAcc>(x) : x;
-            if (t + k >= L) dt = 0.f;                 // identity step past the end
-            if constexpr (kD) du[k] = Dd * nu[k];
-            if constexpr (kZ) zz[k] = nz[k];
-            C[k] = nC[k];
-            p[k] = Dec::make(dt * Ad);
-            bb[k] = dt * nu[k] * nB[k];
+            for (int k = 0; k < kK; k += V) Vec16<Tin>::load(row + t + k, out + k);
+        } else {
+            load_k<Tin, kVec>(row, t, L, ok, out);
         }
-        if (t0 + kChunk < L) prefetch(t + kChunk);
+    };
+    if (L > 0) {
+        const bool full = kChunk <= L;
+        load_run(up, t_l, full, nu);
+        load_run(dp, t_l, full, nd);
+        load_run(Bp, t_l, full, nB);
+        load_run(Cp, t_l, full, nC);
+        if constexpr (kZ) load_run(zp, t_l, full, nz);
+    }
+    for (int64_t t0 = 0; t0 < L; t0 += kChunk) {
+        const int64_t t = t0 + t_l;
+        const bool full = t0 + kChunk <= L;            // warp-uniform
+        const bool next_full = t0 + 2 * kChunk <= L;
+        const bool has_next = t0 + kChunk < L;
+        float du[kK], p[kK], bb[kK];
+        // steps of this lane's run inside the sequence
+        const int nvalid = full ? kK : (int)max((int64_t)0, min((int64_t)kK, L - t));
+        auto first = [&](auto check) {
+#pragma unroll
+            for (int k = 0; k < kK; k++) {
+                const float x = nd[k] + bias;
+                float dt = a.softplus ? softplus_acc<kAcc>(x) : x;
+                if constexpr (decltype(check)::value) {
+                    if (k >= nvalid) dt = 0.f;         // identity step past the end
+                }
+                if constexpr (kD) du[k] = Dd * nu[k];
+                p[k] = Dec::make(dt * Ad);
+                bb[k] = dt * nu[k] * nB[k];
+            }
+        };
+        if (full) first(std::false_type{});
+        else first(std::true_type{});
+        if (has_next) {
+            load_run(up, t + kChunk, next_full, nu);
+            load_run(dp, t + kChunk, next_full, nd);
+            load_run(Bp, t + kChunk, next_full, nB);
+        }
         // fold the lane's steps into one map (P, H), then scan the 8 lane maps
         float P = Dec::one(), H = 0.f;
 #pragma unroll
@@ -153,7 +182,12 @@ __global__ void __maxnreg__((kZ || kD) ? 128 : SSM_SCALAR_MAXNREG) scalar_scan_k
         if (s == 0) { Pe = Dec::one(); He = 0.f; }
         const float Pt = __shfl_sync(0xffffffffu, P, kSeg - 1, kSeg);
         const float Ht = __shfl_sync(0xffffffffu, H, kSeg - 1, kSeg);
-        float y[kK];
+        float y[kK], C[kK], zz[kK];
+#pragma unroll
+        for (int k = 0; k < kK; k++) {
+            C[k] = nC[k];
+            if constexpr (kZ) zz[k] = nz[k];
+        }
         if constexpr (kAcc) {
             float dlt = fmaf(Pe, carry, He) + carry_lo;
             float h = carry + dlt;
@@ -172,6 +206,10 @@ __global__ void __maxnreg__((kZ || kD) ? 128 : SSM_SCALAR_MAXNREG) scalar_scan_k
                 y[k] = C[k] * h;
             }
             carry = Dec::step(Pt, carry, Ht);
+        }
+        if (has_next) {
+            load_run(Cp, t + kChunk, next_full, nC);
+            if constexpr (kZ) load_run(zp, t + kChunk, next_full, nz);
         }
 #pragma unroll
         for (int k = 0; k < kK; k++) {

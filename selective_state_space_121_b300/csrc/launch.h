@@ -65,12 +65,44 @@ struct ConvArgs {
     int width;              // 1..4
     int silu;
     int in_dtype, out_dtype;
-    bool vec;               // x and out rows 16-byte aligned (prefill vector path)
+    bool vec;               // prefill: x and out rows 16-byte aligned (vector path)
     int64_t seg_len;        // prefill: steps per warp segment (a multiple of conv_block_steps)
     int64_t n_seg;
 };
 
+// Backward of the selective scan.
+struct BwdArgs {
+    const void* u;
+    const void* delta;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const void* z;
+    const float* delta_bias;
+    const float* h0;
+    const void* dout;
+    const float* dh_last;
+    void* du;               // in_dtype
+    void* ddelta;           // in_dtype
+    void* dz;               // in_dtype (when z)
+    float* dA;              // accumulated (zeroed by the host first)
+    float* dB;
+    float* dC;
+    float* dD;
+    float* ddelta_bias;
+    float* dh0;
+    void* workspace;        // checkpoints, scan_bwd_workspace_bytes
+    int64_t batch, dim, seqlen;
+    int dstate;
+    int softplus;
+    int in_dtype, dout_dtype;
+    bool vec;               // rows of u/delta/z/dout/du/ddelta/dz 16-byte aligned
+};
+
 // Each returns cudaSuccess or the launch error.
+cudaError_t launch_scan_bwd(const BwdArgs& a, cudaStream_t s);
+size_t scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate);
 cudaError_t launch_causal_conv1d(const ConvArgs& a, cudaStream_t s);
 cudaError_t launch_conv_update(const ConvArgs& a, cudaStream_t s);
 // steps one warp covers per block of the prefill conv (32 16-byte vectors)

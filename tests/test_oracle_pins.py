@@ -48,8 +48,8 @@ MUTANTS = [
     ("conv_update_no_shift", "for (int64_t k = 0; k + 1 < hw; k++) s[k] = s[k + 1];", ""),
     ("bwd_no_softplus_grad", "if (softplus) dx = x > 20.0 ? ddt : ddt / (1.0 + exp(-x));", ""),
     ("bwd_no_decay_propagation", "g[n] *= an;", ""),
-    ("bwd_dC_uses_prev_state", "pC[(ch * N + n) * L + t] = dy * hs[(t + 1) * N + n];",
-     "pC[(ch * N + n) * L + t] = dy * hs[t * N + n];"),
+    ("bwd_dC_uses_prev_state", "dC_b[n * L + t] += dy * hs[(t + 1) * N + n];",
+     "dC_b[n * L + t] += dy * hs[t * N + n];"),
     ("bwd_gate_derivative", "dz[ch * L + t] = dy * yv * sg * (1.0 + zz * (1.0 - sg));",
      "dz[ch * L + t] = dy * yv * sg;"),
     ("bwd_dA_missing_dt", "pA[ch * N + n] += g[n] * hprev * an * dt;", "pA[ch * N + n] += g[n] * hprev * an;"),
