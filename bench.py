@@ -490,9 +490,10 @@ def main():
             rec = time_case("scan", name, "auto", steps, 3, device)
             configs_measured[name] = {k: rec[k] for k in ("case", "ms_median", "Gtokch_s", "GB_s", "hbm_frac")}
             torch.cuda.empty_cache()
-        # the conv that feeds the scan, prefill and decode update (HBM-bound rows)
-        for only, steps in (("conv", 50), ("conv_update", 100)):
-            rec = time_case(only, None, "auto", steps, 5, device)
+        # the conv that feeds the scan (prefill and decode update, HBM-bound) and the
+        # scan's backward on the Mamba-130M-shaped layer
+        for only, cfgname, steps in (("conv", None, 50), ("conv_update", None, 100), ("scan_bwd", "mamba130m", 5)):
+            rec = time_case(only, cfgname, "auto", steps, 3, device)
             configs_measured[only] = {k: rec[k] for k in ("case", "ms_median", "Gtokch_s", "GB_s", "hbm_frac")}
             torch.cuda.empty_cache()
 

@@ -18,17 +18,24 @@
 //
 // Layout: as the forward's serial kernel, G lanes per channel (NPL = min(N, 4)
 // states each), P = 32/G channels per warp, the lanes of one state group
-// consecutive; a CTA holds 4 warps of one batch row. Two phases:
+// consecutive; a CTA holds 4 warps of one batch row. Time goes in tiles of
+// 8-32 steps; each tile's inputs are loaded into registers one tile ahead, then
+// staged in shared memory: B and C for the CTA's batch row, and per (channel,
+// step) {dt, u, dout silu(z), dout silu'(z)} and softplus', computed once (one
+// lane per 16-byte vector of a channel) rather than by each of a channel's G
+// lanes. Two phases:
 //   1. forward over the whole sequence, h only, writing the state at every
 //      8-step chunk start to the workspace (B, D, ceil(L/8), N) fp32;
-//   2. chunks in reverse: the chunk's 8 states are recomputed from its checkpoint
-//      into registers, then the 8 steps run backwards. Per step, the per-channel
-//      sums (y for dz, d(dt), du) are xor-shuffle reductions over the channel's G
-//      lanes; dB and dC of the step are reduce-scattered over the warp's P
-//      channels (each lane ends with one (n, B-or-C) total) and added to global
-//      memory with one atomic per lane. B and C of a chunk are staged in shared
-//      memory for the CTA's channels (one batch row).
+//   2. tiles in reverse, and the tile's 8-step chunks in reverse: the chunk's
+//      states are recomputed from its checkpoint into registers, then its steps
+//      run backwards. Per step, the per-channel sums (y for dz, d(dt), du) are
+//      xor-shuffle reductions over the channel's G lanes; dB and dC of the step
+//      are reduce-scattered over the warp's P channels (each lane ends with one
+//      (n, B-or-C) total), the 4 warps' totals meet in shared memory, and one
+//      atomic add per (step, n, B-or-C) per CTA goes to global memory.
 // fp32 arithmetic; for fp32 inputs exp and softplus take the accurate forms.
+#include <string.h>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -37,43 +44,107 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kT = 8;   // steps per chunk (checkpoint spacing)
+constexpr int kC = 8;   // steps per checkpoint chunk
 
-template <int N> struct BwdCfg {
+template <int N, typename Tin> struct BwdCfg {
     static constexpr int NPL = N < 4 ? N : 4;   // states per lane
     static constexpr int G = N / NPL;           // lanes per channel
     static constexpr int P = 32 / G;            // channels per warp
     static constexpr int M = 2 * NPL;           // dB and dC values per lane-step
+    static constexpr int V = 16 / (int)sizeof(Tin);                    // steps per 16-byte vector
+    static constexpr int kTile = 32 * V / P > kC ? 32 * V / P : kC;    // steps per tile
+    static constexpr int VPT = kTile / V;                              // vectors per (channel, tile)
+    static constexpr int PV = P * VPT / 32;                            // prologue vectors per lane
+    static constexpr int BCV = 2 * N * VPT;                            // B/C vectors per tile
+    static_assert(PV >= 1 && P * VPT % 32 == 0 && kTile % kC == 0, "tile shape");
+    static_assert(BCV <= kThreads, "one B/C vector per thread");
 };
 
-// kT values of row[t ..] as fp32 (zero past L or when !ok)
+// 16 bytes at row[t .. t+V) with zero fill past L (one vector load when whole)
 template <typename T, bool kVec>
-__device__ __forceinline__ void load_run(const T* row, int64_t t, int64_t L, bool ok, float* out) {
-    if (!ok) {
+__device__ __forceinline__ uint4 load_raw(const T* row, int64_t t, int64_t L, bool ok) {
+    constexpr int V = 16 / sizeof(T);
+    uint4 r = make_uint4(0, 0, 0, 0);
+    if (!ok) return r;
+    if (kVec && t + V <= L) return __ldg(reinterpret_cast<const uint4*>(row + t));
+    T tmp[V];
 #pragma unroll
-        for (int k = 0; k < kT; k++) out[k] = 0.f;
-        return;
-    }
-    if (kVec && t + kT <= L) {
-        constexpr int V = Vec16<T>::kN;
-#pragma unroll
-        for (int k = 0; k < kT; k += V) Vec16<T>::load(row + t + k, out + k);
-        return;
-    }
-#pragma unroll
-    for (int k = 0; k < kT; k++) out[k] = (t + k < L) ? to_f32(row[t + k]) : 0.f;
+    for (int k = 0; k < V; k++) tmp[k] = (t + k < L) ? row[t + k] : T(0.f);
+    memcpy(&r, tmp, 16);
+    return r;
 }
 
+template <typename T>
+__device__ __forceinline__ void unpack(const uint4& r, float* out) {
+    if constexpr (sizeof(T) == 2) {
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            out[2 * i] = __uint_as_float(w[i] << 16);
+            out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    } else {
+        out[0] = __uint_as_float(r.x); out[1] = __uint_as_float(r.y);
+        out[2] = __uint_as_float(r.z); out[3] = __uint_as_float(r.w);
+    }
+}
+
+// V consecutive values of a T row held raw (32-bit words): V * sizeof(T) bytes,
+// loaded with 16- or 8-byte vectors when whole and aligned. (dout may be wider or
+// narrower than the inputs whose 16-byte vectors set V.)
+template <typename T, int V>
+struct RawRun {
+    static constexpr int W = V * (int)sizeof(T) / 4;
+    uint32_t w[W];
+    template <bool kVec>
+    __device__ __forceinline__ void load(const T* row, int64_t t, int64_t L, bool ok) {
+#pragma unroll
+        for (int i = 0; i < W; i++) w[i] = 0;
+        if (!ok) return;
+        if (kVec && t + V <= L) {
+            if constexpr (W % 4 == 0) {
+#pragma unroll
+                for (int i = 0; i < W; i += 4) {
+                    const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + t) + i / 4);
+                    w[i] = v.x; w[i + 1] = v.y; w[i + 2] = v.z; w[i + 3] = v.w;
+                }
+            } else {
+                static_assert(W == 2, "8-byte runs");
+                const uint2 v = __ldg(reinterpret_cast<const uint2*>(row + t));
+                w[0] = v.x; w[1] = v.y;
+            }
+            return;
+        }
+        T tmp[V];
+#pragma unroll
+        for (int k = 0; k < V; k++) tmp[k] = (t + k < L) ? row[t + k] : T(0.f);
+        memcpy(w, tmp, sizeof(tmp));
+    }
+    __device__ __forceinline__ void unpack(float* out) const {
+        if constexpr (sizeof(T) == 2) {
+#pragma unroll
+            for (int i = 0; i < W; i++) {
+                out[2 * i] = __uint_as_float(w[i] << 16);
+                out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < W; i++) out[i] = __uint_as_float(w[i]);
+        }
+    }
+};
+
+// kC values at row[t ..], those before L only
 template <typename T, bool kVec>
 __device__ __forceinline__ void store_run(T* row, int64_t t, int64_t L, const float* v) {
-    if (kVec && t + kT <= L) {
+    if (kVec && t + kC <= L) {
         constexpr int V = Vec16<T>::kN;
 #pragma unroll
-        for (int k = 0; k < kT; k += V) Vec16<T>::store(row + t + k, v + k);
+        for (int k = 0; k < kC; k += V) Vec16<T>::store(row + t + k, v + k);
         return;
     }
 #pragma unroll
-    for (int k = 0; k < kT; k++)
+    for (int k = 0; k < kC; k++)
         if (t + k < L) row[t + k] = from_f32<T>(v[k]);
 }
 
@@ -95,7 +166,7 @@ template <bool kAcc> __device__ __forceinline__ float sigmoid_f(float x) {
 }
 
 // sum over the G lanes of a channel (lanes p, p + P, p + 2P, ...)
-template <int G, int P>
+template <int P>
 __device__ __forceinline__ float chan_sum(float v) {
 #pragma unroll
     for (int m = P; m < 32; m <<= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
@@ -104,22 +175,27 @@ __device__ __forceinline__ float chan_sum(float v) {
 
 template <int N, typename Tin, typename Tdo, bool kVec>
 __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(BwdArgs a) {
-    using Cfg = BwdCfg<N>;
-    constexpr int NPL = Cfg::NPL, G = Cfg::G, P = Cfg::P, M = Cfg::M;
+    using Cfg = BwdCfg<N, Tin>;
+    constexpr int NPL = Cfg::NPL, P = Cfg::P, M = Cfg::M, V = Cfg::V, kTile = Cfg::kTile;
+    constexpr int VPT = Cfg::VPT, PV = Cfg::PV, BCV = Cfg::BCV;
     constexpr bool kAcc = sizeof(Tin) == 4;
-    __shared__ __align__(16) float s_bc[kT][2][N];   // the chunk's B (0) and C (1)
+    // per tile: B and C (fp32 [t][which][n]); per (channel, step) {dt, u, dy, dz factor}
+    // and softplus'; the dB/dC totals of each warp per step, summed over warps after
+    __shared__ __align__(16) float s_bc[kTile][2][N];
+    __shared__ __align__(16) float4 s_ch[kWarps][P][kTile];
+    __shared__ float s_sig[kWarps][P][kTile];
+    __shared__ float s_dbc[kWarps][kTile][2 * N];
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int p = lane % P, j = lane / P;
     const int64_t b = blockIdx.y;
-    const int64_t d = ((int64_t)blockIdx.x * kWarps + warp) * P + p;
+    const int64_t d_w = ((int64_t)blockIdx.x * kWarps + warp) * P;   // the warp's first channel
+    const int64_t d = d_w + p;
     const bool ok = d < a.dim;
     const int64_t L = a.seqlen, ch = b * a.dim + d;
-    const int64_t nchunk = (L + kT - 1) / kT;
-    const Tin* u_r = static_cast<const Tin*>(a.u) + ch * L;
-    const Tin* dl_r = static_cast<const Tin*>(a.delta) + ch * L;
-    const Tin* z_r = a.z ? static_cast<const Tin*>(a.z) + ch * L : nullptr;
-    const Tdo* do_r = static_cast<const Tdo*>(a.dout) + ch * L;
+    const int64_t nchunk = (L + kC - 1) / kC;
+    const int64_t ntile = (L + kTile - 1) / kTile;
+    const bool has_z = a.z != nullptr;
     const Tin* B_b = static_cast<const Tin*>(a.B) + b * N * L;
     const Tin* C_b = static_cast<const Tin*>(a.C) + b * N * L;
     float* ws = static_cast<float*>(a.workspace) + ch * nchunk * N + j * NPL;
@@ -132,153 +208,224 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(BwdArgs a) {
         g[i] = (ok && a.dh_last) ? a.dh_last[ch * N + j * NPL + i] : 0.f;
         dA[i] = 0.f;
     }
-    const float bias = (ok && a.delta_bias) ? a.delta_bias[d] : 0.f;
     const float Dd = (ok && a.D) ? a.D[d] : 0.f;
 
-    // the chunk's B (and C) for the CTA's batch row, fp32 [t][which][n]
-    auto stage = [&](int64_t t0, bool with_c) {
-        __syncthreads();   // previous readers are done
-        for (int v = threadIdx.x; v < (with_c ? 2 : 1) * N * kT; v += kThreads) {
-            const int which = v / (N * kT), n = (v / kT) % N, k = v % kT;
-            const int64_t t = t0 + k;
-            const Tin* src = which ? C_b : B_b;
-            s_bc[k][which][n] = t < L ? to_f32(src[(int64_t)n * L + t]) : 0.f;
+    // prologue ownership: vector q of this lane covers channel pc[q] of the warp,
+    // steps pt[q] .. pt[q] + V of the tile
+    int pc[PV], pt[PV];
+    bool pok[PV];
+    float pbias[PV];
+    const Tin *pu[PV], *pdl[PV], *pz[PV];
+    const Tdo* pdo[PV];
+#pragma unroll
+    for (int q = 0; q < PV; q++) {
+        const int v = q * 32 + lane;
+        pc[q] = v % P;
+        pt[q] = (v / P) * V;
+        const int64_t dq = d_w + pc[q];
+        pok[q] = dq < a.dim;
+        const int64_t cq = b * a.dim + (pok[q] ? dq : 0);
+        pbias[q] = (pok[q] && a.delta_bias) ? a.delta_bias[dq] : 0.f;
+        pu[q] = static_cast<const Tin*>(a.u) + cq * L;
+        pdl[q] = static_cast<const Tin*>(a.delta) + cq * L;
+        pz[q] = has_z ? static_cast<const Tin*>(a.z) + cq * L : nullptr;
+        pdo[q] = static_cast<const Tdo*>(a.dout) + cq * L;
+    }
+    // the B/C vector this thread stages
+    const int bv = threadIdx.x;
+    const int bwhich = bv / (N * VPT), bn = (bv / VPT) % N, btt = (bv % VPT) * V;
+
+    uint4 ru[PV], rd[PV], rz[PV], rbc;
+    RawRun<Tdo, V> rdo[PV];
+    auto prefetch = [&](int64_t t0, bool bwd) {
+#pragma unroll
+        for (int q = 0; q < PV; q++) {
+            ru[q] = load_raw<Tin, kVec>(pu[q], t0 + pt[q], L, pok[q]);
+            rd[q] = load_raw<Tin, kVec>(pdl[q], t0 + pt[q], L, pok[q]);
+            if (bwd) {
+                rdo[q].template load<kVec>(pdo[q], t0 + pt[q], L, pok[q]);
+                rz[q] = load_raw<Tin, kVec>(has_z ? pz[q] : pu[q], t0 + pt[q], L, pok[q] && has_z);
+            }
         }
-        __syncthreads();
+        rbc = load_raw<Tin, kVec>((bwhich ? C_b : B_b) + (int64_t)bn * L, t0 + btt, L,
+                                  bv < BCV && (bwd || bwhich == 0));
     };
-    auto dt_of = [&](float x) {
-        if (!a.softplus) return x;
-        return softplus_acc<kAcc>(x);
+    // the tile's shared data from the prefetched registers
+    auto stage = [&](int64_t t0, bool bwd) {
+        if (bv < BCV && (bwd || bwhich == 0)) {
+            float f[V];
+            unpack<Tin>(rbc, f);
+#pragma unroll
+            for (int k = 0; k < V; k++) s_bc[btt + k][bwhich][bn] = f[k];
+        }
+#pragma unroll
+        for (int q = 0; q < PV; q++) {
+            float fu[V], fd[V], fz[V], fo[V];
+            unpack<Tin>(ru[q], fu);
+            unpack<Tin>(rd[q], fd);
+            if (bwd) {
+                rdo[q].unpack(fo);
+                unpack<Tin>(rz[q], fz);
+            }
+#pragma unroll
+            for (int k = 0; k < V; k++) {
+                const bool live = pok[q] && t0 + pt[q] + k < L;
+                const float x = fd[k] + pbias[q];
+                float dt = a.softplus ? softplus_acc<kAcc>(x) : x;
+                float4 e = make_float4(live ? dt : 0.f, fu[k], 0.f, 0.f);
+                if (bwd) {
+                    float dy = live ? fo[k] : 0.f, dzf = 0.f;
+                    if (has_z) {
+                        const float sg = sigmoid_f<kAcc>(fz[k]);
+                        dzf = dy * sg * fmaf(fz[k], 1.f - sg, 1.f);   // dout silu'(z)
+                        dy *= fz[k] * sg;                               // dout silu(z)
+                    }
+                    e.z = dy;
+                    e.w = dzf;
+                    s_sig[warp][pc[q]][pt[q] + k] = live ? (a.softplus ? sigmoid_f<kAcc>(x) : 1.f) : 0.f;
+                }
+                s_ch[warp][pc[q]][pt[q] + k] = e;
+            }
+        }
     };
 
     // 1. forward, checkpointing the state at every chunk start
-    for (int64_t c = 0; c < nchunk; c++) {
-        const int64_t t0 = c * kT;
-        if (ok) {
-            if constexpr (NPL == 4) {
-                *reinterpret_cast<float4*>(ws + c * N) = make_float4(h[0], h[1], h[2], h[3]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < NPL; i++) ws[c * N + i] = h[i];
-            }
-        }
-        float u[kT], dl[kT];
-        load_run<Tin, kVec>(u_r, t0, L, ok, u);
-        load_run<Tin, kVec>(dl_r, t0, L, ok, dl);
+    if (ntile > 0) prefetch(0, false);
+    for (int64_t tile = 0; tile < ntile; tile++) {
+        const int64_t t0 = tile * kTile;
+        __syncthreads();   // the previous tile's readers are done
         stage(t0, false);
+        if (tile + 1 < ntile) prefetch(t0 + kTile, false);
+        __syncthreads();
 #pragma unroll
-        for (int k = 0; k < kT; k++) {
-            float dt = dt_of(dl[k] + bias);
-            if (t0 + k >= L) dt = 0.f;
+        for (int k = 0; k < kTile; k++) {
+            if (k % kC == 0 && ok && t0 + k < L) {
+                float* w = ws + ((t0 + k) / kC) * N;
+                if constexpr (NPL == 4) *reinterpret_cast<float4*>(w) = make_float4(h[0], h[1], h[2], h[3]);
+                else {
+#pragma unroll
+                    for (int i = 0; i < NPL; i++) w[i] = h[i];
+                }
+            }
+            const float4 e = s_ch[warp][p][k];
+            const float dtu = e.x * e.y;
 #pragma unroll
             for (int i = 0; i < NPL; i++)
-                h[i] = fmaf(exp_f<kAcc>(dt * A[i]), h[i], dt * u[k] * s_bc[k][0][j * NPL + i]);
+                h[i] = fmaf(exp_f<kAcc>(e.x * A[i]), h[i], dtu * s_bc[k][0][j * NPL + i]);
         }
     }
 
-    // 2. chunks in reverse
+    // 2. tiles in reverse; inside a tile, chunks in reverse
     float dD = 0.f, dbias = 0.f;
-    for (int64_t c = nchunk - 1; c >= 0; c--) {
-        const int64_t t0 = c * kT;
-        float u[kT], dl[kT], zz[kT], dout[kT];
-        load_run<Tin, kVec>(u_r, t0, L, ok, u);
-        load_run<Tin, kVec>(dl_r, t0, L, ok, dl);
-        load_run<Tdo, kVec>(do_r, t0, L, ok, dout);
-        if (z_r) load_run<Tin, kVec>(z_r, t0, L, ok, zz);
-        float hs[kT + 1][NPL];   // hs[k] = state before step k; hs[kT] after the chunk
-        if (ok) {
-            if constexpr (NPL == 4) {
-                const float4 v = *reinterpret_cast<const float4*>(ws + c * N);
-                hs[0][0] = v.x; hs[0][1] = v.y; hs[0][2] = v.z; hs[0][3] = v.w;
+    if (ntile > 0) prefetch((ntile - 1) * kTile, true);
+    for (int64_t tile = ntile - 1; tile >= 0; tile--) {
+        const int64_t t0 = tile * kTile;
+        __syncthreads();   // the previous tile's readers (and the flush) are done
+        stage(t0, true);
+        if (tile > 0) prefetch(t0 - kTile, true);
+        __syncthreads();
+#pragma unroll 1
+        for (int cc = kTile / kC - 1; cc >= 0; cc--) {
+            const int64_t tc = t0 + cc * kC;
+            if (tc >= L) continue;   // warp-uniform (chunks past the end of the last tile)
+            float hs[kC + 1][NPL];   // hs[k] = state before step k of the chunk
+            if (ok) {
+                const float* w = ws + (tc / kC) * N;
+                if constexpr (NPL == 4) {
+                    const float4 v = *reinterpret_cast<const float4*>(w);
+                    hs[0][0] = v.x; hs[0][1] = v.y; hs[0][2] = v.z; hs[0][3] = v.w;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < NPL; i++) hs[0][i] = w[i];
+                }
             } else {
 #pragma unroll
-                for (int i = 0; i < NPL; i++) hs[0][i] = ws[c * N + i];
+                for (int i = 0; i < NPL; i++) hs[0][i] = 0.f;
             }
-        } else {
 #pragma unroll
-            for (int i = 0; i < NPL; i++) hs[0][i] = 0.f;
-        }
-        stage(t0, true);
-        float dts[kT];
+            for (int k = 0; k < kC; k++) {
+                const int kk = cc * kC + k;
+                const float4 e = s_ch[warp][p][kk];
+                const float dtu = e.x * e.y;
 #pragma unroll
-        for (int k = 0; k < kT; k++) {
-            dts[k] = dt_of(dl[k] + bias);
-            if (t0 + k >= L) dts[k] = 0.f;
-#pragma unroll
-            for (int i = 0; i < NPL; i++)
-                hs[k + 1][i] = fmaf(exp_f<kAcc>(dts[k] * A[i]), hs[k][i], dts[k] * u[k] * s_bc[k][0][j * NPL + i]);
-        }
-        float du[kT], ddl[kT], dz[kT];
-#pragma unroll
-        for (int k = kT - 1; k >= 0; k--) {
-            const bool live = t0 + k < L;
-            const float* Bk = s_bc[k][0] + j * NPL;
-            const float* Ck = s_bc[k][1] + j * NPL;
-            float dy = live ? dout[k] : 0.f;
-            if (z_r) {
-                float part = 0.f;
-#pragma unroll
-                for (int i = 0; i < NPL; i++) part = fmaf(Ck[i], hs[k + 1][i], part);
-                const float y = chan_sum<G, P>(part) + Dd * u[k];
-                const float s = sigmoid_f<kAcc>(zz[k]);
-                dz[k] = dy * y * s * fmaf(zz[k], 1.f - s, 1.f);
-                dy *= zz[k] * s;
+                for (int i = 0; i < NPL; i++)
+                    hs[k + 1][i] = fmaf(exp_f<kAcc>(e.x * A[i]), hs[k][i], dtu * s_bc[kk][0][j * NPL + i]);
             }
-            dD = fmaf(dy, u[k], dD);
-            float vals[M];
-            float ddt_p = 0.f, du_p = 0.f;
+            float du[kC], ddl[kC], dz[kC];
 #pragma unroll
-            for (int i = 0; i < NPL; i++) {
-                g[i] = fmaf(Ck[i], dy, g[i]);
-                vals[NPL + i] = dy * hs[k + 1][i];                    // dC
-                const float an = exp_f<kAcc>(dts[k] * A[i]);
-                const float ga = g[i] * hs[k][i] * an;                  // g h_{t-1} a
-                ddt_p = fmaf(ga, A[i], ddt_p);
-                ddt_p = fmaf(g[i] * Bk[i], u[k], ddt_p);
-                dA[i] = fmaf(ga, dts[k], dA[i]);
-                vals[i] = g[i] * dts[k] * u[k];                         // dB
-                du_p = fmaf(g[i] * dts[k], Bk[i], du_p);
-                g[i] *= an;
-            }
-            const float ddt = chan_sum<G, P>(ddt_p);
-            du[k] = fmaf(Dd, dy, chan_sum<G, P>(du_p));
-            float dx = ddt;
-            if (a.softplus) dx = ddt * sigmoid_f<kAcc>(dl[k] + bias);
-            if (!live) dx = 0.f;
-            ddl[k] = dx;
-            dbias += dx;
-            // dB, dC of this step: reduce-scatter over the warp's P channels
-            int idx = 0;
-            int cnt = M;
+            for (int k = kC - 1; k >= 0; k--) {
+                const int kk = cc * kC + k;
+                const float4 e = s_ch[warp][p][kk];
+                const float dt = e.x, u = e.y, dy = e.z;
+                const float* Bk = s_bc[kk][0] + j * NPL;
+                const float* Ck = s_bc[kk][1] + j * NPL;
+                if (has_z) {
+                    float part = 0.f;
 #pragma unroll
-            for (int m = 1; m < P; m <<= 1) {
-                if (cnt > 1) {
-                    const int half = cnt / 2;
-                    const bool up = (lane & m) != 0;
-#pragma unroll
-                    for (int q = 0; q < M / 2; q++) {
-                        if (q < half) {
-                            const float send = up ? vals[q] : vals[half + q];
-                            const float keep = up ? vals[half + q] : vals[q];
-                            vals[q] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-                        }
-                    }
-                    idx += up ? half : 0;
-                    cnt = half;
-                } else {
-                    vals[0] += __shfl_xor_sync(0xffffffffu, vals[0], m);
+                    for (int i = 0; i < NPL; i++) part = fmaf(Ck[i], hs[k + 1][i], part);
+                    dz[k] = e.w * (chan_sum<P>(part) + Dd * u);
                 }
+                dD = fmaf(dy, u, dD);
+                float vals[M];
+                float ddt_p = 0.f, du_p = 0.f;
+                const float dtu = dt * u;
+#pragma unroll
+                for (int i = 0; i < NPL; i++) {
+                    g[i] = fmaf(Ck[i], dy, g[i]);
+                    vals[NPL + i] = dy * hs[k + 1][i];                    // dC
+                    const float an = exp_f<kAcc>(dt * A[i]);
+                    const float ga = g[i] * hs[k][i] * an;                  // g h_{t-1} a
+                    ddt_p = fmaf(ga, A[i], ddt_p);
+                    ddt_p = fmaf(g[i] * Bk[i], u, ddt_p);
+                    dA[i] = fmaf(ga, dt, dA[i]);
+                    vals[i] = g[i] * dtu;                                   // dB
+                    du_p = fmaf(g[i] * dt, Bk[i], du_p);
+                    g[i] *= an;
+                }
+                du[k] = fmaf(Dd, dy, chan_sum<P>(du_p));
+                const float dx = chan_sum<P>(ddt_p) * s_sig[warp][p][kk];
+                ddl[k] = dx;
+                dbias += dx;
+                // dB, dC of this step: reduce-scatter over the warp's P channels
+                int idx = 0, cnt = M;
+#pragma unroll
+                for (int m = 1; m < P; m <<= 1) {
+                    if (cnt > 1) {
+                        const int half = cnt / 2;
+                        const bool up = (lane & m) != 0;
+#pragma unroll
+                        for (int q = 0; q < M / 2; q++) {
+                            if (q < half) {
+                                const float send = up ? vals[q] : vals[half + q];
+                                const float keep = up ? vals[half + q] : vals[q];
+                                vals[q] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+                            }
+                        }
+                        idx += up ? half : 0;
+                        cnt = half;
+                    } else {
+                        vals[0] += __shfl_xor_sync(0xffffffffu, vals[0], m);
+                    }
+                }
+                if (p < M) s_dbc[warp][kk][j * M + idx] = vals[0];
             }
-            // lanes whose channel bits above the index bits are zero hold the totals
-            if (live && (p / M) == 0) {
-                const int which = idx / NPL, n = j * NPL + idx % NPL;
-                atomicAdd((which ? a.dC : a.dB) + (b * N + n) * L + t0 + k, vals[0]);
+            if (ok && j == 0) {
+                store_run<Tin, kVec>(static_cast<Tin*>(a.du) + ch * L, tc, L, du);
+                store_run<Tin, kVec>(static_cast<Tin*>(a.ddelta) + ch * L, tc, L, ddl);
+                if (has_z) store_run<Tin, kVec>(static_cast<Tin*>(a.dz) + ch * L, tc, L, dz);
             }
         }
-        if (ok && j == 0) {
-            store_run<Tin, kVec>(static_cast<Tin*>(a.du) + ch * L, t0, L, du);
-            store_run<Tin, kVec>(static_cast<Tin*>(a.ddelta) + ch * L, t0, L, ddl);
-            if (z_r) store_run<Tin, kVec>(static_cast<Tin*>(a.dz) + ch * L, t0, L, dz);
+        __syncthreads();
+        // the tile's dB, dC: the warps' totals summed, one atomic per (step, B/C, n)
+        for (int e = threadIdx.x; e < kTile * 2 * N; e += kThreads) {
+            const int kk = e / (2 * N), slot = e % (2 * N);
+            if (t0 + kk >= L) continue;
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; w++) v += s_dbc[w][kk][slot];
+            const int jj = slot / M, idx = slot % M;
+            const int which = idx / NPL, n = jj * NPL + idx % NPL;
+            atomicAdd((which ? a.dC : a.dB) + (b * N + n) * L + t0 + kk, v);
         }
     }
     if (ok) {
@@ -296,7 +443,7 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(BwdArgs a) {
 
 template <int N, typename Tin, typename Tdo>
 cudaError_t launch_n(const BwdArgs& a, cudaStream_t s) {
-    using Cfg = BwdCfg<N>;
+    using Cfg = BwdCfg<N, Tin>;
     if (a.batch == 0 || a.dim == 0) return cudaSuccess;
     dim3 grid((unsigned)((a.dim + kWarps * Cfg::P - 1) / (kWarps * Cfg::P)), (unsigned)a.batch);
     if (a.vec) scan_bwd_kernel<N, Tin, Tdo, true><<<grid, kThreads, 0, s>>>(a);
@@ -319,7 +466,7 @@ cudaError_t by_n(const BwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 size_t scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate) {
-    return (size_t)batch * dim * ((seqlen + kT - 1) / kT) * dstate * 4;
+    return (size_t)batch * dim * ((seqlen + kC - 1) / kC) * dstate * 4;
 }
 
 cudaError_t launch_scan_bwd(const BwdArgs& a, cudaStream_t s) {

@@ -83,6 +83,14 @@ def test_bwd_parity_dstate(ssm, in_dtype, N):
     _check(g, ref, in_dtype)
 
 
+@pytest.mark.parametrize("in_dtype", ["f32", "bf16"])
+def test_bwd_dout_other_width(ssm, in_dtype):
+    """dout narrower (bf16 for fp32 inputs) or wider (fp32 for bf16 inputs) than the inputs."""
+    inp, dout, dhl = _case("mamba130m", 2, 24, 77, 16, W.F32 if in_dtype == "f32" else W.BF16, seed=5)
+    g, ref = _run(ssm, inp, dout, dhl, torch.bfloat16 if in_dtype == "f32" else torch.float32)
+    _check(g, ref, in_dtype)
+
+
 @pytest.mark.parametrize("opts", [dict(with_z=False), dict(with_D=False), dict(with_bias=False),
                                   dict(h0=False), dict(with_z=False, with_D=False, with_bias=False, h0=False)],
                          ids=["no_z", "no_D", "no_bias", "no_h0", "bare"])
