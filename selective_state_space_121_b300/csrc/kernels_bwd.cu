@@ -134,17 +134,16 @@ struct RawRun {
     }
 };
 
-// kC values at row[t ..], those before L only
-template <typename T, bool kVec>
-__device__ __forceinline__ void store_run(T* row, int64_t t, int64_t L, const float* v) {
-    if (kVec && t + kC <= L) {
-        constexpr int V = Vec16<T>::kN;
-#pragma unroll
-        for (int k = 0; k < kC; k += V) Vec16<T>::store(row + t + k, v + k);
+// V values at row[t ..] (a 16-byte vector of T), those before L only
+template <typename T, int V, bool kVec>
+__device__ __forceinline__ void store_vec(T* row, int64_t t, int64_t L, const float* v) {
+    static_assert(V == Vec16<T>::kN, "one 16-byte vector");
+    if (kVec && t + V <= L) {
+        Vec16<T>::store(row + t, v);
         return;
     }
 #pragma unroll
-    for (int k = 0; k < kC; k++)
+    for (int k = 0; k < V; k++)
         if (t + k < L) row[t + k] = from_f32<T>(v[k]);
 }
 
@@ -174,7 +173,8 @@ __device__ __forceinline__ float chan_sum(float v) {
 }
 
 template <int N, typename Tin, typename Tdo, bool kVec>
-__global__ void __launch_bounds__(kThreads) scan_bwd_kernel(BwdArgs a) {
+// three CTAs per SM: the Mamba-130M-shaped layer's 384 CTAs then run in one wave
+__global__ void __launch_bounds__(kThreads, 3) scan_bwd_kernel(BwdArgs a) {
     using Cfg = BwdCfg<N, Tin>;
     constexpr int NPL = Cfg::NPL, P = Cfg::P, M = Cfg::M, V = Cfg::V, kTile = Cfg::kTile;
     constexpr int VPT = Cfg::VPT, PV = Cfg::PV, BCV = Cfg::BCV;
@@ -209,6 +209,14 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(BwdArgs a) {
         dA[i] = 0.f;
     }
     const float Dd = (ok && a.D) ? a.D[d] : 0.f;
+    // exp(dt A_i): on the bf16 path the SFU's 2^x with A pre-scaled by log2(e)
+    float Al[NPL];
+#pragma unroll
+    for (int i = 0; i < NPL; i++) Al[i] = kAcc ? A[i] : A[i] * kLog2e;
+    auto exp_a = [&](float dt, int i) {
+        if constexpr (kAcc) return exp_acc(dt * A[i]);
+        else return ex2(dt * Al[i]);
+    };
 
     // prologue ownership: vector q of this lane covers channel pc[q] of the warp,
     // steps pt[q] .. pt[q] + V of the tile
@@ -311,7 +319,7 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(BwdArgs a) {
             const float dtu = e.x * e.y;
 #pragma unroll
             for (int i = 0; i < NPL; i++)
-                h[i] = fmaf(exp_f<kAcc>(e.x * A[i]), h[i], dtu * s_bc[k][0][j * NPL + i]);
+                h[i] = fmaf(exp_a(e.x, i), h[i], dtu * s_bc[k][0][j * NPL + i]);
         }
     }
 
@@ -349,9 +357,8 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(BwdArgs a) {
                 const float dtu = e.x * e.y;
 #pragma unroll
                 for (int i = 0; i < NPL; i++)
-                    hs[k + 1][i] = fmaf(exp_f<kAcc>(e.x * A[i]), hs[k][i], dtu * s_bc[kk][0][j * NPL + i]);
+                    hs[k + 1][i] = fmaf(exp_a(e.x, i), hs[k][i], dtu * s_bc[kk][0][j * NPL + i]);
             }
-            float du[kC], ddl[kC], dz[kC];
 #pragma unroll
             for (int k = kC - 1; k >= 0; k--) {
                 const int kk = cc * kC + k;
@@ -359,11 +366,12 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(BwdArgs a) {
                 const float dt = e.x, u = e.y, dy = e.z;
                 const float* Bk = s_bc[kk][0] + j * NPL;
                 const float* Ck = s_bc[kk][1] + j * NPL;
+                float dz = 0.f;
                 if (has_z) {
                     float part = 0.f;
 #pragma unroll
                     for (int i = 0; i < NPL; i++) part = fmaf(Ck[i], hs[k + 1][i], part);
-                    dz[k] = e.w * (chan_sum<P>(part) + Dd * u);
+                    dz = e.w * (chan_sum<P>(part) + Dd * u);
                 }
                 dD = fmaf(dy, u, dD);
                 float vals[M];
@@ -373,7 +381,7 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(BwdArgs a) {
                 for (int i = 0; i < NPL; i++) {
                     g[i] = fmaf(Ck[i], dy, g[i]);
                     vals[NPL + i] = dy * hs[k + 1][i];                    // dC
-                    const float an = exp_f<kAcc>(dt * A[i]);
+                    const float an = exp_a(dt, i);
                     const float ga = g[i] * hs[k][i] * an;                  // g h_{t-1} a
                     ddt_p = fmaf(ga, A[i], ddt_p);
                     ddt_p = fmaf(g[i] * Bk[i], u, ddt_p);
@@ -382,10 +390,12 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(BwdArgs a) {
                     du_p = fmaf(g[i] * dt, Bk[i], du_p);
                     g[i] *= an;
                 }
-                du[k] = fmaf(Dd, dy, chan_sum<P>(du_p));
+                const float du = fmaf(Dd, dy, chan_sum<P>(du_p));
                 const float dx = chan_sum<P>(ddt_p) * s_sig[warp][p][kk];
-                ddl[k] = dx;
                 dbias += dx;
+                // every lane of the channel has read this step's entry (the shuffles
+                // above sync the warp): lane j = 0 puts the step's outputs there
+                if (j == 0) s_ch[warp][p][kk] = make_float4(du, dx, dz, 0.f);
                 // dB, dC of this step: reduce-scatter over the warp's P channels
                 int idx = 0, cnt = M;
 #pragma unroll
@@ -409,13 +419,23 @@ __global__ void __launch_bounds__(kThreads) scan_bwd_kernel(BwdArgs a) {
                 }
                 if (p < M) s_dbc[warp][kk][j * M + idx] = vals[0];
             }
-            if (ok && j == 0) {
-                store_run<Tin, kVec>(static_cast<Tin*>(a.du) + ch * L, tc, L, du);
-                store_run<Tin, kVec>(static_cast<Tin*>(a.ddelta) + ch * L, tc, L, ddl);
-                if (has_z) store_run<Tin, kVec>(static_cast<Tin*>(a.dz) + ch * L, tc, L, dz);
-            }
         }
         __syncthreads();
+        // the tile's du, ddelta, dz, with the prologue's ownership (16-byte stores)
+#pragma unroll
+        for (int q = 0; q < PV; q++) {
+            if (!pok[q]) continue;
+            float o0[V], o1[V], o2[V];
+#pragma unroll
+            for (int k = 0; k < V; k++) {
+                const float4 e = s_ch[warp][pc[q]][pt[q] + k];
+                o0[k] = e.x; o1[k] = e.y; o2[k] = e.z;
+            }
+            const int64_t cq = b * a.dim + d_w + pc[q], tq = t0 + pt[q];
+            store_vec<Tin, V, kVec>(static_cast<Tin*>(a.du) + cq * L, tq, L, o0);
+            store_vec<Tin, V, kVec>(static_cast<Tin*>(a.ddelta) + cq * L, tq, L, o1);
+            if (has_z) store_vec<Tin, V, kVec>(static_cast<Tin*>(a.dz) + cq * L, tq, L, o2);
+        }
         // the tile's dB, dC: the warps' totals summed, one atomic per (step, B/C, n)
         for (int e = threadIdx.x; e < kTile * 2 * N; e += kThreads) {
             const int kk = e / (2 * N), slot = e % (2 * N);
