@@ -182,8 +182,10 @@ __global__ void __launch_bounds__(kThreads, 3) scan_bwd_kernel(BwdArgs a) {
     // per tile: B and C (fp32 [t][which][n]); per (channel, step) {dt, u, dy, dz factor}
     // and softplus'; the dB/dC totals of each warp per step, summed over warps after
     __shared__ __align__(16) float s_bc[kTile][2][N];
-    __shared__ __align__(16) float4 s_ch[kWarps][P][kTile];
-    __shared__ float s_sig[kWarps][P][kTile];
+    // rows padded by one entry: the 8 lanes of a quarter-warp read 8 channels' rows
+    // at the same step, which unpadded (a power-of-two stride) share one bank group
+    __shared__ __align__(16) float4 s_ch[kWarps][P][kTile + 1];
+    __shared__ float s_sig[kWarps][P][kTile + 1];
     __shared__ float s_dbc[kWarps][kTile][2 * N];
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -359,52 +361,61 @@ __global__ void __launch_bounds__(kThreads, 3) scan_bwd_kernel(BwdArgs a) {
                 for (int i = 0; i < NPL; i++)
                     hs[k + 1][i] = fmaf(exp_a(e.x, i), hs[k][i], dtu * s_bc[kk][0][j * NPL + i]);
             }
+            // steps in pairs: the dB/dC values of two steps share one reduce-scatter
+            // (same shuffle count, half the dependent rounds per step)
 #pragma unroll
-            for (int k = kC - 1; k >= 0; k--) {
-                const int kk = cc * kC + k;
-                const float4 e = s_ch[warp][p][kk];
-                const float dt = e.x, u = e.y, dy = e.z;
-                const float* Bk = s_bc[kk][0] + j * NPL;
-                const float* Ck = s_bc[kk][1] + j * NPL;
-                float dz = 0.f;
-                if (has_z) {
-                    float part = 0.f;
+            for (int k2 = kC - 1; k2 >= 1; k2 -= 2) {
+                float vals[2 * M];   // [step k2: dB, dC | step k2-1: dB, dC]
 #pragma unroll
-                    for (int i = 0; i < NPL; i++) part = fmaf(Ck[i], hs[k + 1][i], part);
-                    dz = e.w * (chan_sum<P>(part) + Dd * u);
+                for (int sidx = 0; sidx < 2; sidx++) {
+                    const int k = k2 - sidx;
+                    const int kk = cc * kC + k;
+                    const float4 e = s_ch[warp][p][kk];
+                    const float dt = e.x, u = e.y, dy = e.z;
+                    const float* Bk = s_bc[kk][0] + j * NPL;
+                    const float* Ck = s_bc[kk][1] + j * NPL;
+                    float dz = 0.f;
+                    if (has_z) {
+                        float part = 0.f;
+#pragma unroll
+                        for (int i = 0; i < NPL; i++) part = fmaf(Ck[i], hs[k + 1][i], part);
+                        dz = e.w * (chan_sum<P>(part) + Dd * u);
+                    }
+                    dD = fmaf(dy, u, dD);
+                    float ddt_p = 0.f, du_p = 0.f;
+                    const float dtu = dt * u;
+#pragma unroll
+                    for (int i = 0; i < NPL; i++) {
+                        g[i] = fmaf(Ck[i], dy, g[i]);
+                        vals[sidx * M + NPL + i] = dy * hs[k + 1][i];         // dC
+                        const float an = exp_a(dt, i);
+                        const float ga = g[i] * hs[k][i] * an;                  // g h_{t-1} a
+                        ddt_p = fmaf(ga, A[i], ddt_p);
+                        ddt_p = fmaf(g[i] * Bk[i], u, ddt_p);
+                        dA[i] = fmaf(ga, dt, dA[i]);
+                        vals[sidx * M + i] = g[i] * dtu;                        // dB
+                        du_p = fmaf(g[i] * dt, Bk[i], du_p);
+                        g[i] *= an;
+                    }
+                    const float du = fmaf(Dd, dy, chan_sum<P>(du_p));
+                    const float dx = chan_sum<P>(ddt_p) * s_sig[warp][p][kk];
+                    dbias += dx;
+                    // every lane of the channel has read this step's entry (the shuffles
+                    // above sync the warp): lane j = 0 puts the step's outputs there
+                    if (j == 0) s_ch[warp][p][kk] = make_float4(du, dx, dz, 0.f);
                 }
-                dD = fmaf(dy, u, dD);
-                float vals[M];
-                float ddt_p = 0.f, du_p = 0.f;
-                const float dtu = dt * u;
-#pragma unroll
-                for (int i = 0; i < NPL; i++) {
-                    g[i] = fmaf(Ck[i], dy, g[i]);
-                    vals[NPL + i] = dy * hs[k + 1][i];                    // dC
-                    const float an = exp_a(dt, i);
-                    const float ga = g[i] * hs[k][i] * an;                  // g h_{t-1} a
-                    ddt_p = fmaf(ga, A[i], ddt_p);
-                    ddt_p = fmaf(g[i] * Bk[i], u, ddt_p);
-                    dA[i] = fmaf(ga, dt, dA[i]);
-                    vals[i] = g[i] * dtu;                                   // dB
-                    du_p = fmaf(g[i] * dt, Bk[i], du_p);
-                    g[i] *= an;
-                }
-                const float du = fmaf(Dd, dy, chan_sum<P>(du_p));
-                const float dx = chan_sum<P>(ddt_p) * s_sig[warp][p][kk];
-                dbias += dx;
-                // every lane of the channel has read this step's entry (the shuffles
-                // above sync the warp): lane j = 0 puts the step's outputs there
-                if (j == 0) s_ch[warp][p][kk] = make_float4(du, dx, dz, 0.f);
-                // dB, dC of this step: reduce-scatter over the warp's P channels
-                int idx = 0, cnt = M;
+                // reduce-scatter over the warp's P channels: each round a lane keeps one
+                // half of its block of values and adds the partner's copy of that half;
+                // once a lane holds a single value the remaining rounds all-reduce it
+                constexpr int MV = 2 * M;
+                int idx = 0, cnt = MV;
 #pragma unroll
                 for (int m = 1; m < P; m <<= 1) {
                     if (cnt > 1) {
                         const int half = cnt / 2;
                         const bool up = (lane & m) != 0;
 #pragma unroll
-                        for (int q = 0; q < M / 2; q++) {
+                        for (int q = 0; q < MV / 2; q++) {
                             if (q < half) {
                                 const float send = up ? vals[q] : vals[half + q];
                                 const float keep = up ? vals[half + q] : vals[q];
@@ -417,7 +428,16 @@ __global__ void __launch_bounds__(kThreads, 3) scan_bwd_kernel(BwdArgs a) {
                         vals[0] += __shfl_xor_sync(0xffffffffu, vals[0], m);
                     }
                 }
-                if (p < M) s_dbc[warp][kk][j * M + idx] = vals[0];
+                // the lane holds values idx .. idx + cnt - 1 (one step, contiguous); with
+                // cnt == 1 only the lanes p < MV hold distinct ones
+                if (cnt > 1 || p < MV) {
+#pragma unroll
+                    for (int c = 0; c < (MV > P ? MV / P : 1); c++) {
+                        const int v = idx + c;
+                        const int kk = cc * kC + k2 - v / M;
+                        s_dbc[warp][kk][j * M + v % M] = vals[c];
+                    }
+                }
             }
         }
         __syncthreads();
