@@ -71,22 +71,6 @@ constexpr int kWarps = SSM_SERIAL_WARPS;
 #endif
 constexpr int kThreads = 32 * kWarps;
 
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-    float2 d;
-    asm("mul.rn.f32x2 %0, %1, %2;"
-        : "=l"(*reinterpret_cast<unsigned long long*>(&d))
-        : "l"(*reinterpret_cast<unsigned long long*>(&a)), "l"(*reinterpret_cast<unsigned long long*>(&b)));
-    return d;
-}
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-    float2 d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;"
-        : "=l"(*reinterpret_cast<unsigned long long*>(&d))
-        : "l"(*reinterpret_cast<unsigned long long*>(&a)), "l"(*reinterpret_cast<unsigned long long*>(&b)),
-          "l"(*reinterpret_cast<unsigned long long*>(&c)));
-    return d;
-}
-
 // Channels per lane a kernel may use: 2 on the bf16 path when a lane holds 2 to 4
 // states (more would not fit the registers), else 1. The serial kernel keeps 1: at
 // Mamba-130M sizes (12,288 channels) it needs every warp it can get to hide
