@@ -100,7 +100,10 @@ __device__ __forceinline__ void widen(const uint4& r, float* out) {
 // blocks of 32 vectors each lane keeps in flight: 4 x 512 bytes per warp, so the
 // ~32 resident warps of an SM hold ~64 KB of loads in flight (HBM latency x the
 // SM's share of the bandwidth)
-constexpr int kDepth = 4;
+#ifndef SSM_CONV_DEPTH
+#define SSM_CONV_DEPTH 4
+#endif
+constexpr int kDepth = SSM_CONV_DEPTH;
 
 template <typename Tin, typename Tout, int W, bool kVec>
 __global__ void __launch_bounds__(kThreads) causal_conv1d_kernel(ConvArgs a) {

@@ -145,13 +145,19 @@ __global__ void __launch_bounds__(kThreads) state_update_kernel(DecodeArgs a) {
 // bounded; on expiry the CTA records the failure in g_decode_status, waits (again
 // bounded) for its own copies in flight and returns.
 // ---------------------------------------------------------------------------
-constexpr int kTmaThreads = 256;
+// threads per CTA (a build option): 4 per channel at d_state 16, so a CTA's tile
+// is kTmaThreads / 4 channels of one batch row
+#ifndef SSM_DECODE_THREADS
+#define SSM_DECODE_THREADS 256
+#endif
+constexpr int kTmaThreads = SSM_DECODE_THREADS;
 // ring depth (a build option; static shared memory keeps it under 48 KB per CTA)
 #ifndef SSM_DECODE_STAGES
 #define SSM_DECODE_STAGES 4
 #endif
 constexpr int kStages = SSM_DECODE_STAGES;
 constexpr uint32_t kWaitLimit = 1u << 24;
+
 
 __device__ int g_decode_status;   // 0, or the line of a wait that ran out of budget
 

@@ -584,7 +584,8 @@ __device__ __forceinline__ float lane_state(const LaneStateT<N, G, K>& S, int k,
 }
 
 template <int N, int G, typename Tin, typename Tout, bool kVec>
-__global__ void __launch_bounds__(kThreads) serial_scan_kernel(ScanArgs a) {
+// at most 128 registers (4 CTAs per SM): measured ~1% faster than unbounded
+__global__ void __launch_bounds__(kThreads, 4) serial_scan_kernel(ScanArgs a) {
     constexpr int K = 1;
     using Cfg = SerialCfg<N, G, Tin, K>;
     constexpr int NPL = Cfg::NPL, CPW = Cfg::CPW, kT = Cfg::kT;
