@@ -120,3 +120,19 @@ def test_bwd_mamba130m_full_size(ssm):
     inp, dout, dhl = _case("mamba130m", 8, 1536, 2048, 16, W.BF16, seed=11)
     g, ref = _run(ssm, inp, dout, dhl, torch.bfloat16)
     _check(g, ref, "bf16")
+
+
+def test_bwd_empty(ssm):
+    """No time steps: every per-step gradient is empty, the summed ones are zero and
+    dh0 is dh_last (the adjoint passes through zero steps unchanged)."""
+    inp, dout, dhl = _case("mamba130m", 2, 40, 8, 16, W.BF16, seed=1)
+    t = scan_to_torch(inp)
+    e = {k: t[k][..., :0].contiguous() for k in ("u", "delta", "B", "C", "z")}   # zero steps
+    g = ssm.scan_bwd(e["u"], e["delta"], t["A"], e["B"], e["C"], t["D"], e["z"], t["delta_bias"], True, t["h0"],
+                     dout=torch.empty((2, 40, 0), dtype=torch.bfloat16, device="cuda"),
+                     dh_last=torch.from_numpy(dhl).cuda())
+    torch.cuda.synchronize()
+    assert g["du"].numel() == 0 and g["dB"].numel() == 0
+    for k in ("dA", "dD", "ddelta_bias"):
+        assert torch.count_nonzero(g[k]).item() == 0, k
+    assert torch.equal(g["dh0"].cpu(), torch.from_numpy(dhl))
