@@ -69,6 +69,8 @@ class OracleLib:
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_scan_bwd.argtypes = [P] * 8 + [ctypes.c_int] + [P] * 12 + [I64] * 4 + [ctypes.c_int]
         lib.oracle_scan_bwd.restype = ctypes.c_int
+        lib.oracle_ssd_scan.argtypes = [P] * 8 + [ctypes.c_int, P, P, P] + [I64] * 6 + [ctypes.c_int]
+        lib.oracle_ssd_scan.restype = ctypes.c_int
         lib.oracle_causal_conv1d.argtypes = [P] * 4 + [ctypes.c_int, P, P, I64, I64, I64, I64, ctypes.c_int]
         lib.oracle_causal_conv1d.restype = ctypes.c_int
         lib.oracle_conv_update.argtypes = [P] * 4 + [ctypes.c_int, P, I64, I64, I64, ctypes.c_int]
@@ -155,6 +157,23 @@ class OracleLib:
             raise ValueError("oracle_scan_bwd failed")
         return out
 
+    def ssd_scan(self, x, dt, A, B, C, D=None, z=None, dt_bias=None, softplus=True, h0=None, threads: int = 0):
+        """Mamba-2 multi-head SSM by its recurrence in fp64. x, z: (batch, L, H, P); dt: (batch,
+        L, H); B, C: (batch, L, G, N); A, D, dt_bias: (H,); h0: (batch, H, P, N). Returns (y
+        (batch, L, H, P), h_last (batch, H, P, N)) fp64."""
+        x = _f32(x); dt = _f32(dt); A = _f32(A); B = _f32(B); C = _f32(C)
+        D = _f32(D); z = _f32(z); dt_bias = _f32(dt_bias); h0 = _f64(h0)
+        bt, L, H, P = x.shape
+        G, N = B.shape[2], B.shape[3]
+        assert dt.shape == (bt, L, H) and B.shape == (bt, L, G, N) and C.shape == B.shape
+        y = np.empty((bt, L, H, P), dtype=np.float64)
+        hl = np.empty((bt, H, P, N), dtype=np.float64)
+        rc = self.lib.oracle_ssd_scan(_p(x), _p(dt), _p(A), _p(B), _p(C), _p(D), _p(z), _p(dt_bias),
+                                      int(bool(softplus)), _p(h0), _p(y), _p(hl), bt, L, H, P, G, N, int(threads))
+        if rc != 0:
+            raise ValueError("oracle_ssd_scan rejected the sizes")
+        return y, hl
+
     def causal_conv1d(self, x, w, bias=None, conv_state=None, silu=True, threads: int = 0):
         """Causal depthwise conv1d (+ silu) in fp64.
 
@@ -224,6 +243,10 @@ def state_update(*args, **kw):
 
 def scan_bwd(*args, **kw):
     return default().scan_bwd(*args, **kw)
+
+
+def ssd_scan(*args, **kw):
+    return default().ssd_scan(*args, **kw)
 
 
 def causal_conv1d(*args, **kw):

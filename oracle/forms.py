@@ -96,3 +96,68 @@ def tree_scan(gates, tokens, order_rng=None):
     for t in range(T):
         out[t] = reduce(0, t + 1)[1]
     return out
+
+
+def ssd_quadratic(x, dt, A, B, C, D=None, h0=None):
+    """The state space duality form of the Mamba-2 SSM (Mamba SSM complete guide,
+    section 6, "State Space Duality": an SSM with a scalar decay per head is a
+    semi-separable matrix applied to the input). Per (batch, head), with
+    cum_t = A sum_{r<=t} dt_r and the causal mask s <= t:
+        M[t, s] = exp(cum_t - cum_s) (C_t . B_s) dt_s
+        y_t = sum_s M[t, s] x_s + exp(cum_t) H0 C_t + D x_t
+    (dt already discretised: softplus applied by the caller; no gate).
+    x: (batch, L, H, P); dt: (batch, L, H); B, C: (batch, L, G, N); A, D: (H,);
+    h0: (batch, H, P, N). fp64 matrix products."""
+    x = np.asarray(x, np.float64); dt = np.asarray(dt, np.float64)
+    B = np.asarray(B, np.float64); C = np.asarray(C, np.float64)
+    bt, L, H, P = x.shape
+    G = B.shape[2]
+    y = np.zeros_like(x)
+    for b in range(bt):
+        for h in range(H):
+            g = h // (H // G)
+            cum = np.cumsum(dt[b, :, h]) * float(A[h])
+            decay = np.exp(cum[:, None] - cum[None, :])
+            mask = np.tril(np.ones((L, L), dtype=bool))
+            M = np.where(mask, decay, 0.0) * (C[b, :, g, :] @ B[b, :, g, :].T) * dt[b, None, :, h]
+            yh = M @ x[b, :, h, :]
+            if h0 is not None:
+                yh += np.exp(cum)[:, None] * (C[b, :, g, :] @ np.asarray(h0, np.float64)[b, h].T)
+            if D is not None:
+                yh += float(D[h]) * x[b, :, h, :]
+            y[b, :, h, :] = yh
+    return y
+
+
+def ssd_chunked(x, dt, A, B, C, D=None, h0=None, chunk: int = 16):
+    """The chunked SSD algorithm (same section: "inside a chunk, matrix products;
+    across chunks, the recurrence carries the state"): per chunk of `chunk` steps,
+    the intra-chunk part is the quadratic form above restricted to the chunk, the
+    carried state H enters through exp(cum_t) H C_t, and the state leaves the chunk
+    as H <- exp(cum_end) H + sum_s exp(cum_end - cum_s) dt_s x_s B_s^T.
+    Same arguments as ssd_quadratic; returns (y, h_last)."""
+    x = np.asarray(x, np.float64); dt = np.asarray(dt, np.float64)
+    B = np.asarray(B, np.float64); C = np.asarray(C, np.float64)
+    bt, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    y = np.zeros_like(x)
+    hl = np.zeros((bt, H, P, N))
+    for b in range(bt):
+        for h in range(H):
+            g = h // (H // G)
+            S = np.zeros((P, N)) if h0 is None else np.asarray(h0, np.float64)[b, h].copy()
+            for c0 in range(0, L, chunk):
+                c1 = min(L, c0 + chunk)
+                d = dt[b, c0:c1, h]
+                cum = np.cumsum(d) * float(A[h])
+                Bc, Cc, xc = B[b, c0:c1, g, :], C[b, c0:c1, g, :], x[b, c0:c1, h, :]
+                q = c1 - c0
+                decay = np.where(np.tril(np.ones((q, q), dtype=bool)), np.exp(cum[:, None] - cum[None, :]), 0.0)
+                yc = (decay * (Cc @ Bc.T) * d[None, :]) @ xc + np.exp(cum)[:, None] * (Cc @ S.T)
+                if D is not None:
+                    yc += float(D[h]) * xc
+                y[b, c0:c1, h, :] = yc
+                w = np.exp(cum[-1] - cum) * d
+                S = np.exp(cum[-1]) * S + (xc * w[:, None]).T @ Bc
+            hl[b, h] = S
+    return y, hl

@@ -237,6 +237,61 @@ int oracle_scan_bwd(const float *u, const float *delta, const float *A, const fl
     return 0;
 }
 
+/* Mamba-2 multi-head SSM (the next row after the Mamba-1 path; Mamba SSM complete
+ * guide (youngju.dev), section 6 "Mamba 2": a scalar A per head, the state of a
+ * head a (headdim x dstate) matrix, heads grouped over shared B and C), written as
+ * its defining recurrence, sequentially in fp64:
+ *     dt = softplus(dt_raw + dt_bias_h)                (raw sum without softplus)
+ *     H_t = exp(dt A_h) H_{t-1} + dt x_t B_t^T,   y_t = H_t C_t + D_h x_t,   y_t *= silu(z_t)
+ * Readings where the page gives no code (its Mamba2Block.forward is a stub): the
+ * layouts of the upstream package's SSD interface, time-major:
+ *   x, z, y : (batch, seqlen, nheads, headdim)    dt_raw : (batch, seqlen, nheads)
+ *   B, C    : (batch, seqlen, ngroups, dstate)    A, D, dt_bias : (nheads)
+ *   h0, h_last : (batch, nheads, headdim, dstate)
+ * head h reads group h / (nheads / ngroups). z, D, dt_bias, h0, h_last may be NULL. */
+int oracle_ssd_scan(const float *x, const float *dt_raw, const float *A, const float *B,
+                    const float *C, const float *D, const float *z, const float *dt_bias,
+                    int softplus, const double *h0, double *y, double *h_last, int64_t batch,
+                    int64_t seqlen, int64_t nheads, int64_t headdim, int64_t ngroups,
+                    int64_t dstate, int nthreads) {
+    if (batch < 0 || seqlen < 0 || nheads < 1 || headdim < 1 || ngroups < 1 || dstate < 1 ||
+        nheads % ngroups != 0)
+        return -1;
+    int64_t H = nheads, P = headdim, G = ngroups, N = dstate, L = seqlen;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t bh = 0; bh < batch * H; bh++) {
+        int64_t b = bh / H, h = bh % H, g = h / (H / G);
+        double *S = (double *)malloc(sizeof(double) * (size_t)(P * N));
+        for (int64_t k = 0; k < P * N; k++) S[k] = h0 ? h0[bh * P * N + k] : 0.0;
+        for (int64_t t = 0; t < L; t++) {
+            double v = (double)dt_raw[(b * L + t) * H + h] + (dt_bias ? (double)dt_bias[h] : 0.0);
+            double dt = softplus ? oracle_softplus(v) : v;
+            double a = exp(dt * (double)A[h]);
+            const float *Bt = B + ((b * L + t) * G + g) * N, *Ct = C + ((b * L + t) * G + g) * N;
+            for (int64_t p = 0; p < P; p++) {
+                int64_t xi = ((b * L + t) * H + h) * P + p;
+                double xt = (double)x[xi];
+                double acc = 0.0;
+                for (int64_t n = 0; n < N; n++) {
+                    double *s = &S[p * N + n];
+                    *s = a * *s + dt * (double)Bt[n] * xt;
+                    acc += (double)Ct[n] * *s;
+                }
+                double yv = acc + (D ? (double)D[h] * xt : 0.0);
+                if (z) yv *= oracle_silu((double)z[xi]);
+                y[xi] = yv;
+            }
+        }
+        if (h_last)
+            for (int64_t k = 0; k < P * N; k++) h_last[bh * P * N + k] = S[k];
+        free(S);
+    }
+    return 0;
+}
+
 /* Causal depthwise 1-D convolution and SiLU: the step before the scan in the
  * same page's MambaBlock (section 5, "complete Mamba implementation"): __init__
  * builds nn.Conv1d(d_inner, d_inner, kernel_size=d_conv, groups=d_inner,

@@ -442,6 +442,61 @@ def check_bwd_finite_differences(orc):
             assert err < 2e-5, (name, with_z, err)
 
 
+# ---------------------------------------------------------------------------
+# 15. Mamba-2 SSM (the next row): the recurrence oracle against (a) the pinned
+#     Mamba-1 oracle with every state of a head sharing its A, dt, B and C;
+#     (b) the state space duality's quadratic (semi-separable matrix) form; and
+#     (c) the chunked algorithm ([guide] section 6, "State Space Duality").
+# ---------------------------------------------------------------------------
+def _ssd_case(rng, bt=2, L=37, H=4, P=3, G=2, N=5, sp=True):
+    x = rng.standard_normal((bt, L, H, P)).astype(np.float32)
+    dt = (rng.standard_normal((bt, L, H)) * 0.5).astype(np.float32)
+    A = -np.exp(rng.uniform(np.log(0.5), np.log(4.0), size=(H,))).astype(np.float32)
+    B = rng.standard_normal((bt, L, G, N)).astype(np.float32)
+    C = rng.standard_normal((bt, L, G, N)).astype(np.float32)
+    D = rng.standard_normal((H,)).astype(np.float32)
+    bias = (rng.uniform(-4, -2, size=(H,))).astype(np.float32)
+    h0 = rng.standard_normal((bt, H, P, N))
+    return x, dt, A, B, C, D, bias, h0
+
+
+def check_ssd_matches_mamba1(orc):
+    rng = np.random.default_rng(41)
+    x, dt, A, B, C, D, bias, h0 = _ssd_case(rng)
+    z = rng.standard_normal(x.shape).astype(np.float32)
+    bt, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    y, hl = orc.ssd_scan(x, dt, A, B, C, D, z, bias, True, h0)
+    # channel (h, p) of Mamba-1: u = x[:, :, h, p], delta = dt[:, :, h], A_dn = A_h, B/C of the head's group
+    for h in range(H):
+        g = h // (H // G)
+        u1 = np.ascontiguousarray(x[:, :, h, :].transpose(0, 2, 1))
+        d1 = np.ascontiguousarray(np.repeat(dt[:, None, :, h], P, axis=1))
+        z1 = np.ascontiguousarray(z[:, :, h, :].transpose(0, 2, 1))
+        A1 = np.full((P, N), A[h], np.float32)
+        B1 = np.ascontiguousarray(B[:, :, g, :].transpose(0, 2, 1))
+        C1 = np.ascontiguousarray(C[:, :, g, :].transpose(0, 2, 1))
+        y1, h1 = orc.scan(u1, d1, A1, B1, C1, np.full(P, D[h], np.float32), z1, np.full(P, bias[h], np.float32),
+                          True, h0[:, h])
+        assert _rel(y1.transpose(0, 2, 1), y[:, :, h, :]) < 1e-13
+        assert _rel(h1, hl[:, h]) < 1e-13
+
+
+def check_ssd_quadratic_and_chunked(orc):
+    rng = np.random.default_rng(43)
+    x, dt, A, B, C, D, bias, h0 = _ssd_case(rng, L=53)
+    y, hl = orc.ssd_scan(x, dt, A, B, C, D, None, None, False, h0)       # raw dt: no softplus
+    dt64 = dt.astype(np.float64)
+    dtp = np.abs(dt64) + 0.01          # the forms below need the discretised dt itself
+    y2, hl2 = orc.ssd_scan(x, dtp.astype(np.float32), A, B, C, D, None, None, False, h0)
+    yq = forms.ssd_quadratic(x, dtp.astype(np.float32), A, B, C, D, h0)
+    assert _rel(yq, y2) < 1e-11
+    for q in (1, 7, 16, 64):
+        yc, hc = forms.ssd_chunked(x, dtp.astype(np.float32), A, B, C, D, h0, chunk=q)
+        assert _rel(yc, y2) < 1e-11 and _rel(hc, hl2) < 1e-11
+    assert np.all(np.isfinite(y)) and np.all(np.isfinite(hl))
+
+
 ALL_CHECKS = [
     check_bruteforce_rational,
     check_symbolic_two_steps,
@@ -459,4 +514,6 @@ ALL_CHECKS = [
     check_conv_library,
     check_conv_resume_and_decode,
     check_bwd_finite_differences,
+    check_ssd_matches_mamba1,
+    check_ssd_quadratic_and_chunked,
 ]

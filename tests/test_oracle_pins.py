@@ -54,6 +54,12 @@ MUTANTS = [
      "dz[ch * L + t] = dy * yv * sg;"),
     ("bwd_dA_missing_dt", "pA[ch * N + n] += g[n] * hprev * an * dt;", "pA[ch * N + n] += g[n] * hprev * an;"),
     ("bwd_du_missing_skip", "double dut = Dd * dy, ddt = 0.0;", "double dut = 0.0, ddt = 0.0;"),
+    ("ssd_sign_of_A", "double a = exp(dt * (double)A[h]);", "double a = exp(-dt * (double)A[h]);"),
+    ("ssd_no_dt_on_input", "*s = a * *s + dt * (double)Bt[n] * xt;", "*s = a * *s + (double)Bt[n] * xt;"),
+    ("ssd_B_for_C", "acc += (double)Ct[n] * *s;", "acc += (double)Bt[n] * *s;"),
+    ("ssd_group_map", "int64_t b = bh / H, h = bh % H, g = h / (H / G);",
+     "int64_t b = bh / H, h = bh % H, g = h % G;"),
+    ("ssd_drop_D", "double yv = acc + (D ? (double)D[h] * xt : 0.0);", "double yv = acc;"),
     ("conv_update_wrong_weight", "acc += (double)w[d * width + hw] * xt;", "acc += (double)w[d * width] * xt;"),
 ]
 
