@@ -73,7 +73,10 @@ typedef enum {
     SSM_ERR_ALIAS = -9,             /* an output overlaps an input it must not */
     SSM_ERR_ALGO = -10,             /* unknown algorithm selector */
     SSM_ERR_SCRATCH_LIMIT = -11,    /* problem needs more than SSM_STATIC_SCRATCH_BYTES of scratch */
-    SSM_ERR_WIDTH = -12             /* conv width not in 1..4 */
+    SSM_ERR_WIDTH = -12,            /* conv width not in 1..4 */
+    SSM_ERR_SHAPE = -13,            /* SSD: headdim not 64, dstate not 64/128 or
+                                       nheads not a multiple of ngroups */
+    SSM_ERR_WAIT_TIMEOUT = -14      /* device: an SSD tensor-core wait exhausted its budget */
 } ssm_status_t;
 
 /* Algorithm selectors for ssm_scan_fwd_algo. All compute the same result.
@@ -233,6 +236,45 @@ SSM_API int ssm_causal_conv1d_update(float* conv_state, const void* x, const flo
                                      const float* bias, void* out, int64_t batch, int64_t dim,
                                      int64_t width, int silu, int in_dtype, int out_dtype,
                                      void* stream);
+
+/* Mamba-2 state-space-duality (SSD) scan on the tensor cores (Mamba SSM
+ * complete guide (youngju.dev), section 6 "Mamba 2": a multi-head SSM with one
+ * scalar A per head, computed by chunks -- matrix products inside a chunk, the
+ * recurrence between chunks). For batch row b, head h of group g = h / (nheads /
+ * ngroups), step t, head channel p < headdim and state n < dstate:
+ *     dt_t     = softplus(dt[b,t,h] + dt_bias[h])           (raw sum when softplus == 0)
+ *     H_t[p,n] = exp(dt_t * A[h]) * H_{t-1}[p,n] + dt_t * x[b,t,h,p] * B[b,t,g,n]
+ *     y[b,t,h,p] = sum_n C[b,t,g,n] * H_t[p,n] + D[h] * x[b,t,h,p]
+ *     y       *= silu(z[b,t,h,p])                            (only when z != NULL)
+ * starting from H_{-1} = h0[b,h] (zero when h0 == NULL); h_last receives H at the
+ * last step. Chunks of 128 steps; inside a chunk the four products (C B^T, the
+ * decay-masked matrix times x, C times the incoming state, the state update)
+ * run as tcgen05 bf16 MMAs with fp32 accumulators in tensor memory, the computed
+ * operands split into bf16 high and low parts.
+ *   x, z    : (batch, seqlen, nheads, headdim) bf16, headdim == 64  [z optional]
+ *   dt      : (batch, seqlen, nheads) bf16                          [required]
+ *   A       : (nheads) fp32 (negative for a decaying state)         [required]
+ *   B, C    : (batch, seqlen, ngroups, dstate) bf16, dstate 64 or 128 [required]
+ *   D, dt_bias : (nheads) fp32                                      [optional]
+ *   h0, h_last : (batch, nheads, headdim, dstate) fp32; h_last may be h0 itself [optional]
+ *   y       : (batch, seqlen, nheads, headdim), out_dtype (bf16 or fp32) [required]
+ * in_dtype must be SSM_BF16 (SSM_ERR_DTYPE otherwise). x, z, y, B and C must be
+ * 16-byte aligned (SSM_ERR_ALIGN); other shapes give SSM_ERR_SHAPE. y and h_last
+ * overlap no input (except h_last == h0). A tensor-core wait that runs out of
+ * its budget is recorded on the device and read with ssm_device_status(). */
+SSM_API int ssm_ssd_scan_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                             const float* D, const void* z, const float* dt_bias, int softplus,
+                             const float* h0, void* y, float* h_last, int64_t batch, int64_t seqlen,
+                             int64_t nheads, int64_t headdim, int64_t ngroups, int64_t dstate,
+                             int in_dtype, int out_dtype, void* stream);
+
+/* Chunk length (time steps) of ssm_ssd_scan_fwd. */
+SSM_API int64_t ssm_ssd_chunk_len(void);
+
+/* Synchronises `stream`, then returns SSM_ERR_WAIT_TIMEOUT if an SSD launch since
+ * the last clear recorded a wait that ran out of its budget, else SSM_OK
+ * (SSM_ERR_LAUNCH if the read itself failed). clear != 0 resets the record. */
+SSM_API int ssm_device_status(int clear, void* stream);
 
 /* Test hook for the look-back error path. Runs the look-back scan (softplus on,
  * no D, z, bias or h0; y in in_dtype) with segment `drop_segment` withholding

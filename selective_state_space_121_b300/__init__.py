@@ -64,12 +64,20 @@ _lib.ssm_causal_conv1d_fwd.argtypes = [_P] * 6 + [_I64] * 4 + [_I, _I, _I, _P]
 _lib.ssm_causal_conv1d_fwd.restype = _I
 _lib.ssm_causal_conv1d_update.argtypes = [_P] * 5 + [_I64] * 3 + [_I, _I, _I, _P]
 _lib.ssm_causal_conv1d_update.restype = _I
+_lib.ssm_ssd_scan_fwd.argtypes = [_P] * 8 + [_I, _P, _P, _P] + [_I64] * 6 + [_I, _I, _P]
+_lib.ssm_ssd_scan_fwd.restype = _I
+_lib.ssm_ssd_chunk_len.argtypes = []
+_lib.ssm_ssd_chunk_len.restype = _I64
+_lib.ssm_device_status.argtypes = [_I, _P]
+_lib.ssm_device_status.restype = _I
 
 SSM_F32, SSM_BF16 = 0, 1
 ALGOS = {"auto": 0, "thread": 1, "warpscan": 2, "lookback": 3}
 SSM_ERR_LOOKBACK_TIMEOUT = -7
 SSM_ERR_SCRATCH_LIMIT = -11
 SSM_ERR_WIDTH = -12
+SSM_ERR_SHAPE = -13
+SSM_ERR_WAIT_TIMEOUT = -14
 STATIC_SCRATCH_BYTES = 4 << 20   # SSM_STATIC_SCRATCH_BYTES
 
 # the C ABI entry-point names, as declared in include/ssm_scan.h
@@ -77,7 +85,7 @@ EXPORTS = ("ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_size", "s
            "ssm_scan_fwd_algo", "ssm_scalar_scan_fwd", "ssm_state_update",
            "ssm_test_lookback_timeout", "ssm_query_status", "ssm_scan_fwd_lookback_static",
            "ssm_causal_conv1d_fwd", "ssm_causal_conv1d_update", "ssm_scan_bwd_workspace_size",
-           "ssm_scan_bwd")
+           "ssm_scan_bwd", "ssm_ssd_scan_fwd", "ssm_ssd_chunk_len", "ssm_device_status")
 
 
 class SSMError(RuntimeError):
@@ -315,6 +323,37 @@ def causal_conv1d_update(conv_state, x, weight, bias=None, silu=True, *, out_dty
         _dtype_code(x.dtype), _dtype_code(out.dtype), _stream())
     _check(status)
     return out
+
+
+def ssd_scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, softplus=True, h0=None, *,
+                 out_dtype=None, y=None, h_last=None, return_last_state=True):
+    """Mamba-2 SSD scan on the tensor cores. x, z: (batch, L, nheads, 64) bf16; dt: (batch,
+    L, nheads) bf16; A, D, dt_bias: (nheads,) fp32; B, C: (batch, L, ngroups, dstate) bf16
+    with dstate 64 or 128; h0: (batch, nheads, 64, dstate) fp32. Returns (y, h_last)."""
+    bt, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    _same(x, [("dt", dt, (bt, L, H)), ("B", B, (bt, L, G, N)), ("C", C, (bt, L, G, N)), ("z", z, (bt, L, H, P))])
+    _f32(A, (H,), "A"); _f32(D, (H,), "D"); _f32(dt_bias, (H,), "dt_bias"); _f32(h0, (bt, H, P, N), "h0")
+    if y is None:
+        y = torch.empty((bt, L, H, P), dtype=out_dtype or x.dtype, device=x.device)
+    if h_last is None and return_last_state:
+        h_last = torch.empty((bt, H, P, N), dtype=torch.float32, device=x.device)
+    _f32(h_last, (bt, H, P, N), "h_last")
+    status = _lib.ssm_ssd_scan_fwd(
+        _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias), int(bool(softplus)),
+        _ptr(h0), _ptr(y), _ptr(h_last), bt, L, H, P, G, N, _dtype_code(x.dtype), _dtype_code(y.dtype),
+        _stream())
+    _check(status)
+    return y, h_last
+
+
+def ssd_chunk_len() -> int:
+    return int(_lib.ssm_ssd_chunk_len())
+
+
+def device_status(clear: bool = True) -> int:
+    """SSM_ERR_WAIT_TIMEOUT if an SSD launch recorded an exhausted wait (syncs the stream)."""
+    return int(_lib.ssm_device_status(int(bool(clear)), _stream()))
 
 
 def query_status(workspace) -> int:

@@ -11,6 +11,7 @@ namespace {
 using ssm::DecodeArgs;
 using ssm::BwdArgs;
 using ssm::ConvArgs;
+using ssm::SsdArgs;
 using ssm::ScanArgs;
 
 constexpr uint32_t kSpinLimit = 1u << 20;   // look-back waits: ~0.1-1 s before giving up
@@ -212,6 +213,9 @@ const char* ssm_status_string(int status) {
         case SSM_ERR_ALIAS: return "SSM_ERR_ALIAS: an output overlaps an input";
         case SSM_ERR_ALGO: return "SSM_ERR_ALGO: unknown algorithm";
         case SSM_ERR_WIDTH: return "SSM_ERR_WIDTH: conv width must be 1, 2, 3 or 4";
+        case SSM_ERR_SHAPE:
+            return "SSM_ERR_SHAPE: SSD needs headdim 64, dstate 64 or 128 and nheads a multiple of ngroups";
+        case SSM_ERR_WAIT_TIMEOUT: return "SSM_ERR_WAIT_TIMEOUT: a tensor-core wait exhausted its budget";
         case SSM_ERR_SCRATCH_LIMIT:
             return "SSM_ERR_SCRATCH_LIMIT: problem needs more scratch than the library's fixed 4 MiB area";
     }
@@ -477,6 +481,57 @@ int ssm_query_status(const void* workspace, size_t workspace_bytes, void* stream
         return SSM_ERR_LAUNCH;
     if (cudaStreamSynchronize(s) != cudaSuccess) return SSM_ERR_LAUNCH;
     return st;
+}
+
+
+int ssm_ssd_scan_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                     const float* D, const void* z, const float* dt_bias, int softplus, const float* h0,
+                     void* y, float* h_last, int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                     int64_t ngroups, int64_t dstate, int in_dtype, int out_dtype, void* stream) {
+    if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype) || in_dtype != SSM_BF16) return SSM_ERR_DTYPE;
+    if (batch < 0 || seqlen < 0 || nheads < 0 || ngroups < 0) return SSM_ERR_DIM;
+    if (headdim != 64 || (dstate != 64 && dstate != 128)) return SSM_ERR_SHAPE;
+    if (nheads > 0 && (ngroups < 1 || nheads % ngroups != 0)) return SSM_ERR_SHAPE;
+    const int64_t n_bh = mul(batch, nheads);
+    const int64_t n_dt = mul(n_bh, seqlen);
+    const int64_t n_x = mul(n_dt, headdim);
+    const int64_t n_bc = mul(mul(mul(batch, seqlen), ngroups), dstate);
+    const int64_t n_h = mul(mul(n_bh, headdim), dstate);
+    if (n_bh < 0 || n_dt < 0 || n_x < 0 || n_bc < 0 || n_h < 0 || n_bh > INT32_MAX) return SSM_ERR_DIM;
+    if (n_x > 0 && (!x || !dt || !B || !C || !y)) return SSM_ERR_NULL;
+    if (nheads > 0 && !A) return SSM_ERR_NULL;
+    const void* v16[] = {x, z, y, B, C};
+    for (const void* p : v16)
+        if (p && !aligned(p, 16)) return SSM_ERR_ALIGN;
+    if (dt && !aligned(dt, 2)) return SSM_ERR_ALIGN;
+    const void* f32_ptrs[] = {A, D, dt_bias, h0, h_last};
+    for (const void* p : f32_ptrs)
+        if (p && !aligned(p, 4)) return SSM_ERR_ALIGN;
+    const size_t eo = esize(out_dtype);
+    const size_t bx = (size_t)n_x * 2, by = (size_t)n_x * eo, bdt = (size_t)n_dt * 2, bbc = (size_t)n_bc * 2,
+                 bh = (size_t)n_h * 4, bp = (size_t)nheads * 4;
+    const void* ins[] = {x, z, dt, B, C, A, D, dt_bias, h0};
+    const size_t ins_b[] = {bx, bx, bdt, bbc, bbc, bp, bp, bp, bh};
+    for (int i = 0; i < 9; i++)
+        if (overlap(y, by, ins[i], ins_b[i])) return SSM_ERR_ALIAS;
+    for (int i = 0; i < 8; i++)
+        if (overlap(h_last, bh, ins[i], ins_b[i])) return SSM_ERR_ALIAS;
+    if (overlap(h_last, bh, y, by) || (h_last != h0 && overlap(h_last, bh, h0, bh))) return SSM_ERR_ALIAS;
+    if (n_bh == 0) return SSM_OK;
+    SsdArgs a;
+    memset(&a, 0, sizeof(a));
+    a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.dt_bias = dt_bias; a.h0 = h0;
+    a.y = y; a.h_last = h_last; a.batch = batch; a.seqlen = seqlen; a.nheads = nheads;
+    a.ngroups = ngroups; a.dstate = (int)dstate; a.softplus = softplus ? 1 : 0; a.out_dtype = out_dtype;
+    return ssm::launch_ssd_scan(a, (cudaStream_t)stream) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+}
+
+int64_t ssm_ssd_chunk_len(void) { return ssm::ssd_chunk_len(); }
+
+int ssm_device_status(int clear, void* stream) {
+    int line = 0;
+    if (ssm::ssd_status(&line, clear != 0, (cudaStream_t)stream) != cudaSuccess) return SSM_ERR_LAUNCH;
+    return line != 0 ? SSM_ERR_WAIT_TIMEOUT : SSM_OK;
 }
 
 }  // extern "C"

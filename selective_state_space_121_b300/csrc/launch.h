@@ -100,8 +100,32 @@ struct BwdArgs {
     bool vec;               // rows of u/delta/z/dout/du/ddelta/dz 16-byte aligned
 };
 
+// Mamba-2 SSD scan (bf16 x, dt, B, C, z; fp32 A, D, dt_bias, states).
+struct SsdArgs {
+    const void* x;          // (batch, seqlen, nheads, 64)
+    const void* dt;         // (batch, seqlen, nheads)
+    const float* A;         // (nheads)
+    const void* B;          // (batch, seqlen, ngroups, dstate)
+    const void* C;
+    const float* D;         // (nheads) or null
+    const void* z;          // like x, or null
+    const float* dt_bias;   // (nheads) or null
+    const float* h0;        // (batch, nheads, 64, dstate) or null
+    void* y;                // like x, out_dtype
+    float* h_last;          // like h0, or null
+    int64_t batch, seqlen, nheads, ngroups;
+    int dstate;             // 64 or 128
+    int softplus;
+    int out_dtype;
+};
+
 // Each returns cudaSuccess or the launch error.
 cudaError_t launch_scan_bwd(const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_ssd_scan(const SsdArgs& a, cudaStream_t s);
+int64_t ssd_chunk_len();
+// reads (and optionally clears) the SSD kernel's device status word: 0 or the
+// source line of a wait that ran out of budget; synchronises the stream
+cudaError_t ssd_status(int* line, bool clear, cudaStream_t s);
 size_t scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate);
 cudaError_t launch_causal_conv1d(const ConvArgs& a, cudaStream_t s);
 cudaError_t launch_conv_update(const ConvArgs& a, cudaStream_t s);

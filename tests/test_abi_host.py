@@ -43,7 +43,7 @@ def test_abi_version_matches_header(ssm):
 
 
 def test_status_strings(ssm):
-    for code in range(0, -13, -1):
+    for code in range(0, -15, -1):
         assert ssm.status_string(code).startswith("SSM_")
     assert not ssm.status_string(-99).startswith("SSM_")
 
@@ -156,3 +156,31 @@ def test_conv_validation(ssm):
     assert upd(out=FAKE + 8) == -9                    # out inside the state
     assert upd(x=FAKE + 16) == -9                     # state overlaps x
     assert upd(st=FAKE + 2) == -4
+
+
+def test_ssd_validation(ssm):
+    """Argument errors of ssm_ssd_scan_fwd come back before any launch (no GPU needed)."""
+    f = ssm._lib.ssm_ssd_scan_fwd
+
+    def call(**kw):
+        a = dict(x=FAKE, dt=FAKE * 2, A=FAKE * 3, B=FAKE * 4, C=FAKE * 5, D=None, z=None, bias=None, sp=1,
+                 h0=None, y=FAKE * 6, hl=None, batch=2, L=8, H=4, P=64, G=1, N=128, idt=1, odt=1)
+        a.update(kw)
+        return f(a["x"], a["dt"], a["A"], a["B"], a["C"], a["D"], a["z"], a["bias"], a["sp"], a["h0"], a["y"],
+                 a["hl"], a["batch"], a["L"], a["H"], a["P"], a["G"], a["N"], a["idt"], a["odt"], None)
+    assert call(idt=0) == -3                           # fp32 inputs are not taken
+    assert call(odt=5) == -3
+    assert call(P=32) == -13
+    assert call(N=16) == -13
+    assert call(H=3, G=2) == -13                       # heads not a multiple of groups
+    assert call(L=-1) == -2
+    assert call(x=None) == -1
+    assert call(A=None) == -1
+    assert call(x=FAKE + 8) == -4                      # x rows need 16-byte alignment
+    assert call(B=FAKE * 4 + 2) == -4
+    assert call(hl=FAKE * 7 + 2) == -4
+    assert call(y=FAKE + 64) == -9                     # y overlaps x
+    assert call(hl=FAKE * 3) == -9                     # final state over A
+    assert call(h0=FAKE * 7, hl=FAKE * 7 + 4) == -9    # partly over the initial state
+    assert call(batch=1 << 40, H=1 << 30) == -2
+    assert ssm._lib.ssm_ssd_chunk_len() == 128

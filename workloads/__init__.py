@@ -119,6 +119,37 @@ CONV_CONFIGS = {
 }
 
 
+
+@dataclasses.dataclass(frozen=True)
+class SsdConfig:
+    """Mamba-2 SSD workload: x (batch, seqlen, nheads, headdim), B/C (batch, seqlen,
+    ngroups, dstate), all bf16 but A, D, dt_bias and the state (fp32)."""
+    name: str
+    batch: int
+    seqlen: int
+    nheads: int
+    headdim: int
+    ngroups: int
+    dstate: int
+    has_D: bool
+    has_z: bool
+    h0: str                # "zero" | "normal"
+    out_dtype: str
+    seed_base: int
+
+    @property
+    def tokens_channels(self) -> int:
+        return self.batch * self.seqlen * self.nheads * self.headdim
+
+
+SSD_CONFIGS = {
+    # a few ragged chunks, both state widths covered by overriding dstate
+    "ssd_tiny": SsdConfig("ssd_tiny", 2, 300, 4, 64, 2, 64, True, True, "normal", BF16, 8000),
+    # 5120 scan channels as 80 heads of 64 (the 2.8B-shaped layer's width), d_state 64
+    "ssd_5120": SsdConfig("ssd_5120", 4, 4096, 80, 64, 1, 64, True, True, "zero", BF16, 8100),
+}
+
+
 def _rng(seed: int) -> np.random.Generator:
     return np.random.Generator(np.random.PCG64(seed))
 
@@ -274,4 +305,35 @@ def make_conv_inputs(cfg: ConvConfig, batch: Optional[int] = None, dim: Optional
     out["bias"] = _rng(sb + 3).uniform(-bound, bound, size=(Dm,)).astype(np.float32)
     st = Tensor(_normal(sb + 4, (Bt, Dm, W_ - 1)), cfg.in_dtype).f32() if with_state else None
     out["conv_state"] = None if st is None else np.ascontiguousarray(st, dtype=np.float32)
+    return out
+
+
+def make_ssd_inputs(cfg: SsdConfig, batch: Optional[int] = None, seqlen: Optional[int] = None,
+                    nheads: Optional[int] = None, ngroups: Optional[int] = None,
+                    dstate: Optional[int] = None) -> dict:
+    """Seeded inputs of an SSD workload (sizes overridable).
+
+    x, z, B, C ~ N(0, 1) and dt ~ N(0, 0.5), stored bf16; A_h = -exp(A_log_h) with
+    A_log ~ N(0, 1) (the page's Mamba2Block.__init__ draws A_log = randn(n_heads));
+    dt_bias_h = softplus^-1(dt0_h), dt0_h = exp(U(log 1e-3, log 1e-1)); D ~ N(0, 1);
+    h0 ~ N(0, 1) (batch, nheads, headdim, dstate) fp32 or None. Seeds base + k as
+    the prefill recipe (x=1, dt=2, z=3, B=4, C=5, A=6, D=7, bias=8, h0=9).
+    """
+    Bt = batch or cfg.batch
+    L = cfg.seqlen if seqlen is None else seqlen
+    H = nheads or cfg.nheads
+    G = ngroups or cfg.ngroups
+    N = dstate or cfg.dstate
+    P = cfg.headdim
+    sb = cfg.seed_base
+    out = {"batch": Bt, "seqlen": L, "nheads": H, "headdim": P, "ngroups": G, "dstate": N, "cfg": cfg}
+    out["x"] = Tensor(_normal(sb + K_U, (Bt, L, H, P)), BF16)
+    out["dt"] = Tensor(_normal(sb + K_DELTA, (Bt, L, H), std=0.5), BF16)
+    out["z"] = Tensor(_normal(sb + K_Z, (Bt, L, H, P)), BF16) if cfg.has_z else None
+    out["B"] = Tensor(_normal(sb + K_B, (Bt, L, G, N)), BF16)
+    out["C"] = Tensor(_normal(sb + K_C, (Bt, L, G, N)), BF16)
+    out["A"] = (-np.exp(_normal(sb + K_A, (H,)).astype(np.float64))).astype(np.float32)
+    out["D"] = _normal(sb + K_D, (H,)) if cfg.has_D else None
+    out["dt_bias"] = delta_bias(sb + K_BIAS, H)
+    out["h0"] = _normal(sb + K_H0, (Bt, H, P, N)) if cfg.h0 == "normal" else None
     return out

@@ -34,3 +34,8 @@ def scan_to_torch(inp: dict, device="cuda", pin: bool = False) -> dict:
 
 def decode_set_to_torch(s: dict, device="cuda", pin: bool = False) -> dict:
     return {k: to_torch(v, device, pin) for k, v in s.items()}
+
+
+def ssd_to_torch(inp: dict, device="cuda", pin: bool = False) -> dict:
+    keys = ("x", "dt", "z", "B", "C", "A", "D", "dt_bias", "h0")
+    return {k: to_torch(inp[k], device, pin) for k in keys}
