@@ -53,6 +53,15 @@ def _peaks():
     return 6400.0, SM_MAX_MHZ_NOMINAL, "fallback"
 
 
+def _bf16_peak():
+    """Measured dense bf16 tensor TFLOP/s (burst), else the fallback figure."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"])
+    return 1800.0
+
+
 # ------------------------------------------------------------------------------------------
 # workload accounting (algorithmic bytes and work per launch)
 # ------------------------------------------------------------------------------------------
@@ -77,6 +86,24 @@ def conv_bytes(bt, dim, L, width, ei, eo):
 def conv_update_bytes(bt, dim, width, ei, eo):
     """Conv decode update: x in, u out, the state read and written, weights and bias."""
     return bt * dim * (ei + eo + 2 * (width - 1) * 4) + dim * (width + 1) * 4
+
+
+def ssd_bytes(bt, L, H, P, G, N, eo, has_z, has_h0):
+    """Mamba-2 SSD scan: x (, z) in and y out once, dt, B and C once, h_last out (and
+    h0 in), A/D/dt_bias."""
+    x = bt * L * H * P
+    return (x * ((2 if has_z else 1) * 2 + eo) + bt * L * H * 2 + 2 * bt * L * G * N * 2
+            + bt * H * P * N * 4 * (2 if has_h0 else 1) + 3 * H * 4)
+
+
+def ssd_tensor_flops(bt, L, H, P, N, Q=128):
+    """Tensor-core FLOPs the SSD kernel issues per launch: per (b, h, chunk of Q) the
+    products C B^T (Q x Q x N), the masked matrix times x (Q x P x Q, high and low
+    parts), C times the state (Q x P x N, two parts) and the state update (N x P x Q,
+    two parts, M padded to 128 rows when N = 64)."""
+    chunks = bt * H * ((L + Q - 1) // Q)
+    per = 2 * Q * Q * N + 2 * (2 * Q * P * Q) + 2 * (2 * Q * P * N) + 2 * (2 * 128 * P * Q)
+    return chunks * per
 
 
 SFU_HALF_RATE_SLOTS = 2           # lg2 and rcp issue at half the ex2 rate (16/clk/SM measured)
@@ -460,7 +487,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-configs", action="store_true", help="skip timing the other prefill configs")
-    ap.add_argument("--only", choices=["scan", "decode", "conv", "conv_update", "scan_bwd"],
+    ap.add_argument("--only", choices=["scan", "decode", "conv", "conv_update", "scan_bwd", "ssd"],
                     help="time one entry point alone on --config (a kernel case for sweeps and ncu)")
     ap.add_argument("--config", default="mamba130m",
                     help="workload of --only: a prefill-scan config name, or 'decode'")
@@ -553,9 +580,12 @@ def main():
             torch.cuda.empty_cache()
         # the conv that feeds the scan (prefill and decode update, HBM-bound) and the
         # scan's backward on the Mamba-130M-shaped layer
-        for only, cfgname, steps in (("conv", None, 50), ("conv_update", None, 100), ("scan_bwd", "mamba130m", 5)):
+        for only, cfgname, steps in (("conv", None, 50), ("conv_update", None, 100), ("scan_bwd", "mamba130m", 5),
+                                     ("ssd", "ssd_5120", 10)):
             rec = time_case(only, cfgname, "auto", steps, 3, device)
             configs_measured[only] = {k: rec[k] for k in ("case", "ms_median", "Gtokch_s", "GB_s", "hbm_frac")}
+            if "tensor_TFLOP_s" in rec:
+                configs_measured[only].update({k: rec[k] for k in ("tensor_TFLOP_s", "tensor_frac")})
             torch.cuda.empty_cache()
 
     hbm_peak, _, peak_kind = _peaks()
@@ -707,6 +737,24 @@ def time_case(only, config, algo, steps, warmup, dev):
         tokch = cfg.batch * cfg.dim
         nbytes = conv_update_bytes(cfg.batch, cfg.dim, cfg.width, 2, 2)
         label = f"causal_conv1d_update ({cfg.batch},{cfg.dim}) width={cfg.width}"
+    elif only == "ssd":
+        from workloads.torch_io import ssd_to_torch
+        cfg = W.SSD_CONFIGS[config if config in W.SSD_CONFIGS else "ssd_5120"]
+        inp = W.make_ssd_inputs(cfg)
+        t = ssd_to_torch(inp, dev)
+        odt = torch.bfloat16 if cfg.out_dtype == W.BF16 else torch.float32
+        y = torch.empty((cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim), dtype=odt, device=dev)
+        hl = torch.empty((cfg.batch, cfg.nheads, cfg.headdim, cfg.dstate), dtype=torch.float32, device=dev)
+
+        def launch():
+            ssm.ssd_scan_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["z"], t["dt_bias"], True, t["h0"],
+                             y=y, h_last=hl)
+        tokch = cfg.tokens_channels
+        nbytes = ssd_bytes(cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.ngroups, cfg.dstate,
+                           2 if odt == torch.bfloat16 else 4, cfg.has_z, cfg.h0 != "zero")
+        flops = ssd_tensor_flops(cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.dstate)
+        label = (f"ssd {cfg.name} (batch {cfg.batch}, L {cfg.seqlen}, {cfg.nheads} heads x {cfg.headdim}, "
+                 f"groups {cfg.ngroups}, d_state {cfg.dstate})")
     else:
         cfg = W.DECODE_CONFIGS["decode"]
         inp = W.make_decode_inputs(cfg)
@@ -738,10 +786,15 @@ def time_case(only, config, algo, steps, warmup, dev):
     ms = np.array([e0.elapsed_time(e1) for e0, e1 in ev])
     hbm_peak, _, peak_kind = _peaks()
     med = float(np.median(ms))
-    return {"case": label, "launches": steps, "ms_median": med, "ms_mean": float(ms.mean()),
-            "ms_min": float(ms.min()), "Gtokch_s": tokch / (med * 1e-3) / 1e9,
-            "alg_bytes": nbytes, "GB_s": nbytes / (med * 1e-3) / 1e9,
-            "hbm_frac": nbytes / (med * 1e-3) / 1e9 / hbm_peak, "peak_GB_s": hbm_peak, "peak_kind": peak_kind}
+    rec = {"case": label, "launches": steps, "ms_median": med, "ms_mean": float(ms.mean()),
+           "ms_min": float(ms.min()), "Gtokch_s": tokch / (med * 1e-3) / 1e9,
+           "alg_bytes": nbytes, "GB_s": nbytes / (med * 1e-3) / 1e9,
+           "hbm_frac": nbytes / (med * 1e-3) / 1e9 / hbm_peak, "peak_GB_s": hbm_peak, "peak_kind": peak_kind}
+    if only == "ssd":
+        tf = flops / (med * 1e-3) / 1e12
+        rec.update({"tensor_flops": flops, "tensor_TFLOP_s": tf, "tensor_frac": tf / _bf16_peak(),
+                    "inputs_vs_L2": f"inputs {(nbytes - tokch * 2) / 1e6:.0f} MB > 126 MB L2"})
+    return rec
 
 
 def run_reference(args, world, rank):

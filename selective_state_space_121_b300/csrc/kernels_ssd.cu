@@ -35,12 +35,16 @@
 // One CTA of 256 threads per (b, h), walking the chunks in order. Warp w reaches
 // tensor-memory lanes 32 (w % 4) .. +31 and works on column half w / 4.
 // Tensor memory (256 columns): S and then Ye in [0, 128), Yi in [128, 192),
-// H^T in [192, 256). Shared memory holds every operand tile in the unswizzled
-// core-matrix layout (tcgen05.cuh) with 128 rows, stride_r = 128 B and
-// stride_c = 2048 B, so 16-byte chunk (row r, column group j) sits at
-// j * 2048 + r * 16.
+// H^T in [192, 256). The tiles TMA moves (C, B, x, z in; y out) are 128-row tiles
+// of 128-byte rows with 128-byte swizzling (one box per 64 columns); the tiles
+// the threads compute (M, w o x, H) use the unswizzled core-matrix layout with
+// stride_r = 128 B and stride_c = 2048 B, so 16-byte chunk (row r, column group
+// j) sits at j * 2048 + r * 16 (tcgen05.cuh describes both).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "launch.h"
@@ -56,23 +60,51 @@ constexpr int kQ = 128;               // chunk length (steps)
 constexpr int kP = 64;                // head channels
 constexpr int kThreads = 256;
 constexpr uint32_t kWaitLimit = 1u << 24;
-constexpr uint32_t kTileBig = 32768;  // 128 x 128 bf16
-constexpr uint32_t kTileX = 16384;    // 128 x 64 bf16
-// shared-memory map (bytes); the K-major tiles first so that every descriptor
-// reach stays inside the allocation
-constexpr uint32_t kOffMh = 0;
-constexpr uint32_t kOffMl = kOffMh + kTileBig;
-constexpr uint32_t kOffC = kOffMl + kTileBig;
-constexpr uint32_t kOffB = kOffC + kTileBig;
-constexpr uint32_t kOffX = kOffB + kTileBig;
-constexpr uint32_t kOffWh = kOffX + kTileX;
-constexpr uint32_t kOffWl = kOffWh + kTileX;
-constexpr uint32_t kOffHh = kOffWl + kTileX;
-constexpr uint32_t kOffHl = kOffHh + kTileX;
-constexpr uint32_t kSmemBytes = kOffHl + kTileX;   // 212992
-constexpr uint32_t kStrideC = 2048;                 // bytes between column groups
+constexpr uint32_t kStrideC = 2048;   // bytes between column groups of a 128-row tile
 // tensor-memory columns
 constexpr uint32_t kColS = 0, kColYe = 0, kColYi = 128, kColH = 192, kTmemCols = 256;
+
+// Shared-memory map (bytes) for state width N. The K-major tiles come first so
+// that every descriptor reach stays inside the allocation. With N = 64 the
+// inputs of the next chunk (C, B, x) load into a second stage while the current
+// chunk computes; with N = 128 there is room for one stage only.
+//   M hi/lo  : 128 x 128 bf16 each (t x s)
+//   stage k  : C (128 x N), B (128 x N), x (128 x 64), swizzled, 64 columns per 16 KB atom
+//   W hi/lo  : 128 x 64 each (s x p)
+//   H hi/lo  : N x 64 each (n x p), column groups N * 16 bytes apart
+//   z        : 128 x 64 (t x p), one stage; y is staged in the M area for its store
+// G4 reads B^T as a 128-row operand (M = 128 along n); with N = 64 its rows
+// 64..127 fall on whatever follows the B tile (inside the allocation) and only
+// feed state rows 64..127, which nothing reads.
+template <int kN>
+struct Smem {
+    static constexpr int kStages = kN == 64 ? 2 : 1;
+    static constexpr uint32_t kTileM = 32768;
+    static constexpr uint32_t kTileCB = (uint32_t)kN * 256;
+    static constexpr uint32_t kTileX = 16384;
+    static constexpr uint32_t kTileH = (uint32_t)kN * 128;
+    static constexpr uint32_t kStrideH = (uint32_t)kN * 16;
+    static constexpr uint32_t kMh = 0, kMl = kTileM;
+    static constexpr uint32_t kStage0 = 2 * kTileM;
+    static constexpr uint32_t kStageBytes = 2 * kTileCB + kTileX;
+    static constexpr uint32_t kC = 0, kB = kTileCB, kX = 2 * kTileCB;   // within a stage
+    static constexpr uint32_t kWh = kStage0 + kStages * kStageBytes, kWl = kWh + kTileX;
+    static constexpr uint32_t kHh = kWl + kTileX, kHl = kHh + kTileH;
+    static constexpr uint32_t kZ = kHl + kTileH;        // z of the current chunk (128 x 64)
+    static constexpr uint32_t kBytes = kZ + kTileX;
+    static constexpr uint32_t kY = kMh;                 // y staged for its store (M is free by then)
+    static_assert(kBytes + 3072 <= 232448, "shared memory (dynamic + static)");
+    static_assert(kStage0 + kB + 32768 <= kBytes, "G4 reach of stage 0");
+    static_assert(kStage0 + (kStages - 1) * kStageBytes + kB + 32768 <= kBytes, "G4 reach of the last stage");
+};
+
+// Tensor maps of C, B, x, z and y: 3-D views (row elements, seqlen, batch) of the
+// (batch, seqlen, row) arrays with 128-byte swizzling, box = 128 bytes x 128
+// steps x 1 -- one 16 KB atom column of a tile; loads past seqlen arrive as zeros
+// and stores past it are dropped.
+struct SsdMaps {
+    CUtensorMap c, b, x, z, y;
+};
 
 // offset of the 16-byte chunk (row r, column group j) in a tile
 __device__ __forceinline__ uint32_t chunk_off(int r, int j) { return (uint32_t)j * kStrideC + (uint32_t)r * 16u; }
@@ -102,59 +134,95 @@ __device__ __forceinline__ void unpack8(uint4 v, float* out) {
     }
 }
 
-// Issue K/16 MMAs: D (+)= A . B over K. Operand descriptors advance by
-// `astep` / `bstep` bytes per K step of 16.
-__device__ __forceinline__ void mma_chain(uint32_t d, uint32_t a_addr, uint32_t a_lbo, uint32_t a_sbo,
-                                          uint32_t astep, uint32_t b_addr, uint32_t b_lbo, uint32_t b_sbo,
-                                          uint32_t bstep, uint32_t idesc, int ksteps, bool acc) {
-    for (int k = 0; k < ksteps; k++)
-        tc::mma_bf16(d, tc::smem_desc(a_addr + k * astep, a_lbo, a_sbo),
-                     tc::smem_desc(b_addr + k * bstep, b_lbo, b_sbo), idesc, acc || k > 0);
-}
-
 template <int kN, bool kOutF32>
-__global__ void __launch_bounds__(kThreads, 1) ssd_chunk_scan_kernel(SsdArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    ssd_chunk_scan_kernel(const SsdArgs a, const __grid_constant__ SsdMaps m) {
+    using S = Smem<kN>;
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ float s_cs2[kQ];      // cs_t * log2(e)
     __shared__ float s_dt[kQ];
     __shared__ float s_e[kQ];        // exp(cs_t)
     __shared__ float s_w[kQ];        // exp(cs_end - cs_t) dt_t
     __shared__ float s_wsum[4];
-    __shared__ uint64_t s_bar;
+    __shared__ uint64_t s_bar;       // tensor-core completion
+    __shared__ uint64_t s_load[2];   // input stage k loaded
+    __shared__ uint64_t s_zload;     // z tile loaded
     __shared__ uint32_t s_tmem;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int quad = warp & 3, half = warp >> 2;
+    // the swizzled tiles need a 1024-byte aligned base
+    if (tc::smem_u32(smem) & 1023u) {
+        if (tid == 0) atomicExch(&g_ssd_status, __LINE__);
+        return;
+    }
     const int64_t bh = blockIdx.x;
     const int64_t H = a.nheads, L = a.seqlen, G = a.ngroups;
     const int64_t b = bh / H, h = bh % H, g = h / (H / G);
     const float A2 = a.A[h] * kLog2e;
     const float bias = a.dt_bias ? a.dt_bias[h] : 0.f;
     const float Dh = a.D ? a.D[h] : 0.f;
-    const __nv_bfloat16* xg = static_cast<const __nv_bfloat16*>(a.x);
     const __nv_bfloat16* dtg = static_cast<const __nv_bfloat16*>(a.dt);
-    const __nv_bfloat16* Bg = static_cast<const __nv_bfloat16*>(a.B);
-    const __nv_bfloat16* Cg = static_cast<const __nv_bfloat16*>(a.C);
     const __nv_bfloat16* zg = static_cast<const __nv_bfloat16*>(a.z);
 
-    unsigned char* sMh = smem + kOffMh;
-    unsigned char* sMl = smem + kOffMl;
-    unsigned char* sC = smem + kOffC;
-    unsigned char* sB = smem + kOffB;
-    unsigned char* sX = smem + kOffX;
-    unsigned char* sWh = smem + kOffWh;
-    unsigned char* sWl = smem + kOffWl;
-    unsigned char* sHh = smem + kOffHh;
-    unsigned char* sHl = smem + kOffHl;
+    unsigned char* sMh = smem + S::kMh;
+    unsigned char* sMl = smem + S::kMl;
+    unsigned char* sWh = smem + S::kWh;
+    unsigned char* sWl = smem + S::kWl;
+    unsigned char* sHh = smem + S::kHh;
+    unsigned char* sHl = smem + S::kHl;
     const uint32_t base = tc::smem_u32(smem);
+    const int64_t nchunks = (L + kQ - 1) / kQ;
 
-    // B^T serves G4 as a 128-row operand; with N = 64 its rows 64..127 stay zero
-    if (kN < 128)
-        for (int i = tid; i < (int)(kTileBig / 16); i += kThreads)
-            reinterpret_cast<uint4*>(sB)[i] = make_uint4(0, 0, 0, 0);
+    // C, B (128 x N) and x (128 x 64) of chunk c into stage st by TMA (thread 0),
+    // zero-filled past the end of the sequence
+    // chunks whose loads were issued / consumed so far (chunk k uses stage
+    // k % kStages and that stage's (k / kStages)-th phase)
+    int64_t n_issued = 0, n_waited = 0;
+    // (the lanes of warp 0 issue one box each)
+    auto issue_loads = [&](int64_t c, int st) {
+        n_issued = c + 1;
+        if (warp != 0) return;
+        unsigned char* stg = smem + S::kStage0 + st * S::kStageBytes;
+        uint64_t* bar = &s_load[st];
+        if (lane == 0) tc::mbar_expect_tx(bar, S::kStageBytes);
+        __syncwarp();
+        const int y = (int)(c * kQ), z = (int)b;
+        constexpr int kJ = kN / 64;   // 64-column atoms of C and B
+        if (lane < kJ)
+            tc::tma_load_3d(stg + S::kC + lane * 16384, &m.c, (int)(g * kN) + 64 * lane, y, z, bar);
+        else if (lane < 2 * kJ)
+            tc::tma_load_3d(stg + S::kB + (lane - kJ) * 16384, &m.b, (int)(g * kN) + 64 * (lane - kJ), y, z, bar);
+        else if (lane == 2 * kJ)
+            tc::tma_load_3d(stg + S::kX, &m.x, (int)(h * kP), y, z, bar);
+    };
+    // z of chunk c (single stage: issued once the previous chunk's epilogue is done)
+    int64_t n_zissued = 0, n_zwaited = 0;
+    auto issue_z = [&](int64_t c) {
+        n_zissued = c + 1;
+        if (warp != 0) return;
+        if (lane == 0) tc::mbar_expect_tx(&s_zload, S::kTileX);
+        __syncwarp();
+        if (lane == 0) tc::tma_load_3d(smem + S::kZ, &m.z, (int)(h * kP), (int)(c * kQ), (int)b, &s_zload);
+    };
+    // raw dt of step tid of chunk c (0 past the end)
+    auto load_dt = [&](int64_t c) -> float {
+        const int64_t t = c * kQ + tid;
+        return (tid < kQ && c < nchunks && t < L) ? __bfloat162float(dtg[(b * L + t) * H + h]) : 0.f;
+    };
+
+    float dt_next = load_dt(0);
     if (tid == 0) {
         tc::mbar_init(&s_bar, 1);
+        tc::mbar_init(&s_load[0], 1);
+        tc::mbar_init(&s_load[1], 1);
+        tc::mbar_init(&s_zload, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    if (nchunks > 0) {
+        issue_loads(0, 0);
+        if (zg) issue_z(0);
     }
     if (warp == 0) tc::tmem_alloc(&s_tmem, kTmemCols);
     tc::fence_before_sync();
@@ -173,9 +241,12 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_scan_kernel(SsdArgs a) 
             v[j] = (a.h0 && row < kN) ? a.h0[(bh * kP + p) * kN + row] : 0.f;
         }
         tc::tmem_st32(tmem + lane_base + kColH + 32 * half, v);
+        if (row < kN) {
 #pragma unroll
-        for (int k = 0; k < 4; k++)
-            split_store8(v + 8 * k, sHh + chunk_off(row, 4 * half + k), sHl + chunk_off(row, 4 * half + k));
+            for (int k = 0; k < 4; k++)
+                split_store8(v + 8 * k, sHh + (4 * half + k) * S::kStrideH + row * 16,
+                             sHl + (4 * half + k) * S::kStrideH + row * 16);
+        }
         tc::tmem_wait_st();
     }
     tc::fence_proxy_async();
@@ -187,43 +258,40 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_scan_kernel(SsdArgs a) 
     constexpr uint32_t idG4 = tc::idesc_bf16(128, kP, 1, 1);
     uint32_t phase = 0;
     bool failed = false;
-    const int64_t nchunks = (L + kQ - 1) / kQ;
 
     for (int64_t c = 0; c < nchunks; c++) {
         const int64_t t0 = c * kQ;
         const int q = (int)((L - t0) < kQ ? (L - t0) : kQ);
-        // ---- stage C, B (q x N) and x (q x 64) with zero-filled tails ----------
-        {
-            constexpr int kCJ = kN / 8;
-            for (int i = tid; i < kQ * kCJ; i += kThreads) {
-                const int r = i / kCJ, j = i % kCJ;
-                const int rr = r < q ? r : 0;
-                const int64_t gi = ((b * L + t0 + rr) * G + g) * kN + 8 * j;
-                tc::cp_async16(sC + chunk_off(r, j), Cg + gi, r < q ? 16u : 0u);
-                tc::cp_async16(sB + chunk_off(r, j), Bg + gi, r < q ? 16u : 0u);
-            }
-            for (int i = tid; i < kQ * (kP / 8); i += kThreads) {
-                const int r = i & (kQ - 1), j = i >> 7;
-                const int rr = r < q ? r : 0;
-                tc::cp_async16(sX + chunk_off(r, j), xg + ((b * L + t0 + rr) * H + h) * kP + 8 * j,
-                               r < q ? 16u : 0u);
-            }
-            tc::cp_async_commit();
+        const int st = S::kStages == 2 ? (int)(c & 1) : 0;
+        unsigned char* stg = smem + S::kStage0 + st * S::kStageBytes;
+        const uint32_t sC = base + S::kStage0 + st * S::kStageBytes + S::kC;
+        const uint32_t sB = sC + S::kB - S::kC;
+        const uint32_t sX = sC + S::kX - S::kC;
+        // the next chunk's inputs load behind this one (its stage was last read by
+        // chunk c - 1, whose products have completed); one stage: this chunk's now
+        if (S::kStages == 2) {
+            if (c + 1 < nchunks) issue_loads(c + 1, st ^ 1);
+        } else if (c > 0) {
+            issue_loads(c, 0);
         }
         // ---- dt and the in-chunk cumulative sum of dt A (log2 domain) ----------
         float cs = 0.f, dtv = 0.f;
-        if (tid < kQ) {
-            if (tid < q) {
-                const float v = __bfloat162float(dtg[(b * L + t0 + tid) * H + h]) + bias;
-                dtv = a.softplus ? softplus_acc<true>(v) : v;
-            }
-            cs = dtv * A2;
+        {
+            const float raw = dt_next;
+            dt_next = load_dt(c + 1);
+            if (tid < kQ) {
+                if (tid < q) {
+                    const float v = raw + bias;
+                    dtv = a.softplus ? softplus_acc<true>(v) : v;
+                }
+                cs = dtv * A2;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float u = __shfl_up_sync(0xffffffffu, cs, o);
-                if (lane >= o) cs += u;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float u = __shfl_up_sync(0xffffffffu, cs, o);
+                    if (lane >= o) cs += u;
+                }
+                if (lane == 31) s_wsum[warp] = cs;
             }
-            if (lane == 31) s_wsum[warp] = cs;
         }
         __syncthreads();
         if (tid < kQ) {
@@ -231,14 +299,23 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_scan_kernel(SsdArgs a) 
             s_cs2[tid] = cs;
             s_dt[tid] = dtv;
         }
-        tc::cp_async_wait_all();
-        tc::fence_proxy_async();
-        __syncthreads();
+        {
+            const bool ok = tc::mbar_wait(&s_load[st], (uint32_t)(c / S::kStages) & 1u, kWaitLimit);
+            if (__syncthreads_or(!ok)) {
+                if (tid == 0) atomicExch(&g_ssd_status, __LINE__);
+                failed = true;
+                break;
+            }
+            n_waited = c + 1;
+        }
         // ---- G1: S = C B^T ------------------------------------------------------
         if (tid == 0) {
             tc::fence_after_sync();
-            mma_chain(tmem + kColS, base + kOffC, kStrideC, 128, 2 * kStrideC, base + kOffB, kStrideC, 128,
-                      2 * kStrideC, idG1, kN / 16, false);
+            for (int k = 0; k < kN / 16; k++) {
+                const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+                tc::mma_bf16(tmem + kColS, tc::smem_desc_sw128(sC + off, 16, 1024),
+                             tc::smem_desc_sw128(sB + off, 16, 1024), idG1, k > 0);
+            }
             tc::commit(&s_bar);
         }
         const float cs2_end = s_cs2[kQ - 1];
@@ -246,11 +323,12 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_scan_kernel(SsdArgs a) 
             s_e[tid] = ex2(cs);
             s_w[tid] = ex2(cs2_end - cs) * dtv;
         }
+        if (warp == 0) tc::bulk_wait_read();   // the previous y store has left the M area
         __syncthreads();
         // ---- w o x, split; rescale the resident state by exp(cs_end) -------------
         for (int i = tid; i < kQ * (kP / 8); i += kThreads) {
             float v[8];
-            unpack8(*reinterpret_cast<const uint4*>(sX + 16 * i), v);
+            unpack8(*reinterpret_cast<const uint4*>(stg + S::kX + tc::sw128(i & (kQ - 1), i >> 7)), v);
             const float w = s_w[i & (kQ - 1)];
 #pragma unroll
             for (int k = 0; k < 8; k++) v[k] *= w;
@@ -300,21 +378,23 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_scan_kernel(SsdArgs a) 
         // ---- G2, G3, G4 -------------------------------------------------------------
         if (tid == 0) {
             tc::fence_after_sync();
-            // G2: Yi = Mh x + Ml x
-            mma_chain(tmem + kColYi, base + kOffMh, kStrideC, 128, 2 * kStrideC, base + kOffX, 128, kStrideC,
-                      256, idG2, kQ / 16, false);
-            mma_chain(tmem + kColYi, base + kOffMl, kStrideC, 128, 2 * kStrideC, base + kOffX, 128, kStrideC,
-                      256, idG2, kQ / 16, true);
-            // G3: Ye = C Hh^T + C Hl^T
-            mma_chain(tmem + kColYe, base + kOffC, kStrideC, 128, 2 * kStrideC, base + kOffHh, 128, kStrideC,
-                      256, idG2, kN / 16, false);
-            mma_chain(tmem + kColYe, base + kOffC, kStrideC, 128, 2 * kStrideC, base + kOffHl, 128, kStrideC,
-                      256, idG2, kN / 16, true);
-            // G4: H^T += B^T (w o x)_hi + B^T (w o x)_lo
-            mma_chain(tmem + kColH, base + kOffB, 128, kStrideC, 256, base + kOffWh, 128, kStrideC, 256, idG4,
-                      kQ / 16, true);
-            mma_chain(tmem + kColH, base + kOffB, 128, kStrideC, 256, base + kOffWl, 128, kStrideC, 256, idG4,
-                      kQ / 16, true);
+            // G2: Yi = Mh x + Ml x (x: MN-major, swizzled, one atom)
+            for (int hl = 0; hl < 2; hl++)
+                for (int k = 0; k < kQ / 16; k++)
+                    tc::mma_bf16(tmem + kColYi,
+                                 tc::smem_desc(base + (hl ? S::kMl : S::kMh) + k * 2 * kStrideC, kStrideC, 128),
+                                 tc::smem_desc_sw128(sX + k * 2048, 16384, 1024), idG2, hl > 0 || k > 0);
+            // G3: Ye = C Hh^T + C Hl^T (C: K-major, swizzled)
+            for (int hl = 0; hl < 2; hl++)
+                for (int k = 0; k < kN / 16; k++)
+                    tc::mma_bf16(tmem + kColYe, tc::smem_desc_sw128(sC + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
+                                 tc::smem_desc(base + (hl ? S::kHl : S::kHh) + k * 256, 128, S::kStrideH), idG2,
+                                 hl > 0 || k > 0);
+            // G4: H^T += B^T (w o x)_hi + B^T (w o x)_lo (B^T: MN-major, swizzled, 64-row atoms 16 KB apart)
+            for (int hl = 0; hl < 2; hl++)
+                for (int k = 0; k < kQ / 16; k++)
+                    tc::mma_bf16(tmem + kColH, tc::smem_desc_sw128(sB + k * 2048, 16384, 1024),
+                                 tc::smem_desc(base + (hl ? S::kWl : S::kWh) + k * 256, 128, kStrideC), idG4, true);
             tc::commit(&s_bar);
         }
         {
@@ -327,41 +407,49 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_scan_kernel(SsdArgs a) 
             phase ^= 1;
         }
         tc::fence_after_sync();
-        // ---- epilogue: y = Yi + exp(cs_t) Ye + D x, gated ---------------------------
+        // ---- epilogue: y = Yi + exp(cs_t) Ye + D x, gated, staged for a TMA store ----
+        if (zg) {
+            const bool ok = tc::mbar_wait(&s_zload, (uint32_t)(c & 1), kWaitLimit);
+            if (__syncthreads_or(!ok)) {
+                if (tid == 0) atomicExch(&g_ssd_status, __LINE__);
+                failed = true;
+                break;
+            }
+            n_zwaited = c + 1;
+        }
         {
             float yi[32], ye[32];
             tc::tmem_ld32(tmem + lane_base + kColYi + 32 * half, yi);
             tc::tmem_ld32(tmem + lane_base + kColYe + 32 * half, ye);
             tc::tmem_wait_ld();
-            if (row < q) {
-                const float e = s_e[row];
-                const int64_t gi = ((b * L + t0 + row) * H + h) * kP + 32 * half;
-                float out[32];
+            const float e = s_e[row];
+            float out[32];
 #pragma unroll
-                for (int k = 0; k < 4; k++) {
-                    float xv[8];
-                    unpack8(*reinterpret_cast<const uint4*>(sX + chunk_off(row, 4 * half + k)), xv);
-                    float zv[8];
-                    if (zg) unpack8(__ldg(reinterpret_cast<const uint4*>(zg + gi + 8 * k)), zv);
+            for (int k = 0; k < 4; k++) {
+                float xv[8];
+                unpack8(*reinterpret_cast<const uint4*>(stg + S::kX + tc::sw128(row, 4 * half + k)), xv);
+                float zv[8];
+                if (zg) unpack8(*reinterpret_cast<const uint4*>(smem + S::kZ + tc::sw128(row, 4 * half + k)), zv);
 #pragma unroll
-                    for (int i = 0; i < 8; i++) {
-                        float yv = fmaf(e, ye[8 * k + i], yi[8 * k + i]);
-                        yv = fmaf(Dh, xv[i], yv);
-                        if (zg) yv *= silu_acc<false>(zv[i]);
-                        out[8 * k + i] = yv;
-                    }
+                for (int i = 0; i < 8; i++) {
+                    float yv = fmaf(e, ye[8 * k + i], yi[8 * k + i]);
+                    yv = fmaf(Dh, xv[i], yv);
+                    if (zg) yv *= silu_acc<false>(zv[i]);
+                    out[8 * k + i] = yv;
                 }
-                if constexpr (kOutF32) {
-                    float* yo = static_cast<float*>(a.y) + gi;
+            }
+            // rows past seqlen are staged too; the store drops them
+            unsigned char* sy = smem + S::kY;
+            if constexpr (kOutF32) {   // two atoms: columns 0-31 and 32-63
 #pragma unroll
-                    for (int k = 0; k < 8; k++)
-                        reinterpret_cast<float4*>(yo)[k] =
-                            make_float4(out[4 * k], out[4 * k + 1], out[4 * k + 2], out[4 * k + 3]);
-                } else {
-                    __nv_bfloat16* yo = static_cast<__nv_bfloat16*>(a.y) + gi;
+                for (int k = 0; k < 8; k++)
+                    *reinterpret_cast<float4*>(sy + half * 16384 + tc::sw128(row, k)) =
+                        make_float4(out[4 * k], out[4 * k + 1], out[4 * k + 2], out[4 * k + 3]);
+            } else {
 #pragma unroll
-                    for (int k = 0; k < 4; k++) Vec16<__nv_bfloat16>::store(yo + 8 * k, out + 8 * k);
-                }
+                for (int k = 0; k < 4; k++)
+                    Vec16<__nv_bfloat16>::store(reinterpret_cast<__nv_bfloat16*>(sy + tc::sw128(row, 4 * half + k)),
+                                                out + 8 * k);
             }
         }
         // ---- the new state as G3's split operand for the next chunk -----------------
@@ -369,13 +457,25 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_scan_kernel(SsdArgs a) 
             float v[32];
             tc::tmem_ld32(tmem + lane_base + kColH + 32 * half, v);
             tc::tmem_wait_ld();
+            if (row < kN) {
 #pragma unroll
-            for (int k = 0; k < 4; k++)
-                split_store8(v + 8 * k, sHh + chunk_off(row, 4 * half + k), sHl + chunk_off(row, 4 * half + k));
+                for (int k = 0; k < 4; k++)
+                    split_store8(v + 8 * k, sHh + (4 * half + k) * S::kStrideH + row * 16,
+                                 sHl + (4 * half + k) * S::kStrideH + row * 16);
+            }
         }
         tc::fence_proxy_async();
         tc::fence_before_sync();
         __syncthreads();
+        // y out of the staging area (16-byte column groups of 128 steps); then the
+        // next chunk's z into its (now read) tile
+        if (warp == 0) {
+            constexpr int kAtoms = kOutF32 ? 2 : 1;
+            if (lane < kAtoms)
+                tc::tma_store_3d(&m.y, (int)(h * kP) + 32 * lane, (int)t0, (int)b, smem + S::kY + lane * 16384);
+            tc::bulk_commit();
+        }
+        if (zg && c + 1 < nchunks) issue_z(c + 1);
     }
 
     if (!failed && a.h_last && row < kN) {
@@ -387,10 +487,15 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_scan_kernel(SsdArgs a) 
         for (int j = 0; j < 32; j++) a.h_last[(bh * kP + 32 * half + j) * kN + row] = v[j];
     }
     if (failed) {
-        // let whatever the tensor core still owes (the phase that timed out)
-        // complete before its memory goes
+        // let whatever the tensor core and the copy engine still owe (the phases
+        // that timed out, loads issued but not consumed) complete before the
+        // memory they write goes away
         (void)tc::mbar_wait(&s_bar, phase, kWaitLimit);
+        for (int64_t k = n_waited; k < n_issued; k++)
+            (void)tc::mbar_wait(&s_load[k % S::kStages], (uint32_t)(k / S::kStages) & 1u, kWaitLimit);
+        for (int64_t k = n_zwaited; k < n_zissued; k++) (void)tc::mbar_wait(&s_zload, (uint32_t)(k & 1), kWaitLimit);
     }
+    if (warp == 0) tc::bulk_wait_read();
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) {
@@ -399,12 +504,52 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_chunk_scan_kernel(SsdArgs a) 
     }
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// (row elements, seqlen, batch) view of bf16 (esize 2) or fp32 (esize 4) rows,
+// 128-byte x 128-step boxes, 128-byte swizzled in shared memory
+bool encode_rows(CUtensorMap* map, const void* base, int64_t row, int64_t L, int64_t batch, int esize = 2) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)row, (cuuint64_t)L, (cuuint64_t)batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)(row * esize), (cuuint64_t)(row * L * esize)};
+    const cuuint32_t box[3] = {(cuuint32_t)(128 / esize), (cuuint32_t)kQ, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+              const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int kN, bool kOutF32>
 cudaError_t launch_n(const SsdArgs& a, cudaStream_t s) {
+    SsdMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    if (a.seqlen > 0) {
+        const int64_t bc_row = a.ngroups * kN, x_row = a.nheads * kP;
+        if (!encode_rows(&maps.c, a.C, bc_row, a.seqlen, a.batch) ||
+            !encode_rows(&maps.b, a.B, bc_row, a.seqlen, a.batch) ||
+            !encode_rows(&maps.x, a.x, x_row, a.seqlen, a.batch) ||
+            (a.z && !encode_rows(&maps.z, a.z, x_row, a.seqlen, a.batch)) ||
+            !encode_rows(&maps.y, a.y, x_row, a.seqlen, a.batch, kOutF32 ? 4 : 2))
+            return cudaErrorInvalidValue;
+    }
     auto k = ssd_chunk_scan_kernel<kN, kOutF32>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    constexpr uint32_t bytes = Smem<kN>::kBytes;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e != cudaSuccess) return e;
-    k<<<(unsigned)(a.batch * a.nheads), kThreads, kSmemBytes, s>>>(a);
+    k<<<(unsigned)(a.batch * a.nheads), kThreads, bytes, s>>>(a, maps);
     return cudaGetLastError();
 }
 

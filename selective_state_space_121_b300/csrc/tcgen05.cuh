@@ -80,6 +80,19 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
     return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
 }
+// The same with 128-byte swizzling (layout type 2): rows of 128 bytes in atoms of
+// 8 rows (1024 bytes, 1024-byte aligned) whose 16-byte chunks are permuted by
+// XOR with the row index mod 8 -- the layout a TMA copy with 128-byte swizzle
+// writes. K-major: SBO = 1024 between 8-row groups, LBO unused, a K step of 16
+// moves the start 32 bytes within the row. MN-major: LBO = the distance between
+// 64-element atoms along M/N, SBO = 1024 between 8-row groups along K.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return smem_desc(saddr, lbo, sbo) | (2ull << 61);
+}
+// Byte offset of 16-byte chunk j of row r in a 128-byte-swizzled tile (8 chunks a row).
+__host__ __device__ constexpr uint32_t sw128(int r, int j) {
+    return (uint32_t)r * 128u + ((uint32_t)(j ^ (r & 7)) << 4);
+}
 // Instruction descriptor for kind::f16 with bf16 A and B and an fp32 accumulator:
 // D format (bits 4-5) = f32, A format (7-9) = bf16, B format (10-12) = bf16,
 // A and B major-ness (bits 15, 16: 0 = K-major, 1 = MN-major), N >> 3 (17-22),
@@ -144,6 +157,33 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t 
                  "r"(src_bytes)
                  : "memory");
 }
+// ---- TMA (tensor-map bulk copies) ------------------------------------------------
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+// 3-D tiled load of the box at coordinates (x, y, z) of `tmap` (a __grid_constant__
+// kernel parameter) into shared memory; completion counted on `bar`. x times the
+// element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 3-D tiled store of a shared-memory box to (x, y, z) of `tmap`; elements outside
+// the tensor are not written. Tracked by the issuing thread's bulk groups.
+__device__ __forceinline__ void tma_store_3d(const void* tmap, int x, int y, int z, const void* src) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(tmap),
+                 "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until this thread's bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
