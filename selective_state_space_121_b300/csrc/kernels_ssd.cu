@@ -58,11 +58,13 @@ namespace {
 
 constexpr int kQ = 128;               // chunk length (steps)
 constexpr int kP = 64;                // head channels
-constexpr int kThreads = 256;
+constexpr int kCompute = 256;       // eight compute warps
+constexpr int kCtl = 8;             // the control warp: TMA copies and MMA issue
+constexpr int kThreads = kCompute + 32;
 constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr uint32_t kStrideC = 2048;   // bytes between column groups of a 128-row tile
 // tensor-memory columns
-constexpr uint32_t kColS = 0, kColYe = 0, kColYi = 128, kColH = 192, kTmemCols = 256;
+constexpr uint32_t kColS = 0, kColYi = 128, kColYe = 192, kColH = 256, kTmemCols = 512;
 
 // Shared-memory map (bytes) for state width N. The K-major tiles come first so
 // that every descriptor reach stays inside the allocation. With N = 64 the
@@ -134,6 +136,35 @@ __device__ __forceinline__ void unpack8(uint4 v, float* out) {
     }
 }
 
+// Barrier among the eight compute warps only (named barrier 1).
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// The same barrier, returning on every compute thread whether v held on any.
+__device__ __forceinline__ bool compute_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+// Bounded wait that also gives up once another warp has raised the abort flag.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    for (uint32_t i = 0; i < kWaitLimit; i++) {
+        if (tc::mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 63u && *abort_flag) return false;
+    }
+    return false;
+}
+
+// Roles. Warps 0-7 compute (warp w owns tensor-memory lanes 32 (w % 4) .. +31 and
+// column half w / 4); warp 8 (the control warp) issues every TMA copy and every
+// MMA. The two sides meet only through mbarriers, every wait bounded:
+//   TMA -> all        s_load (inputs of a stage), s_zload (z)
+//   MMA -> compute    s_bar[0] G1 done, s_bar[1] G3 + G4 done, s_bar[2] G2 done
+//   compute -> ctl    s_ready[0] w o x and the rescaled state written,
+//                     s_ready[1] M written, s_ready[2] chunk finished (y staged)
+//   ctl -> compute    s_yfree: the previous y store has left the M area
 template <int kN, bool kOutF32>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_chunk_scan_kernel(const SsdArgs a, const __grid_constant__ SsdMaps m) {
@@ -144,10 +175,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ float s_e[kQ];        // exp(cs_t)
     __shared__ float s_w[kQ];        // exp(cs_end - cs_t) dt_t
     __shared__ float s_wsum[4];
-    __shared__ uint64_t s_bar;       // tensor-core completion
-    __shared__ uint64_t s_load[2];   // input stage k loaded
-    __shared__ uint64_t s_zload;     // z tile loaded
+    __shared__ uint64_t s_bar[3];
+    __shared__ uint64_t s_load[2];
+    __shared__ uint64_t s_zload;
+    __shared__ uint64_t s_ready[3];
+    __shared__ uint64_t s_yfree;
+    __shared__ uint64_t s_drain;     // products drained (failure path only)
     __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int quad = warp & 3, half = warp >> 2;
@@ -162,8 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float A2 = a.A[h] * kLog2e;
     const float bias = a.dt_bias ? a.dt_bias[h] : 0.f;
     const float Dh = a.D ? a.D[h] : 0.f;
-    const __nv_bfloat16* dtg = static_cast<const __nv_bfloat16*>(a.dt);
     const __nv_bfloat16* zg = static_cast<const __nv_bfloat16*>(a.z);
+    const unsigned short* dtb = static_cast<const unsigned short*>(a.dt);
 
     unsigned char* sMh = smem + S::kMh;
     unsigned char* sMl = smem + S::kMl;
@@ -173,56 +208,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char* sHl = smem + S::kHl;
     const uint32_t base = tc::smem_u32(smem);
     const int64_t nchunks = (L + kQ - 1) / kQ;
+    volatile int* abort_flag = &s_abort;
+    auto fail = [&](int line) {
+        atomicExch(&g_ssd_status, line);
+        *abort_flag = 1;
+    };
 
-    // C, B (128 x N) and x (128 x 64) of chunk c into stage st by TMA (thread 0),
-    // zero-filled past the end of the sequence
-    // chunks whose loads were issued / consumed so far (chunk k uses stage
-    // k % kStages and that stage's (k / kStages)-th phase)
-    int64_t n_issued = 0, n_waited = 0;
-    // (the lanes of warp 0 issue one box each)
-    auto issue_loads = [&](int64_t c, int st) {
-        n_issued = c + 1;
-        if (warp != 0) return;
+    // ---- control-warp copies (whole warp, converged) ---------------------------------
+    // Two stages (N = 64): C, B and x of chunk c on s_load[c & 1]. One stage
+    // (N = 128): C and B on s_load[0], x on s_load[1]. Issue / consumption counts
+    // per barrier let the failure path wait for exactly the phases in flight.
+    uint32_t ld_issued0 = 0, ld_issued1 = 0, ld_seen0 = 0, ld_seen1 = 0, z_issued = 0, z_seen = 0;
+    auto tma_cb = [&](int64_t c, int st, uint64_t* bar) {
         unsigned char* stg = smem + S::kStage0 + st * S::kStageBytes;
-        uint64_t* bar = &s_load[st];
-        if (lane == 0) tc::mbar_expect_tx(bar, S::kStageBytes);
-        __syncwarp();
-        const int y = (int)(c * kQ), z = (int)b;
         constexpr int kJ = kN / 64;   // 64-column atoms of C and B
         if (lane < kJ)
-            tc::tma_load_3d(stg + S::kC + lane * 16384, &m.c, (int)(g * kN) + 64 * lane, y, z, bar);
+            tc::tma_load_3d(stg + S::kC + lane * 16384, &m.c, (int)(g * kN) + 64 * lane, (int)(c * kQ), (int)b, bar);
         else if (lane < 2 * kJ)
-            tc::tma_load_3d(stg + S::kB + (lane - kJ) * 16384, &m.b, (int)(g * kN) + 64 * (lane - kJ), y, z, bar);
-        else if (lane == 2 * kJ)
-            tc::tma_load_3d(stg + S::kX, &m.x, (int)(h * kP), y, z, bar);
+            tc::tma_load_3d(stg + S::kB + (lane - kJ) * 16384, &m.b, (int)(g * kN) + 64 * (lane - kJ), (int)(c * kQ),
+                            (int)b, bar);
     };
-    // z of chunk c (single stage: issued once the previous chunk's epilogue is done)
-    int64_t n_zissued = 0, n_zwaited = 0;
-    auto issue_z = [&](int64_t c) {
-        n_zissued = c + 1;
-        if (warp != 0) return;
-        if (lane == 0) tc::mbar_expect_tx(&s_zload, S::kTileX);
+    auto tma_x = [&](int64_t c, int st, uint64_t* bar) {
+        if (lane == 31)
+            tc::tma_load_3d(smem + S::kStage0 + st * S::kStageBytes + S::kX, &m.x, (int)(h * kP), (int)(c * kQ),
+                            (int)b, bar);
+    };
+    auto issue_stage = [&](int64_t c) {   // two stages
+        const int st = (int)(c & 1);
+        if (lane == 0) tc::mbar_expect_tx(&s_load[st], S::kStageBytes);
         __syncwarp();
-        if (lane == 0) tc::tma_load_3d(smem + S::kZ, &m.z, (int)(h * kP), (int)(c * kQ), (int)b, &s_zload);
+        tma_cb(c, st, &s_load[st]);
+        tma_x(c, st, &s_load[st]);
+        if (st == 0) ld_issued0++; else ld_issued1++;
     };
-    // raw dt of step tid of chunk c (0 past the end)
-    auto load_dt = [&](int64_t c) -> float {
-        const int64_t t = c * kQ + tid;
-        return (tid < kQ && c < nchunks && t < L) ? __bfloat162float(dtg[(b * L + t) * H + h]) : 0.f;
+    auto issue_cb1 = [&](int64_t c) {     // one stage
+        if (lane == 0) tc::mbar_expect_tx(&s_load[0], 2 * S::kTileCB);
+        __syncwarp();
+        tma_cb(c, 0, &s_load[0]);
+        ld_issued0++;
+    };
+    auto issue_x1 = [&](int64_t c) {
+        if (lane == 0) tc::mbar_expect_tx(&s_load[1], S::kTileX);
+        __syncwarp();
+        tma_x(c, 0, &s_load[1]);
+        ld_issued1++;
+    };
+    auto issue_z = [&](int64_t c) {
+        if (lane == 0) {
+            tc::mbar_expect_tx(&s_zload, S::kTileX);
+            tc::tma_load_3d(smem + S::kZ, &m.z, (int)(h * kP), (int)(c * kQ), (int)b, &s_zload);
+        }
+        z_issued++;
     };
 
-    float dt_next = load_dt(0);
-    if (tid == 0) {
-        tc::mbar_init(&s_bar, 1);
-        tc::mbar_init(&s_load[0], 1);
-        tc::mbar_init(&s_load[1], 1);
-        tc::mbar_init(&s_zload, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncwarp();
-    if (nchunks > 0) {
-        issue_loads(0, 0);
-        if (zg) issue_z(0);
+    if (warp == kCtl) {
+        if (lane == 0) {
+            for (int k = 0; k < 3; k++) tc::mbar_init(&s_bar[k], 1);
+            tc::mbar_init(&s_load[0], 1);
+            tc::mbar_init(&s_load[1], 1);
+            tc::mbar_init(&s_zload, 1);
+            for (int k = 0; k < 3; k++) tc::mbar_init(&s_ready[k], kCtl);   // one arrival per compute warp
+            tc::mbar_init(&s_yfree, 1);
+            tc::mbar_init(&s_drain, 1);
+            *abort_flag = 0;
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncwarp();
+        if (nchunks > 0) {
+            if (S::kStages == 2) {
+                issue_stage(0);
+                if (nchunks > 1) issue_stage(1);
+            } else {
+                issue_cb1(0);
+                issue_x1(0);
+            }
+            if (zg) issue_z(0);
+        }
     }
     if (warp == 0) tc::tmem_alloc(&s_tmem, kTmemCols);
     tc::fence_before_sync();
@@ -231,271 +292,339 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = s_tmem;
     const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
     const int row = 32 * quad + lane;   // this thread's tensor-memory lane: t (G1-G3) or n (G4)
-
-    // initial state: H^T[n][p] = h0[b,h,p,n] (zero for n >= N or without h0)
-    {
-        float v[32];
-#pragma unroll
-        for (int j = 0; j < 32; j++) {
-            const int p = 32 * half + j;
-            v[j] = (a.h0 && row < kN) ? a.h0[(bh * kP + p) * kN + row] : 0.f;
-        }
-        tc::tmem_st32(tmem + lane_base + kColH + 32 * half, v);
-        if (row < kN) {
-#pragma unroll
-            for (int k = 0; k < 4; k++)
-                split_store8(v + 8 * k, sHh + (4 * half + k) * S::kStrideH + row * 16,
-                             sHl + (4 * half + k) * S::kStrideH + row * 16);
-        }
-        tc::tmem_wait_st();
-    }
-    tc::fence_proxy_async();
-    tc::fence_before_sync();
-    __syncthreads();
-
-    constexpr uint32_t idG1 = tc::idesc_bf16(128, 128, 0, 0);
-    constexpr uint32_t idG2 = tc::idesc_bf16(128, kP, 0, 1);
-    constexpr uint32_t idG4 = tc::idesc_bf16(128, kP, 1, 1);
-    uint32_t phase = 0;
     bool failed = false;
+    // the control warp decides every wait as one (a lane that gave up while another
+    // saw the phase complete would leave the warp split at its next __syncwarp)
+    auto ctl_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag));
+    };
 
-    for (int64_t c = 0; c < nchunks; c++) {
-        const int64_t t0 = c * kQ;
-        const int q = (int)((L - t0) < kQ ? (L - t0) : kQ);
-        const int st = S::kStages == 2 ? (int)(c & 1) : 0;
-        unsigned char* stg = smem + S::kStage0 + st * S::kStageBytes;
-        const uint32_t sC = base + S::kStage0 + st * S::kStageBytes + S::kC;
-        const uint32_t sB = sC + S::kB - S::kC;
-        const uint32_t sX = sC + S::kX - S::kC;
-        // the next chunk's inputs load behind this one (its stage was last read by
-        // chunk c - 1, whose products have completed); one stage: this chunk's now
-        if (S::kStages == 2) {
-            if (c + 1 < nchunks) issue_loads(c + 1, st ^ 1);
-        } else if (c > 0) {
-            issue_loads(c, 0);
-        }
-        // ---- dt and the in-chunk cumulative sum of dt A (log2 domain) ----------
-        float cs = 0.f, dtv = 0.f;
-        {
-            const float raw = dt_next;
-            dt_next = load_dt(c + 1);
-            if (tid < kQ) {
-                if (tid < q) {
-                    const float v = raw + bias;
-                    dtv = a.softplus ? softplus_acc<true>(v) : v;
+    if (warp == kCtl) {
+        // =============================== control warp ===============================
+        constexpr uint32_t idG1 = tc::idesc_bf16(128, 128, 0, 0);
+        constexpr uint32_t idG2 = tc::idesc_bf16(128, kP, 0, 1);
+        constexpr uint32_t idG4 = tc::idesc_bf16(128, kP, 1, 1);
+        for (int64_t c = 0; c < nchunks; c++) {
+            const int st = S::kStages == 2 ? (int)(c & 1) : 0;
+            const uint32_t par = (uint32_t)(c & 1);
+            const uint32_t sC = base + S::kStage0 + st * S::kStageBytes + S::kC;
+            const uint32_t sB = sC + S::kB - S::kC;
+            const uint32_t sX = sC + S::kX - S::kC;
+            // G1: S = C B^T once C and B are in
+            {
+                uint64_t* bar = S::kStages == 2 ? &s_load[st] : &s_load[0];
+                const uint32_t p = S::kStages == 2 ? (uint32_t)((c >> 1) & 1) : par;
+                if (!ctl_wait(bar, p)) {
+                    if (lane == 0) fail(__LINE__);
+                    failed = true;
+                    break;
                 }
-                cs = dtv * A2;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float u = __shfl_up_sync(0xffffffffu, cs, o);
-                    if (lane >= o) cs += u;
-                }
-                if (lane == 31) s_wsum[warp] = cs;
+                if (S::kStages == 2 && st == 1) ld_seen1++; else ld_seen0++;
             }
-        }
-        __syncthreads();
-        if (tid < kQ) {
-            for (int w = 0; w < warp; w++) cs += s_wsum[w];
-            s_cs2[tid] = cs;
-            s_dt[tid] = dtv;
-        }
-        {
-            const bool ok = tc::mbar_wait(&s_load[st], (uint32_t)(c / S::kStages) & 1u, kWaitLimit);
-            if (__syncthreads_or(!ok)) {
-                if (tid == 0) atomicExch(&g_ssd_status, __LINE__);
+            if (lane == 0) {
+                tc::fence_after_sync();
+                for (int k = 0; k < kN / 16; k++) {
+                    const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+                    tc::mma_bf16(tmem + kColS, tc::smem_desc_sw128(sC + off, 16, 1024),
+                                 tc::smem_desc_sw128(sB + off, 16, 1024), idG1, k > 0);
+                }
+                tc::commit(&s_bar[0]);
+            }
+            __syncwarp();
+            // G3, G4 once w o x and the rescaled state are written
+            if (!ctl_wait(&s_ready[0], par)) {
+                if (lane == 0) fail(__LINE__);
                 failed = true;
                 break;
             }
-            n_waited = c + 1;
-        }
-        // ---- G1: S = C B^T ------------------------------------------------------
-        if (tid == 0) {
-            tc::fence_after_sync();
-            for (int k = 0; k < kN / 16; k++) {
-                const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-                tc::mma_bf16(tmem + kColS, tc::smem_desc_sw128(sC + off, 16, 1024),
-                             tc::smem_desc_sw128(sB + off, 16, 1024), idG1, k > 0);
+            if (lane == 0) {
+                tc::fence_after_sync();
+                // G3: Ye = C Hh^T + C Hl^T (C: K-major, swizzled)
+                for (int hl = 0; hl < 2; hl++)
+                    for (int k = 0; k < kN / 16; k++)
+                        tc::mma_bf16(tmem + kColYe,
+                                     tc::smem_desc_sw128(sC + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
+                                     tc::smem_desc(base + (hl ? S::kHl : S::kHh) + k * 256, 128, S::kStrideH), idG2,
+                                     hl > 0 || k > 0);
+                // G4: H^T += B^T (w o x)_hi + B^T (w o x)_lo (B^T: MN-major, swizzled,
+                // 64-row atoms 16 KB apart)
+                for (int hl = 0; hl < 2; hl++)
+                    for (int k = 0; k < kQ / 16; k++)
+                        tc::mma_bf16(tmem + kColH, tc::smem_desc_sw128(sB + k * 2048, 16384, 1024),
+                                     tc::smem_desc(base + (hl ? S::kWl : S::kWh) + k * 256, 128, kStrideC), idG4,
+                                     true);
+                tc::commit(&s_bar[1]);
             }
-            tc::commit(&s_bar);
+            __syncwarp();
+            // G2 once M is written (and, with one stage, x is in)
+            bool ok = ctl_wait(&s_ready[1], par);
+            if (ok && S::kStages == 1) {
+                ok = ctl_wait(&s_load[1], par);
+                if (ok) ld_seen1++;
+            }
+            if (!ok) {
+                if (lane == 0) fail(__LINE__);
+                failed = true;
+                break;
+            }
+            if (lane == 0) {
+                tc::fence_after_sync();
+                // G2: Yi = Mh x + Ml x (x: MN-major, swizzled, one atom)
+                for (int hl = 0; hl < 2; hl++)
+                    for (int k = 0; k < kQ / 16; k++)
+                        tc::mma_bf16(tmem + kColYi,
+                                     tc::smem_desc(base + (hl ? S::kMl : S::kMh) + k * 2 * kStrideC, kStrideC, 128),
+                                     tc::smem_desc_sw128(sX + k * 2048, 16384, 1024), idG2, hl > 0 || k > 0);
+                tc::commit(&s_bar[2]);
+            }
+            __syncwarp();
+            // one stage: the next chunk's C and B as soon as this chunk's products are done
+            if (S::kStages == 1 && c + 1 < nchunks) {
+                if (!ctl_wait(&s_bar[2], par)) {
+                    if (lane == 0) fail(__LINE__);
+                    failed = true;
+                    break;
+                }
+                issue_cb1(c + 1);
+            }
+            // chunk finished: y out; the next z and x (or the stage after next) in
+            if (!ctl_wait(&s_ready[2], par)) {
+                if (lane == 0) fail(__LINE__);
+                failed = true;
+                break;
+            }
+            {
+                constexpr int kAtoms = kOutF32 ? 2 : 1;
+                if (lane < kAtoms)
+                    tc::tma_store_3d(&m.y, (int)(h * kP) + 32 * lane, (int)(c * kQ), (int)b,
+                                     smem + S::kY + lane * 16384);
+                tc::bulk_commit();
+            }
+            if (zg) {
+                z_seen = (uint32_t)c + 1;   // the compute warps consumed z(c) before finishing
+                if (c + 1 < nchunks) issue_z(c + 1);
+            }
+            if (S::kStages == 2) {
+                if (c + 2 < nchunks) issue_stage(c + 2);
+            } else if (c + 1 < nchunks) {
+                issue_x1(c + 1);
+            }
+            tc::bulk_wait_read();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&s_yfree);
         }
-        const float cs2_end = s_cs2[kQ - 1];
-        if (tid < kQ) {
-            s_e[tid] = ex2(cs);
-            s_w[tid] = ex2(cs2_end - cs) * dtv;
+        if (failed) {
+            // let the tensor core and the copy engine finish what they still owe
+            // before the memory they write goes away
+            if (lane == 0) {
+                tc::commit(&s_drain);
+                (void)tc::mbar_wait(&s_drain, 0, kWaitLimit);
+            }
+            for (; ld_seen0 < ld_issued0; ld_seen0++) (void)tc::mbar_wait(&s_load[0], ld_seen0 & 1u, kWaitLimit);
+            for (; ld_seen1 < ld_issued1; ld_seen1++) (void)tc::mbar_wait(&s_load[1], ld_seen1 & 1u, kWaitLimit);
+            for (; z_seen < z_issued; z_seen++) (void)tc::mbar_wait(&s_zload, z_seen & 1u, kWaitLimit);
         }
-        if (warp == 0) tc::bulk_wait_read();   // the previous y store has left the M area
-        __syncthreads();
-        // ---- w o x, split; rescale the resident state by exp(cs_end) -------------
-        for (int i = tid; i < kQ * (kP / 8); i += kThreads) {
-            float v[8];
-            unpack8(*reinterpret_cast<const uint4*>(stg + S::kX + tc::sw128(i & (kQ - 1), i >> 7)), v);
-            const float w = s_w[i & (kQ - 1)];
-#pragma unroll
-            for (int k = 0; k < 8; k++) v[k] *= w;
-            split_store8(v, sWh + 16 * i, sWl + 16 * i);
-        }
+        tc::bulk_wait_read();
+    } else {
+        // =============================== compute warps ==============================
+        // initial state: H^T[n][p] = h0[b,h,p,n] (zero for n >= N or without h0)
         {
-            const float e_end = ex2(cs2_end);
             float v[32];
-            tc::tmem_ld32(tmem + lane_base + kColH + 32 * half, v);
-            tc::tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; j++) v[j] *= e_end;
+            for (int j = 0; j < 32; j++) {
+                const int p = 32 * half + j;
+                v[j] = (a.h0 && row < kN) ? a.h0[(bh * kP + p) * kN + row] : 0.f;
+            }
             tc::tmem_st32(tmem + lane_base + kColH + 32 * half, v);
-            tc::tmem_wait_st();
-        }
-        tc::fence_proxy_async();
-        // ---- M from S: decay mask, split into the two A operands of G2 -----------
-        {
-            const bool ok = tc::mbar_wait(&s_bar, phase, kWaitLimit);
-            if (__syncthreads_or(!ok)) {
-                if (tid == 0) atomicExch(&g_ssd_status, __LINE__);
-                failed = true;
-                break;
-            }
-            phase ^= 1;
-            tc::fence_after_sync();
-            const float cs_t = s_cs2[row];
-#pragma unroll
-            for (int blk = 0; blk < 2; blk++) {
-                const int s0 = 64 * half + 32 * blk;
-                float v[32];
-                tc::tmem_ld32(tmem + lane_base + kColS + s0, v);
-                tc::tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; j++) {
-                    const int s = s0 + j;
-                    v[j] = s <= row ? v[j] * ex2(cs_t - s_cs2[s]) * s_dt[s] : 0.f;
-                }
-#pragma unroll
-                for (int k = 0; k < 4; k++)
-                    split_store8(v + 8 * k, sMh + chunk_off(row, s0 / 8 + k), sMl + chunk_off(row, s0 / 8 + k));
-            }
-        }
-        tc::fence_proxy_async();
-        tc::fence_before_sync();
-        __syncthreads();
-        // ---- G2, G3, G4 -------------------------------------------------------------
-        if (tid == 0) {
-            tc::fence_after_sync();
-            // G2: Yi = Mh x + Ml x (x: MN-major, swizzled, one atom)
-            for (int hl = 0; hl < 2; hl++)
-                for (int k = 0; k < kQ / 16; k++)
-                    tc::mma_bf16(tmem + kColYi,
-                                 tc::smem_desc(base + (hl ? S::kMl : S::kMh) + k * 2 * kStrideC, kStrideC, 128),
-                                 tc::smem_desc_sw128(sX + k * 2048, 16384, 1024), idG2, hl > 0 || k > 0);
-            // G3: Ye = C Hh^T + C Hl^T (C: K-major, swizzled)
-            for (int hl = 0; hl < 2; hl++)
-                for (int k = 0; k < kN / 16; k++)
-                    tc::mma_bf16(tmem + kColYe, tc::smem_desc_sw128(sC + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
-                                 tc::smem_desc(base + (hl ? S::kHl : S::kHh) + k * 256, 128, S::kStrideH), idG2,
-                                 hl > 0 || k > 0);
-            // G4: H^T += B^T (w o x)_hi + B^T (w o x)_lo (B^T: MN-major, swizzled, 64-row atoms 16 KB apart)
-            for (int hl = 0; hl < 2; hl++)
-                for (int k = 0; k < kQ / 16; k++)
-                    tc::mma_bf16(tmem + kColH, tc::smem_desc_sw128(sB + k * 2048, 16384, 1024),
-                                 tc::smem_desc(base + (hl ? S::kWl : S::kWh) + k * 256, 128, kStrideC), idG4, true);
-            tc::commit(&s_bar);
-        }
-        {
-            const bool ok = tc::mbar_wait(&s_bar, phase, kWaitLimit);
-            if (__syncthreads_or(!ok)) {
-                if (tid == 0) atomicExch(&g_ssd_status, __LINE__);
-                failed = true;
-                break;
-            }
-            phase ^= 1;
-        }
-        tc::fence_after_sync();
-        // ---- epilogue: y = Yi + exp(cs_t) Ye + D x, gated, staged for a TMA store ----
-        if (zg) {
-            const bool ok = tc::mbar_wait(&s_zload, (uint32_t)(c & 1), kWaitLimit);
-            if (__syncthreads_or(!ok)) {
-                if (tid == 0) atomicExch(&g_ssd_status, __LINE__);
-                failed = true;
-                break;
-            }
-            n_zwaited = c + 1;
-        }
-        {
-            float yi[32], ye[32];
-            tc::tmem_ld32(tmem + lane_base + kColYi + 32 * half, yi);
-            tc::tmem_ld32(tmem + lane_base + kColYe + 32 * half, ye);
-            tc::tmem_wait_ld();
-            const float e = s_e[row];
-            float out[32];
-#pragma unroll
-            for (int k = 0; k < 4; k++) {
-                float xv[8];
-                unpack8(*reinterpret_cast<const uint4*>(stg + S::kX + tc::sw128(row, 4 * half + k)), xv);
-                float zv[8];
-                if (zg) unpack8(*reinterpret_cast<const uint4*>(smem + S::kZ + tc::sw128(row, 4 * half + k)), zv);
-#pragma unroll
-                for (int i = 0; i < 8; i++) {
-                    float yv = fmaf(e, ye[8 * k + i], yi[8 * k + i]);
-                    yv = fmaf(Dh, xv[i], yv);
-                    if (zg) yv *= silu_acc<false>(zv[i]);
-                    out[8 * k + i] = yv;
-                }
-            }
-            // rows past seqlen are staged too; the store drops them
-            unsigned char* sy = smem + S::kY;
-            if constexpr (kOutF32) {   // two atoms: columns 0-31 and 32-63
-#pragma unroll
-                for (int k = 0; k < 8; k++)
-                    *reinterpret_cast<float4*>(sy + half * 16384 + tc::sw128(row, k)) =
-                        make_float4(out[4 * k], out[4 * k + 1], out[4 * k + 2], out[4 * k + 3]);
-            } else {
-#pragma unroll
-                for (int k = 0; k < 4; k++)
-                    Vec16<__nv_bfloat16>::store(reinterpret_cast<__nv_bfloat16*>(sy + tc::sw128(row, 4 * half + k)),
-                                                out + 8 * k);
-            }
-        }
-        // ---- the new state as G3's split operand for the next chunk -----------------
-        if (c + 1 < nchunks) {
-            float v[32];
-            tc::tmem_ld32(tmem + lane_base + kColH + 32 * half, v);
-            tc::tmem_wait_ld();
             if (row < kN) {
 #pragma unroll
                 for (int k = 0; k < 4; k++)
                     split_store8(v + 8 * k, sHh + (4 * half + k) * S::kStrideH + row * 16,
                                  sHl + (4 * half + k) * S::kStrideH + row * 16);
             }
+            tc::tmem_wait_st();
         }
-        tc::fence_proxy_async();
-        tc::fence_before_sync();
-        __syncthreads();
-        // y out of the staging area (16-byte column groups of 128 steps); then the
-        // next chunk's z into its (now read) tile
-        if (warp == 0) {
-            constexpr int kAtoms = kOutF32 ? 2 : 1;
-            if (lane < kAtoms)
-                tc::tma_store_3d(&m.y, (int)(h * kP) + 32 * lane, (int)t0, (int)b, smem + S::kY + lane * 16384);
-            tc::bulk_commit();
-        }
-        if (zg && c + 1 < nchunks) issue_z(c + 1);
-    }
-
-    if (!failed && a.h_last && row < kN) {
-        tc::fence_after_sync();
-        float v[32];
-        tc::tmem_ld32(tmem + lane_base + kColH + 32 * half, v);
-        tc::tmem_wait_ld();
+        // raw dt bits of step tid of chunk c, widened only where used so that the
+        // next chunk's load stays in flight through this chunk
+        auto load_dt = [&](int64_t c) -> uint32_t {
+            const int64_t t = c * kQ + tid;
+            return (tid < kQ && c < nchunks && t < L) ? (uint32_t)__ldg(dtb + (b * L + t) * H + h) : 0u;
+        };
+        uint32_t dt_next = load_dt(0);
+        for (int64_t c = 0; c < nchunks; c++) {
+            const int q = (int)((L - c * kQ) < kQ ? (L - c * kQ) : kQ);
+            const int st = S::kStages == 2 ? (int)(c & 1) : 0;
+            const uint32_t par = (uint32_t)(c & 1);
+            unsigned char* stg = smem + S::kStage0 + st * S::kStageBytes;
+            // ---- dt and the in-chunk cumulative sum of dt A (log2 domain) ----------
+            float cs = 0.f, dtv = 0.f;
+            {
+                const float raw = __uint_as_float(dt_next << 16);
+                dt_next = load_dt(c + 1);
+                if (tid < kQ) {
+                    if (tid < q) {
+                        const float v = raw + bias;
+                        dtv = a.softplus ? softplus_acc<true>(v) : v;
+                    }
+                    cs = dtv * A2;
 #pragma unroll
-        for (int j = 0; j < 32; j++) a.h_last[(bh * kP + 32 * half + j) * kN + row] = v[j];
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float u = __shfl_up_sync(0xffffffffu, cs, o);
+                        if (lane >= o) cs += u;
+                    }
+                    if (lane == 31) s_wsum[warp] = cs;
+                }
+            }
+            compute_sync();
+            if (tid < kQ) {
+                for (int w = 0; w < warp; w++) cs += s_wsum[w];
+                s_cs2[tid] = cs;
+                s_dt[tid] = dtv;
+            }
+            // ---- this chunk's x in --------------------------------------------------
+            {
+                uint64_t* bar = S::kStages == 2 ? &s_load[st] : &s_load[1];
+                const uint32_t p = S::kStages == 2 ? (uint32_t)((c >> 1) & 1) : par;
+                const bool ok = wait_or_abort(bar, p, abort_flag);
+                if (compute_any(!ok)) {
+                    if (tid == 0) fail(__LINE__);
+                    failed = true;
+                    break;
+                }
+            }
+            const float cs2_end = s_cs2[kQ - 1];
+            if (tid < kQ) {
+                s_e[tid] = ex2(cs);
+                s_w[tid] = ex2(cs2_end - cs) * dtv;
+            }
+            compute_sync();
+            // ---- w o x, split; rescale the resident state by exp(cs_end) -------------
+            for (int i = tid; i < kQ * (kP / 8); i += kCompute) {
+                float v[8];
+                unpack8(*reinterpret_cast<const uint4*>(stg + S::kX + tc::sw128(i & (kQ - 1), i >> 7)), v);
+                const float w = s_w[i & (kQ - 1)];
+#pragma unroll
+                for (int k = 0; k < 8; k++) v[k] *= w;
+                split_store8(v, sWh + 16 * i, sWl + 16 * i);
+            }
+            {
+                const float e_end = ex2(cs2_end);
+                float v[32];
+                tc::tmem_ld32(tmem + lane_base + kColH + 32 * half, v);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; j++) v[j] *= e_end;
+                tc::tmem_st32(tmem + lane_base + kColH + 32 * half, v);
+                tc::tmem_wait_st();
+            }
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&s_ready[0]);
+            // ---- M from S: decay mask, split into the two A operands of G2 -----------
+            {
+                bool ok = wait_or_abort(&s_bar[0], par, abort_flag);
+                if (ok && c > 0) ok = wait_or_abort(&s_yfree, (uint32_t)((c - 1) & 1), abort_flag);
+                if (compute_any(!ok)) {
+                    if (tid == 0) fail(__LINE__);
+                    failed = true;
+                    break;
+                }
+            }
+            tc::fence_after_sync();
+            {
+                const float cs_t = s_cs2[row];
+#pragma unroll
+                for (int blk = 0; blk < 2; blk++) {
+                    const int s0 = 64 * half + 32 * blk;
+                    float v[32];
+                    tc::tmem_ld32(tmem + lane_base + kColS + s0, v);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; j++) {
+                        const int s = s0 + j;
+                        v[j] = s <= row ? v[j] * ex2(cs_t - s_cs2[s]) * s_dt[s] : 0.f;
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; k++)
+                        split_store8(v + 8 * k, sMh + chunk_off(row, s0 / 8 + k), sMl + chunk_off(row, s0 / 8 + k));
+                }
+            }
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&s_ready[1]);
+            // ---- products in; epilogue: y = Yi + exp(cs_t) Ye + D x, gated, staged ----
+            {
+                bool ok = wait_or_abort(&s_bar[2], par, abort_flag) && wait_or_abort(&s_bar[1], par, abort_flag);
+                if (ok && zg) ok = wait_or_abort(&s_zload, par, abort_flag);
+                if (compute_any(!ok)) {
+                    if (tid == 0) fail(__LINE__);
+                    failed = true;
+                    break;
+                }
+            }
+            tc::fence_after_sync();
+            {
+                float yi[32], ye[32];
+                tc::tmem_ld32(tmem + lane_base + kColYi + 32 * half, yi);
+                tc::tmem_ld32(tmem + lane_base + kColYe + 32 * half, ye);
+                tc::tmem_wait_ld();
+                const float e = s_e[row];
+                float out[32];
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    float xv[8];
+                    unpack8(*reinterpret_cast<const uint4*>(stg + S::kX + tc::sw128(row, 4 * half + k)), xv);
+                    float zv[8];
+                    if (zg) unpack8(*reinterpret_cast<const uint4*>(smem + S::kZ + tc::sw128(row, 4 * half + k)), zv);
+#pragma unroll
+                    for (int i = 0; i < 8; i++) {
+                        float yv = fmaf(e, ye[8 * k + i], yi[8 * k + i]);
+                        yv = fmaf(Dh, xv[i], yv);
+                        if (zg) yv *= silu_acc<false>(zv[i]);
+                        out[8 * k + i] = yv;
+                    }
+                }
+                // rows past seqlen are staged too; the store drops them
+                unsigned char* sy = smem + S::kY;
+                if constexpr (kOutF32) {   // two atoms: columns 0-31 and 32-63
+#pragma unroll
+                    for (int k = 0; k < 8; k++)
+                        *reinterpret_cast<float4*>(sy + half * 16384 + tc::sw128(row, k)) =
+                            make_float4(out[4 * k], out[4 * k + 1], out[4 * k + 2], out[4 * k + 3]);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 4; k++)
+                        Vec16<__nv_bfloat16>::store(
+                            reinterpret_cast<__nv_bfloat16*>(sy + tc::sw128(row, 4 * half + k)), out + 8 * k);
+                }
+            }
+            // ---- the new state as G3's split operand for the next chunk -----------------
+            if (c + 1 < nchunks) {
+                float v[32];
+                tc::tmem_ld32(tmem + lane_base + kColH + 32 * half, v);
+                tc::tmem_wait_ld();
+                if (row < kN) {
+#pragma unroll
+                    for (int k = 0; k < 4; k++)
+                        split_store8(v + 8 * k, sHh + (4 * half + k) * S::kStrideH + row * 16,
+                                     sHl + (4 * half + k) * S::kStrideH + row * 16);
+                }
+            }
+            tc::fence_proxy_async();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&s_ready[2]);
+        }
+        if (!failed && a.h_last && row < kN) {
+            float v[32];
+            tc::tmem_ld32(tmem + lane_base + kColH + 32 * half, v);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; j++) a.h_last[(bh * kP + 32 * half + j) * kN + row] = v[j];
+        }
     }
-    if (failed) {
-        // let whatever the tensor core and the copy engine still owe (the phases
-        // that timed out, loads issued but not consumed) complete before the
-        // memory they write goes away
-        (void)tc::mbar_wait(&s_bar, phase, kWaitLimit);
-        for (int64_t k = n_waited; k < n_issued; k++)
-            (void)tc::mbar_wait(&s_load[k % S::kStages], (uint32_t)(k / S::kStages) & 1u, kWaitLimit);
-        for (int64_t k = n_zwaited; k < n_zissued; k++) (void)tc::mbar_wait(&s_zload, (uint32_t)(k & 1), kWaitLimit);
-    }
-    if (warp == 0) tc::bulk_wait_read();
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) {
