@@ -95,7 +95,7 @@ struct Smem {
     static constexpr uint32_t kZ = kHl + kTileH;        // z of the current chunk (128 x 64)
     static constexpr uint32_t kBytes = kZ + kTileX;
     static constexpr uint32_t kY = kMh;                 // y staged for its store (M is free by then)
-    static_assert(kBytes + 3072 <= 232448, "shared memory (dynamic + static)");
+    static_assert(kBytes <= 232448 - 3072, "shared memory (dynamic + up to 3 KB static)");
     static_assert(kStage0 + kB + 32768 <= kBytes, "G4 reach of stage 0");
     static_assert(kStage0 + (kStages - 1) * kStageBytes + kB + 32768 <= kBytes, "G4 reach of the last stage");
 };
@@ -170,9 +170,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ssd_chunk_scan_kernel(const SsdArgs a, const __grid_constant__ SsdMaps m) {
     using S = Smem<kN>;
     extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ float s_cs2[kQ];      // cs_t * log2(e)
-    __shared__ float s_dt[kQ];
-    __shared__ float s_e[kQ];        // exp(cs_t)
+    __shared__ float s_cs2[2][kQ];   // cs_t * log2(e), by chunk parity
+    __shared__ float s_dt[2][kQ];
     __shared__ float s_w[kQ];        // exp(cs_end - cs_t) dt_t
     __shared__ float s_wsum[4];
     __shared__ uint64_t s_bar[3];
@@ -444,43 +443,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc::tmem_wait_st();
         }
-        // raw dt bits of step tid of chunk c, widened only where used so that the
-        // next chunk's load stays in flight through this chunk
+        // raw dt bits of step tid of chunk c (widened only where used, so loads stay
+        // in flight across a chunk)
         auto load_dt = [&](int64_t c) -> uint32_t {
             const int64_t t = c * kQ + tid;
             return (tid < kQ && c < nchunks && t < L) ? (uint32_t)__ldg(dtb + (b * L + t) * H + h) : 0u;
         };
-        uint32_t dt_next = load_dt(0);
-        for (int64_t c = 0; c < nchunks; c++) {
-            const int q = (int)((L - c * kQ) < kQ ? (L - c * kQ) : kQ);
-            const int st = S::kStages == 2 ? (int)(c & 1) : 0;
-            const uint32_t par = (uint32_t)(c & 1);
-            unsigned char* stg = smem + S::kStage0 + st * S::kStageBytes;
-            // ---- dt and the in-chunk cumulative sum of dt A (log2 domain) ----------
-            float cs = 0.f, dtv = 0.f;
-            {
-                const float raw = __uint_as_float(dt_next << 16);
-                dt_next = load_dt(c + 1);
-                if (tid < kQ) {
-                    if (tid < q) {
-                        const float v = raw + bias;
-                        dtv = a.softplus ? softplus_acc<true>(v) : v;
-                    }
-                    cs = dtv * A2;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const float u = __shfl_up_sync(0xffffffffu, cs, o);
-                        if (lane >= o) cs += u;
-                    }
-                    if (lane == 31) s_wsum[warp] = cs;
+        // dt and the in-chunk cumulative sum of dt A (log2 domain) of chunk k into
+        // s_cs2[k & 1], s_dt[k & 1] (and this thread's cs, dtv); all compute threads
+        auto scan_chunk = [&](int64_t k, uint32_t bits, float& cs, float& dtv) {
+            const int q = (int)((L - k * kQ) < kQ ? (L - k * kQ) : kQ);
+            cs = 0.f;
+            dtv = 0.f;
+            if (tid < kQ) {
+                if (tid < q) {
+                    const float v = __uint_as_float(bits << 16) + bias;
+                    dtv = a.softplus ? softplus_acc<true>(v) : v;
                 }
+                cs = dtv * A2;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float u = __shfl_up_sync(0xffffffffu, cs, o);
+                    if (lane >= o) cs += u;
+                }
+                if (lane == 31) s_wsum[warp] = cs;
             }
             compute_sync();
             if (tid < kQ) {
                 for (int w = 0; w < warp; w++) cs += s_wsum[w];
-                s_cs2[tid] = cs;
-                s_dt[tid] = dtv;
+                s_cs2[k & 1][tid] = cs;
+                s_dt[k & 1][tid] = dtv;
             }
+        };
+        float cs = 0.f, dtv = 0.f;
+        uint32_t dt_next = load_dt(1);
+        if (nchunks > 0) scan_chunk(0, load_dt(0), cs, dtv);
+        for (int64_t c = 0; c < nchunks; c++) {
+            const int st = S::kStages == 2 ? (int)(c & 1) : 0;
+            const uint32_t par = (uint32_t)(c & 1);
+            unsigned char* stg = smem + S::kStage0 + st * S::kStageBytes;
+            const float* cs2 = s_cs2[c & 1];
+            const float* dts = s_dt[c & 1];
             // ---- this chunk's x in --------------------------------------------------
             {
                 uint64_t* bar = S::kStages == 2 ? &s_load[st] : &s_load[1];
@@ -492,11 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
             }
-            const float cs2_end = s_cs2[kQ - 1];
-            if (tid < kQ) {
-                s_e[tid] = ex2(cs);
-                s_w[tid] = ex2(cs2_end - cs) * dtv;
-            }
+            const float cs2_end = cs2[kQ - 1];
+            if (tid < kQ) s_w[tid] = ex2(cs2_end - cs) * dtv;
             compute_sync();
             // ---- w o x, split; rescale the resident state by exp(cs_end) -------------
             for (int i = tid; i < kQ * (kP / 8); i += kCompute) {
@@ -533,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc::fence_after_sync();
             {
-                const float cs_t = s_cs2[row];
+                const float cs_t = cs2[row];
 #pragma unroll
                 for (int blk = 0; blk < 2; blk++) {
                     const int s0 = 64 * half + 32 * blk;
@@ -543,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 32; j++) {
                         const int s = s0 + j;
-                        v[j] = s <= row ? v[j] * ex2(cs_t - s_cs2[s]) * s_dt[s] : 0.f;
+                        v[j] = s <= row ? v[j] * ex2(cs_t - cs2[s]) * dts[s] : 0.f;
                     }
 #pragma unroll
                     for (int k = 0; k < 4; k++)
@@ -554,6 +554,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&s_ready[1]);
+            // the next chunk's dt scan while the last product runs
+            float cs_next = 0.f, dtv_next = 0.f;
+            if (c + 1 < nchunks) {
+                scan_chunk(c + 1, dt_next, cs_next, dtv_next);
+                dt_next = load_dt(c + 2);
+            }
             // ---- products in; epilogue: y = Yi + exp(cs_t) Ye + D x, gated, staged ----
             {
                 bool ok = wait_or_abort(&s_bar[2], par, abort_flag) && wait_or_abort(&s_bar[1], par, abort_flag);
@@ -570,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::tmem_ld32(tmem + lane_base + kColYi + 32 * half, yi);
                 tc::tmem_ld32(tmem + lane_base + kColYe + 32 * half, ye);
                 tc::tmem_wait_ld();
-                const float e = s_e[row];
+                const float e = ex2(cs2[row]);   // exp(cs_t)
                 float out[32];
 #pragma unroll
                 for (int k = 0; k < 4; k++) {
@@ -616,6 +622,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&s_ready[2]);
+            cs = cs_next;
+            dtv = dtv_next;
         }
         if (!failed && a.h_last && row < kN) {
             float v[32];
@@ -676,7 +684,11 @@ cudaError_t launch_n(const SsdArgs& a, cudaStream_t s) {
     }
     auto k = ssd_chunk_scan_kernel<kN, kOutF32>;
     constexpr uint32_t bytes = Smem<kN>::kBytes;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, k);
+    if (e != cudaSuccess) return e;
+    if (fa.sharedSizeBytes + bytes > 232448) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e != cudaSuccess) return e;
     k<<<(unsigned)(a.batch * a.nheads), kThreads, bytes, s>>>(a, maps);
     return cudaGetLastError();
