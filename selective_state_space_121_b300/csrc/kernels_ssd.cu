@@ -426,23 +426,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::bulk_wait_read();
     } else {
         // =============================== compute warps ==============================
-        // initial state: H^T[n][p] = h0[b,h,p,n] (zero for n >= N or without h0)
-        {
-            float v[32];
-#pragma unroll
-            for (int j = 0; j < 32; j++) {
-                const int p = 32 * half + j;
-                v[j] = (a.h0 && row < kN) ? a.h0[(bh * kP + p) * kN + row] : 0.f;
-            }
-            tc::tmem_st32(tmem + lane_base + kColH + 32 * half, v);
-            if (row < kN) {
-#pragma unroll
-                for (int k = 0; k < 4; k++)
-                    split_store8(v + 8 * k, sHh + (4 * half + k) * S::kStrideH + row * 16,
-                                 sHl + (4 * half + k) * S::kStrideH + row * 16);
-            }
-            tc::tmem_wait_st();
-        }
         // raw dt bits of step tid of chunk c (widened only where used, so loads stay
         // in flight across a chunk)
         auto load_dt = [&](int64_t c) -> uint32_t {
@@ -478,6 +461,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         float cs = 0.f, dtv = 0.f;
         uint32_t dt_next = load_dt(1);
         if (nchunks > 0) scan_chunk(0, load_dt(0), cs, dtv);
+        compute_sync();   // chunk 0's cumulative decays are visible
+        // initial state: H^T[n][p] = h0[b,h,p,n] (zero for n >= N or without h0): split
+        // for G3, and resident rescaled by chunk 0's total decay for G4
+        {
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; j++) {
+                const int p = 32 * half + j;
+                v[j] = (a.h0 && row < kN) ? a.h0[(bh * kP + p) * kN + row] : 0.f;
+            }
+            if (row < kN) {
+#pragma unroll
+                for (int k = 0; k < 4; k++)
+                    split_store8(v + 8 * k, sHh + (4 * half + k) * S::kStrideH + row * 16,
+                                 sHl + (4 * half + k) * S::kStrideH + row * 16);
+            }
+            const float e0 = nchunks > 0 ? ex2(s_cs2[0][kQ - 1]) : 1.f;
+#pragma unroll
+            for (int j = 0; j < 32; j++) v[j] *= e0;
+            tc::tmem_st32(tmem + lane_base + kColH + 32 * half, v);
+            tc::tmem_wait_st();
+        }
         for (int64_t c = 0; c < nchunks; c++) {
             const int st = S::kStages == 2 ? (int)(c & 1) : 0;
             const uint32_t par = (uint32_t)(c & 1);
@@ -507,16 +512,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < 8; k++) v[k] *= w;
                 split_store8(v, sWh + 16 * i, sWl + 16 * i);
             }
-            {
-                const float e_end = ex2(cs2_end);
-                float v[32];
-                tc::tmem_ld32(tmem + lane_base + kColH + 32 * half, v);
-                tc::tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; j++) v[j] *= e_end;
-                tc::tmem_st32(tmem + lane_base + kColH + 32 * half, v);
-                tc::tmem_wait_st();
-            }
             tc::fence_proxy_async();
             tc::fence_before_sync();
             __syncwarp();
@@ -534,16 +529,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_after_sync();
             {
                 const float cs_t = cs2[row];
+                // a 32-column block is, for this warp's 32 rows, all above the
+                // diagonal (zeros), all on or below it (no mask), or crossing it
 #pragma unroll
                 for (int blk = 0; blk < 2; blk++) {
                     const int s0 = 64 * half + 32 * blk;
+                    if (s0 > 32 * quad + 31) {
+                        const uint4 zero = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                        for (int k = 0; k < 4; k++) {
+                            *reinterpret_cast<uint4*>(sMh + chunk_off(row, s0 / 8 + k)) = zero;
+                            *reinterpret_cast<uint4*>(sMl + chunk_off(row, s0 / 8 + k)) = zero;
+                        }
+                        continue;
+                    }
                     float v[32];
                     tc::tmem_ld32(tmem + lane_base + kColS + s0, v);
                     tc::tmem_wait_ld();
+                    if (s0 + 31 <= 32 * quad) {
 #pragma unroll
-                    for (int j = 0; j < 32; j++) {
-                        const int s = s0 + j;
-                        v[j] = s <= row ? v[j] * ex2(cs_t - cs2[s]) * dts[s] : 0.f;
+                        for (int j = 0; j < 32; j++) v[j] = v[j] * ex2(cs_t - cs2[s0 + j]) * dts[s0 + j];
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; j++) {
+                            const int s = s0 + j;
+                            v[j] = s <= row ? v[j] * ex2(cs_t - cs2[s]) * dts[s] : 0.f;
+                        }
                     }
 #pragma unroll
                     for (int k = 0; k < 4; k++)
@@ -606,7 +617,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             reinterpret_cast<__nv_bfloat16*>(sy + tc::sw128(row, 4 * half + k)), out + 8 * k);
                 }
             }
-            // ---- the new state as G3's split operand for the next chunk -----------------
+            // ---- the new state: G3's split operand for the next chunk, and the resident
+            // copy rescaled by the next chunk's total decay for G4 to accumulate into
             if (c + 1 < nchunks) {
                 float v[32];
                 tc::tmem_ld32(tmem + lane_base + kColH + 32 * half, v);
@@ -617,6 +629,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         split_store8(v + 8 * k, sHh + (4 * half + k) * S::kStrideH + row * 16,
                                      sHl + (4 * half + k) * S::kStrideH + row * 16);
                 }
+                const float e_next = ex2(s_cs2[(c + 1) & 1][kQ - 1]);
+#pragma unroll
+                for (int j = 0; j < 32; j++) v[j] *= e_next;
+                tc::tmem_st32(tmem + lane_base + kColH + 32 * half, v);
+                tc::tmem_wait_st();
             }
             tc::fence_proxy_async();
             tc::fence_before_sync();
