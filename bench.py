@@ -586,6 +586,7 @@ def main():
             configs_measured[only] = {k: rec[k] for k in ("case", "ms_median", "Gtokch_s", "GB_s", "hbm_frac")}
             if "tensor_TFLOP_s" in rec:
                 configs_measured[only].update({k: rec[k] for k in ("tensor_TFLOP_s", "tensor_frac")})
+                configs_measured[only]["traffic"] = _traffic_record("ssd_5120")
             torch.cuda.empty_cache()
 
     hbm_peak, _, peak_kind = _peaks()
