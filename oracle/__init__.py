@@ -69,6 +69,9 @@ class OracleLib:
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_scan_bwd.argtypes = [P] * 8 + [ctypes.c_int] + [P] * 12 + [I64] * 4 + [ctypes.c_int]
         lib.oracle_scan_bwd.restype = ctypes.c_int
+        lib.oracle_scan_dir.argtypes = [P] * 8 + [ctypes.c_int, P, P, P] + [I64] * 4 + [ctypes.c_int, I64, I64,
+                                                                                  ctypes.c_int, ctypes.c_int]
+        lib.oracle_scan_dir.restype = ctypes.c_int
         lib.oracle_ssd_scan.argtypes = [P] * 8 + [ctypes.c_int, P, P, P] + [I64] * 6 + [ctypes.c_int]
         lib.oracle_ssd_scan.restype = ctypes.c_int
         lib.oracle_causal_conv1d.argtypes = [P] * 4 + [ctypes.c_int, P, P, I64, I64, I64, I64, ctypes.c_int]
@@ -110,6 +113,27 @@ class OracleLib:
                                   bt, dim, L, N, int(threads))
         if rc != 0:
             raise ValueError("oracle_scan rejected the sizes")
+        return y, hl
+
+    def scan_dir(self, u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, h0=None,
+                 order=0, rows=0, cols=0, zoh=False, threads: int = 0):
+        """The fp64 scan along traversal `order` (0 raster, 1 reversed, 2 column-major
+        of a rows x cols image, 3 reversed columns), outputs in raster order, with the
+        zero-order-hold input matrix when zoh. Shapes as scan()."""
+        u = _f32(u); delta = _f32(delta); A = _f32(A); B = _f32(B); C = _f32(C)
+        D = _f32(D); z = _f32(z); delta_bias = _f32(delta_bias); h0 = _f64(h0)
+        bt, dim, L = u.shape
+        N = A.shape[1]
+        assert delta.shape == u.shape and B.shape == (bt, N, L) and C.shape == (bt, N, L)
+        assert z is None or z.shape == u.shape
+        assert h0 is None or h0.shape == (bt, dim, N)
+        y = np.empty((bt, dim, L), dtype=np.float64)
+        hl = np.empty((bt, dim, N), dtype=np.float64)
+        rc = self.lib.oracle_scan_dir(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
+                                      int(bool(softplus)), _p(h0), _p(y), _p(hl), bt, dim, L, N, int(order),
+                                      int(rows), int(cols), int(bool(zoh)), int(threads))
+        if rc != 0:
+            raise ValueError("oracle_scan_dir rejected the sizes")
         return y, hl
 
     def state_update(self, state, x, delta, A, B, C, D=None, z=None, delta_bias=None,
@@ -239,6 +263,10 @@ def scan(*args, **kw):
 
 def state_update(*args, **kw):
     return default().state_update(*args, **kw)
+
+
+def scan_dir(*args, **kw):
+    return default().scan_dir(*args, **kw)
 
 
 def scan_bwd(*args, **kw):

@@ -84,6 +84,81 @@ int oracle_scan(const float *u, const float *delta, const float *A, const float 
     return 0;
 }
 
+/* The same selective scan along another traversal of the sequence, with the
+ * exact zero-order-hold input matrix as an option.
+ *
+ * Traversal (Mamba SSM complete guide, section 9 "Mamba applications", VMamba:
+ * an image of rows x cols patches, stored in raster order, is scanned in four
+ * directions). Step k = 0 .. seqlen-1 of the scan visits position pos(k):
+ *   order 0  raster             pos(k) = k
+ *   order 1  reversed raster    pos(k) = seqlen - 1 - k
+ *   order 2  column-major       pos(k) = (k % rows) * cols + k / rows
+ *   order 3  reversed columns   pos(k) = column-major pos(seqlen - 1 - k)
+ * (rows * cols == seqlen for orders 2 and 3). Every input is read at pos(k)
+ * and the step's output is written to y at pos(k): each direction's output
+ * lands in raster order. h0 is the state before the first visited step,
+ * h_last the state after the last.
+ *
+ * Input matrix. zoh == 0: dt * B (the selective_scan form, as oracle_scan).
+ * zoh != 0: the zero-order hold of the same guide's section 2
+ * ("Discretization"), B_bar = (dt A)^-1 (exp(dt A) - 1) dt B, which for the
+ * diagonal A of the scan is (exp(dt A) - 1) / A * B, and dt * B where A = 0.
+ * Layouts and other arguments as oracle_scan.
+ */
+static int64_t oracle_pos(int order, int64_t k, int64_t L, int64_t rows, int64_t cols) {
+    if (order == 1 || order == 3) k = L - 1 - k;
+    if (order >= 2) return (k % rows) * cols + k / rows;
+    return k;
+}
+
+int oracle_scan_dir(const float *u, const float *delta, const float *A, const float *B,
+                    const float *C, const float *D, const float *z, const float *delta_bias,
+                    int softplus, const double *h0, double *y, double *h_last, int64_t batch,
+                    int64_t dim, int64_t seqlen, int64_t dstate, int order, int64_t rows,
+                    int64_t cols, int zoh, int nthreads) {
+    if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 1 || order < 0 || order > 3) return -1;
+    if (order >= 2 && (rows < 1 || cols < 1 || rows * cols != seqlen)) return -1;
+    int64_t nch = batch * dim;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 4)
+#endif
+    for (int64_t ch = 0; ch < nch; ch++) {
+        int64_t b = ch / dim, d = ch % dim;
+        double *h = (double *)malloc(sizeof(double) * (size_t)dstate);
+        const double *h0_r = h0 ? h0 + ch * dstate : NULL;
+        for (int64_t n = 0; n < dstate; n++) h[n] = h0_r ? h0_r[n] : 0.0;
+        const float *u_r = u + ch * seqlen, *dl_r = delta + ch * seqlen;
+        const float *z_r = z ? z + ch * seqlen : NULL;
+        const float *B_b = B + b * dstate * seqlen, *C_b = C + b * dstate * seqlen;
+        const float *A_row = A + d * dstate;
+        for (int64_t k = 0; k < seqlen; k++) {
+            int64_t t = oracle_pos(order, k, seqlen, rows, cols);
+            double ut = (double)u_r[t];
+            double v = (double)dl_r[t];
+            if (delta_bias) v += (double)delta_bias[d];
+            double dt = softplus ? oracle_softplus(v) : v;
+            double acc = 0.0;
+            for (int64_t n = 0; n < dstate; n++) {
+                double an = (double)A_row[n];
+                double a = exp(dt * an);
+                double bbar = zoh ? (an != 0.0 ? expm1(dt * an) / an : dt) : dt;
+                h[n] = a * h[n] + bbar * (double)B_b[n * seqlen + t] * ut;
+                acc += (double)C_b[n * seqlen + t] * h[n];
+            }
+            if (D) acc += (double)D[d] * ut;
+            if (z_r) acc *= oracle_silu((double)z_r[t]);
+            y[ch * seqlen + t] = acc;
+        }
+        if (h_last) {
+            double *hl_r = h_last + ch * dstate;
+            for (int64_t n = 0; n < dstate; n++) hl_r[n] = h[n];
+        }
+        free(h);
+    }
+    return 0;
+}
+
 /* One decode token, in place on the fp64 state: the body of the same loop
  * applied once (the O(1)-per-token recurrent form).
  *   state : (batch, dim, dstate) in/out     x, delta, z, y : (batch, dim)

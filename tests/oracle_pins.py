@@ -497,6 +497,79 @@ def check_ssd_quadratic_and_chunked(orc):
     assert np.all(np.isfinite(y)) and np.all(np.isfinite(hl))
 
 
+# ---------------------------------------------------------------------------
+# 16. Directional scans and the zero-order hold (the next row after Mamba-2):
+#     (a) each traversal order equals the raster scan run on the inputs
+#     rearranged by numpy (flip, transpose of the rows x cols image) with its
+#     output rearranged back; (b) one zero-order-hold step equals the exact
+#     solution of h' = A h + B u over the step (u held constant), taken from the
+#     matrix exponential of the augmented 2 x 2 system ([guide] section 2,
+#     "Discretization"), A = 0 included.
+# ---------------------------------------------------------------------------
+def _dir_case(rng, bt=2, dim=3, rows=5, cols=7, N=4):
+    L = rows * cols
+    u = rng.standard_normal((bt, dim, L)).astype(np.float32)
+    delta = (rng.standard_normal((bt, dim, L)) * 0.5).astype(np.float32)
+    z = rng.standard_normal((bt, dim, L)).astype(np.float32)
+    A = -np.exp(rng.uniform(np.log(0.5), np.log(4.0), size=(dim, N))).astype(np.float32)
+    B = rng.standard_normal((bt, N, L)).astype(np.float32)
+    C = rng.standard_normal((bt, N, L)).astype(np.float32)
+    D = rng.standard_normal((dim,)).astype(np.float32)
+    bias = rng.uniform(-4, -1, size=(dim,)).astype(np.float32)
+    h0 = rng.standard_normal((bt, dim, N))
+    return u, delta, z, A, B, C, D, bias, h0
+
+
+def check_scan_dir_orders(orc):
+    rng = np.random.default_rng(47)
+    rows, cols = 5, 7
+    u, delta, z, A, B, C, D, bias, h0 = _dir_case(rng, rows=rows, cols=cols)
+    bt, dim, L = u.shape
+
+    def colmajor(a):   # raster (.., rows*cols) -> column-major sequence
+        return np.ascontiguousarray(a.reshape(a.shape[:-1] + (rows, cols)).swapaxes(-1, -2).reshape(a.shape))
+
+    def raster(a):     # inverse of colmajor
+        return np.ascontiguousarray(a.reshape(a.shape[:-1] + (cols, rows)).swapaxes(-1, -2).reshape(a.shape))
+
+    def flip(a):
+        return np.ascontiguousarray(a[..., ::-1])
+
+    forward = {1: (flip, flip), 2: (colmajor, raster), 3: (lambda a: flip(colmajor(a)), lambda a: raster(flip(a)))}
+    for order, (to_seq, back) in forward.items():
+        y, hl = orc.scan_dir(u, delta, A, B, C, D, z, bias, True, h0, order=order, rows=rows, cols=cols)
+        y1, h1 = orc.scan(to_seq(u), to_seq(delta), A, to_seq(B), to_seq(C), D, to_seq(z), bias, True, h0)
+        assert _rel(back(y1), y) < 1e-13, order
+        assert _rel(h1, hl) < 1e-13, order
+    y, hl = orc.scan_dir(u, delta, A, B, C, D, z, bias, True, h0, order=0)
+    y1, h1 = orc.scan(u, delta, A, B, C, D, z, bias, True, h0)
+    assert _rel(y1, y) == 0 and _rel(h1, hl) == 0
+
+
+def check_scan_zoh_exact_step(orc):
+    from scipy.linalg import expm
+    rng = np.random.default_rng(53)
+    bt, dim, N = 2, 3, 5
+    u = rng.standard_normal((bt, dim, 1)).astype(np.float32)
+    dt = np.exp(rng.uniform(np.log(0.05), np.log(1.5), size=(bt, dim, 1))).astype(np.float32)
+    A = -np.exp(rng.uniform(np.log(0.3), np.log(4.0), size=(dim, N))).astype(np.float32)
+    A[1, 2] = 0.0                                   # the A = 0 limit: dt * B
+    B = rng.standard_normal((bt, N, 1)).astype(np.float32)
+    C = rng.standard_normal((bt, N, 1)).astype(np.float32)
+    h0 = rng.standard_normal((bt, dim, N))
+    _, hl = orc.scan_dir(u, dt, A, B, C, None, None, None, False, h0, zoh=True)
+    for b in range(bt):
+        for d in range(dim):
+            for n in range(N):
+                # d/ds [h, 1] = [[A, B u], [0, 0]] [h, 1]  over s in [0, dt]
+                M = np.array([[float(A[d, n]), float(B[b, n, 0]) * float(u[b, d, 0])], [0.0, 0.0]])
+                e = expm(M * float(dt[b, d, 0])) @ np.array([h0[b, d, n], 1.0])
+                assert abs(e[0] - hl[b, d, n]) <= 1e-12 * max(1.0, abs(e[0])), (b, d, n)
+    # the simplified form differs from the hold wherever dt A is not small
+    _, hs = orc.scan_dir(u, dt, A, B, C, None, None, None, False, h0, zoh=False)
+    assert _rel(hs, hl) > 1e-3
+
+
 ALL_CHECKS = [
     check_bruteforce_rational,
     check_symbolic_two_steps,
@@ -516,4 +589,6 @@ ALL_CHECKS = [
     check_bwd_finite_differences,
     check_ssd_matches_mamba1,
     check_ssd_quadratic_and_chunked,
+    check_scan_dir_orders,
+    check_scan_zoh_exact_step,
 ]

@@ -61,6 +61,13 @@ MUTANTS = [
      "int64_t b = bh / H, h = bh % H, g = h % G;"),
     ("ssd_drop_D", "double yv = acc + (D ? (double)D[h] * xt : 0.0);", "double yv = acc;"),
     ("conv_update_wrong_weight", "acc += (double)w[d * width + hw] * xt;", "acc += (double)w[d * width] * xt;"),
+    ("dir_rows_cols_swapped", "if (order >= 2) return (k % rows) * cols + k / rows;",
+     "if (order >= 2) return (k % cols) * rows + k / cols;"),
+    ("dir_column_reverse_lost", "if (order == 1 || order == 3) k = L - 1 - k;", "if (order == 1) k = L - 1 - k;"),
+    ("zoh_sign", "double bbar = zoh ? (an != 0.0 ? expm1(dt * an) / an : dt) : dt;",
+     "double bbar = zoh ? (an != 0.0 ? -expm1(-dt * an) / an : dt) : dt;"),
+    ("zoh_zero_A_limit", "double bbar = zoh ? (an != 0.0 ? expm1(dt * an) / an : dt) : dt;",
+     "double bbar = zoh ? (an != 0.0 ? expm1(dt * an) / an : 0.0) : dt;"),
 ]
 
 
