@@ -487,7 +487,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-configs", action="store_true", help="skip timing the other prefill configs")
-    ap.add_argument("--only", choices=["scan", "decode", "conv", "conv_update", "scan_bwd", "ssd"],
+    ap.add_argument("--only", choices=["scan", "decode", "conv", "conv_update", "scan_bwd", "ssd", "scan_dir"],
                     help="time one entry point alone on --config (a kernel case for sweeps and ncu)")
     ap.add_argument("--config", default="mamba130m",
                     help="workload of --only: a prefill-scan config name, or 'decode'")
@@ -581,7 +581,7 @@ def main():
         # the conv that feeds the scan (prefill and decode update, HBM-bound) and the
         # scan's backward on the Mamba-130M-shaped layer
         for only, cfgname, steps in (("conv", None, 50), ("conv_update", None, 100), ("scan_bwd", "mamba130m", 5),
-                                     ("ssd", "ssd_5120", 10)):
+                                     ("ssd", "ssd_5120", 10), ("scan_dir", "vmamba56", 10)):
             rec = time_case(only, cfgname, "auto", steps, 3, device)
             configs_measured[only] = {k: rec[k] for k in ("case", "ms_median", "Gtokch_s", "GB_s", "hbm_frac")}
             if "tensor_TFLOP_s" in rec:
@@ -738,6 +738,22 @@ def time_case(only, config, algo, steps, warmup, dev):
         tokch = cfg.batch * cfg.dim
         nbytes = conv_update_bytes(cfg.batch, cfg.dim, cfg.width, 2, 2)
         label = f"causal_conv1d_update ({cfg.batch},{cfg.dim}) width={cfg.width}"
+    elif only == "scan_dir":
+        # the four-direction image scan: one timed unit runs all four traversals
+        cfg = W.CONFIGS["vmamba56"]
+        rows, cols = W.IMAGE_GRIDS["vmamba56"]
+        inp = W.make_scan_inputs(cfg)
+        t = scan_to_torch(inp, dev)
+        ys = [torch.empty((cfg.batch, cfg.dim, cfg.seqlen), dtype=torch.bfloat16, device=dev) for _ in range(4)]
+        hs = [torch.empty((cfg.batch, cfg.dim, cfg.dstate), dtype=torch.float32, device=dev) for _ in range(4)]
+
+        def launch():
+            for k, order in enumerate(("raster", "reverse", "columns", "columns_reverse")):
+                ssm.scan_fwd_dir(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], True,
+                                 None, order=order, rows=rows, cols=cols, y=ys[k], h_last=hs[k])
+        tokch = 4 * cfg.tokens_channels
+        nbytes = 4 * scan_bytes(cfg.batch, cfg.dim, cfg.seqlen, cfg.dstate, 2, 2, True, False)
+        label = f"scan_dir vmamba56 ({cfg.batch},{cfg.dim},{rows}x{cols},{cfg.dstate}) x 4 directions"
     elif only == "ssd":
         from workloads.torch_io import ssd_to_torch
         cfg = W.SSD_CONFIGS[config if config in W.SSD_CONFIGS else "ssd_5120"]

@@ -76,7 +76,8 @@ typedef enum {
     SSM_ERR_WIDTH = -12,            /* conv width not in 1..4 */
     SSM_ERR_SHAPE = -13,            /* SSD: headdim not 64, dstate not 64/128 or
                                        nheads not a multiple of ngroups */
-    SSM_ERR_WAIT_TIMEOUT = -14      /* device: an SSD tensor-core wait exhausted its budget */
+    SSM_ERR_WAIT_TIMEOUT = -14,     /* device: an SSD tensor-core wait exhausted its budget */
+    SSM_ERR_ORDER = -15             /* traversal order not in 0..3, or rows * cols != seqlen */
 } ssm_status_t;
 
 /* Algorithm selectors for ssm_scan_fwd_algo. All compute the same result.
@@ -236,6 +237,39 @@ SSM_API int ssm_causal_conv1d_update(float* conv_state, const void* x, const flo
                                      const float* bias, void* out, int64_t batch, int64_t dim,
                                      int64_t width, int silu, int in_dtype, int out_dtype,
                                      void* stream);
+
+/* The selective scan along another traversal of the sequence, and with the
+ * exact zero-order-hold input matrix as an option.
+ *
+ * Traversal (Mamba SSM complete guide (youngju.dev), section 9, VMamba: an image
+ * of rows x cols patches stored in raster order is scanned in four directions).
+ * Step k = 0 .. seqlen-1 of the recurrence visits sequence position pos(k):
+ *   SSM_ORDER_RASTER          (0)  pos(k) = k
+ *   SSM_ORDER_REVERSE         (1)  pos(k) = seqlen - 1 - k
+ *   SSM_ORDER_COLUMNS         (2)  pos(k) = (k % rows) * cols + k / rows
+ *   SSM_ORDER_COLUMNS_REVERSE (3)  the column order of step seqlen - 1 - k
+ * Every input is read at pos(k) and the step's output is written to y at pos(k),
+ * so each direction's y is in raster order (rows and cols are used by orders 2
+ * and 3 only, where rows * cols must equal seqlen). h0 is the state before the
+ * first visited step, h_last the state after the last.
+ * zoh != 0: the input matrix is the zero-order hold of the same guide's section
+ * 2 ("Discretization"), (dt A)^-1 (exp(dt A) - 1) dt B = (exp(dt A) - 1) / A * B
+ * per (d, n), and dt * B where A = 0; zoh == 0 gives ssm_scan_fwd's dt * B.
+ * Tensors, layouts and the remaining arguments are those of ssm_scan_fwd (no
+ * workspace: the warp-scan algorithm). Errors as ssm_scan_fwd, plus
+ * SSM_ERR_ORDER. */
+typedef enum {
+    SSM_ORDER_RASTER = 0,
+    SSM_ORDER_REVERSE = 1,
+    SSM_ORDER_COLUMNS = 2,
+    SSM_ORDER_COLUMNS_REVERSE = 3
+} ssm_order_t;
+
+SSM_API int ssm_scan_fwd_dir(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                             const float* D, const void* z, const float* delta_bias, int softplus,
+                             const float* h0, void* y, float* h_last, int64_t batch, int64_t dim,
+                             int64_t seqlen, int64_t dstate, int order, int64_t rows, int64_t cols, int zoh,
+                             int in_dtype, int out_dtype, void* stream);
 
 /* Mamba-2 state-space-duality (SSD) scan on the tensor cores (Mamba SSM
  * complete guide (youngju.dev), section 6 "Mamba 2": a multi-head SSM with one

@@ -68,6 +68,8 @@ _lib.ssm_ssd_scan_fwd.argtypes = [_P] * 8 + [_I, _P, _P, _P] + [_I64] * 6 + [_I,
 _lib.ssm_ssd_scan_fwd.restype = _I
 _lib.ssm_ssd_chunk_len.argtypes = []
 _lib.ssm_ssd_chunk_len.restype = _I64
+_lib.ssm_scan_fwd_dir.argtypes = [_P] * 8 + [_I, _P, _P, _P] + [_I64] * 4 + [_I, _I64, _I64, _I, _I, _I, _P]
+_lib.ssm_scan_fwd_dir.restype = _I
 _lib.ssm_device_status.argtypes = [_I, _P]
 _lib.ssm_device_status.restype = _I
 
@@ -78,6 +80,8 @@ SSM_ERR_SCRATCH_LIMIT = -11
 SSM_ERR_WIDTH = -12
 SSM_ERR_SHAPE = -13
 SSM_ERR_WAIT_TIMEOUT = -14
+SSM_ERR_ORDER = -15
+ORDERS = {"raster": 0, "reverse": 1, "columns": 2, "columns_reverse": 3}
 STATIC_SCRATCH_BYTES = 4 << 20   # SSM_STATIC_SCRATCH_BYTES
 
 # the C ABI entry-point names, as declared in include/ssm_scan.h
@@ -85,7 +89,7 @@ EXPORTS = ("ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_size", "s
            "ssm_scan_fwd_algo", "ssm_scalar_scan_fwd", "ssm_state_update",
            "ssm_test_lookback_timeout", "ssm_query_status", "ssm_scan_fwd_lookback_static",
            "ssm_causal_conv1d_fwd", "ssm_causal_conv1d_update", "ssm_scan_bwd_workspace_size",
-           "ssm_scan_bwd", "ssm_ssd_scan_fwd", "ssm_ssd_chunk_len", "ssm_device_status")
+           "ssm_scan_bwd", "ssm_ssd_scan_fwd", "ssm_ssd_chunk_len", "ssm_device_status", "ssm_scan_fwd_dir")
 
 
 class SSMError(RuntimeError):
@@ -184,6 +188,30 @@ def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, 
         _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
         int(bool(softplus)), _ptr(h0), _ptr(y), _ptr(h_last), bt, dim, L, N, in_code,
         _dtype_code(y.dtype), _ptr(workspace), _nbytes(workspace), ALGOS[algo], _stream())
+    _check(status)
+    return y, h_last
+
+
+def scan_fwd_dir(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, h0=None, *,
+                 order="raster", rows=0, cols=0, zoh=False, out_dtype=None, return_last_state=True, y=None,
+                 h_last=None):
+    """Selective scan along a traversal order ("raster", "reverse", "columns",
+    "columns_reverse" of a rows x cols image stored in raster order), outputs in
+    raster order; zoh selects the zero-order-hold input matrix. Shapes as scan_fwd."""
+    bt, dim, L = u.shape
+    N = A.shape[1]
+    in_code = _dtype_code(u.dtype)
+    _same(u, (("delta", delta, u.shape), ("B", B, (bt, N, L)), ("C", C, (bt, N, L)), ("z", z, u.shape)))
+    _f32(A, (dim, N), "A"); _f32(D, (dim,), "D"); _f32(delta_bias, (dim,), "delta_bias")
+    _f32(h0, (bt, dim, N), "h0")
+    if y is None:
+        y = torch.empty((bt, dim, L), dtype=out_dtype or u.dtype, device=u.device)
+    if h_last is None and return_last_state:
+        h_last = torch.empty((bt, dim, N), dtype=torch.float32, device=u.device)
+    status = _lib.ssm_scan_fwd_dir(
+        _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+        int(bool(softplus)), _ptr(h0), _ptr(y), _ptr(h_last), bt, dim, L, N, ORDERS[order] if isinstance(order, str)
+        else int(order), int(rows), int(cols), int(bool(zoh)), in_code, _dtype_code(y.dtype), _stream())
     _check(status)
     return y, h_last
 

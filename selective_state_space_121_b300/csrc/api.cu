@@ -124,9 +124,13 @@ int scan_impl(const void* u, const void* delta, const float* A, const void* B, c
               const float* h0, void* y, float* h_last, int64_t batch, int64_t dim,
               int64_t seqlen, int64_t dstate, int in_dtype, int out_dtype, void* workspace,
               size_t workspace_bytes, int algo, void* stream, int64_t drop_segment,
-              uint32_t spin_limit) {
+              uint32_t spin_limit, int order = -1, int64_t rows = 0, int64_t cols = 0, int zoh = 0) {
     if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype)) return SSM_ERR_DTYPE;
     if (batch < 0 || dim < 0 || seqlen < 0) return SSM_ERR_DIM;
+    // directional scans (order >= 0): the traversal must be one of the four and, for
+    // the column orders, cover the rows x cols image exactly
+    if (order >= 0 && (order > 3 || (order >= 2 && (rows < 1 || cols < 1 || mul(rows, cols) != seqlen))))
+        return SSM_ERR_ORDER;
     if (!valid_n(dstate)) return SSM_ERR_UNSUPPORTED_N;
     if (algo < SSM_ALGO_AUTO || algo > SSM_ALGO_LOOKBACK) return SSM_ERR_ALGO;
     const int64_t n_rows = mul(batch, dim);
@@ -175,6 +179,10 @@ int scan_impl(const void* u, const void* delta, const float* A, const void* B, c
     a.drop_segment = drop_segment;
     a.spin_limit = spin_limit;
     cudaStream_t s = (cudaStream_t)stream;
+    if (order >= 0) {
+        a.order = order; a.rows = rows; a.cols = cols; a.zoh = zoh ? 1 : 0;
+        return ssm::launch_scan_dir(a, s) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+    }
     if (p.algo == SSM_ALGO_LOOKBACK) {
         const size_t need = ssm::lookback_workspace_bytes(batch, dim, (int)dstate, p.n_seg);
         if (!workspace || workspace_bytes < need) return SSM_ERR_WORKSPACE;
@@ -216,6 +224,8 @@ const char* ssm_status_string(int status) {
         case SSM_ERR_SHAPE:
             return "SSM_ERR_SHAPE: SSD needs headdim 64, dstate 64 or 128 and nheads a multiple of ngroups";
         case SSM_ERR_WAIT_TIMEOUT: return "SSM_ERR_WAIT_TIMEOUT: a tensor-core wait exhausted its budget";
+        case SSM_ERR_ORDER:
+            return "SSM_ERR_ORDER: traversal order not in 0..3, or rows * cols != seqlen for a column order";
         case SSM_ERR_SCRATCH_LIMIT:
             return "SSM_ERR_SCRATCH_LIMIT: problem needs more scratch than the library's fixed 4 MiB area";
     }
@@ -532,6 +542,16 @@ int ssm_device_status(int clear, void* stream) {
     int line = 0;
     if (ssm::ssd_status(&line, clear != 0, (cudaStream_t)stream) != cudaSuccess) return SSM_ERR_LAUNCH;
     return line != 0 ? SSM_ERR_WAIT_TIMEOUT : SSM_OK;
+}
+
+int ssm_scan_fwd_dir(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                     const float* D, const void* z, const float* delta_bias, int softplus, const float* h0,
+                     void* y, float* h_last, int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                     int order, int64_t rows, int64_t cols, int zoh, int in_dtype, int out_dtype, void* stream) {
+    if (order < 0) return SSM_ERR_ORDER;
+    return scan_impl(u, delta, A, B, C, D, z, delta_bias, softplus, h0, y, h_last, batch, dim, seqlen, dstate,
+                     in_dtype, out_dtype, nullptr, 0, SSM_ALGO_WARPSCAN, stream, -1, kSpinLimit, order, rows, cols,
+                     zoh);
 }
 
 }  // extern "C"

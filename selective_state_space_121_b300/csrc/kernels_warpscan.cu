@@ -29,6 +29,16 @@
 //    Every a_t = exp(dt A) is evaluated exactly once.
 //  * The N-wide carry (state at the chunk boundary) lives in registers; across
 //    chunks it is carried serially by the warp.
+//
+// Directional form (launch_scan_dir, kDir): the same scan along another
+// traversal of the sequence -- the four scans of an image of rows x cols patches
+// stored in raster order (Mamba SSM complete guide, section 9, VMamba): raster,
+// reversed, column-major, reversed columns. Traversal step k reads every input
+// at position pos(k) and writes y there, so each direction's output is already
+// in raster order; the lanes still own consecutive traversal steps, with the
+// loads gathered by position. Optionally the input matrix is the exact
+// zero-order hold of section 2 ("Discretization"), (exp(dt A) - 1) / A * B
+// (dt * B where A = 0), from the decay already computed for the step.
 #include "common.cuh"
 #include "launch.h"
 
@@ -40,6 +50,13 @@ constexpr int T = kWarpScanChunk;     // 256 steps per chunk
 constexpr int W = 8;                  // warps (channels) per CTA
 constexpr int kThreads = 32 * W;
 
+// Sequence position of traversal step k (see the directional form above).
+__device__ __forceinline__ int64_t pos_of(const ScanArgs& a, int64_t k) {
+    if (a.order == 1 || a.order == 3) k = a.seqlen - 1 - k;
+    if (a.order >= 2) return (k % a.rows) * a.cols + k / a.rows;
+    return k;
+}
+
 template <int N>
 struct Smem {
     float B[N][T];
@@ -47,12 +64,23 @@ struct Smem {
 };
 
 // Stage B (and C) of batch row b, steps t0 .. t0+T-1, into shared memory as fp32.
-template <int N, typename Tin, bool kVec, bool kWithC>
+template <int N, typename Tin, bool kVec, bool kWithC, bool kDir = false>
 __device__ __forceinline__ void stage_bc(const ScanArgs& a, int64_t b, int64_t t0, Smem<N>& sm) {
     const Tin* Bp = static_cast<const Tin*>(a.B) + b * N * a.seqlen;
     const Tin* Cp = static_cast<const Tin*>(a.C) + b * N * a.seqlen;
     const int64_t L = a.seqlen;
-    if constexpr (kVec) {
+    if constexpr (kDir) {
+        // traversal steps t0 .. t0+T-1, gathered from their positions
+        for (int i = threadIdx.x; i < T; i += kThreads) {
+            const bool in = t0 + i < L;
+            const int64_t t = in ? pos_of(a, t0 + i) : 0;
+#pragma unroll
+            for (int n = 0; n < N; n++) {
+                sm.B[n][i] = in ? to_f32(Bp[n * L + t]) : 0.f;
+                if constexpr (kWithC) sm.C[n][i] = in ? to_f32(Cp[n * L + t]) : 0.f;
+            }
+        }
+    } else if constexpr (kVec) {
         constexpr int V = Vec16<Tin>::kN;
         constexpr int kVecs = N * T / V;
         for (int idx = threadIdx.x; idx < kVecs; idx += kThreads) {
@@ -128,15 +156,35 @@ __device__ __forceinline__ void store_items(Tout* row, int64_t t, int64_t L, con
     }
 }
 
+// The lane's K items at sequence positions pos[k] (-1: past the end, reads 0).
+template <typename Tin>
+__device__ __forceinline__ void load_at(const Tin* row, const int64_t* pos, float* out) {
+#pragma unroll
+    for (int k = 0; k < K; k++) out[k] = pos[k] >= 0 ? to_f32(row[pos[k]]) : 0.f;
+}
+template <typename Tout>
+__device__ __forceinline__ void store_at(Tout* row, const int64_t* pos, const float* v) {
+#pragma unroll
+    for (int k = 0; k < K; k++)
+        if (pos[k] >= 0) row[pos[k]] = from_f32<Tout>(v[k]);
+}
+
 // Per-lane step inputs of one chunk: dtl = dt*log2(e), bu = dt*u (zero past L).
-template <typename Tin, bool kVec>
+// kDir: items gathered from positions pos[] instead of steps t .. t+K-1.
+template <typename Tin, bool kVec, bool kDir = false>
 __device__ __forceinline__ float prepare_items(const ScanArgs& a, int64_t row_off, int64_t d,
-                                               int64_t t, float* dtl, float* bu, float* u) {
+                                               int64_t t, float* dtl, float* bu, float* u,
+                                               const int64_t* pos = nullptr) {
     const Tin* up = static_cast<const Tin*>(a.u) + row_off;
     const Tin* dp = static_cast<const Tin*>(a.delta) + row_off;
     float dl[K];
-    load_items<Tin, kVec>(up, t, a.seqlen, u);
-    load_items<Tin, kVec>(dp, t, a.seqlen, dl);
+    if constexpr (kDir) {
+        load_at<Tin>(up, pos, u);
+        load_at<Tin>(dp, pos, dl);
+    } else {
+        load_items<Tin, kVec>(up, t, a.seqlen, u);
+        load_items<Tin, kVec>(dp, t, a.seqlen, dl);
+    }
     const float bias = a.delta_bias ? a.delta_bias[d] : 0.f;
     float sdtl = 0.f;
 #pragma unroll
@@ -174,7 +222,7 @@ __device__ __forceinline__ void warp_scan_maps(float& P, float& H, int lane) {
 // large state is then rounded once per output instead of once per step, which
 // keeps the fp32 result within ~1e-6 of its scale over thousands of steps. With
 // bf16 inputs carry_lo stays zero and the plain recurrence runs.
-template <int N, typename Tin, typename Tout, bool kVec>
+template <int N, typename Tin, typename Tout, bool kVec, bool kDir = false>
 __device__ __forceinline__ void chunk_full(const ScanArgs& a, int64_t b, int64_t d, int64_t t0,
                                            const Smem<N>& sm, const float* Ad, float* carry,
                                            float* carry_lo, int lane) {
@@ -182,8 +230,14 @@ __device__ __forceinline__ void chunk_full(const ScanArgs& a, int64_t b, int64_t
     using Dec = Decay<kAnchored>;
     const int64_t row_off = (b * a.dim + d) * a.seqlen;
     const int64_t t = t0 + lane * K;
+    int64_t pos[K];
+    if constexpr (kDir) {
+#pragma unroll
+        for (int k = 0; k < K; k++) pos[k] = t + k < a.seqlen ? pos_of(a, t + k) : -1;
+    }
     float dtl[K], bu[K], u[K], y[K];
-    const float sdtl = prepare_items<Tin, kVec>(a, row_off, d, t, dtl, bu, u);
+    const float sdtl = prepare_items<Tin, kVec, kDir>(a, row_off, d, t, dtl, bu, u, pos);
+    const bool zoh = kDir && a.zoh;
 #pragma unroll
     for (int k = 0; k < K; k++) y[k] = 0.f;
 #pragma unroll
@@ -192,10 +246,14 @@ __device__ __forceinline__ void chunk_full(const ScanArgs& a, int64_t b, int64_t
         const float* sc = &sm.C[n][lane * K];
         float an[K], bn[K];
         float H = 0.f;
+        // zero-order hold: (a - 1) / A replaces dt (a - 1 is what the fp32 form carries)
+        const bool hold = zoh && Ad[n] != 0.f;
+        const float inv_a = hold ? 1.f / Ad[n] : 0.f;
 #pragma unroll
         for (int k = 0; k < K; k++) {
             an[k] = Dec::make(dtl[k] * Ad[n]);
-            bn[k] = bu[k] * sb[k];
+            if (hold) bn[k] = (kAnchored ? an[k] : an[k] - 1.f) * inv_a * u[k] * sb[k];
+            else bn[k] = bu[k] * sb[k];
             H = Dec::step(an[k], H, bn[k]);
         }
         float P = Dec::make(sdtl * Ad[n]);
@@ -228,14 +286,16 @@ __device__ __forceinline__ void chunk_full(const ScanArgs& a, int64_t b, int64_t
     const float Dd = a.D ? a.D[d] : 0.f;
     if (a.z) {
         float zz[K];
-        load_items<Tin, kVec>(static_cast<const Tin*>(a.z) + row_off, t, a.seqlen, zz);
+        if constexpr (kDir) load_at<Tin>(static_cast<const Tin*>(a.z) + row_off, pos, zz);
+        else load_items<Tin, kVec>(static_cast<const Tin*>(a.z) + row_off, t, a.seqlen, zz);
 #pragma unroll
         for (int k = 0; k < K; k++) y[k] = fmaf(Dd, u[k], y[k]) * silu(zz[k]);
     } else {
 #pragma unroll
         for (int k = 0; k < K; k++) y[k] = fmaf(Dd, u[k], y[k]);
     }
-    store_items<Tout, kVec>(static_cast<Tout*>(a.y) + row_off, t, a.seqlen, y);
+    if constexpr (kDir) store_at<Tout>(static_cast<Tout*>(a.y) + row_off, pos, y);
+    else store_items<Tout, kVec>(static_cast<Tout*>(a.y) + row_off, t, a.seqlen, y);
 }
 
 template <int N>
@@ -266,7 +326,7 @@ __device__ __forceinline__ void store_hlast(const ScanArgs& a, int64_t b, int64_
 // Serial-carry kernel: grid (ceil(dim / 8), batch); each warp walks its
 // channel's whole sequence chunk by chunk.
 // ---------------------------------------------------------------------------
-template <int N, typename Tin, typename Tout, bool kVec>
+template <int N, typename Tin, typename Tout, bool kVec, bool kDir = false>
 __global__ void __launch_bounds__(kThreads) warp_scan_kernel(ScanArgs a) {
     __shared__ __align__(16) Smem<N> sm;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -279,31 +339,33 @@ __global__ void __launch_bounds__(kThreads) warp_scan_kernel(ScanArgs a) {
         load_h0<N>(a, b, d, carry, carry_lo);
     }
     for (int64_t t0 = 0; t0 < a.seqlen; t0 += T) {
-        stage_bc<N, Tin, kVec, true>(a, b, t0, sm);
+        stage_bc<N, Tin, kVec, true, kDir>(a, b, t0, sm);
         __syncthreads();
-        if (active) chunk_full<N, Tin, Tout, kVec>(a, b, d, t0, sm, Ad, carry, carry_lo, lane);
+        if (active) chunk_full<N, Tin, Tout, kVec, kDir>(a, b, d, t0, sm, Ad, carry, carry_lo, lane);
         __syncthreads();
     }
     if (active) store_hlast<N>(a, b, d, carry, carry_lo, lane);
 }
 
-template <int N, typename Tin, typename Tout>
+template <int N, typename Tin, typename Tout, bool kDir>
 cudaError_t launch_ws_n(const ScanArgs& a, cudaStream_t s) {
     if (a.batch == 0 || a.dim == 0) return cudaSuccess;
     dim3 grid((unsigned)((a.dim + W - 1) / W), (unsigned)a.batch);
-    if (a.vec) warp_scan_kernel<N, Tin, Tout, true><<<grid, kThreads, 0, s>>>(a);
+    // the raster order with dt * B is the plain scan: its vectorised form
+    if (kDir && (a.order != 0 || a.zoh)) warp_scan_kernel<N, Tin, Tout, false, true><<<grid, kThreads, 0, s>>>(a);
+    else if (a.vec) warp_scan_kernel<N, Tin, Tout, true><<<grid, kThreads, 0, s>>>(a);
     else warp_scan_kernel<N, Tin, Tout, false><<<grid, kThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
-template <typename Tin, typename Tout>
+template <typename Tin, typename Tout, bool kDir = false>
 cudaError_t dispatch_n(const ScanArgs& a, cudaStream_t s) {
     switch (a.dstate) {
-        case 1: return launch_ws_n<1, Tin, Tout>(a, s);
-        case 2: return launch_ws_n<2, Tin, Tout>(a, s);
-        case 4: return launch_ws_n<4, Tin, Tout>(a, s);
-        case 8: return launch_ws_n<8, Tin, Tout>(a, s);
-        case 16: return launch_ws_n<16, Tin, Tout>(a, s);
+        case 1: return launch_ws_n<1, Tin, Tout, kDir>(a, s);
+        case 2: return launch_ws_n<2, Tin, Tout, kDir>(a, s);
+        case 4: return launch_ws_n<4, Tin, Tout, kDir>(a, s);
+        case 8: return launch_ws_n<8, Tin, Tout, kDir>(a, s);
+        case 16: return launch_ws_n<16, Tin, Tout, kDir>(a, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -315,6 +377,13 @@ cudaError_t launch_scan_warp(const ScanArgs& a, cudaStream_t s) {
         return a.out_dtype == kBF16 ? dispatch_n<__nv_bfloat16, __nv_bfloat16>(a, s)
                                     : dispatch_n<__nv_bfloat16, float>(a, s);
     return a.out_dtype == kBF16 ? dispatch_n<float, __nv_bfloat16>(a, s) : dispatch_n<float, float>(a, s);
+}
+
+cudaError_t launch_scan_dir(const ScanArgs& a, cudaStream_t s) {
+    if (a.in_dtype == kBF16)
+        return a.out_dtype == kBF16 ? dispatch_n<__nv_bfloat16, __nv_bfloat16, true>(a, s)
+                                    : dispatch_n<__nv_bfloat16, float, true>(a, s);
+    return a.out_dtype == kBF16 ? dispatch_n<float, __nv_bfloat16, true>(a, s) : dispatch_n<float, float, true>(a, s);
 }
 
 }  // namespace ssm

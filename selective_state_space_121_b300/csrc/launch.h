@@ -32,6 +32,12 @@ struct ScanArgs {
     int64_t n_seg;
     uint32_t spin_limit;
     int64_t drop_segment;   // test hook: this segment withholds its publication (-1: none)
+    // directional scans (launch_scan_dir only): traversal order 0 raster, 1 reversed,
+    // 2 column-major of a rows x cols image, 3 reversed columns; zoh: exact
+    // zero-order-hold input matrix (exp(dt A) - 1) / A * B instead of dt * B
+    int order;
+    int64_t rows, cols;
+    int zoh;
 };
 
 struct DecodeArgs {
@@ -133,6 +139,7 @@ cudaError_t launch_conv_update(const ConvArgs& a, cudaStream_t s);
 int conv_block_steps(int in_dtype);
 cudaError_t launch_state_update(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_scan_warp(const ScanArgs& a, cudaStream_t s);
+cudaError_t launch_scan_dir(const ScanArgs& a, cudaStream_t s);
 cudaError_t launch_scan_serial_lookback(const ScanArgs& a, int lanes_per_channel, cudaStream_t s);
 // channels one CTA of the look-back kernel covers (its segments are planned with it)
 int lookback_channels_per_cta(int dstate, int lanes_per_channel, int in_dtype);

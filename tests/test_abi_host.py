@@ -43,7 +43,7 @@ def test_abi_version_matches_header(ssm):
 
 
 def test_status_strings(ssm):
-    for code in range(0, -15, -1):
+    for code in range(0, -16, -1):
         assert ssm.status_string(code).startswith("SSM_")
     assert not ssm.status_string(-99).startswith("SSM_")
 
@@ -184,3 +184,25 @@ def test_ssd_validation(ssm):
     assert call(h0=FAKE * 7, hl=FAKE * 7 + 4) == -9    # partly over the initial state
     assert call(batch=1 << 40, H=1 << 30) == -2
     assert ssm._lib.ssm_ssd_chunk_len() == 128
+
+
+def test_scan_dir_validation(ssm):
+    """Argument errors of ssm_scan_fwd_dir come back before any launch (no GPU needed)."""
+    f = ssm._lib.ssm_scan_fwd_dir
+
+    def call(**kw):
+        a = dict(u=FAKE, d=FAKE * 2, A=FAKE * 3, B=FAKE * 4, C=FAKE * 5, D=None, z=None, bias=None, sp=1, h0=None,
+                 y=FAKE * 6, hl=None, batch=2, dim=4, L=12, N=16, order=2, rows=3, cols=4, zoh=0, idt=1, odt=1)
+        a.update(kw)
+        return f(a["u"], a["d"], a["A"], a["B"], a["C"], a["D"], a["z"], a["bias"], a["sp"], a["h0"], a["y"],
+                 a["hl"], a["batch"], a["dim"], a["L"], a["N"], a["order"], a["rows"], a["cols"], a["zoh"], a["idt"],
+                 a["odt"], None)
+    assert call(order=4) == -15
+    assert call(order=-1) == -15
+    assert call(order=2, rows=5, cols=4) == -15        # rows * cols != seqlen
+    assert call(order=3, rows=0, cols=12) == -15
+    assert call(N=3) == -8
+    assert call(idt=7) == -3
+    assert call(u=None) == -1
+    assert call(y=FAKE + 16) == -9                     # y overlaps u
+    assert call(batch=1 << 40, dim=1 << 30) == -2

@@ -90,7 +90,14 @@ CONFIGS = {
     # long context, small batch x channels
     "long": ScanConfig("long", 1, 1536, 131072, 16, BF16, BF16, True, True, True, "zero",
                        "s4d_real", 4500),
+    # the four-direction image scan: a 56 x 56 patch grid (3136 tokens in raster
+    # order), 192 scan channels (a 96-wide embedding, expand 2), batch 8
+    "vmamba56": ScanConfig("vmamba56", 8, 192, 56 * 56, 16, BF16, BF16, True, True, True, "zero",
+                           "s4d_real", 9000),
 }
+
+# image grid (rows, cols) of the directional-scan workloads (seqlen = rows * cols)
+IMAGE_GRIDS = {"vmamba56": (56, 56)}
 
 DECODE_CONFIGS = {
     "decode": DecodeConfig("decode", 256, 5120, 16, BF16, BF16, 1000, 16, 5000),
