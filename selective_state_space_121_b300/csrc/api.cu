@@ -131,6 +131,7 @@ int scan_impl(const void* u, const void* delta, const float* A, const void* B, c
     // the column orders, cover the rows x cols image exactly
     if (order >= 0 && (order > 3 || (order >= 2 && (rows < 1 || cols < 1 || mul(rows, cols) != seqlen))))
         return SSM_ERR_ORDER;
+    if (order >= 0 && seqlen >= ((int64_t)1 << 31)) return SSM_ERR_DIM;   // 32-bit traversal positions
     if (!valid_n(dstate)) return SSM_ERR_UNSUPPORTED_N;
     if (algo < SSM_ALGO_AUTO || algo > SSM_ALGO_LOOKBACK) return SSM_ERR_ALGO;
     const int64_t n_rows = mul(batch, dim);

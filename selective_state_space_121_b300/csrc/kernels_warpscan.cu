@@ -50,11 +50,43 @@ constexpr int T = kWarpScanChunk;     // 256 steps per chunk
 constexpr int W = 8;                  // warps (channels) per CTA
 constexpr int kThreads = 32 * W;
 
-// Sequence position of traversal step k (see the directional form above).
+// Sequence position of traversal step k (see the directional form above);
+// seqlen < 2^31 for the directional form, so 32-bit arithmetic.
 __device__ __forceinline__ int64_t pos_of(const ScanArgs& a, int64_t k) {
-    if (a.order == 1 || a.order == 3) k = a.seqlen - 1 - k;
-    if (a.order >= 2) return (k % a.rows) * a.cols + k / a.rows;
-    return k;
+    uint32_t kk = (uint32_t)k;
+    if (a.order == 1 || a.order == 3) kk = (uint32_t)a.seqlen - 1u - kk;
+    if (a.order >= 2) {
+        const uint32_t rows = (uint32_t)a.rows, q = kk / rows;
+        return (int64_t)(kk - q * rows) * a.cols + q;
+    }
+    return kk;
+}
+// Positions of K consecutive traversal steps k0 .. k0+K-1 (-1 past the end): one
+// division, then the column walk steps row by row.
+__device__ __forceinline__ void positions(const ScanArgs& a, int64_t k0, int64_t* pos) {
+    const uint32_t L = (uint32_t)a.seqlen;
+    if (a.order < 2) {
+#pragma unroll
+        for (int k = 0; k < K; k++) {
+            const uint32_t kk = (uint32_t)k0 + k;
+            pos[k] = kk < L ? (a.order == 1 ? (int64_t)(L - 1u - kk) : (int64_t)kk) : -1;
+        }
+        return;
+    }
+    const uint32_t rows = (uint32_t)a.rows;
+    const bool rev = a.order == 3;
+    uint32_t kk = (uint32_t)k0 < L ? (uint32_t)k0 : 0u;
+    if (rev) kk = L - 1u - kk;
+    uint32_t q = kk / rows, r = kk - q * rows;   // column q, row r
+#pragma unroll
+    for (int k = 0; k < K; k++) {
+        pos[k] = (uint32_t)k0 + k < L ? (int64_t)r * a.cols + q : -1;
+        if (!rev) {
+            if (++r == rows) { r = 0; ++q; }
+        } else {
+            if (r == 0) { r = rows - 1u; --q; } else { --r; }
+        }
+    }
 }
 
 template <int N>
@@ -231,10 +263,7 @@ __device__ __forceinline__ void chunk_full(const ScanArgs& a, int64_t b, int64_t
     const int64_t row_off = (b * a.dim + d) * a.seqlen;
     const int64_t t = t0 + lane * K;
     int64_t pos[K];
-    if constexpr (kDir) {
-#pragma unroll
-        for (int k = 0; k < K; k++) pos[k] = t + k < a.seqlen ? pos_of(a, t + k) : -1;
-    }
+    if constexpr (kDir) positions(a, t, pos);
     float dtl[K], bu[K], u[K], y[K];
     const float sdtl = prepare_items<Tin, kVec, kDir>(a, row_off, d, t, dtl, bu, u, pos);
     const bool zoh = kDir && a.zoh;
