@@ -101,7 +101,33 @@ __device__ __forceinline__ void stage_bc(const ScanArgs& a, int64_t b, int64_t t
     const Tin* Bp = static_cast<const Tin*>(a.B) + b * N * a.seqlen;
     const Tin* Cp = static_cast<const Tin*>(a.C) + b * N * a.seqlen;
     const int64_t L = a.seqlen;
-    if constexpr (kDir) {
+    if (kDir && a.vec && a.order == 1) {
+        // reversed raster: steps t0+i0 .. t0+i0+V-1 are the V positions ending at
+        // L-1-(t0+i0), one aligned 16-byte block (L is a multiple of V when rows
+        // are 16-byte aligned), stored reversed
+        constexpr int V = Vec16<Tin>::kN;
+        for (int idx = threadIdx.x; idx < N * T / V; idx += kThreads) {
+            const int n = idx / (T / V);
+            const int i0 = (idx % (T / V)) * V;
+            const int64_t kk = t0 + i0;
+            float vb[V], vc[V];
+            if (kk + V <= L) {
+                Vec16<Tin>::load(Bp + n * L + (L - V - kk), vb);
+                if constexpr (kWithC) Vec16<Tin>::load(Cp + n * L + (L - V - kk), vc);
+            } else {
+#pragma unroll
+                for (int j = 0; j < V; j++) {   // reversed below, so index by V-1-j
+                    vb[V - 1 - j] = kk + j < L ? to_f32(Bp[n * L + (L - 1 - kk - j)]) : 0.f;
+                    if constexpr (kWithC) vc[V - 1 - j] = kk + j < L ? to_f32(Cp[n * L + (L - 1 - kk - j)]) : 0.f;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < V; j++) {
+                sm.B[n][i0 + j] = vb[V - 1 - j];
+                if constexpr (kWithC) sm.C[n][i0 + j] = vc[V - 1 - j];
+            }
+        }
+    } else if (kDir && !(a.vec && a.order == 0)) {
         // traversal steps t0 .. t0+T-1, gathered from their positions
         for (int i = threadIdx.x; i < T; i += kThreads) {
             const bool in = t0 + i < L;
@@ -112,7 +138,7 @@ __device__ __forceinline__ void stage_bc(const ScanArgs& a, int64_t b, int64_t t
                 if constexpr (kWithC) sm.C[n][i] = in ? to_f32(Cp[n * L + t]) : 0.f;
             }
         }
-    } else if constexpr (kVec) {
+    } else if (kVec || (kDir && a.vec)) {
         constexpr int V = Vec16<Tin>::kN;
         constexpr int kVecs = N * T / V;
         for (int idx = threadIdx.x; idx < kVecs; idx += kThreads) {
@@ -201,8 +227,43 @@ __device__ __forceinline__ void store_at(Tout* row, const int64_t* pos, const fl
         if (pos[k] >= 0) row[pos[k]] = from_f32<Tout>(v[k]);
 }
 
+// Directional loads and stores of the lane's K items (steps t .. t+K-1): with
+// 16-byte aligned rows the raster order reads them as consecutive positions and
+// the reversed order as the block ending at L-1-t, reversed in registers; any
+// other case gathers by position.
+template <typename Tin>
+__device__ __forceinline__ void load_dir(const ScanArgs& a, const Tin* row, int64_t t, const int64_t* pos,
+                                         float* out) {
+    const int64_t L = a.seqlen;
+    if (a.vec && a.order == 0) {
+        load_items<Tin, true>(row, t, L, out);
+    } else if (a.vec && a.order == 1 && t + K <= L) {
+        float tmp[K];
+        load_items<Tin, true>(row, L - K - t, L, tmp);
+#pragma unroll
+        for (int k = 0; k < K; k++) out[k] = tmp[K - 1 - k];
+    } else {
+        load_at<Tin>(row, pos, out);
+    }
+}
+template <typename Tout>
+__device__ __forceinline__ void store_dir(const ScanArgs& a, Tout* row, int64_t t, const int64_t* pos,
+                                          const float* v) {
+    const int64_t L = a.seqlen;
+    if (a.vec && a.order == 0) {
+        store_items<Tout, true>(row, t, L, v);
+    } else if (a.vec && a.order == 1 && t + K <= L) {
+        float tmp[K];
+#pragma unroll
+        for (int k = 0; k < K; k++) tmp[k] = v[K - 1 - k];
+        store_items<Tout, true>(row, L - K - t, L, tmp);
+    } else {
+        store_at<Tout>(row, pos, v);
+    }
+}
+
 // Per-lane step inputs of one chunk: dtl = dt*log2(e), bu = dt*u (zero past L).
-// kDir: items gathered from positions pos[] instead of steps t .. t+K-1.
+// kDir: items of the traversal (load_dir) instead of steps t .. t+K-1.
 template <typename Tin, bool kVec, bool kDir = false>
 __device__ __forceinline__ float prepare_items(const ScanArgs& a, int64_t row_off, int64_t d,
                                                int64_t t, float* dtl, float* bu, float* u,
@@ -211,8 +272,8 @@ __device__ __forceinline__ float prepare_items(const ScanArgs& a, int64_t row_of
     const Tin* dp = static_cast<const Tin*>(a.delta) + row_off;
     float dl[K];
     if constexpr (kDir) {
-        load_at<Tin>(up, pos, u);
-        load_at<Tin>(dp, pos, dl);
+        load_dir<Tin>(a, up, t, pos, u);
+        load_dir<Tin>(a, dp, t, pos, dl);
     } else {
         load_items<Tin, kVec>(up, t, a.seqlen, u);
         load_items<Tin, kVec>(dp, t, a.seqlen, dl);
@@ -254,7 +315,7 @@ __device__ __forceinline__ void warp_scan_maps(float& P, float& H, int lane) {
 // large state is then rounded once per output instead of once per step, which
 // keeps the fp32 result within ~1e-6 of its scale over thousands of steps. With
 // bf16 inputs carry_lo stays zero and the plain recurrence runs.
-template <int N, typename Tin, typename Tout, bool kVec, bool kDir = false>
+template <int N, typename Tin, typename Tout, bool kVec, bool kDir = false, bool kZoh = false>
 __device__ __forceinline__ void chunk_full(const ScanArgs& a, int64_t b, int64_t d, int64_t t0,
                                            const Smem<N>& sm, const float* Ad, float* carry,
                                            float* carry_lo, int lane) {
@@ -266,7 +327,7 @@ __device__ __forceinline__ void chunk_full(const ScanArgs& a, int64_t b, int64_t
     if constexpr (kDir) positions(a, t, pos);
     float dtl[K], bu[K], u[K], y[K];
     const float sdtl = prepare_items<Tin, kVec, kDir>(a, row_off, d, t, dtl, bu, u, pos);
-    const bool zoh = kDir && a.zoh;
+
 #pragma unroll
     for (int k = 0; k < K; k++) y[k] = 0.f;
 #pragma unroll
@@ -276,7 +337,7 @@ __device__ __forceinline__ void chunk_full(const ScanArgs& a, int64_t b, int64_t
         float an[K], bn[K];
         float H = 0.f;
         // zero-order hold: (a - 1) / A replaces dt (a - 1 is what the fp32 form carries)
-        const bool hold = zoh && Ad[n] != 0.f;
+        const bool hold = kZoh && Ad[n] != 0.f;
         const float inv_a = hold ? 1.f / Ad[n] : 0.f;
 #pragma unroll
         for (int k = 0; k < K; k++) {
@@ -315,7 +376,7 @@ __device__ __forceinline__ void chunk_full(const ScanArgs& a, int64_t b, int64_t
     const float Dd = a.D ? a.D[d] : 0.f;
     if (a.z) {
         float zz[K];
-        if constexpr (kDir) load_at<Tin>(static_cast<const Tin*>(a.z) + row_off, pos, zz);
+        if constexpr (kDir) load_dir<Tin>(a, static_cast<const Tin*>(a.z) + row_off, t, pos, zz);
         else load_items<Tin, kVec>(static_cast<const Tin*>(a.z) + row_off, t, a.seqlen, zz);
 #pragma unroll
         for (int k = 0; k < K; k++) y[k] = fmaf(Dd, u[k], y[k]) * silu(zz[k]);
@@ -323,7 +384,7 @@ __device__ __forceinline__ void chunk_full(const ScanArgs& a, int64_t b, int64_t
 #pragma unroll
         for (int k = 0; k < K; k++) y[k] = fmaf(Dd, u[k], y[k]);
     }
-    if constexpr (kDir) store_at<Tout>(static_cast<Tout*>(a.y) + row_off, pos, y);
+    if constexpr (kDir) store_dir<Tout>(a, static_cast<Tout*>(a.y) + row_off, t, pos, y);
     else store_items<Tout, kVec>(static_cast<Tout*>(a.y) + row_off, t, a.seqlen, y);
 }
 
@@ -355,8 +416,10 @@ __device__ __forceinline__ void store_hlast(const ScanArgs& a, int64_t b, int64_
 // Serial-carry kernel: grid (ceil(dim / 8), batch); each warp walks its
 // channel's whole sequence chunk by chunk.
 // ---------------------------------------------------------------------------
-template <int N, typename Tin, typename Tout, bool kVec, bool kDir = false>
-__global__ void __launch_bounds__(kThreads) warp_scan_kernel(ScanArgs a) {
+// Two CTAs per SM (128 registers): at the few-channel shapes this algorithm serves,
+// latency is hidden by warps, and the grid then fits one round more often.
+template <int N, typename Tin, typename Tout, bool kVec, bool kDir = false, bool kZoh = false>
+__global__ void __launch_bounds__(kThreads, 2) warp_scan_kernel(ScanArgs a) {
     __shared__ __align__(16) Smem<N> sm;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t b = blockIdx.y;
@@ -370,7 +433,7 @@ __global__ void __launch_bounds__(kThreads) warp_scan_kernel(ScanArgs a) {
     for (int64_t t0 = 0; t0 < a.seqlen; t0 += T) {
         stage_bc<N, Tin, kVec, true, kDir>(a, b, t0, sm);
         __syncthreads();
-        if (active) chunk_full<N, Tin, Tout, kVec, kDir>(a, b, d, t0, sm, Ad, carry, carry_lo, lane);
+        if (active) chunk_full<N, Tin, Tout, kVec, kDir, kZoh>(a, b, d, t0, sm, Ad, carry, carry_lo, lane);
         __syncthreads();
     }
     if (active) store_hlast<N>(a, b, d, carry, carry_lo, lane);
@@ -381,7 +444,8 @@ cudaError_t launch_ws_n(const ScanArgs& a, cudaStream_t s) {
     if (a.batch == 0 || a.dim == 0) return cudaSuccess;
     dim3 grid((unsigned)((a.dim + W - 1) / W), (unsigned)a.batch);
     // the raster order with dt * B is the plain scan: its vectorised form
-    if (kDir && (a.order != 0 || a.zoh)) warp_scan_kernel<N, Tin, Tout, false, true><<<grid, kThreads, 0, s>>>(a);
+    if (kDir && a.zoh) warp_scan_kernel<N, Tin, Tout, false, true, true><<<grid, kThreads, 0, s>>>(a);
+    else if (kDir && a.order != 0) warp_scan_kernel<N, Tin, Tout, false, true, false><<<grid, kThreads, 0, s>>>(a);
     else if (a.vec) warp_scan_kernel<N, Tin, Tout, true><<<grid, kThreads, 0, s>>>(a);
     else warp_scan_kernel<N, Tin, Tout, false><<<grid, kThreads, 0, s>>>(a);
     return cudaGetLastError();
