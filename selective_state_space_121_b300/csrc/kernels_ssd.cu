@@ -32,8 +32,9 @@
 // accuracy. With plain bf16 rounding the state's relative error of 2^-9 per
 // chunk accumulates over its memory and leaves y far outside a 2e-3 bound.
 //
-// One CTA of 256 threads per (b, h), walking the chunks in order. Warp w reaches
-// tensor-memory lanes 32 (w % 4) .. +31 and works on column half w / 4.
+// One CTA per (b, h), walking the chunks in order: sixteen compute warps (warp w
+// reaches tensor-memory lanes 32 (w % 4) .. +31 and works on column quarter w / 4)
+// and one control warp.
 // Tensor memory (256 columns): S and then Ye in [0, 128), Yi in [128, 192),
 // H^T in [192, 256). The tiles TMA moves (C, B, x, z in; y out) are 128-row tiles
 // of 128-byte rows with 128-byte swizzling (one box per 64 columns); the tiles
@@ -58,8 +59,11 @@ namespace {
 
 constexpr int kQ = 128;               // chunk length (steps)
 constexpr int kP = 64;                // head channels
-constexpr int kCompute = 256;       // eight compute warps
-constexpr int kCtl = 8;             // the control warp: TMA copies and MMA issue
+constexpr int kCompute = 512;       // sixteen compute warps
+constexpr int kCtl = kCompute / 32; // the control warp: TMA copies and MMA issue
+constexpr int kParts = kCompute / 128;   // column parts: warps per tensor-memory lane quarter
+constexpr int kPc = kP / kParts;         // head channels (state / output columns) per warp: 16
+constexpr int kSc = kQ / kParts;         // columns of S / M per warp: 32
 constexpr int kThreads = kCompute + 32;
 constexpr uint32_t kWaitLimit = 1u << 24;
 constexpr uint32_t kStrideC = 2048;   // bytes between column groups of a 128-row tile
@@ -137,12 +141,12 @@ __device__ __forceinline__ void unpack8(uint4 v, float* out) {
 }
 
 // Barrier among the eight compute warps only (named barrier 1).
-__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 // The same barrier, returning on every compute thread whether v held on any.
 __device__ __forceinline__ bool compute_any(bool v) {
     uint32_t r;
     asm volatile(
-        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, 512, p;\n selp.u32 %0, 1, 0, q;\n}\n"
         : "=r"(r)
         : "r"((uint32_t)v)
         : "memory");
@@ -157,9 +161,9 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
     return false;
 }
 
-// Roles. Warps 0-7 compute (warp w owns tensor-memory lanes 32 (w % 4) .. +31 and
-// column half w / 4); warp 8 (the control warp) issues every TMA copy and every
-// MMA. The two sides meet only through mbarriers, every wait bounded:
+// Roles. Warps 0-15 compute (warp w owns tensor-memory lanes 32 (w % 4) .. +31 and
+// column quarter w / 4); warp 16 (the control warp) issues every TMA copy and
+// every MMA. The two sides meet only through mbarriers, every wait bounded:
 //   TMA -> all        s_load (inputs of a stage), s_zload (z)
 //   MMA -> compute    s_bar[0] G1 done, s_bar[1] G3 + G4 done, s_bar[2] G2 done
 //   compute -> ctl    s_ready[0] w o x and the rescaled state written,
@@ -184,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int quad = warp & 3, half = warp >> 2;
+    const int quad = warp & 3, part = warp >> 2;   // lane quarter, column part
     // the swizzled tiles need a 1024-byte aligned base
     if (tc::smem_u32(smem) & 1023u) {
         if (tid == 0) atomicExch(&g_ssd_status, __LINE__);
@@ -465,22 +469,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         // initial state: H^T[n][p] = h0[b,h,p,n] (zero for n >= N or without h0): split
         // for G3, and resident rescaled by chunk 0's total decay for G4
         {
-            float v[32];
+            float v[kPc];
 #pragma unroll
-            for (int j = 0; j < 32; j++) {
-                const int p = 32 * half + j;
+            for (int j = 0; j < kPc; j++) {
+                const int p = kPc * part + j;
                 v[j] = (a.h0 && row < kN) ? a.h0[(bh * kP + p) * kN + row] : 0.f;
             }
             if (row < kN) {
 #pragma unroll
-                for (int k = 0; k < 4; k++)
-                    split_store8(v + 8 * k, sHh + (4 * half + k) * S::kStrideH + row * 16,
-                                 sHl + (4 * half + k) * S::kStrideH + row * 16);
+                for (int k = 0; k < kPc / 8; k++)
+                    split_store8(v + 8 * k, sHh + ((kPc / 8) * part + k) * S::kStrideH + row * 16,
+                                 sHl + ((kPc / 8) * part + k) * S::kStrideH + row * 16);
             }
             const float e0 = nchunks > 0 ? ex2(s_cs2[0][kQ - 1]) : 1.f;
 #pragma unroll
-            for (int j = 0; j < 32; j++) v[j] *= e0;
-            tc::tmem_st32(tmem + lane_base + kColH + 32 * half, v);
+            for (int j = 0; j < kPc; j++) v[j] *= e0;
+            tc::tmem_st16(tmem + lane_base + kColH + kPc * part, v);
             tc::tmem_wait_st();
         }
         for (int64_t c = 0; c < nchunks; c++) {
@@ -532,8 +536,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // a 32-column block is, for this warp's 32 rows, all above the
                 // diagonal (zeros), all on or below it (no mask), or crossing it
 #pragma unroll
-                for (int blk = 0; blk < 2; blk++) {
-                    const int s0 = 64 * half + 32 * blk;
+                for (int blk = 0; blk < kSc / 32; blk++) {
+                    const int s0 = kSc * part + 32 * blk;
                     if (s0 > 32 * quad + 31) {
                         const uint4 zero = make_uint4(0, 0, 0, 0);
 #pragma unroll
@@ -583,18 +587,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc::fence_after_sync();
             {
-                float yi[32], ye[32];
-                tc::tmem_ld32(tmem + lane_base + kColYi + 32 * half, yi);
-                tc::tmem_ld32(tmem + lane_base + kColYe + 32 * half, ye);
+                float yi[kPc], ye[kPc];
+                tc::tmem_ld16(tmem + lane_base + kColYi + kPc * part, yi);
+                tc::tmem_ld16(tmem + lane_base + kColYe + kPc * part, ye);
                 tc::tmem_wait_ld();
                 const float e = ex2(cs2[row]);   // exp(cs_t)
-                float out[32];
+                float out[kPc];
 #pragma unroll
-                for (int k = 0; k < 4; k++) {
+                for (int k = 0; k < kPc / 8; k++) {
                     float xv[8];
-                    unpack8(*reinterpret_cast<const uint4*>(stg + S::kX + tc::sw128(row, 4 * half + k)), xv);
+                    unpack8(*reinterpret_cast<const uint4*>(stg + S::kX + tc::sw128(row, (kPc / 8) * part + k)), xv);
                     float zv[8];
-                    if (zg) unpack8(*reinterpret_cast<const uint4*>(smem + S::kZ + tc::sw128(row, 4 * half + k)), zv);
+                    if (zg)
+                        unpack8(*reinterpret_cast<const uint4*>(smem + S::kZ + tc::sw128(row, (kPc / 8) * part + k)),
+                                zv);
 #pragma unroll
                     for (int i = 0; i < 8; i++) {
                         float yv = fmaf(e, ye[8 * k + i], yi[8 * k + i]);
@@ -605,34 +611,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // rows past seqlen are staged too; the store drops them
                 unsigned char* sy = smem + S::kY;
-                if constexpr (kOutF32) {   // two atoms: columns 0-31 and 32-63
+                if constexpr (kOutF32) {   // two atoms: columns 0-31 and 32-63, 4 per chunk
+                    constexpr int kPerAtom = 32 / kPc;
 #pragma unroll
-                    for (int k = 0; k < 8; k++)
-                        *reinterpret_cast<float4*>(sy + half * 16384 + tc::sw128(row, k)) =
+                    for (int k = 0; k < kPc / 4; k++)
+                        *reinterpret_cast<float4*>(sy + (part / kPerAtom) * 16384 +
+                                                   tc::sw128(row, (kPc / 4) * (part % kPerAtom) + k)) =
                             make_float4(out[4 * k], out[4 * k + 1], out[4 * k + 2], out[4 * k + 3]);
                 } else {
 #pragma unroll
-                    for (int k = 0; k < 4; k++)
+                    for (int k = 0; k < kPc / 8; k++)
                         Vec16<__nv_bfloat16>::store(
-                            reinterpret_cast<__nv_bfloat16*>(sy + tc::sw128(row, 4 * half + k)), out + 8 * k);
+                            reinterpret_cast<__nv_bfloat16*>(sy + tc::sw128(row, (kPc / 8) * part + k)), out + 8 * k);
                 }
             }
             // ---- the new state: G3's split operand for the next chunk, and the resident
             // copy rescaled by the next chunk's total decay for G4 to accumulate into
             if (c + 1 < nchunks) {
-                float v[32];
-                tc::tmem_ld32(tmem + lane_base + kColH + 32 * half, v);
+                float v[kPc];
+                tc::tmem_ld16(tmem + lane_base + kColH + kPc * part, v);
                 tc::tmem_wait_ld();
                 if (row < kN) {
 #pragma unroll
-                    for (int k = 0; k < 4; k++)
-                        split_store8(v + 8 * k, sHh + (4 * half + k) * S::kStrideH + row * 16,
-                                     sHl + (4 * half + k) * S::kStrideH + row * 16);
+                    for (int k = 0; k < kPc / 8; k++)
+                        split_store8(v + 8 * k, sHh + ((kPc / 8) * part + k) * S::kStrideH + row * 16,
+                                     sHl + ((kPc / 8) * part + k) * S::kStrideH + row * 16);
                 }
                 const float e_next = ex2(s_cs2[(c + 1) & 1][kQ - 1]);
 #pragma unroll
-                for (int j = 0; j < 32; j++) v[j] *= e_next;
-                tc::tmem_st32(tmem + lane_base + kColH + 32 * half, v);
+                for (int j = 0; j < kPc; j++) v[j] *= e_next;
+                tc::tmem_st16(tmem + lane_base + kColH + kPc * part, v);
                 tc::tmem_wait_st();
             }
             tc::fence_proxy_async();
@@ -643,11 +651,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             dtv = dtv_next;
         }
         if (!failed && a.h_last && row < kN) {
-            float v[32];
-            tc::tmem_ld32(tmem + lane_base + kColH + 32 * half, v);
+            float v[kPc];
+            tc::tmem_ld16(tmem + lane_base + kColH + kPc * part, v);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; j++) a.h_last[(bh * kP + 32 * half + j) * kN + row] = v[j];
+            for (int j = 0; j < kPc; j++) a.h_last[(bh * kP + kPc * part + j) * kN + row] = v[j];
         }
     }
     tc::fence_before_sync();
