@@ -98,7 +98,11 @@ struct Smem {
     static constexpr uint32_t kHh = kWl + kTileX, kHl = kHh + kTileH;
     static constexpr uint32_t kZ = kHl + kTileH;        // z of the current chunk (128 x 64)
     static constexpr uint32_t kBytes = kZ + kTileX;
-    static constexpr uint32_t kY = kMh;                 // y staged for its store (M is free by then)
+    // y staged for its store: a bf16 y tile has the z tile's shape and swizzle and
+    // is written over it in place (each thread reads its z chunks, then writes its
+    // y chunks there), so the next M does not wait for the store; an fp32 y (twice
+    // the size) goes to the M area, free once G2 is done
+    static constexpr uint32_t kYbf16 = kZ, kYf32 = kMh;
     static_assert(kBytes <= 232448 - 3072, "shared memory (dynamic + up to 3 KB static)");
     static_assert(kStage0 + kB + 32768 <= kBytes, "G4 reach of stage 0");
     static_assert(kStage0 + (kStages - 1) * kStageBytes + kB + 32768 <= kBytes, "G4 reach of the last stage");
@@ -211,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char* sHl = smem + S::kHl;
     const uint32_t base = tc::smem_u32(smem);
     const int64_t nchunks = (L + kQ - 1) / kQ;
+    constexpr uint32_t kY = kOutF32 ? S::kYf32 : S::kYbf16;
     volatile int* abort_flag = &s_abort;
     auto fail = [&](int line) {
         atomicExch(&g_ssd_status, line);
@@ -400,19 +405,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 constexpr int kAtoms = kOutF32 ? 2 : 1;
                 if (lane < kAtoms)
                     tc::tma_store_3d(&m.y, (int)(h * kP) + 32 * lane, (int)(c * kQ), (int)b,
-                                     smem + S::kY + lane * 16384);
+                                     smem + kY + lane * 16384);
                 tc::bulk_commit();
-            }
-            if (zg) {
-                z_seen = (uint32_t)c + 1;   // the compute warps consumed z(c) before finishing
-                if (c + 1 < nchunks) issue_z(c + 1);
             }
             if (S::kStages == 2) {
                 if (c + 2 < nchunks) issue_stage(c + 2);
             } else if (c + 1 < nchunks) {
                 issue_x1(c + 1);
             }
-            tc::bulk_wait_read();
+            tc::bulk_wait_read();   // y has left its staging tile (z's, or M's for fp32)
+            if (zg) {
+                z_seen = (uint32_t)c + 1;   // the compute warps consumed z(c) before finishing
+                if (c + 1 < nchunks) issue_z(c + 1);
+            }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&s_yfree);
         }
@@ -523,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- M from S: decay mask, split into the two A operands of G2 -----------
             {
                 bool ok = wait_or_abort(&s_bar[0], par, abort_flag);
-                if (ok && c > 0) ok = wait_or_abort(&s_yfree, (uint32_t)((c - 1) & 1), abort_flag);
+                if (ok && kOutF32 && c > 0) ok = wait_or_abort(&s_yfree, (uint32_t)((c - 1) & 1), abort_flag);
                 if (compute_any(!ok)) {
                     if (tid == 0) fail(__LINE__);
                     failed = true;
@@ -610,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 // rows past seqlen are staged too; the store drops them
-                unsigned char* sy = smem + S::kY;
+                unsigned char* sy = smem + kY;
                 if constexpr (kOutF32) {   // two atoms: columns 0-31 and 32-63, 4 per chunk
                     constexpr int kPerAtom = 32 / kPc;
 #pragma unroll
