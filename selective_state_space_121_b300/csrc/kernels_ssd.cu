@@ -312,33 +312,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t idG1 = tc::idesc_bf16(128, 128, 0, 0);
         constexpr uint32_t idG2 = tc::idesc_bf16(128, kP, 0, 1);
         constexpr uint32_t idG4 = tc::idesc_bf16(128, kP, 1, 1);
-        for (int64_t c = 0; c < nchunks; c++) {
+        // G1 of chunk k: S = C B^T once C and B are in (S was last read by M(k-1)).
+        // With two input stages it is issued right after G2 of the previous chunk, so
+        // it runs under that chunk's epilogue; with one stage, when its C and B land.
+        auto issue_g1 = [&](int64_t k) -> bool {
+            const int stk = S::kStages == 2 ? (int)(k & 1) : 0;
+            const uint32_t sCk = base + S::kStage0 + stk * S::kStageBytes + S::kC;
+            const uint32_t sBk = sCk + S::kB - S::kC;
+            uint64_t* bar = S::kStages == 2 ? &s_load[stk] : &s_load[0];
+            const uint32_t p = S::kStages == 2 ? (uint32_t)((k >> 1) & 1) : (uint32_t)(k & 1);
+            if (!ctl_wait(bar, p)) return false;
+            if (S::kStages == 2 && stk == 1) ld_seen1++; else ld_seen0++;
+            if (lane == 0) {
+                tc::fence_after_sync();
+                for (int j = 0; j < kN / 16; j++) {
+                    const uint32_t off = (j >> 2) * 16384 + (j & 3) * 32;
+                    tc::mma_bf16(tmem + kColS, tc::smem_desc_sw128(sCk + off, 16, 1024),
+                                 tc::smem_desc_sw128(sBk + off, 16, 1024), idG1, j > 0);
+                }
+                tc::commit(&s_bar[0]);
+            }
+            __syncwarp();
+            return true;
+        };
+        if (S::kStages == 2 && nchunks > 0 && !issue_g1(0)) {
+            if (lane == 0) fail(__LINE__);
+            failed = true;
+        }
+        for (int64_t c = 0; c < nchunks && !failed; c++) {
             const int st = S::kStages == 2 ? (int)(c & 1) : 0;
             const uint32_t par = (uint32_t)(c & 1);
             const uint32_t sC = base + S::kStage0 + st * S::kStageBytes + S::kC;
             const uint32_t sB = sC + S::kB - S::kC;
             const uint32_t sX = sC + S::kX - S::kC;
-            // G1: S = C B^T once C and B are in
-            {
-                uint64_t* bar = S::kStages == 2 ? &s_load[st] : &s_load[0];
-                const uint32_t p = S::kStages == 2 ? (uint32_t)((c >> 1) & 1) : par;
-                if (!ctl_wait(bar, p)) {
-                    if (lane == 0) fail(__LINE__);
-                    failed = true;
-                    break;
-                }
-                if (S::kStages == 2 && st == 1) ld_seen1++; else ld_seen0++;
+            if (S::kStages == 1 && !issue_g1(c)) {
+                if (lane == 0) fail(__LINE__);
+                failed = true;
+                break;
             }
-            if (lane == 0) {
-                tc::fence_after_sync();
-                for (int k = 0; k < kN / 16; k++) {
-                    const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-                    tc::mma_bf16(tmem + kColS, tc::smem_desc_sw128(sC + off, 16, 1024),
-                                 tc::smem_desc_sw128(sB + off, 16, 1024), idG1, k > 0);
-                }
-                tc::commit(&s_bar[0]);
-            }
-            __syncwarp();
             // G3, G4 once w o x and the rescaled state are written
             if (!ctl_wait(&s_ready[0], par)) {
                 if (lane == 0) fail(__LINE__);
@@ -386,6 +397,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::commit(&s_bar[2]);
             }
             __syncwarp();
+            // two stages: the next chunk's G1 now (M(c) has read S)
+            if (S::kStages == 2 && c + 1 < nchunks && !issue_g1(c + 1)) {
+                if (lane == 0) fail(__LINE__);
+                failed = true;
+                break;
+            }
             // one stage: the next chunk's C and B as soon as this chunk's products are done
             if (S::kStages == 1 && c + 1 < nchunks) {
                 if (!ctl_wait(&s_bar[2], par)) {
