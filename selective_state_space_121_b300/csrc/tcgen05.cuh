@@ -1,7 +1,8 @@
 // tcgen05.cuh -- thin inline-PTX wrappers for the 5th-generation tensor core on
 // sm_103a: tensor-memory (TMEM) allocation, shared-memory matrix descriptors,
-// the bf16 MMA with an fp32 accumulator in TMEM, its commit to an mbarrier, and
-// TMEM <-> register moves. Device code only.
+// the bf16 MMA with an fp32 accumulator in TMEM, its commit to an mbarrier,
+// TMEM <-> register moves, and the tensor-map (TMA) copies that feed it. Device
+// code only.
 //
 // Operand tiles in shared memory use the unswizzled core-matrix layout. A core
 // matrix is 8 rows of 16 contiguous bytes (8 bf16), 128 bytes in all. A tile with
@@ -52,8 +53,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
 }
 
 // ---- fences -----------------------------------------------------------------
-// Generic-proxy writes to shared memory (st.shared, cp.async) become visible to
-// the tensor core's reads after this fence and a CTA barrier.
+// Generic-proxy writes to shared memory (st.shared) become visible to the tensor
+// core's and the copy engine's reads after this fence and a barrier or mbarrier
+// hand-off.
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -173,43 +175,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* r) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// ---- asynchronous 16-byte global -> shared copies ---------------------------------
-// Copies `src_bytes` (0 or 16) and zero-fills the rest of the 16 bytes.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-// ---- TMA (tensor-map bulk copies) ------------------------------------------------
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-// 3-D tiled load of the box at coordinates (x, y, z) of `tmap` (a __grid_constant__
-// kernel parameter) into shared memory; completion counted on `bar`. x times the
-// element size must be a multiple of 16 bytes.
-__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int x, int y, int z, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-        "[%5];" ::"r"(smem_u32(dst)),
-        "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// 3-D tiled store of a shared-memory box to (x, y, z) of `tmap`; elements outside
-// the tensor are not written. Tracked by the issuing thread's bulk groups.
-__device__ __forceinline__ void tma_store_3d(const void* tmap, int x, int y, int z, const void* src) {
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(tmap),
-                 "r"(x), "r"(y), "r"(z), "r"(smem_u32(src))
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Wait until this thread's bulk stores have finished reading shared memory.
-__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 }  // namespace tc
 }  // namespace ssm
