@@ -139,6 +139,21 @@ def _f32(t, shape, name):
     return t
 
 
+def _out(t, shape, name, dtypes=(torch.float32, torch.bfloat16), device=None):
+    """A caller-provided output: the library writes exactly `shape` elements of its
+    dtype there, so a smaller tensor (or another dtype's element size) would be
+    overrun on the device. Checked before any call."""
+    if t is None:
+        return None
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} must have dtype in {[str(d) for d in dtypes]}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the inputs on {device}")
+    return t
+
+
 def _same(ref, named_shapes):
     for name, t, shp in named_shapes:
         if t is None:
@@ -182,6 +197,8 @@ def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, 
         y = torch.empty((bt, dim, L), dtype=out_dtype or u.dtype, device=u.device)
     if h_last is None and return_last_state:
         h_last = torch.empty((bt, dim, N), dtype=torch.float32, device=u.device)
+    _out(y, (bt, dim, L), "y", device=u.device)
+    _out(h_last, (bt, dim, N), "h_last", (torch.float32,), u.device)
     if workspace is None and algo in ("auto", "lookback"):
         workspace = alloc_workspace(bt, dim, L, N, u.device)
     status = _lib.ssm_scan_fwd_algo(
@@ -208,6 +225,8 @@ def scan_fwd_dir(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=Tr
         y = torch.empty((bt, dim, L), dtype=out_dtype or u.dtype, device=u.device)
     if h_last is None and return_last_state:
         h_last = torch.empty((bt, dim, N), dtype=torch.float32, device=u.device)
+    _out(y, (bt, dim, L), "y", device=u.device)
+    _out(h_last, (bt, dim, N), "h_last", (torch.float32,), u.device)
     status = _lib.ssm_scan_fwd_dir(
         _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
         int(bool(softplus)), _ptr(h0), _ptr(y), _ptr(h_last), bt, dim, L, N, ORDERS[order] if isinstance(order, str)
@@ -229,6 +248,8 @@ def scalar_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus
         y = torch.empty((bt, dim, L), dtype=out_dtype or u.dtype, device=u.device)
     if h_last is None and return_last_state:
         h_last = torch.empty((bt, dim), dtype=torch.float32, device=u.device)
+    _out(y, (bt, dim, L), "y", device=u.device)
+    _out(h_last, (bt, dim), "h_last", (torch.float32,), u.device)
     if workspace is None:
         workspace = alloc_workspace(bt, dim, L, 1, u.device)
     status = _lib.ssm_scalar_scan_fwd(
@@ -250,6 +271,7 @@ def state_update(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, soft
     _f32(A, (dim, N), "A"); _f32(D, (dim,), "D"); _f32(delta_bias, (dim,), "delta_bias")
     if y is None:
         y = torch.empty((bt, dim), dtype=out_dtype or x.dtype, device=x.device)
+    _out(y, (bt, dim), "y", device=x.device)
     status = _lib.ssm_state_update(
         _ptr(state), _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
         _ptr(delta_bias), int(bool(softplus)), _ptr(y), bt, dim, N, in_code, _dtype_code(y.dtype),
@@ -270,7 +292,9 @@ def scan_fwd_lookback_static(u, delta, A, B, C, D=None, z=None, delta_bias=None,
     in_code = _dtype_code(u.dtype)
     _same(u, (("delta", delta, u.shape), ("B", B, (bt, N, L)), ("C", C, (bt, N, L)), ("z", z, u.shape)))
     _f32(A, (dim, N), "A"); _f32(D, (dim,), "D"); _f32(delta_bias, (dim,), "delta_bias")
-    _f32(h0, (bt, dim, N), "h0"); _f32(h_last, (bt, dim, N), "h_last")
+    _f32(h0, (bt, dim, N), "h0")
+    _out(y, (bt, dim, L), "y", device=u.device)
+    _out(h_last, (bt, dim, N), "h_last", (torch.float32,), u.device)
     return int(_lib.ssm_scan_fwd_lookback_static(
         _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
         int(bool(softplus)), _ptr(h0), _ptr(y), _ptr(h_last), bt, dim, L, N, in_code, _dtype_code(y.dtype),
@@ -329,7 +353,8 @@ def causal_conv1d_fwd(x, weight, bias=None, conv_state=None, silu=True, *, out_d
         out = torch.empty((bt, dim, L), dtype=out_dtype or x.dtype, device=x.device)
     if conv_state_out is None and return_state:
         conv_state_out = torch.empty((bt, dim, width - 1), dtype=torch.float32, device=x.device)
-    _f32(conv_state_out, (bt, dim, width - 1), "conv_state_out")
+    _out(out, (bt, dim, L), "out", device=x.device)
+    _out(conv_state_out, (bt, dim, width - 1), "conv_state_out", (torch.float32,), x.device)
     status = _lib.ssm_causal_conv1d_fwd(
         _ptr(x), _ptr(weight), _ptr(bias), _ptr(conv_state), _ptr(conv_state_out), _ptr(out), bt, dim, L,
         width, int(bool(silu)), _dtype_code(x.dtype), _dtype_code(out.dtype), _stream())
@@ -346,6 +371,7 @@ def causal_conv1d_update(conv_state, x, weight, bias=None, silu=True, *, out_dty
     _f32(conv_state, (bt, dim, width - 1), "conv_state")
     if out is None:
         out = torch.empty((bt, dim), dtype=out_dtype or x.dtype, device=x.device)
+    _out(out, (bt, dim), "out", device=x.device)
     status = _lib.ssm_causal_conv1d_update(
         _ptr(conv_state), _ptr(x), _ptr(weight), _ptr(bias), _ptr(out), bt, dim, width, int(bool(silu)),
         _dtype_code(x.dtype), _dtype_code(out.dtype), _stream())
@@ -366,7 +392,8 @@ def ssd_scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, softplus=True, h0
         y = torch.empty((bt, L, H, P), dtype=out_dtype or x.dtype, device=x.device)
     if h_last is None and return_last_state:
         h_last = torch.empty((bt, H, P, N), dtype=torch.float32, device=x.device)
-    _f32(h_last, (bt, H, P, N), "h_last")
+    _out(y, (bt, L, H, P), "y", device=x.device)
+    _out(h_last, (bt, H, P, N), "h_last", (torch.float32,), x.device)
     status = _lib.ssm_ssd_scan_fwd(
         _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias), int(bool(softplus)),
         _ptr(h0), _ptr(y), _ptr(h_last), bt, L, H, P, G, N, _dtype_code(x.dtype), _dtype_code(y.dtype),

@@ -206,3 +206,48 @@ def test_scan_dir_validation(ssm):
     assert call(u=None) == -1
     assert call(y=FAKE + 16) == -9                     # y overlaps u
     assert call(batch=1 << 40, dim=1 << 30) == -2
+
+
+def test_outputs_are_checked_before_any_call(ssm):
+    """Every entry point that takes caller-provided outputs checks their shape and dtype
+    before calling the library: the library writes the full output shape, so a smaller
+    tensor would be overrun on the device. CPU tensors suffice here: the checks raise
+    before any pointer is taken."""
+    import torch
+    bt, dim, L, N = 2, 8, 16, 4
+    f32, bf = torch.float32, torch.bfloat16
+    u = torch.zeros(bt, dim, L, dtype=bf)
+    Bm = torch.zeros(bt, N, L, dtype=bf)
+    A = torch.zeros(dim, N, dtype=f32)
+    short_y = torch.zeros(bt, dim, L - 1, dtype=bf)
+    with pytest.raises(ValueError, match="y has shape"):
+        ssm.scan_fwd_lookback_static(u, u, A, Bm, Bm, y=short_y)
+    with pytest.raises(TypeError, match="y must have dtype"):
+        ssm.scan_fwd_lookback_static(u, u, A, Bm, Bm, y=torch.zeros(bt, dim, L, dtype=torch.float16))
+    with pytest.raises(ValueError, match="h_last has shape"):
+        ssm.scan_fwd_lookback_static(u, u, A, Bm, Bm, y=torch.zeros(bt, dim, L, dtype=bf),
+                                     h_last=torch.zeros(bt, dim, N - 1, dtype=f32))
+    with pytest.raises(ValueError, match="y has shape"):
+        ssm.scan_fwd(u, u, A, Bm, Bm, y=short_y)
+    with pytest.raises(ValueError, match="h_last has shape"):
+        ssm.scan_fwd(u, u, A, Bm, Bm, y=torch.zeros(bt, dim, L, dtype=bf), h_last=torch.zeros(bt, dim, 1))
+    with pytest.raises(ValueError, match="y has shape"):
+        ssm.scan_fwd_dir(u, u, A, Bm, Bm, y=short_y)
+    with pytest.raises(ValueError, match="y has shape"):
+        ssm.scalar_scan_fwd(u, u, torch.zeros(dim), torch.zeros(bt, L, dtype=bf), torch.zeros(bt, L, dtype=bf),
+                            y=short_y)
+    state = torch.zeros(bt, dim, N, dtype=f32)
+    x = torch.zeros(bt, dim, dtype=bf)
+    with pytest.raises(ValueError, match="y has shape"):
+        ssm.state_update(state, x, x, A, torch.zeros(bt, N, dtype=bf), torch.zeros(bt, N, dtype=bf),
+                         y=torch.zeros(bt, dim - 1, dtype=bf))
+    w = torch.zeros(dim, 4, dtype=f32)
+    with pytest.raises(ValueError, match="out has shape"):
+        ssm.causal_conv1d_fwd(u, w, out=short_y)
+    with pytest.raises(ValueError, match="out has shape"):
+        ssm.causal_conv1d_update(torch.zeros(bt, dim, 3), x, w, out=torch.zeros(bt, 1, dtype=bf))
+    xs = torch.zeros(1, 16, 2, 64, dtype=bf)
+    Bs = torch.zeros(1, 16, 1, 64, dtype=bf)
+    with pytest.raises(ValueError, match="y has shape"):
+        ssm.ssd_scan_fwd(xs, torch.zeros(1, 16, 2, dtype=bf), torch.zeros(2), Bs, Bs,
+                         y=torch.zeros(1, 15, 2, 64, dtype=bf))
