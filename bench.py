@@ -487,7 +487,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-configs", action="store_true", help="skip timing the other prefill configs")
-    ap.add_argument("--only", choices=["scan", "decode", "conv", "conv_update", "scan_bwd", "ssd", "scan_dir"],
+    ap.add_argument("--only", choices=["scan", "decode", "conv", "conv_update", "scan_bwd", "ssd", "scan_dir",
+                                       "pipes"],
                     help="time one entry point alone on --config (a kernel case for sweeps and ncu)")
     ap.add_argument("--config", default="mamba130m",
                     help="workload of --only: a prefill-scan config name, or 'decode'")
@@ -656,9 +657,15 @@ def main():
 def run_case(args):
     """One entry point alone on one workload: W warm-up launches, then K launches each
     timed with CUDA events on the launching stream. Prints one JSON line (not the
-    bench contract line): median/mean ms, Gtoken*channel/s, algorithmic GB/s."""
+    bench contract line): median/mean ms, Gtoken*channel/s, algorithmic GB/s.
+    `--only pipes` instead prints the measured per-SM pipe throughputs
+    (selective_state_space_121_b300.pipes) the compute roof is derived from."""
     import torch
     torch.cuda.set_device(0)
+    if args.only == "pipes":
+        from selective_state_space_121_b300 import pipes
+        print(json.dumps({"pipes": pipes.pipe_rates(), "device": torch.cuda.get_device_name(0)}))
+        return
     print(json.dumps(time_case(args.only, args.config, args.algo, args.steps, args.warmup, torch.device("cuda", 0))))
 
 

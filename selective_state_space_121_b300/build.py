@@ -4,8 +4,9 @@
 
 Each translation unit under csrc/ compiles in parallel to an object file, then
 they link (with the CUDA runtime linked statically) into
-selective_state_space_121_b300/libssmscan.so. No GPU is needed to build (nvcc
-cross-compiles).
+selective_state_space_121_b300/libssmscan.so. The pipe-throughput probes under
+probe/ build separately into libssmprobe.so (measurement only; the scan library
+does not use them). No GPU is needed to build (nvcc cross-compiles).
 """
 from __future__ import annotations
 
@@ -19,6 +20,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libssmscan.so")
+PROBE_SRC = os.path.join(PKG, "probe", "pipe_rates.cu")
+PROBE_LIB = os.path.join(PKG, "libssmprobe.so")
 OBJDIR = os.path.join(PKG, "_build")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -46,7 +49,22 @@ def _obj(src):
     return os.path.join(OBJDIR, os.path.basename(src)[:-3] + ".o")
 
 
+def build_probe(force: bool = False, verbose: bool = False) -> str:
+    """libssmprobe.so from probe/pipe_rates.cu (one translation unit)."""
+    deps = [PROBE_SRC, os.path.join(INCLUDE, "ssm_probe.h"), os.path.abspath(__file__)]
+    if not force and os.path.exists(PROBE_LIB) and os.path.getmtime(PROBE_LIB) > max(map(os.path.getmtime, deps)):
+        return PROBE_LIB
+    tmp = PROBE_LIB + ".tmp"
+    cmd = [NVCC, *ARCH, *FLAGS, "-shared", "-cudart", "static", "-o", tmp, PROBE_SRC]
+    if verbose:
+        print(" ".join(cmd))
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, PROBE_LIB)
+    return PROBE_LIB
+
+
 def build(force: bool = False, verbose: bool = False, extra=()) -> str:
+    build_probe(force, verbose)
     if not force and not stale():
         return LIB
     os.makedirs(OBJDIR, exist_ok=True)

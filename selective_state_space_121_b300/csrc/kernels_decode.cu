@@ -7,7 +7,11 @@
 // on a resident fp32 (batch, dim, dstate) state, in place.
 //
 // The kernel is HBM-bound: 8 bytes of state traffic per (b, d, n) (read + write)
-// against one exp and four FP32 operations. Layout of the work:
+// against one exp and four FP32 operations, provided the per-element instruction
+// count stays small (the streaming form below measured issue-bound at ~60
+// instructions per element with a library log1p softplus). Precision as in the
+// scan kernels: bf16 inputs take softplus and silu through the SFU (ex2, lg2,
+// rcp), fp32 inputs the accurate forms of common.cuh. Layout of the work:
 //  * a thread owns NPL = min(dstate, 4) consecutive states of one channel d
 //    (G = dstate/NPL lanes per channel, adjacent lanes), so a warp reads and writes
 //    512 contiguous bytes of state per batch row with 16-byte accesses;
@@ -103,10 +107,19 @@ __global__ void __launch_bounds__(kThreads) state_update_kernel(DecodeArgs a) {
                 float Bv[NPL], Cv[NPL];
                 load_vec<NPL, kVec>(Bp + b * N + j * NPL, Bv);
                 load_vec<NPL, kVec>(Cp + b * N + j * NPL, Cv);
+                // bf16 inputs: SFU softplus in the log2 domain, its argument formed as
+                // the prefill scan forms it; fp32 inputs: accurate
+                float dts, dtx;
                 const float v = dv[r] + bias;
-                const float dt = a.softplus ? softplus(v) : v;
-                const float dts = dt * Dec::scale;
-                const float dtx = dt * xt[r];
+                if constexpr (sizeof(Tin) == 2) {
+                    const float xl = fmaf(dv[r], kLog2e, bias * kLog2e);
+                    dts = a.softplus ? softplus_log2(xl) : xl;
+                    dtx = dts * (kLn2 * xt[r]);
+                } else {
+                    const float dt = a.softplus ? softplus_acc<true>(v) : v;
+                    dts = dt * Dec::scale;
+                    dtx = dt * xt[r];
+                }
 #pragma unroll
                 for (int i = 0; i < NPL; i++) {
                     s[r][i] = Dec::step(Dec::make(dts * Al[i]), s[r][i], dtx * Bv[i]);
@@ -124,7 +137,7 @@ __global__ void __launch_bounds__(kThreads) state_update_kernel(DecodeArgs a) {
             for (int off = 1; off < G; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
             if (ok[r] && j == 0) {
                 float yv = fmaf(Dd, xt[r], acc);
-                if (zp) yv *= silu(zv[r]);
+                if (zp) yv *= silu_acc<sizeof(Tin) == 4>(zv[r]);
                 y[b * a.dim + d] = from_f32<Tout>(yv);
             }
         }
@@ -261,6 +274,9 @@ __global__ void __launch_bounds__(kTmaThreads) state_update_tma_kernel(DecodeArg
     if (threadIdx.x == 0)
         for (int k = 0; k < kStages; k++) issue(k);
 
+    // this lane's 4 states of channel d in batch row b: sp0 + b * row_stride
+    float* const sp0 = a.state + d * N + j * 4;
+    const int64_t row_stride = a.dim * N;
     bool failed = false;
     int64_t k = 0;
     for (; k < n_rows; k++) {
@@ -278,26 +294,50 @@ __global__ void __launch_bounds__(kTmaThreads) state_update_tma_kernel(DecodeArg
         float acc = 0.f, xt = 0.f, zt = 0.f;
         if (ok) {
             const float4 s4 = *reinterpret_cast<const float4*>(&t.state[c * N + j * 4]);
-            float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+            float sv[4] = {s4.x, s4.y, s4.z, s4.w}, Bv[4], Cv[4];
+            if constexpr (sizeof(Tin) == 2) {
+                // the lane's 4 B and 4 C values: one 8-byte shared load each
+                const uint2 bw = *reinterpret_cast<const uint2*>(&t.B[j * 4]);
+                const uint2 cw = *reinterpret_cast<const uint2*>(&t.C[j * 4]);
+                Bv[0] = __uint_as_float(bw.x << 16); Bv[1] = __uint_as_float(bw.x & 0xffff0000u);
+                Bv[2] = __uint_as_float(bw.y << 16); Bv[3] = __uint_as_float(bw.y & 0xffff0000u);
+                Cv[0] = __uint_as_float(cw.x << 16); Cv[1] = __uint_as_float(cw.x & 0xffff0000u);
+                Cv[2] = __uint_as_float(cw.y << 16); Cv[3] = __uint_as_float(cw.y & 0xffff0000u);
+            } else {
+                const float4 b4 = *reinterpret_cast<const float4*>(&t.B[j * 4]);
+                const float4 c4 = *reinterpret_cast<const float4*>(&t.C[j * 4]);
+                Bv[0] = b4.x; Bv[1] = b4.y; Bv[2] = b4.z; Bv[3] = b4.w;
+                Cv[0] = c4.x; Cv[1] = c4.y; Cv[2] = c4.z; Cv[3] = c4.w;
+            }
             xt = to_f32(t.x[c]);
-            const float v = to_f32(t.dl[c]) + bias;
-            const float dt = a.softplus ? softplus(v) : v;
-            const float dts = dt * Dec::scale, dtx = dt * xt;
+            const float dlv = to_f32(t.dl[c]);
+            // bf16 inputs: softplus through the SFU in the log2 domain (dtl = dt
+            // log2 e, the ex2 argument scale), its argument formed as the prefill
+            // scan forms it; fp32 inputs: the accurate form
+            float dts, dtx;
+            if constexpr (sizeof(Tin) == 2) {
+                const float xl = fmaf(dlv, kLog2e, bias * kLog2e);
+                dts = a.softplus ? softplus_log2(xl) : xl;
+                dtx = dts * (kLn2 * xt);
+            } else {
+                const float v = dlv + bias;
+                const float dt = a.softplus ? softplus_acc<true>(v) : v;
+                dts = dt * Dec::scale;
+                dtx = dt * xt;
+            }
 #pragma unroll
             for (int i = 0; i < 4; i++) {
-                const float Bv = to_f32(t.B[j * 4 + i]), Cv = to_f32(t.C[j * 4 + i]);
-                sv[i] = Dec::step(Dec::make(dts * Av[i]), sv[i], dtx * Bv);
-                acc = fmaf(Cv, sv[i], acc);
+                sv[i] = Dec::step(Dec::make(dts * Av[i]), sv[i], dtx * Bv[i]);
+                acc = fmaf(Cv[i], sv[i], acc);
             }
-            *reinterpret_cast<float4*>(a.state + (b * a.dim + d) * N + j * 4) =
-                make_float4(sv[0], sv[1], sv[2], sv[3]);
+            *reinterpret_cast<float4*>(sp0 + b * row_stride) = make_float4(sv[0], sv[1], sv[2], sv[3]);
             if (zp) zt = to_f32(t.z[c]);
         }
 #pragma unroll
         for (int off = 1; off < G; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (ok && j == 0) {
             float yv = fmaf(Dd, xt, acc);
-            if (zp) yv *= silu(zt);
+            if (zp) yv *= silu_acc<sizeof(Tin) == 4>(zt);
             y[b * a.dim + d] = from_f32<Tout>(yv);
         }
         __syncthreads();   // every thread is done with stage st

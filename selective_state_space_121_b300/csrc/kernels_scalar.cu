@@ -221,6 +221,212 @@ __global__ void __maxnreg__((kZ || kD) ? 128 : SSM_SCALAR_MAXNREG) scalar_scan_k
     if (ok && s == 0 && a.h_last) a.h_last[row] = carry + carry_lo;
 }
 
+
+// ---------------------------------------------------------------------------
+// Streaming form of the same kernel for 16-byte aligned rows with dim % 4 == 0
+// (a warp's 4 channels then share one batch row, hence one B and one C row): the
+// inputs of each 64-step chunk arrive by bulk asynchronous copies
+// (cp.async.bulk: 4 rows of u and of delta, one row of B and of C, 4 rows of z)
+// in a kRing-deep shared-memory ring per warp, completion counted on an mbarrier,
+// so kRing chunks are in flight per warp without holding registers; the lanes
+// read their 8 steps from shared memory. The arithmetic is the kernel above's.
+// Every mbarrier wait is bounded; on expiry the warp records the failure in
+// g_scalar_status, waits (again bounded) for its copies in flight and returns.
+// ---------------------------------------------------------------------------
+#ifndef SSM_SCALAR_RING
+#define SSM_SCALAR_RING 3
+#endif
+constexpr int kRing = SSM_SCALAR_RING;
+constexpr uint32_t kRingWaitLimit = 1u << 24;
+__device__ int g_scalar_status;   // 0, or the line of a wait that ran out of budget
+
+__device__ __forceinline__ uint32_t sm_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void ring_bar_init(uint64_t* bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sm_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void ring_expect(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sm_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kRingWaitLimit; i++) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(sm_u32(bar)), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+__device__ __forceinline__ void ring_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     sm_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(sm_u32(bar))
+                 : "memory");
+}
+
+template <typename Tin, bool kZ>
+struct RingStage {
+    Tin u[kChPerWarp][kChunk], dl[kChPerWarp][kChunk];
+    Tin B[kChunk], C[kChunk];
+    Tin z[kZ ? kChPerWarp : 1][kZ ? kChunk : 8];
+};
+
+template <typename Tin, typename Tout, bool kZ, bool kD>
+__global__ void __launch_bounds__(32) __maxnreg__((kZ || kD) ? 128 : SSM_SCALAR_MAXNREG)
+    scalar_scan_ring_kernel(ScanArgs a) {
+    constexpr bool kAcc = sizeof(Tin) == 4;
+    using Dec = Decay<kAcc>;
+    __shared__ __align__(128) RingStage<Tin, kZ> s_st[kRing];
+    __shared__ __align__(8) uint64_t s_full[kRing];
+    const int lane = threadIdx.x & 31;
+    const int c = lane / kSeg, s = lane % kSeg;
+    const int64_t rows = a.batch * a.dim;
+    const int64_t row0 = (int64_t)blockIdx.x * kChPerWarp;    // dim % 4 == 0: rows share b
+    const int64_t row = row0 + c;
+    const bool ok = row < rows;
+    const int nrow = (int)min((int64_t)kChPerWarp, rows - row0);
+    const int64_t b = row0 / a.dim, d = ok ? row % a.dim : 0;
+    const int64_t L = a.seqlen;
+    const int64_t n_chunks = (L + kChunk - 1) / kChunk;
+    const Tin* ub = static_cast<const Tin*>(a.u) + row0 * L;
+    const Tin* db = static_cast<const Tin*>(a.delta) + row0 * L;
+    const Tin* zb = kZ ? static_cast<const Tin*>(a.z) + row0 * L : nullptr;
+    const Tin* Bb = static_cast<const Tin*>(a.B) + b * L;
+    const Tin* Cb = static_cast<const Tin*>(a.C) + b * L;
+    Tout* yp = static_cast<Tout*>(a.y) + row * L;
+    const float Ad = ok ? a.A[d] * Dec::scale : 0.f;
+    const float bias = (ok && a.delta_bias) ? a.delta_bias[d] : 0.f;
+    const float Dd = (kD && ok) ? a.D[d] : 0.f;
+    float carry = (ok && a.h0) ? a.h0[row] : 0.f, carry_lo = 0.f;
+
+    // lanes 0 .. nrow-1 copy the u rows, nrow .. 2 nrow-1 the delta rows, then B,
+    // C and (z) the z rows: one bulk copy per lane, lane 0 first posts the bytes
+    auto issue = [&](int64_t k) {
+        const int st = (int)(k % kRing);
+        const int64_t t0 = k * kChunk;
+        const uint32_t n = (uint32_t)min((int64_t)kChunk, L - t0) * (uint32_t)sizeof(Tin);
+        const uint32_t copies = (uint32_t)(2 * nrow + 2 + (kZ ? nrow : 0));
+        if (lane == 0) ring_expect(&s_full[st], copies * n);
+        __syncwarp();
+        RingStage<Tin, kZ>& S = s_st[st];
+        if (lane < nrow) ring_copy(S.u[lane], ub + lane * L + t0, n, &s_full[st]);
+        else if (lane < 2 * nrow) ring_copy(S.dl[lane - nrow], db + (lane - nrow) * L + t0, n, &s_full[st]);
+        else if (lane == 2 * nrow) ring_copy(S.B, Bb + t0, n, &s_full[st]);
+        else if (lane == 2 * nrow + 1) ring_copy(S.C, Cb + t0, n, &s_full[st]);
+        else if constexpr (kZ) {
+            if (lane < 3 * nrow + 2) ring_copy(S.z[lane - 2 * nrow - 2], zb + (lane - 2 * nrow - 2) * L + t0, n, &s_full[st]);
+        }
+    };
+    if (lane == 0) {
+        for (int st = 0; st < kRing; st++) ring_bar_init(&s_full[st]);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    for (int64_t k = 0; k < kRing && k < n_chunks; k++) issue(k);
+
+    bool failed = false;
+    int64_t k = 0;
+    for (; k < n_chunks; k++) {
+        const int st = (int)(k % kRing);
+        const bool got = ring_wait(&s_full[st], (uint32_t)((k / kRing) & 1));
+        if (__any_sync(0xffffffffu, !got)) { failed = true; break; }
+        const RingStage<Tin, kZ>& S = s_st[st];
+        const int64_t t0 = k * kChunk;
+        const int64_t t = t0 + (int64_t)s * kK;
+        const bool full = t0 + kChunk <= L;                       // warp-uniform
+        const int nvalid = full ? kK : (int)max((int64_t)0, min((int64_t)kK, L - t));
+        float nu[kK], nd[kK], nB[kK], nC[kK], nz[kK];
+        {
+            constexpr int V = Vec16<Tin>::kN;
+#pragma unroll
+            for (int q = 0; q < kK; q += V) {
+                Vec16<Tin>::load_shared(&S.u[c][s * kK + q], nu + q);
+                Vec16<Tin>::load_shared(&S.dl[c][s * kK + q], nd + q);
+                Vec16<Tin>::load_shared(&S.B[s * kK + q], nB + q);
+                Vec16<Tin>::load_shared(&S.C[s * kK + q], nC + q);
+                if constexpr (kZ) Vec16<Tin>::load_shared(&S.z[c][s * kK + q], nz + q);
+            }
+        }
+        if (!full) {
+            // steps past the end hold stale shared memory: make them identity steps
+#pragma unroll
+            for (int q = 0; q < kK; q++)
+                if (q >= nvalid) { nu[q] = 0.f; nd[q] = 0.f; nB[q] = 0.f; nC[q] = 0.f; nz[q] = 0.f; }
+        }
+        // this lane's reads of the stage (generic proxy) precede the refill's bulk
+        // writes (async proxy)
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (k + kRing < n_chunks) issue(k + kRing);
+
+        float du[kK], p[kK], bb[kK];
+#pragma unroll
+        for (int q = 0; q < kK; q++) {
+            const float x = nd[q] + bias;
+            float dt = a.softplus ? softplus_acc<kAcc>(x) : x;
+            if (!full && q >= nvalid) dt = 0.f;                    // identity step past the end
+            if constexpr (kD) du[q] = Dd * nu[q];
+            p[q] = Dec::make(dt * Ad);
+            bb[q] = dt * nu[q] * nB[q];
+        }
+        float P = Dec::one(), H = 0.f;
+#pragma unroll
+        for (int q = 0; q < kK; q++) {
+            H = Dec::step(p[q], H, bb[q]);
+            P = Dec::mul(p[q], P);
+        }
+#pragma unroll
+        for (int off = 1; off < kSeg; off <<= 1) {
+            const float Pp = __shfl_up_sync(0xffffffffu, P, off, kSeg);
+            const float Hp = __shfl_up_sync(0xffffffffu, H, off, kSeg);
+            if (s >= off) {
+                H = Dec::step(P, Hp, H);
+                P = Dec::mul(P, Pp);
+            }
+        }
+        float Pe = __shfl_up_sync(0xffffffffu, P, 1, kSeg);
+        float He = __shfl_up_sync(0xffffffffu, H, 1, kSeg);
+        if (s == 0) { Pe = Dec::one(); He = 0.f; }
+        const float Pt = __shfl_sync(0xffffffffu, P, kSeg - 1, kSeg);
+        const float Ht = __shfl_sync(0xffffffffu, H, kSeg - 1, kSeg);
+        float y[kK];
+        if constexpr (kAcc) {
+            float dlt = fmaf(Pe, carry, He) + carry_lo;
+            float h = carry + dlt;
+#pragma unroll
+            for (int q = 0; q < kK; q++) {
+                dlt += fmaf(p[q], h, bb[q]);
+                h = carry + dlt;
+                y[q] = nC[q] * h;
+            }
+            two_sum(carry, fmaf(Pt, carry, Ht) + carry_lo, carry, carry_lo);
+        } else {
+            float h = Dec::step(Pe, carry, He);
+#pragma unroll
+            for (int q = 0; q < kK; q++) {
+                h = Dec::step(p[q], h, bb[q]);
+                y[q] = nC[q] * h;
+            }
+            carry = Dec::step(Pt, carry, Ht);
+        }
+#pragma unroll
+        for (int q = 0; q < kK; q++) {
+            if constexpr (kD) y[q] += du[q];
+            if constexpr (kZ) y[q] *= silu_acc<kAcc>(nz[q]);
+        }
+        if (ok) store_k<Tout, true>(yp, t, L, y);
+    }
+    if (failed) {
+        if (lane == 0) atomicExch(&g_scalar_status, __LINE__);
+        for (int64_t kk = k; kk < k + kRing && kk < n_chunks; kk++)
+            (void)ring_wait(&s_full[kk % kRing], (uint32_t)((kk / kRing) & 1));
+        return;
+    }
+    if (ok && s == 0 && a.h_last) a.h_last[row] = carry + carry_lo;
+}
+
 template <typename Tin, typename Tout>
 cudaError_t launch(const ScanArgs& a, cudaStream_t s) {
     const int64_t rows = a.batch * a.dim;
@@ -230,8 +436,17 @@ cudaError_t launch(const ScanArgs& a, cudaStream_t s) {
     if (ctas > ((int64_t)1 << 31) - 1) return cudaErrorInvalidValue;
     // z (the gate) and D (the skip) are template switches: without them the kernel
     // holds no registers for them
-    const int sel = (a.vec ? 4 : 0) | (a.z ? 2 : 0) | (a.D ? 1 : 0);
     const unsigned g = (unsigned)ctas;
+    if (a.vec && a.dim % kChPerWarp == 0 && a.seqlen > 0) {
+        switch ((a.z ? 2 : 0) | (a.D ? 1 : 0)) {
+            case 0: scalar_scan_ring_kernel<Tin, Tout, false, false><<<g, 32, 0, s>>>(a); break;
+            case 1: scalar_scan_ring_kernel<Tin, Tout, false, true><<<g, 32, 0, s>>>(a); break;
+            case 2: scalar_scan_ring_kernel<Tin, Tout, true, false><<<g, 32, 0, s>>>(a); break;
+            default: scalar_scan_ring_kernel<Tin, Tout, true, true><<<g, 32, 0, s>>>(a); break;
+        }
+        return cudaGetLastError();
+    }
+    const int sel = (a.vec ? 4 : 0) | (a.z ? 2 : 0) | (a.D ? 1 : 0);
     switch (sel) {
         case 0: scalar_scan_kernel<Tin, Tout, false, false, false><<<g, kThreads, 0, s>>>(a); break;
         case 1: scalar_scan_kernel<Tin, Tout, false, false, true><<<g, kThreads, 0, s>>>(a); break;

@@ -251,3 +251,14 @@ def test_outputs_are_checked_before_any_call(ssm):
     with pytest.raises(ValueError, match="y has shape"):
         ssm.ssd_scan_fwd(xs, torch.zeros(1, 16, 2, dtype=bf), torch.zeros(2), Bs, Bs,
                          y=torch.zeros(1, 15, 2, 64, dtype=bf))
+
+
+def test_probe_library_exports_its_declared_symbol():
+    """libssmprobe.so (the pipe-throughput probes behind bench.py --only pipes) exports
+    every entry point include/ssm_probe.h declares."""
+    probe_h = os.path.join(ROOT, "include", "ssm_probe.h")
+    names = sorted(set(re.findall(r"^SSM_PROBE_API\s+[\w\s\*]+?\b(ssm_\w+)\(", open(probe_h).read(), flags=re.M)))
+    assert names == ["ssm_probe_pipe_rate"]
+    lib = ctypes.CDLL(os.path.join(ROOT, "selective_state_space_121_b300", "libssmprobe.so"))
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in ssm_probe.h but not exported"

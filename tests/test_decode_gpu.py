@@ -68,10 +68,13 @@ def test_decode_full_size_1000_steps_rows(ssm):
 
 
 def test_decode_equals_prefill_on_gpu(ssm):
-    """L decode tokens from h0 give the prefill scan's y and h_last (both fp32
-    arithmetic; they round differently -- sequential against tree composition --
-    so they agree to ~1e-5 of the output scale, well inside the 2e-3 bound each
-    meets against the oracle for these bf16 inputs)."""
+    """L decode tokens from h0 give the prefill scan's y and h_last. Both are fp32
+    arithmetic but round differently: sequential against tree composition, and,
+    for these bf16 inputs, softplus evaluated in different forms (at this small
+    size the prefill runs the warp-scan kernel's accurate log1p softplus, the
+    decode the SFU form log2(1 + 2^x), whose dt carries up to ~1e-4 relative
+    error at dt ~ 1e-3 from rounding 1 + 2^x). They agree to a few 1e-4 of the
+    output scale, inside the 2e-3 bound each meets against the oracle."""
     inp = W.make_scan_inputs(W.CONFIGS["mamba130m"], batch=2, dim=24, seqlen=64)
     t = scan_to_torch(inp)
     h0 = torch.randn(2, 24, 16, device="cuda", generator=torch.Generator("cuda").manual_seed(3))
@@ -84,5 +87,5 @@ def test_decode_equals_prefill_on_gpu(ssm):
                                    t["B"][..., k].contiguous(), t["C"][..., k].contiguous(), t["D"],
                                    t["z"][..., k].contiguous(), t["delta_bias"], True, out_dtype=torch.float32))
     yd = torch.stack(ys, dim=-1)
-    assert (yd - y).abs().max().item() <= 1e-4 * y.pow(2).mean().sqrt().item()
-    assert (state - h).abs().max().item() <= 1e-4 * h.pow(2).mean().sqrt().item()
+    assert (yd - y).abs().max().item() <= 5e-4 * y.pow(2).mean().sqrt().item()
+    assert (state - h).abs().max().item() <= 5e-4 * h.pow(2).mean().sqrt().item()
