@@ -17,13 +17,10 @@ using ssm::ScanArgs;
 constexpr uint32_t kSpinLimit = 1u << 20;   // look-back waits: ~0.1-1 s before giving up
 constexpr int64_t kSMs = 148;               // B300
 // look-back geometry (build options): CTAs per SM aimed at, shortest segment
-#ifndef SSM_LB_CTAS_PER_SM
-#define SSM_LB_CTAS_PER_SM 3
-#endif
 #ifndef SSM_LB_MIN_SEG
 #define SSM_LB_MIN_SEG 2048
 #endif
-constexpr int64_t kLookbackCtasPerSM = SSM_LB_CTAS_PER_SM;
+constexpr int64_t kLookbackCtasPerSM = ssm::kLookbackCtasPerSM;
 constexpr int64_t kLookbackMinSeg = SSM_LB_MIN_SEG;
 // lanes per channel of the time-serial kernel at dstate >= 4 (a build option; 2 is
 // also built for dstate 16)
@@ -66,17 +63,22 @@ struct Plan {
 // Channels are the unit of parallel work for the serial-carry algorithms; the
 // look-back cuts time into segments when there are too few channels to fill the
 // B300's 148 SMs.
-// Segments of the serial look-back: one CTA per (channel group, segment); about
-// kLookbackCtasPerSM CTAs per SM in all, segments a multiple of 256 steps (a
-// whole number of chunks) and at least kLookbackMinSeg steps long.
+// Segments of the serial look-back: one CTA per (channel group, segment); at most
+// kLookbackCtasPerSM CTAs per SM in all (one wave), segments a multiple of 256
+// steps (a whole number of chunks) and at least kLookbackMinSeg steps long.
 void plan_lookback(Plan& p, int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int in_dtype) {
     const int G = dstate >= 4 ? kSerialLanes : (int)dstate;
     p.lanes_per_channel = G;
     const int64_t ch_per_cta = ssm::lookback_channels_per_cta((int)dstate, G, in_dtype);
     const int64_t groups = dim > 0 ? (dim + ch_per_cta - 1) / ch_per_cta : 1;
     const int64_t ctas_per_seg = groups * (batch > 0 ? batch : 1);
+    // all CTAs resident at once (the kernel's launch bounds guarantee
+    // kLookbackCtasPerSM per SM): a CTA that starts only when a first-wave CTA
+    // leaves runs its segment after the whole first wave -- at (1, 1536, 131072, 16)
+    // rounding up to 19 segments (456 CTAs for 444 slots) cost 60%
     const int64_t target_ctas = kSMs * kLookbackCtasPerSM;
-    const int64_t want = (target_ctas + ctas_per_seg - 1) / ctas_per_seg;
+    int64_t want = target_ctas / ctas_per_seg;
+    if (want < 1) want = 1;
     const int64_t gran = ssm::kWarpScanChunk;
     int64_t seg_len = (seqlen + want - 1) / want;
     seg_len = ((seg_len + gran - 1) / gran) * gran;

@@ -282,17 +282,13 @@ __global__ void __launch_bounds__(kTmaThreads) state_update_tma_kernel(DecodeArg
     for (; k < n_rows; k++) {
         const int st = (int)(k % kStages);
         const uint32_t parity = (uint32_t)((k / kStages) & 1);
-        // a wait that runs out of budget in any thread stops the whole CTA (the
-        // decision has to be uniform: the loop holds __syncthreads)
+        // a wait that runs out of budget skips this thread's work; the end-of-row
+        // barrier then stops the whole CTA (the decision has to be uniform)
         const bool got = mbar_wait(&s_full[st], parity);
-        if (__syncthreads_or(!got)) {
-            failed = true;
-            break;
-        }
         const Tile& t = s_tile[st];
         const int64_t b = q + k * R;
         float acc = 0.f, xt = 0.f, zt = 0.f;
-        if (ok) {
+        if (ok && got) {
             const float4 s4 = *reinterpret_cast<const float4*>(&t.state[c * N + j * 4]);
             float sv[4] = {s4.x, s4.y, s4.z, s4.w}, Bv[4], Cv[4];
             if constexpr (sizeof(Tin) == 2) {
@@ -335,12 +331,19 @@ __global__ void __launch_bounds__(kTmaThreads) state_update_tma_kernel(DecodeArg
         }
 #pragma unroll
         for (int off = 1; off < G; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (ok && j == 0) {
+        if (ok && got && j == 0) {
             float yv = fmaf(Dd, xt, acc);
             if (zp) yv *= silu_acc<sizeof(Tin) == 4>(zt);
             y[b * a.dim + d] = from_f32<Tout>(yv);
         }
-        __syncthreads();   // every thread is done with stage st
+        // every thread is done with stage st (its reads, generic proxy, ordered
+        // before the refill's bulk writes, async proxy); a failed wait anywhere
+        // stops the CTA here
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (__syncthreads_or(!got)) {
+            failed = true;
+            break;
+        }
         if (threadIdx.x == 0) issue(k + kStages);
     }
     if (failed) {
@@ -350,6 +353,7 @@ __global__ void __launch_bounds__(kTmaThreads) state_update_tma_kernel(DecodeArg
             (void)mbar_wait(&s_full[kk % kStages], (uint32_t)((kk / kStages) & 1));
     }
 }
+
 
 template <int N, typename Tin, typename Tout>
 cudaError_t launch_n(const DecodeArgs& a, cudaStream_t s) {

@@ -664,8 +664,10 @@ __device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// kLookbackCtasPerSM CTAs per SM at least (the host plans the segments for exactly
+// that many resident CTAs: none may wait for a slot)
 template <int N, int G, typename Tin, typename Tout, bool kVec>
-__global__ void __launch_bounds__(kThreads) serial_lookback_kernel(ScanArgs a) {
+__global__ void __launch_bounds__(kThreads, kLookbackCtasPerSM) serial_lookback_kernel(ScanArgs a) {
     constexpr int K = max_k<N, G, Tin>();
     using Cfg = SerialCfg<N, G, Tin, K>;
     constexpr int NPL = Cfg::NPL, CPW = Cfg::CPW, kT = Cfg::kT;

@@ -146,6 +146,14 @@ int lookback_channels_per_cta(int dstate, int lanes_per_channel, int in_dtype);
 cudaError_t launch_scan_thread(const ScanArgs& a, int lanes_per_channel, cudaStream_t s);
 cudaError_t launch_scan_scalar(const ScanArgs& a, cudaStream_t s);
 
+// Look-back residency: the look-back kernel's launch bounds guarantee this many CTAs
+// per SM and the host plans its segments so that every CTA is resident at once
+// (a build option).
+#ifndef SSM_LB_CTAS_PER_SM
+#define SSM_LB_CTAS_PER_SM 3
+#endif
+constexpr int kLookbackCtasPerSM = SSM_LB_CTAS_PER_SM;
+
 // Look-back workspace geometry (bytes), shared by api.cu and the look-back kernel
 // (kernels_serial.cu): a 16-byte header and one descriptor of 16*dstate bytes per
 // (channel, segment).
