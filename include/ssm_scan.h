@@ -322,6 +322,30 @@ SSM_API int ssm_test_lookback_timeout(const void* u, const void* delta, const fl
                                       void* workspace, size_t workspace_bytes,
                                       int64_t drop_segment, uint32_t spin_limit, void* stream);
 
+/* Test hook for the device math behind the scan's softplus, decays and gate
+ * (Mamba SSM complete guide, section 5: dt = softplus(dt_proj), dA = exp(dt A),
+ * the silu(z) gate of the block's forward). Evaluates helper `fn` on n fp32
+ * device values x, writing n fp32 device values y, on `stream`:
+ *   SSM_MATH_EXP          exp(x), the accurate form (x <= 88)
+ *   SSM_MATH_LOG1P01      log1p(x) for x in [0, 1] (the fitted polynomial)
+ *   SSM_MATH_EXPM1        expm1(x), the accurate form (the fp32-input decays)
+ *   SSM_MATH_SOFTPLUS     softplus(x), the accurate form (fp32 inputs)
+ *   SSM_MATH_SILU         silu(x), the accurate form (fp32 inputs)
+ *   SSM_MATH_SOFTPLUS_SFU softplus(x) through the SFU (bf16 inputs)
+ *   SSM_MATH_SILU_SFU     silu(x) through the SFU (bf16 inputs)
+ * Returns SSM_OK, SSM_ERR_ALGO for an unknown fn, SSM_ERR_NULL, SSM_ERR_DIM or
+ * SSM_ERR_LAUNCH. */
+enum {
+    SSM_MATH_EXP = 0,
+    SSM_MATH_LOG1P01 = 1,
+    SSM_MATH_EXPM1 = 2,
+    SSM_MATH_SOFTPLUS = 3,
+    SSM_MATH_SILU = 4,
+    SSM_MATH_SOFTPLUS_SFU = 5,
+    SSM_MATH_SILU_SFU = 6
+};
+SSM_API int ssm_test_math(int fn, const float* x, float* y, int64_t n, void* stream);
+
 /* Size of the library's own device scratch area used by
  * ssm_scan_fwd_lookback_static (4 MiB). */
 #define SSM_STATIC_SCRATCH_BYTES ((size_t)4 << 20)

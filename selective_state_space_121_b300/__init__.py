@@ -72,6 +72,8 @@ _lib.ssm_scan_fwd_dir.argtypes = [_P] * 8 + [_I, _P, _P, _P] + [_I64] * 4 + [_I,
 _lib.ssm_scan_fwd_dir.restype = _I
 _lib.ssm_device_status.argtypes = [_I, _P]
 _lib.ssm_device_status.restype = _I
+_lib.ssm_test_math.argtypes = [_I, _P, _P, _I64, _P]
+_lib.ssm_test_math.restype = _I
 
 SSM_F32, SSM_BF16 = 0, 1
 ALGOS = {"auto": 0, "thread": 1, "warpscan": 2, "lookback": 3}
@@ -89,7 +91,9 @@ EXPORTS = ("ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_size", "s
            "ssm_scan_fwd_algo", "ssm_scalar_scan_fwd", "ssm_state_update",
            "ssm_test_lookback_timeout", "ssm_query_status", "ssm_scan_fwd_lookback_static",
            "ssm_causal_conv1d_fwd", "ssm_causal_conv1d_update", "ssm_scan_bwd_workspace_size",
-           "ssm_scan_bwd", "ssm_ssd_scan_fwd", "ssm_ssd_chunk_len", "ssm_device_status", "ssm_scan_fwd_dir")
+           "ssm_scan_bwd", "ssm_ssd_scan_fwd", "ssm_ssd_chunk_len", "ssm_device_status", "ssm_scan_fwd_dir",
+           "ssm_test_math")
+MATH = {"exp": 0, "log1p01": 1, "expm1": 2, "softplus": 3, "silu": 4, "softplus_sfu": 5, "silu_sfu": 6}
 
 
 class SSMError(RuntimeError):
@@ -414,6 +418,16 @@ def device_status(clear: bool = True) -> int:
 def query_status(workspace) -> int:
     """Device status word of the last look-back scan that used `workspace` (syncs the stream)."""
     return int(_lib.ssm_query_status(_ptr(workspace), _nbytes(workspace), _stream()))
+
+
+def test_math(fn: str, x: torch.Tensor) -> torch.Tensor:
+    """Evaluates one device math helper (ssm_test_math) on fp32 CUDA values x."""
+    if x.dtype != torch.float32:
+        raise TypeError("x must be float32")
+    x = x.contiguous()
+    y = torch.empty_like(x)
+    _check(_lib.ssm_test_math(MATH[fn], _ptr(x), _ptr(y), x.numel(), _stream()))
+    return y
 
 
 def run_lookback_timeout_test(u, delta, A, B, C, y, workspace, drop_segment: int, spin_limit: int) -> int:

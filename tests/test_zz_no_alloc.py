@@ -7,11 +7,14 @@ device). For them the library runs its look-back scan on a fixed 4 MiB scratch
 array of its own. These tests call that entry point through the C ABI and check
 that two calls in a row (different sizes, so the second one meets what the first
 left in the shared array) match the workspace entry point within the parity
-tolerance for bf16 inputs, and that a problem needing more scratch is refused
-before anything is launched. The file name makes pytest collect it last."""
+tolerance for bf16 inputs and meet the fp64 oracle's 2e-3 bound themselves, and
+that a problem needing more scratch is refused before anything is launched. The
+file name makes pytest collect it last."""
+import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as W
 from workloads.torch_io import scan_to_torch
 from tests.parity import TOL_BF16, assert_state_close, assert_y_close, to_np
@@ -40,6 +43,13 @@ def test_static_scratch_matches_workspace_entry_point(ssm):
         torch.cuda.synchronize()
         assert_y_close(to_np(y), to_np(y_ref), TOL_BF16, False)
         assert_state_close(to_np(h), to_np(h_ref), TOL_BF16)
+        # and against the oracle on a sample of the channels
+        chans = [(0, 0), (0, dim // 2), (0, dim - 1)]
+        ref = oracle.scan_inputs(inp, chans)
+        for (b, d) in chans:
+            yr, hr = ref[(b, d)]
+            assert_y_close(to_np(y[b, d]), yr, TOL_BF16, False, f"y channel {d}")
+            assert_state_close(to_np(h[b, d]), hr, TOL_BF16, f"h_last channel {d}")
 
 
 def test_static_scratch_refuses_oversized_problem(ssm):
