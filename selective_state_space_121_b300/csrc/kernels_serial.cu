@@ -51,10 +51,13 @@
 // dlt, where the anchor is an unevaluated fp32 pair and dlt the change since the
 // chunk start, so a slowly decaying large state is rounded once per output, not
 // once per step.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <string.h>
 
 #include "common.cuh"
 #include "launch.h"
+#include "tcgen05.cuh"
 
 namespace ssm {
 namespace {
@@ -180,14 +183,41 @@ struct LaneState {
     float sdt[K], sdt_c[K];
 };
 
+// Tensor maps of the bulk-copy (TMA) input path: u, delta, z as (L, dim, batch)
+// and B, C as (L, N, batch), bf16, boxes of one chunk of the CTA's channels (the
+// B and C boxes hold all N states).
+struct ScanMaps {
+    CUtensorMap u, d, z, B, C;
+};
+
+__device__ int g_prefill_status;   // 0, or the line of a bulk-copy wait that ran out of budget
+constexpr uint32_t kTmaWaitLimit = 1u << 24;
+
 // The chunk tiles of a CTA (separate arrays, not one struct, so the compiler sees
-// that the partial-sum stores cannot alias the operand loads of later steps).
+// that the partial-sum stores cannot alias the operand loads of later steps), and
+// for the bulk-copy path the one-chunk input stage, its mbarrier, the tensor maps
+// and the CTA's first channel.
 template <int N, int G, typename Tin, int K>
 struct Tiles {
     using Cfg = SerialCfg<N, G, Tin, K>;
     float (*bc)[Cfg::kT][2 * N];                  // [buf][t][B n.. | C n..]
     float (*db)[Cfg::CPW / Cfg::K][Cfg::DBS];     // [warp][lane group][t][K][dt, dt*u]
     float4 (*p)[Cfg::K][Cfg::kT / 4][Cfg::PS];    // [warp][k][t/4][lane]: partial C.h
+    unsigned char* stage;                         // u, delta, z tiles, then B, C (bulk-copy path)
+    uint64_t* full;                               // its mbarrier
+    const ScanMaps* maps;
+    int64_t cta_d0;
+};
+
+// Bytes of the bulk-copy stage: u, delta, z tiles of the CTA's channels for one
+// chunk, then the B and C tiles.
+template <int N, int G, typename Tin, int K>
+struct StageGeom {
+    using Cfg = SerialCfg<N, G, Tin, K>;
+    static constexpr int CPC = kWarps * Cfg::CPW;                              // channels per CTA
+    static constexpr int XB = CPC * Cfg::kT * (int)sizeof(Tin);
+    static constexpr int BB = N * Cfg::kT * (int)sizeof(Tin);
+    static constexpr int BYTES = 3 * XB + 2 * BB;
 };
 
 template <int N, int G, int K>
@@ -202,10 +232,15 @@ using LaneStateT = LaneState<K, N / G>;
 //           staged, no C, no y) plus the sum of dt*scale, so the caller can form
 //           the map of the segment: decay exp(A * sum dt), offset = S.
 // Every thread of the CTA must call it with the same (tb, te).
-template <int N, int G, int K, typename Tin, typename Tout, bool kVec, bool kFull>
-__device__ __forceinline__ void serial_pass(const ScanArgs& a, int64_t b, int64_t d_warp0, int64_t tb,
+//   kTma:   the chunk inputs arrive by bulk tensor copies (TMA) into the CTA's
+//           stage, one chunk ahead, instead of per-lane global loads into
+//           registers; `phase` counts the stage mbarrier's completed phases across
+//           passes. Returns false when a copy wait ran out of budget (recorded in
+//           g_prefill_status; the outputs are then unspecified).
+template <int N, int G, int K, typename Tin, typename Tout, bool kVec, bool kFull, bool kTma = false>
+__device__ __forceinline__ bool serial_pass(const ScanArgs& a, int64_t b, int64_t d_warp0, int64_t tb,
                                             int64_t te, const A2Arr<N, G, K>& A2, LaneStateT<N, G, K>& S,
-                                            const Tiles<N, G, Tin, K>& tl) {
+                                            const Tiles<N, G, Tin, K>& tl, uint32_t* phase = nullptr) {
     using Cfg = SerialCfg<N, G, Tin, K>;
     constexpr int NPL = Cfg::NPL, V = Cfg::V, VPR = Cfg::VPR, PV = Cfg::PV, kT = Cfg::kT, CPW = Cfg::CPW;
     constexpr int NP2 = LaneState<K, NPL>::NP2;
@@ -279,11 +314,57 @@ __device__ __forceinline__ void serial_pass(const ScanArgs& a, int64_t b, int64_
         }
     };
 
+    // bulk-copy path: thread 0 posts the chunk's bytes and issues its tile copies;
+    // every thread later reads the same vectors the global loads above would have
+    using SG = StageGeom<N, G, Tin, K>;
+    auto issue = [&](int64_t t0) {
+        const uint32_t bytes = (uint32_t)(2 * SG::XB + (has_z ? SG::XB : 0) + (kFull ? 2 : 1) * SG::BB);
+        tc::mbar_expect_tx(tl.full, bytes);
+        const int x = (int)t0, y0 = (int)tl.cta_d0, zb = (int)b;
+        tc::tma_load_3d(tl.stage, &tl.maps->u, x, y0, zb, tl.full);
+        tc::tma_load_3d(tl.stage + SG::XB, &tl.maps->d, x, y0, zb, tl.full);
+        if (has_z) tc::tma_load_3d(tl.stage + 2 * SG::XB, &tl.maps->z, x, y0, zb, tl.full);
+        tc::tma_load_3d(tl.stage + 3 * SG::XB, &tl.maps->B, x, 0, zb, tl.full);
+        if (kFull) tc::tma_load_3d(tl.stage + 3 * SG::XB + SG::BB, &tl.maps->C, x, 0, zb, tl.full);
+    };
+    auto read_stage = [&]() {
+        const Tin* st = reinterpret_cast<const Tin*>(tl.stage);
+#pragma unroll
+        for (int q = 0; q < PV; q++) {
+            const int row = warp * CPW + pc[q];
+            ru[q] = *reinterpret_cast<const uint4*>(st + row * kT + pt[q]);
+            rd[q] = *reinterpret_cast<const uint4*>(st + (SG::CPC + row) * kT + pt[q]);
+            rz[q] = has_z ? *reinterpret_cast<const uint4*>(st + (2 * SG::CPC + row) * kT + pt[q])
+                          : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int r = 0; r < BCPT; r++) {
+            const int v = r * kThreads + threadIdx.x;
+            const int which = v / (N * VPR), rem = v % (N * VPR);
+            const int n = rem / VPR, tt = (rem % VPR) * V;
+            rbc[r] = v < BCV ? *reinterpret_cast<const uint4*>(st + (3 * SG::CPC + which * N + n) * kT + tt)
+                             : make_uint4(0, 0, 0, 0);
+        }
+    };
+
     const int64_t n_chunks = te > tb ? (te - tb + kT - 1) / kT : 0;
-    if (n_chunks > 0) prefetch(tb);
+    bool ok = true;
+    if constexpr (kTma) {
+        if (n_chunks > 0 && threadIdx.x == 0) issue(tb);
+    } else {
+        if (n_chunks > 0) prefetch(tb);
+    }
     for (int64_t c = 0; c < n_chunks; c++) {
         const int64_t t0 = tb + c * kT;
         const int buf = (int)(c & 1);
+        bool got = true;
+        if constexpr (kTma) {
+            got = tc::mbar_wait(tl.full, *phase & 1u, kTmaWaitLimit);
+            if (got) read_stage();
+            // these reads of the stage (generic proxy) precede the refill's bulk
+            // writes (async proxy) issued after the barrier below
+            tc::fence_proxy_async();
+        }
         // B/C tile of this chunk, [t][...]: fp32 [n], B then C (B carries ln2 on
         // the bf16 path), or the raw bf16 slots above (ln2 then goes into dt*u)
 #pragma unroll
@@ -333,8 +414,17 @@ __device__ __forceinline__ void serial_pass(const ScanArgs& a, int64_t b, int64_
                 *reinterpret_cast<float2*>(dbrow + (pt[q] + k) * 2 * K) = make_float2(dts, bu);
             }
         }
-        if (c + 1 < n_chunks) prefetch(t0 + kT);
-        __syncthreads();
+        if constexpr (kTma) {
+            if (__syncthreads_or(!got)) {
+                ok = false;
+                break;
+            }
+            ++*phase;
+            if (threadIdx.x == 0 && c + 1 < n_chunks) issue(t0 + kT);   // the stage was read by all
+        } else {
+            if (c + 1 < n_chunks) prefetch(t0 + kT);
+            __syncthreads();
+        }
 
         // B. recurrence, in groups of 4 steps: the loads and exps of a group do not
         // depend on the state, only its chained state updates do
@@ -545,8 +635,16 @@ __device__ __forceinline__ void serial_pass(const ScanArgs& a, int64_t b, int64_
         }
         (void)ku; (void)kz;
     }
+    if constexpr (kTma) {
+        if (!ok && threadIdx.x == 0) {
+            // record, then let the copy still in flight land before leaving
+            atomicExch(&g_prefill_status, __LINE__);
+            (void)tc::mbar_wait(tl.full, *phase & 1u, kTmaWaitLimit);
+        }
+    }
     // the next pass (or caller) reuses the tiles: all warps must be done with them
     __syncthreads();
+    return ok;
 }
 
 // The lane's A values (pairs) and states initialised to h[k] (anchor h, nothing
@@ -583,16 +681,27 @@ __device__ __forceinline__ float lane_state(const LaneStateT<N, G, K>& S, int k,
     else return lo_hi(S.h2[k][i / 2], i);
 }
 
-template <int N, int G, typename Tin, typename Tout, bool kVec>
+template <int N, int G, typename Tin, typename Tout, bool kVec, bool kTma>
 // at most 128 registers (4 CTAs per SM): measured ~1% faster than unbounded
-__global__ void __launch_bounds__(kThreads, 4) serial_scan_kernel(ScanArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) serial_scan_kernel(ScanArgs a, const __grid_constant__ ScanMaps maps) {
     constexpr int K = 1;
     using Cfg = SerialCfg<N, G, Tin, K>;
     constexpr int NPL = Cfg::NPL, CPW = Cfg::CPW, kT = Cfg::kT;
     __shared__ __align__(16) float s_bc[2][kT][2 * N];
     __shared__ __align__(16) float s_db[kWarps][CPW / K][Cfg::DBS];
     __shared__ __align__(16) float4 s_p[kWarps][K][kT / 4][Cfg::PS];
-    const Tiles<N, G, Tin, K> tl{s_bc, s_db, s_p};
+    __shared__ __align__(128) unsigned char s_stage[kTma ? StageGeom<N, G, Tin, K>::BYTES : 16];
+    __shared__ __align__(8) uint64_t s_full;
+    const Tiles<N, G, Tin, K> tl{s_bc, s_db, s_p, s_stage, &s_full, &maps,
+                                 (int64_t)blockIdx.x * kWarps * CPW};
+    uint32_t phase = 0;
+    if (kTma) {
+        if (threadIdx.x == 0) {
+            tc::mbar_init(&s_full, 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncthreads();
+    }
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t b = blockIdx.y;
@@ -612,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 4) serial_scan_kernel(ScanArgs a) {
     A2Arr<N, G, K> A2;
     LaneStateT<N, G, K> S;
     lane_init<N, G, K>(a, dR, okR, j, A2, S, h0);
-    serial_pass<N, G, K, Tin, Tout, kVec, true>(a, b, d_warp0, 0, a.seqlen, A2, S, tl);
+    if (!serial_pass<N, G, K, Tin, Tout, kVec, true, kTma>(a, b, d_warp0, 0, a.seqlen, A2, S, tl, &phase)) return;
     if (a.h_last) {
 #pragma unroll
         for (int k = 0; k < K; k++)
@@ -666,8 +775,9 @@ __device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
 
 // kLookbackCtasPerSM CTAs per SM at least (the host plans the segments for exactly
 // that many resident CTAs: none may wait for a slot)
-template <int N, int G, typename Tin, typename Tout, bool kVec>
-__global__ void __launch_bounds__(kThreads, kLookbackCtasPerSM) serial_lookback_kernel(ScanArgs a) {
+template <int N, int G, typename Tin, typename Tout, bool kVec, bool kTma>
+__global__ void __launch_bounds__(kThreads, kLookbackCtasPerSM)
+    serial_lookback_kernel(ScanArgs a, const __grid_constant__ ScanMaps maps) {
     constexpr int K = max_k<N, G, Tin>();
     using Cfg = SerialCfg<N, G, Tin, K>;
     constexpr int NPL = Cfg::NPL, CPW = Cfg::CPW, kT = Cfg::kT;
@@ -677,13 +787,21 @@ __global__ void __launch_bounds__(kThreads, kLookbackCtasPerSM) serial_lookback_
     __shared__ __align__(16) float s_db[kWarps][CPW / K][Cfg::DBS];
     __shared__ __align__(16) float4 s_p[kWarps][K][kT / 4][Cfg::PS];
     __shared__ uint32_t s_ticket;
-    const Tiles<N, G, Tin, K> tl{s_bc, s_db, s_p};
+    __shared__ __align__(128) unsigned char s_stage[kTma ? StageGeom<N, G, Tin, K>::BYTES : 16];
+    __shared__ __align__(8) uint64_t s_full;
+    uint32_t phase = 0;
 
     int32_t* status = static_cast<int32_t*>(a.workspace);
     uint32_t* ticket_ctr = reinterpret_cast<uint32_t*>(status + 1);
     LbDesc<N>* desc = reinterpret_cast<LbDesc<N>*>(static_cast<char*>(a.workspace) + 16);
 
-    if (threadIdx.x == 0) s_ticket = atomicAdd(ticket_ctr, 1u);
+    if (threadIdx.x == 0) {
+        s_ticket = atomicAdd(ticket_ctr, 1u);
+        if (kTma) {
+            tc::mbar_init(&s_full, 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+    }
     __syncthreads();
     const int64_t ch_per_cta = (int64_t)kWarps * CPW;
     const int64_t groups = (a.dim + ch_per_cta - 1) / ch_per_cta;
@@ -700,6 +818,7 @@ __global__ void __launch_bounds__(kThreads, kLookbackCtasPerSM) serial_lookback_
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t d_warp0 = (grp * kWarps + warp) * CPW;
+    const Tiles<N, G, Tin, K> tl{s_bc, s_db, s_p, s_stage, &s_full, &maps, grp * kWarps * CPW};
     const int p = lane_grp<G, K>(lane), j = lane_sgrp<G, K>(lane);
     int64_t dR[K], ch[K];
     bool okR[K];
@@ -720,7 +839,12 @@ __global__ void __launch_bounds__(kThreads, kLookbackCtasPerSM) serial_lookback_
 #pragma unroll
         for (int i = 0; i < NPL; i++) { aggP[k][i] = Dec::one(); aggH[k][i] = 0.f; }
     if (!last) {
-        serial_pass<N, G, K, Tin, Tout, kVec, false>(a, b, d_warp0, ts, te, A2, S, tl);
+        if (!serial_pass<N, G, K, Tin, Tout, kVec, false, kTma>(a, b, d_warp0, ts, te, A2, S, tl, &phase)) {
+            // a failed copy wait: record it where the look-back reports, publish nothing
+            // (later segments time out on their bounded waits and finish) and leave
+            if (threadIdx.x == 0) atomicExch(status, kErrLookbackTimeout);
+            return;
+        }
 #pragma unroll
         for (int k = 0; k < K; k++)
 #pragma unroll
@@ -794,7 +918,10 @@ __global__ void __launch_bounds__(kThreads, kLookbackCtasPerSM) serial_lookback_
     }
     // (5) the full pass from the carry
     lane_init<N, G, K>(a, dR, okR, j, A2, S, carry);
-    serial_pass<N, G, K, Tin, Tout, kVec, true>(a, b, d_warp0, ts, te, A2, S, tl);
+    if (!serial_pass<N, G, K, Tin, Tout, kVec, true, kTma>(a, b, d_warp0, ts, te, A2, S, tl, &phase)) {
+        if (threadIdx.x == 0) atomicExch(status, kErrLookbackTimeout);
+        return;
+    }
     if (last && a.h_last) {
 #pragma unroll
         for (int k = 0; k < K; k++)
@@ -805,26 +932,95 @@ __global__ void __launch_bounds__(kThreads, kLookbackCtasPerSM) serial_lookback_
     }
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// bf16 (L, rows, batch) view with (kT, box_rows, 1) boxes, unswizzled: rows beyond
+// `rows` (a CTA's last channels) and steps beyond L read as zeros
+bool encode_bf16(CUtensorMap* map, const void* base, int64_t L, int64_t rows, int64_t batch, int kT, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn || !base) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)L, (cuuint64_t)rows, (cuuint64_t)batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)(L * 2), (cuuint64_t)(L * rows * 2)};
+    const cuuint32_t box[3] = {(cuuint32_t)kT, (cuuint32_t)box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The bulk-copy input path is taken for bf16 inputs whose rows are 16-byte
+// aligned (a.vec) when the tensor maps encode; `maps` is left zero otherwise.
+template <int N, int G, int K, typename Tin>
+bool make_maps(const ScanArgs& a, ScanMaps* maps) {
+    memset(maps, 0, sizeof(*maps));
+    if constexpr (sizeof(Tin) != 2) {
+        return false;
+    } else {
+        using Cfg = SerialCfg<N, G, Tin, K>;
+        constexpr int CPC = StageGeom<N, G, Tin, K>::CPC;
+        if (!a.vec || a.seqlen <= 0 || a.seqlen >= ((int64_t)1 << 31) || a.dim >= ((int64_t)1 << 31)) return false;
+        return encode_bf16(&maps->u, a.u, a.seqlen, a.dim, a.batch, Cfg::kT, CPC) &&
+               encode_bf16(&maps->d, a.delta, a.seqlen, a.dim, a.batch, Cfg::kT, CPC) &&
+               (!a.z || encode_bf16(&maps->z, a.z, a.seqlen, a.dim, a.batch, Cfg::kT, CPC)) &&
+               encode_bf16(&maps->B, a.B, a.seqlen, N, a.batch, Cfg::kT, N) &&
+               encode_bf16(&maps->C, a.C, a.seqlen, N, a.batch, Cfg::kT, N);
+    }
+}
+
 template <int N, int G, typename Tin, typename Tout>
 cudaError_t launch_serial(const ScanArgs& a, cudaStream_t s) {
     using Cfg = SerialCfg<N, G, Tin, 1>;
     if (a.batch == 0 || a.dim == 0) return cudaSuccess;
     const int64_t ch_per_cta = (int64_t)kWarps * Cfg::CPW;
     dim3 grid((unsigned)((a.dim + ch_per_cta - 1) / ch_per_cta), (unsigned)a.batch);
-    if (a.vec) serial_scan_kernel<N, G, Tin, Tout, true><<<grid, kThreads, 0, s>>>(a);
-    else serial_scan_kernel<N, G, Tin, Tout, false><<<grid, kThreads, 0, s>>>(a);
+    ScanMaps maps;
+    bool launched = false;
+    if constexpr (sizeof(Tin) == 2) {
+        if (make_maps<N, G, 1, Tin>(a, &maps)) {
+            serial_scan_kernel<N, G, Tin, Tout, true, true><<<grid, kThreads, 0, s>>>(a, maps);
+            launched = true;
+        }
+    } else {
+        memset(&maps, 0, sizeof(maps));
+    }
+    if (launched) {
+    } else if (a.vec) serial_scan_kernel<N, G, Tin, Tout, true, false><<<grid, kThreads, 0, s>>>(a, maps);
+    else serial_scan_kernel<N, G, Tin, Tout, false, false><<<grid, kThreads, 0, s>>>(a, maps);
     return cudaGetLastError();
 }
 
 template <int N, int G, typename Tin, typename Tout>
 cudaError_t launch_lookback(const ScanArgs& a, cudaStream_t s) {
-    using Cfg = SerialCfg<N, G, Tin, max_k<N, G, Tin>()>;
+    constexpr int K = max_k<N, G, Tin>();
+    using Cfg = SerialCfg<N, G, Tin, K>;
     if (a.batch == 0 || a.dim == 0) return cudaSuccess;
     const int64_t ch_per_cta = (int64_t)kWarps * Cfg::CPW;
     const int64_t ctas = ((a.dim + ch_per_cta - 1) / ch_per_cta) * a.batch * a.n_seg;
     if (ctas > ((int64_t)1 << 31) - 1) return cudaErrorInvalidValue;
-    if (a.vec) serial_lookback_kernel<N, G, Tin, Tout, true><<<(unsigned)ctas, kThreads, 0, s>>>(a);
-    else serial_lookback_kernel<N, G, Tin, Tout, false><<<(unsigned)ctas, kThreads, 0, s>>>(a);
+    ScanMaps maps;
+    bool launched = false;
+    if constexpr (sizeof(Tin) == 2) {
+        if (make_maps<N, G, K, Tin>(a, &maps)) {
+            serial_lookback_kernel<N, G, Tin, Tout, true, true><<<(unsigned)ctas, kThreads, 0, s>>>(a, maps);
+            launched = true;
+        }
+    } else {
+        memset(&maps, 0, sizeof(maps));
+    }
+    if (launched) {
+    } else if (a.vec) serial_lookback_kernel<N, G, Tin, Tout, true, false><<<(unsigned)ctas, kThreads, 0, s>>>(a, maps);
+    else serial_lookback_kernel<N, G, Tin, Tout, false, false><<<(unsigned)ctas, kThreads, 0, s>>>(a, maps);
     return cudaGetLastError();
 }
 
@@ -876,6 +1072,17 @@ cudaError_t launch_scan_thread(const ScanArgs& a, int lanes_per_channel, cudaStr
 
 cudaError_t launch_scan_serial_lookback(const ScanArgs& a, int lanes_per_channel, cudaStream_t s) {
     return dispatch<true>(a, lanes_per_channel, s);
+}
+
+cudaError_t prefill_status(int* line, bool clear, cudaStream_t s) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(line, g_prefill_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess && clear && *line != 0) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbolAsync(g_prefill_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    }
+    return e;
 }
 
 size_t lookback_workspace_bytes(int64_t batch, int64_t dim, int dstate, int64_t n_seg) {

@@ -132,6 +132,8 @@ int64_t ssd_chunk_len();
 // reads (and optionally clears) the SSD kernel's device status word: 0 or the
 // source line of a wait that ran out of budget; synchronises the stream
 cudaError_t ssd_status(int* line, bool clear, cudaStream_t s);
+// the same for the prefill kernels' bulk-copy waits (kernels_serial.cu)
+cudaError_t prefill_status(int* line, bool clear, cudaStream_t s);
 size_t scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate);
 cudaError_t launch_causal_conv1d(const ConvArgs& a, cudaStream_t s);
 cudaError_t launch_conv_update(const ConvArgs& a, cudaStream_t s);
