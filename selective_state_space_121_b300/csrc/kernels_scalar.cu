@@ -362,15 +362,22 @@ __global__ void __launch_bounds__(32) __maxnreg__((kZ || kD) ? 128 : SSM_SCALAR_
         if (k + kRing < n_chunks) issue(k + kRing);
 
         float du[kK], p[kK], bb[kK];
+        // whole chunks (all but the last) take no per-step bounds test
+        auto first = [&](auto check) {
 #pragma unroll
-        for (int q = 0; q < kK; q++) {
-            const float x = nd[q] + bias;
-            float dt = a.softplus ? softplus_acc<kAcc>(x) : x;
-            if (!full && q >= nvalid) dt = 0.f;                    // identity step past the end
-            if constexpr (kD) du[q] = Dd * nu[q];
-            p[q] = Dec::make(dt * Ad);
-            bb[q] = dt * nu[q] * nB[q];
-        }
+            for (int q = 0; q < kK; q++) {
+                const float x = nd[q] + bias;
+                float dt = a.softplus ? softplus_acc<kAcc>(x) : x;
+                if constexpr (decltype(check)::value) {
+                    if (q >= nvalid) dt = 0.f;                     // identity step past the end
+                }
+                if constexpr (kD) du[q] = Dd * nu[q];
+                p[q] = Dec::make(dt * Ad);
+                bb[q] = dt * nu[q] * nB[q];
+            }
+        };
+        if (full) first(std::false_type{});
+        else first(std::true_type{});
         float P = Dec::one(), H = 0.f;
 #pragma unroll
         for (int q = 0; q < kK; q++) {

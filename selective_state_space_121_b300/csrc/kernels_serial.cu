@@ -218,6 +218,17 @@ struct StageGeom {
     static constexpr int XB = CPC * Cfg::kT * (int)sizeof(Tin);
     static constexpr int BB = N * Cfg::kT * (int)sizeof(Tin);
     static constexpr int BYTES = 3 * XB + 2 * BB;
+    // 64-byte tile rows (the time-serial kernel's 32-step bf16 chunks) take the
+    // 64-byte TMA swizzle: a quarter-warp reads one 16-byte chunk of 8 consecutive
+    // rows, which unswizzled puts 4 lanes on each bank group (16 wavefronts per
+    // warp load instead of 4); the swizzle stores chunk j of row r at chunk
+    // j ^ ((r >> 1) & 3) of the row
+    static constexpr bool kSw64 = Cfg::kT * (int)sizeof(Tin) == 64;
+    // byte offset of elements [t, t + 8) of tile row r (t a multiple of 8)
+    static __device__ __forceinline__ int off(int r, int t) {
+        const int j = t * (int)sizeof(Tin) / 16;
+        return r * Cfg::kT * (int)sizeof(Tin) + ((kSw64 ? (j ^ ((r >> 1) & 3)) : j) << 4);
+    }
 };
 
 template <int N, int G, int K>
@@ -328,13 +339,13 @@ __device__ __forceinline__ bool serial_pass(const ScanArgs& a, int64_t b, int64_
         if (kFull) tc::tma_load_3d(tl.stage + 3 * SG::XB + SG::BB, &tl.maps->C, x, 0, zb, tl.full);
     };
     auto read_stage = [&]() {
-        const Tin* st = reinterpret_cast<const Tin*>(tl.stage);
+        const unsigned char* st = tl.stage;
 #pragma unroll
         for (int q = 0; q < PV; q++) {
             const int row = warp * CPW + pc[q];
-            ru[q] = *reinterpret_cast<const uint4*>(st + row * kT + pt[q]);
-            rd[q] = *reinterpret_cast<const uint4*>(st + (SG::CPC + row) * kT + pt[q]);
-            rz[q] = has_z ? *reinterpret_cast<const uint4*>(st + (2 * SG::CPC + row) * kT + pt[q])
+            ru[q] = *reinterpret_cast<const uint4*>(st + SG::off(row, pt[q]));
+            rd[q] = *reinterpret_cast<const uint4*>(st + SG::off(SG::CPC + row, pt[q]));
+            rz[q] = has_z ? *reinterpret_cast<const uint4*>(st + SG::off(2 * SG::CPC + row, pt[q]))
                           : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
@@ -342,7 +353,7 @@ __device__ __forceinline__ bool serial_pass(const ScanArgs& a, int64_t b, int64_
             const int v = r * kThreads + threadIdx.x;
             const int which = v / (N * VPR), rem = v % (N * VPR);
             const int n = rem / VPR, tt = (rem % VPR) * V;
-            rbc[r] = v < BCV ? *reinterpret_cast<const uint4*>(st + (3 * SG::CPC + which * N + n) * kT + tt)
+            rbc[r] = v < BCV ? *reinterpret_cast<const uint4*>(st + SG::off(3 * SG::CPC + which * N + n, tt))
                              : make_uint4(0, 0, 0, 0);
         }
     };
@@ -690,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 4) serial_scan_kernel(ScanArgs a, co
     __shared__ __align__(16) float s_bc[2][kT][2 * N];
     __shared__ __align__(16) float s_db[kWarps][CPW / K][Cfg::DBS];
     __shared__ __align__(16) float4 s_p[kWarps][K][kT / 4][Cfg::PS];
-    __shared__ __align__(128) unsigned char s_stage[kTma ? StageGeom<N, G, Tin, K>::BYTES : 16];
+    __shared__ __align__(1024) unsigned char s_stage[kTma ? StageGeom<N, G, Tin, K>::BYTES : 16];
     __shared__ __align__(8) uint64_t s_full;
     const Tiles<N, G, Tin, K> tl{s_bc, s_db, s_p, s_stage, &s_full, &maps,
                                  (int64_t)blockIdx.x * kWarps * CPW};
@@ -787,7 +798,7 @@ __global__ void __launch_bounds__(kThreads, kLookbackCtasPerSM)
     __shared__ __align__(16) float s_db[kWarps][CPW / K][Cfg::DBS];
     __shared__ __align__(16) float4 s_p[kWarps][K][kT / 4][Cfg::PS];
     __shared__ uint32_t s_ticket;
-    __shared__ __align__(128) unsigned char s_stage[kTma ? StageGeom<N, G, Tin, K>::BYTES : 16];
+    __shared__ __align__(1024) unsigned char s_stage[kTma ? StageGeom<N, G, Tin, K>::BYTES : 16];
     __shared__ __align__(8) uint64_t s_full;
     uint32_t phase = 0;
 
@@ -945,9 +956,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// bf16 (L, rows, batch) view with (kT, box_rows, 1) boxes, unswizzled: rows beyond
+// bf16 (L, rows, batch) view with (kT, box_rows, 1) boxes (64-byte swizzled when
+// sw64, see StageGeom): rows beyond
 // `rows` (a CTA's last channels) and steps beyond L read as zeros
-bool encode_bf16(CUtensorMap* map, const void* base, int64_t L, int64_t rows, int64_t batch, int kT, int box_rows) {
+bool encode_bf16(CUtensorMap* map, const void* base, int64_t L, int64_t rows, int64_t batch, int kT, int box_rows,
+                 bool sw64) {
     auto fn = encode_fn();
     if (!fn || !base) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)L, (cuuint64_t)rows, (cuuint64_t)batch};
@@ -955,8 +968,8 @@ bool encode_bf16(CUtensorMap* map, const void* base, int64_t L, int64_t rows, in
     const cuuint32_t box[3] = {(cuuint32_t)kT, (cuuint32_t)box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // The bulk-copy input path is taken for bf16 inputs whose rows are 16-byte
@@ -970,11 +983,12 @@ bool make_maps(const ScanArgs& a, ScanMaps* maps) {
         using Cfg = SerialCfg<N, G, Tin, K>;
         constexpr int CPC = StageGeom<N, G, Tin, K>::CPC;
         if (!a.vec || a.seqlen <= 0 || a.seqlen >= ((int64_t)1 << 31) || a.dim >= ((int64_t)1 << 31)) return false;
-        return encode_bf16(&maps->u, a.u, a.seqlen, a.dim, a.batch, Cfg::kT, CPC) &&
-               encode_bf16(&maps->d, a.delta, a.seqlen, a.dim, a.batch, Cfg::kT, CPC) &&
-               (!a.z || encode_bf16(&maps->z, a.z, a.seqlen, a.dim, a.batch, Cfg::kT, CPC)) &&
-               encode_bf16(&maps->B, a.B, a.seqlen, N, a.batch, Cfg::kT, N) &&
-               encode_bf16(&maps->C, a.C, a.seqlen, N, a.batch, Cfg::kT, N);
+        constexpr bool sw = StageGeom<N, G, Tin, K>::kSw64;
+        return encode_bf16(&maps->u, a.u, a.seqlen, a.dim, a.batch, Cfg::kT, CPC, sw) &&
+               encode_bf16(&maps->d, a.delta, a.seqlen, a.dim, a.batch, Cfg::kT, CPC, sw) &&
+               (!a.z || encode_bf16(&maps->z, a.z, a.seqlen, a.dim, a.batch, Cfg::kT, CPC, sw)) &&
+               encode_bf16(&maps->B, a.B, a.seqlen, N, a.batch, Cfg::kT, N, sw) &&
+               encode_bf16(&maps->C, a.C, a.seqlen, N, a.batch, Cfg::kT, N, sw);
     }
 }
 
