@@ -409,20 +409,42 @@ __device__ __forceinline__ bool serial_pass(const ScanArgs& a, int64_t b, int64_
             ku[q] = ru[q];
             kz[q] = rz[q];
             float* dbrow = tl.db[warp][pc[q] / K] + (pc[q] % K) * 2;
+            float dts[V];   // dt * Dec::scale
+            if constexpr (kAcc) {
 #pragma unroll
-            for (int k = 0; k < V; k++) {
-                float dts;   // dt * Dec::scale
-                if constexpr (kAcc) {
+                for (int k = 0; k < V; k++) {
                     const float x = fd[k] + bias[q];
-                    dts = a.softplus ? softplus_acc<true>(x) : x;
-                } else {
-                    // x*log2(e); log2(1 + 2^xl) equals xl in fp32 once xl > 24
-                    const float xl = fmaf(fd[k], kLog2e, bias[q]);
-                    dts = a.softplus ? softplus_log2(xl) : xl;
+                    dts[k] = a.softplus ? softplus_acc<true>(x) : x;
                 }
-                if (t0 + pt[q] + k >= te || !chan_ok[q]) dts = 0.f;   // identity step past the end
-                const float bu = kRawBC ? dts * (fu[k] * kLn2) : dts * fu[k];
-                *reinterpret_cast<float2*>(dbrow + (pt[q] + k) * 2 * K) = make_float2(dts, bu);
+            } else {
+                // x*log2(e) in pairs; log2(1 + 2^xl) equals xl in fp32 once xl > 24
+#pragma unroll
+                for (int k = 0; k < V; k += 2) {
+                    const float2 xl = fma2(make_float2(fd[k], fd[k + 1]), make_float2(kLog2e, kLog2e),
+                                           make_float2(bias[q], bias[q]));
+                    dts[k] = a.softplus ? softplus_log2(xl.x) : xl.x;
+                    dts[k + 1] = a.softplus ? softplus_log2(xl.y) : xl.y;
+                }
+            }
+            // identity steps past the end (and for channels past dim)
+            if (!chan_ok[q] || t0 + pt[q] + V > te) {
+#pragma unroll
+                for (int k = 0; k < V; k++)
+                    if (t0 + pt[q] + k >= te || !chan_ok[q]) dts[k] = 0.f;
+            }
+            // (dt, dt*u) pairs, two steps per 16-byte store where the K = 1 layout
+            // puts consecutive steps side by side
+#pragma unroll
+            for (int k = 0; k < V; k += 2) {
+                float2 u2 = make_float2(fu[k], fu[k + 1]);
+                if constexpr (kRawBC) u2 = mul2(u2, make_float2(kLn2, kLn2));
+                const float2 bu = mul2(make_float2(dts[k], dts[k + 1]), u2);
+                if constexpr (K == 1) {
+                    *reinterpret_cast<float4*>(dbrow + (pt[q] + k) * 2) = make_float4(dts[k], bu.x, dts[k + 1], bu.y);
+                } else {
+                    *reinterpret_cast<float2*>(dbrow + (pt[q] + k) * 2 * K) = make_float2(dts[k], bu.x);
+                    *reinterpret_cast<float2*>(dbrow + (pt[q] + k + 1) * 2 * K) = make_float2(dts[k + 1], bu.y);
+                }
             }
         }
         if constexpr (kTma) {
@@ -612,24 +634,44 @@ __device__ __forceinline__ bool serial_pass(const ScanArgs& a, int64_t b, int64_
             // C. epilogue: y = (sum of the G partials + D*u) * silu(z)
 #pragma unroll
             for (int q = 0; q < PV; q++) {
+                // in pairs of steps: y = D*u + the G partials, then times silu(z)
                 float fu[V], yv[V];
                 unpack<Tin>(ku[q], fu);
+                float2 y2[V / 2];
 #pragma unroll
-                for (int k = 0; k < V; k++) yv[k] = fu[k] * Dd[q];
+                for (int k = 0; k < V; k += 2)
+                    y2[k / 2] = mul2(make_float2(fu[k], fu[k + 1]), make_float2(Dd[q], Dd[q]));
                 const int pk = pc[q] % K, pg = pc[q] / K;
 #pragma unroll
                 for (int jj = 0; jj < G; jj++) {
 #pragma unroll
                     for (int k = 0; k < V; k += 4) {
                         const float4 p4 = tl.p[warp][pk][(pt[q] + k) / 4][lane_of<G, K>(pg, jj)];
-                        yv[k] += p4.x; yv[k + 1] += p4.y; yv[k + 2] += p4.z; yv[k + 3] += p4.w;
+                        y2[k / 2] = add2(y2[k / 2], make_float2(p4.x, p4.y));
+                        y2[k / 2 + 1] = add2(y2[k / 2 + 1], make_float2(p4.z, p4.w));
                     }
                 }
                 if (has_z) {
                     float fz[V];
                     unpack<Tin>(kz[q], fz);
 #pragma unroll
-                    for (int k = 0; k < V; k++) yv[k] *= silu_acc<kAcc>(fz[k]);
+                    for (int k = 0; k < V; k += 2) {
+                        float2 s;
+                        if constexpr (kAcc) {
+                            s = make_float2(silu_acc<true>(fz[k]), silu_acc<true>(fz[k + 1]));
+                        } else {
+                            // z * rcp(1 + 2^(-z log2 e)), the SFU form
+                            const float2 e = mul2(make_float2(fz[k], fz[k + 1]), make_float2(-kLog2e, -kLog2e));
+                            const float2 den = add2(make_float2(ex2(e.x), ex2(e.y)), make_float2(1.f, 1.f));
+                            s = mul2(make_float2(fz[k], fz[k + 1]), make_float2(rcp(den.x), rcp(den.y)));
+                        }
+                        y2[k / 2] = mul2(y2[k / 2], s);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < V; k += 2) {
+                    yv[k] = y2[k / 2].x;
+                    yv[k + 1] = y2[k / 2].y;
                 }
                 if (chan_ok[q]) {
                     Tout* yrow = y_base + (b * a.dim + d_warp0 + pc[q]) * L;
