@@ -310,6 +310,21 @@ SSM_API int64_t ssm_ssd_chunk_len(void);
  * (SSM_ERR_LAUNCH if the read itself failed). clear != 0 resets the record. */
 SSM_API int ssm_device_status(int clear, void* stream);
 
+/* Test hook for the SSD kernel's failure path (Mamba SSM complete guide, section 6:
+ * the same chunked SSD computation as ssm_ssd_scan_fwd, softplus on, no D, z,
+ * dt_bias, h0 or h_last; bf16 x, dt, B, C and y). Every pipeline wait of the
+ * launch polls its mbarrier at most `wait_limit` times (1 .. 2^31 - 1, else
+ * SSM_ERR_DIM); with withhold_arrive != 0 compute warp 0 skips its first
+ * "w o x ready" arrival, so the control warp's wait for it runs out: the kernel
+ * records the wait's source line, raises its abort flag, lets the tensor core and
+ * the copies in flight finish, frees tensor memory and returns (y is then
+ * unspecified). Returns the launch status; read the record with
+ * ssm_device_status(). Nothing faults or hangs. */
+SSM_API int ssm_test_ssd_wait_fault(const void* x, const void* dt, const float* A, const void* B,
+                                    const void* C, void* y, int64_t batch, int64_t seqlen, int64_t nheads,
+                                    int64_t ngroups, int64_t dstate, int64_t wait_limit,
+                                    int withhold_arrive, void* stream);
+
 /* Test hook for the look-back error path. Runs the look-back scan (softplus on,
  * no D, z, bias or h0; y in in_dtype) with segment `drop_segment` withholding
  * its publication, so the waits of the next segment run out after `spin_limit`

@@ -497,10 +497,13 @@ int ssm_query_status(const void* workspace, size_t workspace_bytes, void* stream
 }
 
 
-int ssm_ssd_scan_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C,
-                     const float* D, const void* z, const float* dt_bias, int softplus, const float* h0,
-                     void* y, float* h_last, int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
-                     int64_t ngroups, int64_t dstate, int in_dtype, int out_dtype, void* stream) {
+}  // extern "C"
+
+// ssm_ssd_scan_fwd with the kernel's test hooks (wait budget, withheld arrival)
+static int ssd_impl(const void* x, const void* dt, const float* A, const void* B, const void* C, const float* D,
+                    const void* z, const float* dt_bias, int softplus, const float* h0, void* y, float* h_last,
+                    int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t ngroups, int64_t dstate,
+                    int in_dtype, int out_dtype, uint32_t wait_limit, int withhold_arrive, void* stream) {
     if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype) || in_dtype != SSM_BF16) return SSM_ERR_DTYPE;
     if (batch < 0 || seqlen < 0 || nheads < 0 || ngroups < 0) return SSM_ERR_DIM;
     if (headdim != 64 || (dstate != 64 && dstate != 128)) return SSM_ERR_SHAPE;
@@ -536,7 +539,26 @@ int ssm_ssd_scan_fwd(const void* x, const void* dt, const float* A, const void* 
     a.x = x; a.dt = dt; a.A = A; a.B = B; a.C = C; a.D = D; a.z = z; a.dt_bias = dt_bias; a.h0 = h0;
     a.y = y; a.h_last = h_last; a.batch = batch; a.seqlen = seqlen; a.nheads = nheads;
     a.ngroups = ngroups; a.dstate = (int)dstate; a.softplus = softplus ? 1 : 0; a.out_dtype = out_dtype;
+    a.wait_limit = wait_limit; a.withhold_arrive = withhold_arrive ? 1 : 0;
     return ssm::launch_ssd_scan(a, (cudaStream_t)stream) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+}
+
+extern "C" {
+
+int ssm_ssd_scan_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                     const float* D, const void* z, const float* dt_bias, int softplus, const float* h0,
+                     void* y, float* h_last, int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                     int64_t ngroups, int64_t dstate, int in_dtype, int out_dtype, void* stream) {
+    return ssd_impl(x, dt, A, B, C, D, z, dt_bias, softplus, h0, y, h_last, batch, seqlen, nheads, headdim, ngroups,
+                    dstate, in_dtype, out_dtype, 0, 0, stream);
+}
+
+int ssm_test_ssd_wait_fault(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                            void* y, int64_t batch, int64_t seqlen, int64_t nheads, int64_t ngroups, int64_t dstate,
+                            int64_t wait_limit, int withhold_arrive, void* stream) {
+    if (wait_limit < 1 || wait_limit > INT32_MAX) return SSM_ERR_DIM;
+    return ssd_impl(x, dt, A, B, C, nullptr, nullptr, nullptr, 1, nullptr, y, nullptr, batch, seqlen, nheads, 64,
+                    ngroups, dstate, SSM_BF16, SSM_BF16, (uint32_t)wait_limit, withhold_arrive, stream);
 }
 
 int64_t ssm_ssd_chunk_len(void) { return ssm::ssd_chunk_len(); }

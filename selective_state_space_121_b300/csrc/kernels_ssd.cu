@@ -157,8 +157,9 @@ __device__ __forceinline__ bool compute_any(bool v) {
     return r != 0;
 }
 // Bounded wait that also gives up once another warp has raised the abort flag.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-    for (uint32_t i = 0; i < kWaitLimit; i++) {
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              uint32_t limit) {
+    for (uint32_t i = 0; i < limit; i++) {
         if (tc::mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 63u && *abort_flag) return false;
     }
@@ -217,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t nchunks = (L + kQ - 1) / kQ;
     constexpr uint32_t kY = kOutF32 ? S::kYf32 : S::kYbf16;
     volatile int* abort_flag = &s_abort;
+    const uint32_t wlim = a.wait_limit ? a.wait_limit : kWaitLimit;   // pipeline waits (not the drain)
     auto fail = [&](int line) {
         atomicExch(&g_ssd_status, line);
         *abort_flag = 1;
@@ -304,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the control warp decides every wait as one (a lane that gave up while another
     // saw the phase complete would leave the warp split at its next __syncwarp)
     auto ctl_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-        return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag));
+        return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag, wlim));
     };
 
     if (warp == kCtl) {
@@ -519,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             {
                 uint64_t* bar = S::kStages == 2 ? &s_load[st] : &s_load[1];
                 const uint32_t p = S::kStages == 2 ? (uint32_t)((c >> 1) & 1) : par;
-                const bool ok = wait_or_abort(bar, p, abort_flag);
+                const bool ok = wait_or_abort(bar, p, abort_flag, wlim);
                 if (compute_any(!ok)) {
                     if (tid == 0) fail(__LINE__);
                     failed = true;
@@ -541,11 +543,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_proxy_async();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&s_ready[0]);
+            if (lane == 0 && !(a.withhold_arrive && warp == 0 && c == 0)) tc::mbar_arrive(&s_ready[0]);
             // ---- M from S: decay mask, split into the two A operands of G2 -----------
             {
-                bool ok = wait_or_abort(&s_bar[0], par, abort_flag);
-                if (ok && kOutF32 && c > 0) ok = wait_or_abort(&s_yfree, (uint32_t)((c - 1) & 1), abort_flag);
+                bool ok = wait_or_abort(&s_bar[0], par, abort_flag, wlim);
+                if (ok && kOutF32 && c > 0) ok = wait_or_abort(&s_yfree, (uint32_t)((c - 1) & 1), abort_flag, wlim);
                 if (compute_any(!ok)) {
                     if (tid == 0) fail(__LINE__);
                     failed = true;
@@ -599,8 +601,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // ---- products in; epilogue: y = Yi + exp(cs_t) Ye + D x, gated, staged ----
             {
-                bool ok = wait_or_abort(&s_bar[2], par, abort_flag) && wait_or_abort(&s_bar[1], par, abort_flag);
-                if (ok && zg) ok = wait_or_abort(&s_zload, par, abort_flag);
+                bool ok = wait_or_abort(&s_bar[2], par, abort_flag, wlim) &&
+                          wait_or_abort(&s_bar[1], par, abort_flag, wlim);
+                if (ok && zg) ok = wait_or_abort(&s_zload, par, abort_flag, wlim);
                 if (compute_any(!ok)) {
                     if (tid == 0) fail(__LINE__);
                     failed = true;

@@ -123,6 +123,11 @@ struct SsdArgs {
     int dstate;             // 64 or 128
     int softplus;
     int out_dtype;
+    // test hooks (0 in every product launch): wait budget of the pipeline waits in
+    // mbarrier polls (0: the default), and a withheld compute-side arrival (warp 0
+    // skips its first "w o x ready" arrive, so the control warp's wait runs out)
+    uint32_t wait_limit;
+    int withhold_arrive;
 };
 
 // Each returns cudaSuccess or the launch error.
