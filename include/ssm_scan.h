@@ -106,7 +106,7 @@ SSM_API const char* ssm_status_string(int status);
 /* Bytes of device workspace ssm_scan_fwd / ssm_scan_fwd_algo need for these
  * sizes under any algorithm (always >= 16 so that the status word fits). The
  * caller allocates it; the library zeroes what it uses, on `stream`, inside
- * each look-back call. */
+ * each look-back or time-serial call. */
 SSM_API size_t ssm_scan_workspace_size(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate);
 
 /* Selective scan, forward (prefill). See the operation above.
@@ -120,8 +120,12 @@ SSM_API size_t ssm_scan_workspace_size(int64_t batch, int64_t dim, int64_t seqle
  *   h0         : (batch, dim, dstate) fp32 initial state  [optional, zero]
  *   y          : (batch, dim, seqlen), out_dtype output   [required]
  *   h_last     : (batch, dim, dstate) fp32 final state    [optional]
- *   workspace  : device scratch of ssm_scan_workspace_size() bytes; may be NULL
- *                when the chosen algorithm needs none (only the look-back does).
+ *   workspace  : device scratch of ssm_scan_workspace_size() bytes, 16-byte
+ *                aligned; the look-back needs it (SSM_ERR_WORKSPACE without). The
+ *                time-serial algorithm uses it when given (NULL is allowed): its
+ *                CTAs then split the (channel group, time chunk) work evenly over
+ *                the SMs and pass the state across each split through it; without
+ *                it every CTA walks one channel group over the whole sequence.
  * y must not overlap any input; h_last may equal h0 (in-place resume). */
 SSM_API int ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
                          const void* C, const float* D, const void* z, const float* delta_bias,

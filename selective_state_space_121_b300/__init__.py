@@ -206,7 +206,7 @@ def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, 
         h_last = torch.empty((bt, dim, N), dtype=torch.float32, device=u.device)
     _out(y, (bt, dim, L), "y", device=u.device)
     _out(h_last, (bt, dim, N), "h_last", (torch.float32,), u.device)
-    if workspace is None and algo in ("auto", "lookback"):
+    if workspace is None and algo in ("auto", "thread", "lookback"):
         workspace = alloc_workspace(bt, dim, L, N, u.device)
     status = _lib.ssm_scan_fwd_algo(
         _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),

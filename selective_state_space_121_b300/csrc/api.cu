@@ -3,6 +3,8 @@
 // allocates nothing and never synchronises except in ssm_query_status.
 #include <string.h>
 
+#include <algorithm>
+
 #include "launch.h"
 #include "ssm_scan.h"
 
@@ -16,6 +18,9 @@ using ssm::ScanArgs;
 
 constexpr uint32_t kSpinLimit = 1u << 20;   // look-back waits: ~0.1-1 s before giving up
 constexpr int64_t kSMs = 148;               // B300
+// CTAs per SM the work-balanced time-serial form may use (its workspace is sized
+// for this many; the launch uses the kernel's actual occupancy, if smaller)
+constexpr int64_t kSerialBalCtasPerSM = 8;
 // look-back geometry (build options): CTAs per SM aimed at, shortest segment
 #ifndef SSM_LB_MIN_SEG
 #define SSM_LB_MIN_SEG 2048
@@ -117,6 +122,14 @@ Plan plan_scan(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int a
 
 size_t workspace_for(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int algo, int in_dtype) {
     Plan p = plan_scan(batch, dim, seqlen, dstate, algo, in_dtype);
+    if (p.algo == SSM_ALGO_THREAD && dstate > 1) {
+        // the work-balanced time-serial form: at most one CTA per channel group and
+        // kSerialBalCtasPerSM per SM
+        const int64_t cpc = ssm::serial_channels_per_cta((int)dstate, p.lanes_per_channel);
+        const int64_t units = ((dim + cpc - 1) / cpc) * batch;
+        const int64_t ctas = std::min<int64_t>(units, kSMs * kSerialBalCtasPerSM);
+        return std::max<size_t>(16, ssm::serial_bal_workspace_bytes(ctas, (int)dstate, p.lanes_per_channel));
+    }
     if (p.algo != SSM_ALGO_LOOKBACK) return 16;
     return ssm::lookback_workspace_bytes(batch, dim, (int)dstate, p.n_seg);
 }
@@ -196,6 +209,11 @@ int scan_impl(const void* u, const void* delta, const float* A, const void* B, c
                                                                                        : SSM_ERR_LAUNCH;
     }
     if (p.algo == SSM_ALGO_THREAD) {
+        // an optional workspace enables the work-balanced form of the time-serial kernel
+        if (workspace && aligned(workspace, 16)) {
+            a.workspace = workspace;
+            a.workspace_bytes = workspace_bytes;
+        }
         const cudaError_t e = dstate == 1 ? ssm::launch_scan_scalar(a, s)
                                           : ssm::launch_scan_thread(a, p.lanes_per_channel, s);
         return e == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
@@ -242,7 +260,7 @@ size_t ssm_scan_workspace_size(int64_t batch, int64_t dim, int64_t seqlen, int64
     // segments depend on how many channels one CTA holds, which depends on dtype)
     size_t need = 16;
     for (int dt : {(int)SSM_F32, (int)SSM_BF16})
-        for (int algo : {(int)SSM_ALGO_AUTO, (int)SSM_ALGO_LOOKBACK}) {
+        for (int algo : {(int)SSM_ALGO_AUTO, (int)SSM_ALGO_THREAD, (int)SSM_ALGO_LOOKBACK}) {
             const size_t w = workspace_for(batch, dim, seqlen, dstate, algo, dt);
             if (w > need) need = w;
         }

@@ -55,6 +55,8 @@
 #include <cudaTypedefs.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 #include "tcgen05.cuh"
@@ -192,6 +194,15 @@ struct ScanMaps {
 
 __device__ int g_prefill_status;   // 0, or the line of a bulk-copy wait that ran out of budget
 constexpr uint32_t kTmaWaitLimit = 1u << 24;
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 // The chunk tiles of a CTA (separate arrays, not one struct, so the compiler sees
 // that the partial-sum stores cannot alias the operand loads of later steps), and
@@ -734,55 +745,137 @@ __device__ __forceinline__ float lane_state(const LaneStateT<N, G, K>& S, int k,
     else return lo_hi(S.h2[k][i / 2], i);
 }
 
+// Two launch forms of the time-serial kernel.
+//   Plain (bal_ctas == 0): CTA (x, y) walks channel group x of batch row y over all
+//     L steps. Every CTA does the same work, so the kernel takes as long as the SM
+//     holding the most CTAs: at (4, 5120, 4096) 640 CTAs leave 48 SMs with five and
+//     100 with four, and the kernel ran as long as with five on every SM.
+//   Work-balanced (bal_ctas = P > 0, a multiple of the SM count, at most the number
+//     of channel groups U): the U (channel group, batch row) units, each of
+//     nch = ceil(L / T) chunks, are laid end to end and cut into P equal runs at
+//     chunk boundaries. A run of at least nch chunks is the tail of one unit (from
+//     chunk kF), any whole units, and the head of the last (to chunk kLe). The CTA
+//     takes its run by an atomic ticket, walks the head first (from h0) and
+//     publishes the state at its end in its workspace slot, then the whole units,
+//     then the tail, whose starting state is the previous ticket's published slot.
+//     That CTA published after kF chunks of work and this one reaches its tail after
+//     kLe + (whole units) nch >= kF chunks, so at equal speed the wait is free; a
+//     CTA only waits on an earlier ticket, whose CTA is running, so the wait always
+//     ends. Each wait is bounded; on expiry the kernel records the line in
+//     g_prefill_status and continues from a zero state (y is then unspecified).
+//   Workspace: [4] ticket counter (zeroed by the host), flags[P] at 16, then P state
+//   slots of (channels per CTA) x N floats.
 template <int N, int G, typename Tin, typename Tout, bool kVec, bool kTma>
 // at most 128 registers (4 CTAs per SM): measured ~1% faster than unbounded
 __global__ void __launch_bounds__(kThreads, 4) serial_scan_kernel(ScanArgs a, const __grid_constant__ ScanMaps maps) {
     constexpr int K = 1;
     using Cfg = SerialCfg<N, G, Tin, K>;
     constexpr int NPL = Cfg::NPL, CPW = Cfg::CPW, kT = Cfg::kT;
+    constexpr int CPC = kWarps * CPW;
     __shared__ __align__(16) float s_bc[2][kT][2 * N];
     __shared__ __align__(16) float s_db[kWarps][CPW / K][Cfg::DBS];
     __shared__ __align__(16) float4 s_p[kWarps][K][kT / 4][Cfg::PS];
     __shared__ __align__(1024) unsigned char s_stage[kTma ? StageGeom<N, G, Tin, K>::BYTES : 16];
     __shared__ __align__(8) uint64_t s_full;
-    const Tiles<N, G, Tin, K> tl{s_bc, s_db, s_p, s_stage, &s_full, &maps,
-                                 (int64_t)blockIdx.x * kWarps * CPW};
+    __shared__ uint32_t s_ticket;
+    const bool bal = a.bal_ctas > 0;
     uint32_t phase = 0;
-    if (kTma) {
-        if (threadIdx.x == 0) {
+    if (threadIdx.x == 0) {
+        if (kTma) {
             tc::mbar_init(&s_full, 1);
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
-        __syncthreads();
+        if (bal) s_ticket = atomicAdd(reinterpret_cast<uint32_t*>(static_cast<char*>(a.workspace) + 4), 1u);
     }
+    __syncthreads();
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t b = blockIdx.y;
-    const int64_t d_warp0 = ((int64_t)blockIdx.x * kWarps + warp) * CPW;
     const int p = lane_grp<G, K>(lane), j = lane_sgrp<G, K>(lane);
-    int64_t dR[K];
-    bool okR[K];
-    float h0[K][NPL];
-#pragma unroll
-    for (int k = 0; k < K; k++) {
-        dR[k] = d_warp0 + p * K + k;
-        okR[k] = dR[k] < a.dim;
-#pragma unroll
-        for (int i = 0; i < NPL; i++)
-            h0[k][i] = (okR[k] && a.h0) ? a.h0[(b * a.dim + dR[k]) * N + j * NPL + i] : 0.f;
+    const int64_t L = a.seqlen;
+    const int64_t groups = (a.dim + CPC - 1) / CPC;
+    const int64_t nch = (L + kT - 1) / kT;
+    uint32_t* flags = nullptr;
+    float* slots = nullptr;
+    int64_t c = 0, uF, kF, uL, kLe;
+    if (bal) {
+        const int64_t P = a.bal_ctas, W = groups * a.batch * nch;
+        const int64_t Wq = W / P, Wr = W % P;
+        auto cut = [&](int64_t i) { return i * Wq + (i * Wr) / P; };
+        c = s_ticket;
+        const int64_t w0 = cut(c), w1 = cut(c + 1);
+        uF = w0 / nch; kF = w0 % nch;
+        uL = (w1 - 1) / nch; kLe = w1 - uL * nch;
+        flags = reinterpret_cast<uint32_t*>(static_cast<char*>(a.workspace) + kSerialBalFlags);
+        slots = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + serial_bal_slots_offset(P));
+    } else {
+        uF = uL = (int64_t)blockIdx.y * groups + blockIdx.x;
+        kF = 0; kLe = nch;
     }
-    A2Arr<N, G, K> A2;
-    LaneStateT<N, G, K> S;
-    lane_init<N, G, K>(a, dR, okR, j, A2, S, h0);
-    if (!serial_pass<N, G, K, Tin, Tout, kVec, true, kTma>(a, b, d_warp0, 0, a.seqlen, A2, S, tl, &phase)) return;
-    if (a.h_last) {
+    // pieces in order: the head of unit uL, whole units uF+1 .. uL-1, the tail of uF
+    // (one piece when the run lies in one unit)
+    const int64_t n_pieces = uF == uL ? 1 : uL - uF + 1;
+    for (int64_t pi = 0; pi < n_pieces; pi++) {
+        int64_t u, kb, ke;
+        if (n_pieces == 1) { u = uF; kb = kF; ke = kLe; }
+        else if (pi == 0) { u = uL; kb = 0; ke = kLe; }
+        else if (pi + 1 < n_pieces) { u = uF + pi; kb = 0; ke = nch; }
+        else { u = uF; kb = kF; ke = nch; }
+        const int64_t b = u / groups, grp = u % groups;
+        const int64_t tb = kb * kT, te = min(L, ke * kT);
+        const bool dep = bal && kb > 0, pub = bal && ke < nch;
+        const int64_t d_warp0 = (grp * kWarps + warp) * CPW;
+        // starting state: h0 at step 0, else the previous ticket's published slot
+        bool got = true;
+        if (dep) {
+            uint32_t spins = 0;
+            while (ld_acquire(&flags[c - 1]) == 0 && spins < a.spin_limit) {
+                ++spins;
+                __nanosleep(64);
+            }
+            got = ld_acquire(&flags[c - 1]) != 0;
+            if (!got && threadIdx.x == 0) atomicExch(&g_prefill_status, __LINE__);
+        }
+        int64_t dR[K];
+        bool okR[K];
+        float h0[K][NPL];
 #pragma unroll
-        for (int k = 0; k < K; k++)
-            if (okR[k]) {
+        for (int k = 0; k < K; k++) {
+            dR[k] = d_warp0 + p * K + k;
+            okR[k] = dR[k] < a.dim;
+            const int slot_ch = warp * CPW + p * K + k;
+#pragma unroll
+            for (int i = 0; i < NPL; i++) {
+                float v = 0.f;
+                if (dep) v = got ? __ldcg(slots + ((c - 1) * CPC + slot_ch) * N + j * NPL + i) : 0.f;
+                else if (okR[k] && a.h0) v = a.h0[(b * a.dim + dR[k]) * N + j * NPL + i];
+                h0[k][i] = v;
+            }
+        }
+        A2Arr<N, G, K> A2;
+        LaneStateT<N, G, K> S;
+        lane_init<N, G, K>(a, dR, okR, j, A2, S, h0);
+        const Tiles<N, G, Tin, K> tl{s_bc, s_db, s_p, s_stage, &s_full, &maps, grp * CPC};
+        if (!serial_pass<N, G, K, Tin, Tout, kVec, true, kTma>(a, b, d_warp0, tb, te, A2, S, tl, &phase)) return;
+        if (te == L && a.h_last) {
+#pragma unroll
+            for (int k = 0; k < K; k++)
+                if (okR[k]) {
+#pragma unroll
+                    for (int i = 0; i < NPL; i++)
+                        a.h_last[(b * a.dim + dR[k]) * N + j * NPL + i] = lane_state<N, G, K, Tin>(S, k, i);
+                }
+        }
+        if (pub) {
+            const int slot_ch0 = warp * CPW + p * K;
+#pragma unroll
+            for (int k = 0; k < K; k++)
 #pragma unroll
                 for (int i = 0; i < NPL; i++)
-                    a.h_last[(b * a.dim + dR[k]) * N + j * NPL + i] = lane_state<N, G, K, Tin>(S, k, i);
-            }
+                    slots[(c * CPC + slot_ch0 + k) * N + j * NPL + i] = lane_state<N, G, K, Tin>(S, k, i);
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) st_release(&flags[c], 1u);
+        }
     }
 }
 
@@ -816,15 +909,6 @@ struct LbDesc {
     float H[N];
     float I[N];
 };
-
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 
 // kLookbackCtasPerSM CTAs per SM at least (the host plans the segments for exactly
 // that many resident CTAs: none may wait for a slot)
@@ -1035,24 +1119,44 @@ bool make_maps(const ScanArgs& a, ScanMaps* maps) {
 }
 
 template <int N, int G, typename Tin, typename Tout>
-cudaError_t launch_serial(const ScanArgs& a, cudaStream_t s) {
+cudaError_t launch_serial(const ScanArgs& a_in, cudaStream_t s) {
     using Cfg = SerialCfg<N, G, Tin, 1>;
-    if (a.batch == 0 || a.dim == 0) return cudaSuccess;
+    if (a_in.batch == 0 || a_in.dim == 0) return cudaSuccess;
+    ScanArgs a = a_in;
+    a.bal_ctas = 0;
     const int64_t ch_per_cta = (int64_t)kWarps * Cfg::CPW;
-    dim3 grid((unsigned)((a.dim + ch_per_cta - 1) / ch_per_cta), (unsigned)a.batch);
+    const int64_t groups = (a.dim + ch_per_cta - 1) / ch_per_cta;
+    const int64_t units = groups * a.batch;
     ScanMaps maps;
-    bool launched = false;
+    memset(&maps, 0, sizeof(maps));
+    using KernelFn = void (*)(ScanArgs, ScanMaps);
+    KernelFn k = nullptr;
     if constexpr (sizeof(Tin) == 2) {
-        if (make_maps<N, G, 1, Tin>(a, &maps)) {
-            serial_scan_kernel<N, G, Tin, Tout, true, true><<<grid, kThreads, 0, s>>>(a, maps);
-            launched = true;
-        }
-    } else {
-        memset(&maps, 0, sizeof(maps));
+        if (make_maps<N, G, 1, Tin>(a, &maps)) k = serial_scan_kernel<N, G, Tin, Tout, true, true>;
     }
-    if (launched) {
-    } else if (a.vec) serial_scan_kernel<N, G, Tin, Tout, true, false><<<grid, kThreads, 0, s>>>(a, maps);
-    else serial_scan_kernel<N, G, Tin, Tout, false, false><<<grid, kThreads, 0, s>>>(a, maps);
+    if (!k) k = a.vec ? serial_scan_kernel<N, G, Tin, Tout, true, false> : serial_scan_kernel<N, G, Tin, Tout, false, false>;
+    // the work-balanced form when a workspace is given and the units do not already
+    // divide evenly over the SMs: a multiple of the SM count, all CTAs resident
+    int64_t P = 0;
+    if (a.workspace && a.seqlen > 0) {
+        int dev = 0, sms = 0, occ = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kThreads, 0) == cudaSuccess && sms > 0 &&
+            units >= sms) {
+            P = std::min<int64_t>((int64_t)occ * sms, (units / sms) * sms);
+            if (P >= units || serial_bal_workspace_bytes(P, N, G) > a.workspace_bytes) P = 0;
+        }
+    }
+    if (P > 0) {
+        a.bal_ctas = P;
+        const cudaError_t e = cudaMemsetAsync(a.workspace, 0, serial_bal_slots_offset(P), s);
+        if (e != cudaSuccess) return e;
+        k<<<(unsigned)P, kThreads, 0, s>>>(a, maps);
+    } else {
+        if (groups > 0x7fffffff || a.batch > 65535) return cudaErrorInvalidValue;
+        k<<<dim3((unsigned)groups, (unsigned)a.batch), kThreads, 0, s>>>(a, maps);
+    }
     return cudaGetLastError();
 }
 
@@ -1139,6 +1243,13 @@ cudaError_t prefill_status(int* line, bool clear, cudaStream_t s) {
         if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     }
     return e;
+}
+
+int serial_channels_per_cta(int dstate, int lanes_per_channel) { return kWarps * 32 / lanes_per_channel; }
+
+size_t serial_bal_workspace_bytes(int64_t ctas, int dstate, int lanes_per_channel) {
+    return serial_bal_slots_offset(ctas) +
+           (size_t)ctas * (size_t)serial_channels_per_cta(dstate, lanes_per_channel) * (size_t)dstate * sizeof(float);
 }
 
 size_t lookback_workspace_bytes(int64_t batch, int64_t dim, int dstate, int64_t n_seg) {

@@ -26,12 +26,17 @@ struct ScanArgs {
     int softplus;
     int in_dtype, out_dtype;
     bool vec;          // rows of u/delta/z/y/B/C are 16-byte aligned (vector loads allowed)
-    // look-back only
+    // look-back, and the work-balanced time-serial form
     void* workspace;
+    size_t workspace_bytes;
     int64_t seg_len;   // time steps per look-back segment (multiple of the chunk)
     int64_t n_seg;
     uint32_t spin_limit;
     int64_t drop_segment;   // test hook: this segment withholds its publication (-1: none)
+    // time-serial kernel: 0, or the CTA count of the work-balanced form (the CTAs
+    // split the (channel group, chunk) work evenly and pass the state across each
+    // split point through `workspace`)
+    int64_t bal_ctas;
     // directional scans (launch_scan_dir only): traversal order 0 raster, 1 reversed,
     // 2 column-major of a rows x cols image, 3 reversed columns; zoh: exact
     // zero-order-hold input matrix (exp(dt A) - 1) / A * B instead of dt * B
@@ -167,5 +172,13 @@ constexpr int kLookbackCtasPerSM = SSM_LB_CTAS_PER_SM;
 constexpr int kWarpScanItems = 8;                    // time steps per lane per chunk
 constexpr int kWarpScanChunk = 32 * kWarpScanItems;  // time steps per warp chunk
 size_t lookback_workspace_bytes(int64_t batch, int64_t dim, int dstate, int64_t n_seg);
+// Work-balanced time-serial scan: channels one CTA holds, and the workspace bytes
+// for `ctas` CTAs (a 16-byte header with the ticket counter, one flag per CTA, one
+// state slot of channels x dstate floats per CTA).
+int serial_channels_per_cta(int dstate, int lanes_per_channel);
+size_t serial_bal_workspace_bytes(int64_t ctas, int dstate, int lanes_per_channel);
+// byte offset of the flags and of the state slots in that workspace
+constexpr size_t kSerialBalFlags = 16;
+__host__ __device__ inline size_t serial_bal_slots_offset(int64_t ctas) { return kSerialBalFlags + (((size_t)ctas * 4 + 15) / 16) * 16; }
 
 }  // namespace ssm

@@ -215,3 +215,56 @@ def test_full_size_long_fp32_y_every_algorithm(ssm):
     inp = W.make_scan_inputs(W.CONFIGS["long"])
     for algo in ("thread", "warpscan", "lookback"):
         _check_sampled(ssm, inp, algo, count=12, out_dtype=torch.float32)
+
+
+# -- the work-balanced form of the time-serial kernel ------------------------------------
+# With a workspace and at least one channel group (32 channels of one batch row) per
+# SM, the time-serial kernel cuts the (channel group, chunk) work into runs of equal
+# length, a multiple of the SM count of them, and hands the state across each cut.
+# (5, 1000): 160 groups on 148 CTAs, runs of 1.08 groups (a tail and a head each);
+# (16, 3000): 1504 groups on at most 148 x (resident CTAs per SM) CTAs, runs of two
+# or more groups (a tail, whole groups, a head).
+BAL_SHAPES = [(5, 1000, 1000), (16, 3000, 256)]
+
+
+def _serial(ssm, inp, balanced, out_dtype=torch.float32):
+    t = scan_to_torch(inp)
+    ws = None if balanced else torch.empty(16, dtype=torch.uint8, device="cuda")   # too small: plain form
+    y, h = ssm.scan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"],
+                        inp["softplus"], t["h0"], out_dtype=out_dtype, algo="thread", workspace=ws)
+    torch.cuda.synchronize()
+    assert ssm.device_status() == 0
+    return y, h
+
+
+@pytest.mark.parametrize("shape", BAL_SHAPES)
+def test_balanced_serial_matches_oracle(ssm, shape):
+    bt, dim, L = shape
+    inp = W.make_scan_inputs(W.CONFIGS["mamba130m"], batch=bt, dim=dim, seqlen=L)
+    y, h = _serial(ssm, inp, True)
+    yr, hr = oracle.scan_inputs(inp)
+    tol = tol_for(inp["cfg"].in_dtype)
+    assert_y_close(to_np(y), yr, tol, False)
+    assert_state_close(to_np(h), hr, tol)
+
+
+@pytest.mark.parametrize("shape", BAL_SHAPES)
+def test_balanced_serial_bitwise_equals_plain(ssm, shape):
+    """bf16 inputs: the state crosses each cut as the fp32 values the lane holds, so
+    the balanced form does exactly the plain form's arithmetic."""
+    bt, dim, L = shape
+    inp = W.make_scan_inputs(W.CONFIGS["mamba130m"], batch=bt, dim=dim, seqlen=L)
+    y1, h1 = _serial(ssm, inp, True, None)
+    y2, h2 = _serial(ssm, inp, False, None)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    assert torch.equal(h1.view(torch.int32), h2.view(torch.int32))
+
+
+def test_balanced_serial_fp32_inputs(ssm):
+    """fp32 inputs (1e-5): the anchored state is handed over as one fp32 value."""
+    inp = W.make_scan_inputs(W.CONFIGS["tiny"], batch=5, dim=1000, seqlen=700, dstate=16)
+    y, h = _serial(ssm, inp, True)
+    yr, hr = oracle.scan_inputs(inp)
+    tol = tol_for(inp["cfg"].in_dtype)
+    assert_y_close(to_np(y), yr, tol, False)
+    assert_state_close(to_np(h), hr, tol)
