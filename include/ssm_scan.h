@@ -309,8 +309,11 @@ SSM_API int ssm_ssd_scan_fwd(const void* x, const void* dt, const float* A, cons
 /* Chunk length (time steps) of ssm_ssd_scan_fwd. */
 SSM_API int64_t ssm_ssd_chunk_len(void);
 
-/* Synchronises `stream`, then returns SSM_ERR_WAIT_TIMEOUT if an SSD launch since
- * the last clear recorded a wait that ran out of its budget, else SSM_OK
+/* Synchronises `stream`, then returns SSM_ERR_WAIT_TIMEOUT if, since the last
+ * clear, a launch recorded a wait that ran out of its budget -- an SSD
+ * tensor-core or copy wait, a bulk-copy wait of the prefill kernels (the
+ * d_state = 1 kernel's included), or the state hand-over wait of the
+ * work-balanced time-serial kernel -- else SSM_OK
  * (SSM_ERR_LAUNCH if the read itself failed). clear != 0 resets the record. */
 SSM_API int ssm_device_status(int clear, void* stream);
 

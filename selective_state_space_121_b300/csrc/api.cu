@@ -582,10 +582,11 @@ int ssm_test_ssd_wait_fault(const void* x, const void* dt, const float* A, const
 int64_t ssm_ssd_chunk_len(void) { return ssm::ssd_chunk_len(); }
 
 int ssm_device_status(int clear, void* stream) {
-    int line = 0, line2 = 0;
+    int line = 0, line2 = 0, line3 = 0;
     if (ssm::ssd_status(&line, clear != 0, (cudaStream_t)stream) != cudaSuccess) return SSM_ERR_LAUNCH;
     if (ssm::prefill_status(&line2, clear != 0, (cudaStream_t)stream) != cudaSuccess) return SSM_ERR_LAUNCH;
-    return (line != 0 || line2 != 0) ? SSM_ERR_WAIT_TIMEOUT : SSM_OK;
+    if (ssm::scalar_status(&line3, clear != 0, (cudaStream_t)stream) != cudaSuccess) return SSM_ERR_LAUNCH;
+    return (line != 0 || line2 != 0 || line3 != 0) ? SSM_ERR_WAIT_TIMEOUT : SSM_OK;
 }
 
 int ssm_scan_fwd_dir(const void* u, const void* delta, const float* A, const void* B, const void* C,

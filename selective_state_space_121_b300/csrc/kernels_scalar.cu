@@ -469,6 +469,17 @@ cudaError_t launch(const ScanArgs& a, cudaStream_t s) {
 
 }  // namespace
 
+cudaError_t scalar_status(int* line, bool clear, cudaStream_t s) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(line, g_scalar_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess && clear && *line != 0) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbolAsync(g_scalar_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    }
+    return e;
+}
+
 cudaError_t launch_scan_scalar(const ScanArgs& a, cudaStream_t s) {
     if (a.in_dtype == kBF16)
         return a.out_dtype == kBF16 ? launch<__nv_bfloat16, __nv_bfloat16>(a, s) : launch<__nv_bfloat16, float>(a, s);

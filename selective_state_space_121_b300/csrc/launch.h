@@ -157,6 +157,9 @@ cudaError_t launch_scan_serial_lookback(const ScanArgs& a, int lanes_per_channel
 int lookback_channels_per_cta(int dstate, int lanes_per_channel, int in_dtype);
 cudaError_t launch_scan_thread(const ScanArgs& a, int lanes_per_channel, cudaStream_t s);
 cudaError_t launch_scan_scalar(const ScanArgs& a, cudaStream_t s);
+// the d_state = 1 kernel's device status word: 0 or the line of a bulk-copy wait
+// that ran out of budget (synchronises the stream)
+cudaError_t scalar_status(int* line, bool clear, cudaStream_t s);
 
 // Look-back residency: the look-back kernel's launch bounds guarantee this many CTAs
 // per SM and the host plans its segments so that every CTA is resident at once
