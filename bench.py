@@ -825,10 +825,11 @@ def time_case(only, config, algo, steps, warmup, dev):
         odt = torch.bfloat16 if cfg.out_dtype == W.BF16 else torch.float32
         y = torch.empty((cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim), dtype=odt, device=dev)
         hl = torch.empty((cfg.batch, cfg.nheads, cfg.headdim, cfg.dstate), dtype=torch.float32, device=dev)
+        ssd_ws = torch.empty(ssm.ssd_workspace_size(cfg.batch, cfg.nheads, cfg.dstate), dtype=torch.uint8, device=dev)
 
         def launch():
             ssm.ssd_scan_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["z"], t["dt_bias"], True, t["h0"],
-                             y=y, h_last=hl)
+                             y=y, h_last=hl, workspace=ssd_ws)
         tokch = cfg.tokens_channels
         nbytes = ssd_bytes(cfg.batch, cfg.seqlen, cfg.nheads, cfg.headdim, cfg.ngroups, cfg.dstate,
                            2 if odt == torch.bfloat16 else 4, cfg.has_z, cfg.h0 != "zero")

@@ -306,6 +306,25 @@ SSM_API int ssm_ssd_scan_fwd(const void* x, const void* dt, const float* A, cons
                              int64_t nheads, int64_t headdim, int64_t ngroups, int64_t dstate,
                              int in_dtype, int out_dtype, void* stream);
 
+/* ssm_ssd_scan_fwd with a device workspace (16-byte aligned, `workspace_bytes`
+ * of it; ssm_ssd_workspace_size() bytes enable everything). When the batch *
+ * nheads sequences do not fill whole rounds of the resident CTAs, the CTAs then
+ * split the (sequence, 128-step chunk) work into equal runs, a multiple of the SM
+ * count of them, each walking the head of one sequence, any whole sequences and
+ * the tail of another, and pass the 64 x dstate state across each split through
+ * the workspace (the library zeroes what it uses, on `stream`). Otherwise, or with
+ * a NULL or smaller workspace, it is ssm_ssd_scan_fwd. A state hand-over wait
+ * that runs out is recorded like the other waits (ssm_device_status). */
+SSM_API int ssm_ssd_scan_fwd_ws(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                                const float* D, const void* z, const float* dt_bias, int softplus,
+                                const float* h0, void* y, float* h_last, int64_t batch, int64_t seqlen,
+                                int64_t nheads, int64_t headdim, int64_t ngroups, int64_t dstate,
+                                int in_dtype, int out_dtype, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/* Bytes of device workspace ssm_ssd_scan_fwd_ws uses for these sizes (>= 16). */
+SSM_API size_t ssm_ssd_workspace_size(int64_t batch, int64_t nheads, int64_t dstate);
+
 /* Chunk length (time steps) of ssm_ssd_scan_fwd. */
 SSM_API int64_t ssm_ssd_chunk_len(void);
 

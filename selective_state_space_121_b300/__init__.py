@@ -52,6 +52,10 @@ _lib.ssm_state_update.argtypes = [_P] * 9 + [_I, _P] + [_I64] * 3 + [_I, _I, _P]
 _lib.ssm_state_update.restype = _I
 _lib.ssm_test_lookback_timeout.argtypes = [_P] * 6 + [_I64] * 4 + [_I, _P, _SZ, _I64, ctypes.c_uint32, _P]
 _lib.ssm_test_lookback_timeout.restype = _I
+_lib.ssm_ssd_scan_fwd_ws.argtypes = [_P] * 8 + [_I, _P, _P, _P] + [_I64] * 6 + [_I, _I, _P, _SZ, _P]
+_lib.ssm_ssd_scan_fwd_ws.restype = _I
+_lib.ssm_ssd_workspace_size.argtypes = [_I64] * 3
+_lib.ssm_ssd_workspace_size.restype = _SZ
 _lib.ssm_test_ssd_wait_fault.argtypes = [_P] * 6 + [_I64] * 6 + [_I, _P]
 _lib.ssm_test_ssd_wait_fault.restype = _I
 _lib.ssm_query_status.argtypes = [_P, _SZ, _P]
@@ -95,7 +99,7 @@ EXPORTS = ("ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_size", "s
            "ssm_test_lookback_timeout", "ssm_query_status", "ssm_scan_fwd_lookback_static",
            "ssm_causal_conv1d_fwd", "ssm_causal_conv1d_update", "ssm_scan_bwd_workspace_size",
            "ssm_scan_bwd", "ssm_ssd_scan_fwd", "ssm_ssd_chunk_len", "ssm_device_status", "ssm_scan_fwd_dir",
-           "ssm_test_math", "ssm_test_ssd_wait_fault")
+           "ssm_test_math", "ssm_test_ssd_wait_fault", "ssm_ssd_scan_fwd_ws", "ssm_ssd_workspace_size")
 MATH = {"exp": 0, "log1p01": 1, "expm1": 2, "softplus": 3, "silu": 4, "softplus_sfu": 5, "silu_sfu": 6}
 
 
@@ -386,11 +390,17 @@ def causal_conv1d_update(conv_state, x, weight, bias=None, silu=True, *, out_dty
     return out
 
 
+def ssd_workspace_size(batch: int, nheads: int, dstate: int) -> int:
+    return int(_lib.ssm_ssd_workspace_size(batch, nheads, dstate))
+
+
 def ssd_scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, softplus=True, h0=None, *,
-                 out_dtype=None, y=None, h_last=None, return_last_state=True):
+                 out_dtype=None, y=None, h_last=None, return_last_state=True, workspace="auto"):
     """Mamba-2 SSD scan on the tensor cores. x, z: (batch, L, nheads, 64) bf16; dt: (batch,
     L, nheads) bf16; A, D, dt_bias: (nheads,) fp32; B, C: (batch, L, ngroups, dstate) bf16
-    with dstate 64 or 128; h0: (batch, nheads, 64, dstate) fp32. Returns (y, h_last)."""
+    with dstate 64 or 128; h0: (batch, nheads, 64, dstate) fp32. workspace: a uint8 device
+    tensor (ssd_workspace_size bytes enable the work-balanced launch), "auto" to allocate
+    one, or None for the one-sequence-per-CTA launch. Returns (y, h_last)."""
     bt, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     _same(x, [("dt", dt, (bt, L, H)), ("B", B, (bt, L, G, N)), ("C", C, (bt, L, G, N)), ("z", z, (bt, L, H, P))])
@@ -401,10 +411,12 @@ def ssd_scan_fwd(x, dt, A, B, C, D=None, z=None, dt_bias=None, softplus=True, h0
         h_last = torch.empty((bt, H, P, N), dtype=torch.float32, device=x.device)
     _out(y, (bt, L, H, P), "y", device=x.device)
     _out(h_last, (bt, H, P, N), "h_last", (torch.float32,), x.device)
-    status = _lib.ssm_ssd_scan_fwd(
+    if isinstance(workspace, str):
+        workspace = torch.empty(ssd_workspace_size(bt, H, N), dtype=torch.uint8, device=x.device)
+    status = _lib.ssm_ssd_scan_fwd_ws(
         _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias), int(bool(softplus)),
         _ptr(h0), _ptr(y), _ptr(h_last), bt, L, H, P, G, N, _dtype_code(x.dtype), _dtype_code(y.dtype),
-        _stream())
+        _ptr(workspace), _nbytes(workspace), _stream())
     _check(status)
     return y, h_last
 

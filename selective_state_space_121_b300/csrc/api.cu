@@ -21,6 +21,8 @@ constexpr int64_t kSMs = 148;               // B300
 // CTAs per SM the work-balanced time-serial form may use (its workspace is sized
 // for this many; the launch uses the kernel's actual occupancy, if smaller)
 constexpr int64_t kSerialBalCtasPerSM = 8;
+// CTAs per SM the work-balanced SSD launch may use (its workspace is sized for this many)
+constexpr int64_t kSsdBalCtasPerSM = 2;
 // look-back geometry (build options): CTAs per SM aimed at, shortest segment
 #ifndef SSM_LB_MIN_SEG
 #define SSM_LB_MIN_SEG 2048
@@ -521,7 +523,8 @@ int ssm_query_status(const void* workspace, size_t workspace_bytes, void* stream
 static int ssd_impl(const void* x, const void* dt, const float* A, const void* B, const void* C, const float* D,
                     const void* z, const float* dt_bias, int softplus, const float* h0, void* y, float* h_last,
                     int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t ngroups, int64_t dstate,
-                    int in_dtype, int out_dtype, uint32_t wait_limit, int withhold_arrive, void* stream) {
+                    int in_dtype, int out_dtype, void* workspace, size_t workspace_bytes, uint32_t wait_limit,
+                    int withhold_arrive, void* stream) {
     if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype) || in_dtype != SSM_BF16) return SSM_ERR_DTYPE;
     if (batch < 0 || seqlen < 0 || nheads < 0 || ngroups < 0) return SSM_ERR_DIM;
     if (headdim != 64 || (dstate != 64 && dstate != 128)) return SSM_ERR_SHAPE;
@@ -558,6 +561,12 @@ static int ssd_impl(const void* x, const void* dt, const float* A, const void* B
     a.y = y; a.h_last = h_last; a.batch = batch; a.seqlen = seqlen; a.nheads = nheads;
     a.ngroups = ngroups; a.dstate = (int)dstate; a.softplus = softplus ? 1 : 0; a.out_dtype = out_dtype;
     a.wait_limit = wait_limit; a.withhold_arrive = withhold_arrive ? 1 : 0;
+    if (workspace) {
+        if (!aligned(workspace, 16)) return SSM_ERR_ALIGN;
+        a.workspace = workspace;
+        a.workspace_bytes = workspace_bytes;
+    }
+    a.spin_limit = kSpinLimit;
     return ssm::launch_ssd_scan(a, (cudaStream_t)stream) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
 
@@ -568,7 +577,25 @@ int ssm_ssd_scan_fwd(const void* x, const void* dt, const float* A, const void* 
                      void* y, float* h_last, int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
                      int64_t ngroups, int64_t dstate, int in_dtype, int out_dtype, void* stream) {
     return ssd_impl(x, dt, A, B, C, D, z, dt_bias, softplus, h0, y, h_last, batch, seqlen, nheads, headdim, ngroups,
-                    dstate, in_dtype, out_dtype, 0, 0, stream);
+                    dstate, in_dtype, out_dtype, nullptr, 0, 0, 0, stream);
+}
+
+int ssm_ssd_scan_fwd_ws(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                        const float* D, const void* z, const float* dt_bias, int softplus, const float* h0,
+                        void* y, float* h_last, int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim,
+                        int64_t ngroups, int64_t dstate, int in_dtype, int out_dtype, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+    return ssd_impl(x, dt, A, B, C, D, z, dt_bias, softplus, h0, y, h_last, batch, seqlen, nheads, headdim, ngroups,
+                    dstate, in_dtype, out_dtype, workspace, workspace_bytes, 0, 0, stream);
+}
+
+size_t ssm_ssd_workspace_size(int64_t batch, int64_t nheads, int64_t dstate) {
+    if (batch < 0 || nheads < 0 || (dstate != 64 && dstate != 128)) return 16;
+    const int64_t units = mul(batch, nheads);
+    if (units < 0) return 16;
+    // at most one CTA per sequence and kSsdBalCtasPerSM per SM
+    const int64_t ctas = std::min<int64_t>(units, kSMs * kSsdBalCtasPerSM);
+    return std::max<size_t>(16, ssm::ssd_bal_workspace_bytes(ctas, (int)dstate));
 }
 
 int ssm_test_ssd_wait_fault(const void* x, const void* dt, const float* A, const void* B, const void* C,
@@ -576,7 +603,7 @@ int ssm_test_ssd_wait_fault(const void* x, const void* dt, const float* A, const
                             int64_t wait_limit, int withhold_arrive, void* stream) {
     if (wait_limit < 1 || wait_limit > INT32_MAX) return SSM_ERR_DIM;
     return ssd_impl(x, dt, A, B, C, nullptr, nullptr, nullptr, 1, nullptr, y, nullptr, batch, seqlen, nheads, 64,
-                    ngroups, dstate, SSM_BF16, SSM_BF16, (uint32_t)wait_limit, withhold_arrive, stream);
+                    ngroups, dstate, SSM_BF16, SSM_BF16, nullptr, 0, (uint32_t)wait_limit, withhold_arrive, stream);
 }
 
 int64_t ssm_ssd_chunk_len(void) { return ssm::ssd_chunk_len(); }

@@ -133,7 +133,17 @@ struct SsdArgs {
     // skips its first "w o x ready" arrive, so the control warp's wait runs out)
     uint32_t wait_limit;
     int withhold_arrive;
+    // work-balanced launch: 0, or the CTA count; the CTAs split the (sequence, chunk)
+    // work evenly and pass the state across each split through `workspace` (a
+    // 16-byte header with the ticket counter at byte 4, one flag per CTA, one state
+    // slot of 64 x dstate floats per CTA), waiting at most spin_limit polls
+    void* workspace;
+    size_t workspace_bytes;
+    int64_t bal_ctas;
+    uint32_t spin_limit;
 };
+__host__ __device__ inline size_t ssd_bal_slots_offset(int64_t ctas) { return 16 + (((size_t)ctas * 4 + 15) / 16) * 16; }
+size_t ssd_bal_workspace_bytes(int64_t ctas, int dstate);
 
 // Each returns cudaSuccess or the launch error.
 cudaError_t launch_scan_bwd(const BwdArgs& a, cudaStream_t s);

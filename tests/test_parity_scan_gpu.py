@@ -268,4 +268,3 @@ def test_balanced_serial_fp32_inputs(ssm):
     tol = tol_for(inp["cfg"].in_dtype)
     assert_y_close(to_np(y), yr, tol, False)
     assert_state_close(to_np(h), hr, tol)
-

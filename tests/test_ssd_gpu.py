@@ -163,3 +163,40 @@ def test_ssd_full_size_sampled(ssm):
                                  z[b:b + 1, :, h:h + 1], inp["dt_bias"][h:h + 1], True, None)
         assert_y_close(to_np(y[b:b + 1, :, h:h + 1]), yr, TOL, True, f"(b={b}, h={h})")
         assert_state_close(to_np(hl[b:b + 1, h:h + 1]), hr, TOL, f"h_last (b={b}, h={h})")
+
+
+# -- the work-balanced launch (a workspace, more sequences than SMs, not whole rounds) --
+# (2, 300, 80 heads): 160 sequences of 3 chunks on 148 CTAs, runs of 3.2 chunks (the
+# tail of one sequence and the head of the next); (3, 260, 100 heads), d_state 128,
+# 2 groups: 300 sequences, runs of 6.1 chunks (a tail, whole sequences, a head).
+BAL_CASES = [dict(batch=2, seqlen=300, nheads=80, ngroups=1, dstate=64),
+             dict(batch=3, seqlen=260, nheads=100, ngroups=2, dstate=128)]
+
+
+def _run_ws(ssm, inp, workspace, out_dtype=torch.float32):
+    t = ssd_to_torch(inp)
+    y, hl = ssm.ssd_scan_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["z"], t["dt_bias"], True, t["h0"],
+                             out_dtype=out_dtype, workspace=workspace)
+    torch.cuda.synchronize()
+    assert ssm.device_status() == 0
+    return y, hl
+
+
+@pytest.mark.parametrize("case", BAL_CASES, ids=["160seq", "300seq_N128"])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["y_f32", "y_bf16"])
+def test_ssd_balanced_matches_oracle(ssm, case, out_dtype):
+    inp = _inputs(**case)
+    y, hl = _run_ws(ssm, inp, "auto", out_dtype)
+    _check(y, hl, _oracle(inp), out_dtype, "balanced")
+
+
+@pytest.mark.parametrize("case", BAL_CASES, ids=["160seq", "300seq_N128"])
+def test_ssd_balanced_bitwise_equals_plain(ssm, case):
+    """The state crosses each split as the fp32 values in tensor memory and enters the
+    next piece on the path h0 takes (split for G3, rescaled for G4): the same
+    arithmetic as the one-sequence-per-CTA launch."""
+    inp = _inputs(**case)
+    y1, h1 = _run_ws(ssm, inp, "auto", torch.bfloat16)
+    y2, h2 = _run_ws(ssm, inp, None, torch.bfloat16)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    assert torch.equal(h1.view(torch.int32), h2.view(torch.int32))
