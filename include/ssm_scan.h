@@ -336,20 +336,37 @@ SSM_API int64_t ssm_ssd_chunk_len(void);
  * (SSM_ERR_LAUNCH if the read itself failed). clear != 0 resets the record. */
 SSM_API int ssm_device_status(int clear, void* stream);
 
-/* Test hook for the SSD kernel's failure path (Mamba SSM complete guide, section 6:
- * the same chunked SSD computation as ssm_ssd_scan_fwd, softplus on, no D, z,
+/* Test hook for the SSD kernel's failure paths (Mamba SSM complete guide, section 6:
+ * the same chunked SSD computation as ssm_ssd_scan_fwd_ws, softplus on, no D, z,
  * dt_bias, h0 or h_last; bf16 x, dt, B, C and y). Every pipeline wait of the
- * launch polls its mbarrier at most `wait_limit` times (1 .. 2^31 - 1, else
- * SSM_ERR_DIM); with withhold_arrive != 0 compute warp 0 skips its first
- * "w o x ready" arrival, so the control warp's wait for it runs out: the kernel
- * records the wait's source line, raises its abort flag, lets the tensor core and
- * the copies in flight finish, frees tensor memory and returns (y is then
- * unspecified). Returns the launch status; read the record with
+ * launch polls its mbarrier at most `wait_limit` times, and a state hand-over wait
+ * of the work-balanced launch polls its flag at most that many times (1 .. 2^31 - 1,
+ * else SSM_ERR_DIM). withhold_arrive != 0: compute warp 0 skips its first "w o x
+ * ready" arrival, so the control warp's wait for it runs out. drop_ticket >= 0 (with
+ * a workspace, as ssm_ssd_scan_fwd_ws): that ticket of the work-balanced launch
+ * withholds its state publication, so the next ticket's hand-over wait runs out.
+ * Either way the kernel records the wait's source line, raises its abort flag, lets
+ * the tensor core and the copies in flight finish, frees tensor memory and returns
+ * (y is then unspecified). Returns the launch status; read the record with
  * ssm_device_status(). Nothing faults or hangs. */
 SSM_API int ssm_test_ssd_wait_fault(const void* x, const void* dt, const float* A, const void* B,
                                     const void* C, void* y, int64_t batch, int64_t seqlen, int64_t nheads,
                                     int64_t ngroups, int64_t dstate, int64_t wait_limit,
-                                    int withhold_arrive, void* stream);
+                                    int withhold_arrive, void* workspace, size_t workspace_bytes,
+                                    int64_t drop_ticket, void* stream);
+
+/* Test hook for the state hand-over of the work-balanced time-serial scan (the
+ * time-serial algorithm of ssm_scan_fwd_algo with a workspace; softplus on, no D,
+ * z, bias, h0 or h_last; y in in_dtype): ticket `drop_ticket` withholds its state
+ * publication, so the next ticket's wait runs out after `spin_limit` polls; the
+ * kernel records it (ssm_device_status reports SSM_ERR_WAIT_TIMEOUT), continues
+ * from a zero state and finishes (y is then unspecified). Returns the launch
+ * status. */
+SSM_API int ssm_test_serial_handover_timeout(const void* u, const void* delta, const float* A,
+                                             const void* B, const void* C, void* y, int64_t batch,
+                                             int64_t dim, int64_t seqlen, int64_t dstate, int in_dtype,
+                                             void* workspace, size_t workspace_bytes,
+                                             int64_t drop_ticket, uint32_t spin_limit, void* stream);
 
 /* Test hook for the look-back error path. Runs the look-back scan (softplus on,
  * no D, z, bias or h0; y in in_dtype) with segment `drop_segment` withholding

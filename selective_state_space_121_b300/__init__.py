@@ -56,7 +56,9 @@ _lib.ssm_ssd_scan_fwd_ws.argtypes = [_P] * 8 + [_I, _P, _P, _P] + [_I64] * 6 + [
 _lib.ssm_ssd_scan_fwd_ws.restype = _I
 _lib.ssm_ssd_workspace_size.argtypes = [_I64] * 3
 _lib.ssm_ssd_workspace_size.restype = _SZ
-_lib.ssm_test_ssd_wait_fault.argtypes = [_P] * 6 + [_I64] * 6 + [_I, _P]
+_lib.ssm_test_ssd_wait_fault.argtypes = [_P] * 6 + [_I64] * 6 + [_I, _P, _SZ, _I64, _P]
+_lib.ssm_test_serial_handover_timeout.argtypes = [_P] * 6 + [_I64] * 4 + [_I, _P, _SZ, _I64, ctypes.c_uint32, _P]
+_lib.ssm_test_serial_handover_timeout.restype = _I
 _lib.ssm_test_ssd_wait_fault.restype = _I
 _lib.ssm_query_status.argtypes = [_P, _SZ, _P]
 _lib.ssm_query_status.restype = _I
@@ -99,7 +101,8 @@ EXPORTS = ("ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_size", "s
            "ssm_test_lookback_timeout", "ssm_query_status", "ssm_scan_fwd_lookback_static",
            "ssm_causal_conv1d_fwd", "ssm_causal_conv1d_update", "ssm_scan_bwd_workspace_size",
            "ssm_scan_bwd", "ssm_ssd_scan_fwd", "ssm_ssd_chunk_len", "ssm_device_status", "ssm_scan_fwd_dir",
-           "ssm_test_math", "ssm_test_ssd_wait_fault", "ssm_ssd_scan_fwd_ws", "ssm_ssd_workspace_size")
+           "ssm_test_math", "ssm_test_ssd_wait_fault", "ssm_ssd_scan_fwd_ws", "ssm_ssd_workspace_size",
+           "ssm_test_serial_handover_timeout")
 MATH = {"exp": 0, "log1p01": 1, "expm1": 2, "softplus": 3, "silu": 4, "softplus_sfu": 5, "silu_sfu": 6}
 
 
@@ -445,15 +448,26 @@ def test_math(fn: str, x: torch.Tensor) -> torch.Tensor:
     return y
 
 
-def run_ssd_wait_fault_test(x, dt, A, B, C, y, wait_limit: int, withhold_arrive: bool) -> int:
-    """Runs the SSD kernel's failure path (see ssm_test_ssd_wait_fault); returns the launch status."""
+def run_ssd_wait_fault_test(x, dt, A, B, C, y, wait_limit: int, withhold_arrive: bool, workspace=None,
+                            drop_ticket: int = -1) -> int:
+    """Runs the SSD kernel's failure paths (see ssm_test_ssd_wait_fault); returns the launch status."""
     bt, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     _same(x, [("dt", dt, (bt, L, H)), ("B", B, (bt, L, G, N)), ("C", C, (bt, L, G, N))])
     _f32(A, (H,), "A")
     _out(y, (bt, L, H, P), "y", (torch.bfloat16,), x.device)
     return int(_lib.ssm_test_ssd_wait_fault(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(y), bt, L, H, G, N,
-                                            int(wait_limit), int(bool(withhold_arrive)), _stream()))
+                                            int(wait_limit), int(bool(withhold_arrive)), _ptr(workspace),
+                                            _nbytes(workspace), int(drop_ticket), _stream()))
+
+
+def run_serial_handover_timeout_test(u, delta, A, B, C, y, workspace, drop_ticket: int, spin_limit: int) -> int:
+    """Runs the balanced time-serial scan with one ticket withholding its state
+    (see ssm_test_serial_handover_timeout); returns the launch status."""
+    bt, dim, L = u.shape
+    return int(_lib.ssm_test_serial_handover_timeout(
+        _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(y), bt, dim, L, A.shape[1], _dtype_code(u.dtype),
+        _ptr(workspace), _nbytes(workspace), int(drop_ticket), int(spin_limit), _stream()))
 
 
 def run_lookback_timeout_test(u, delta, A, B, C, y, workspace, drop_segment: int, spin_limit: int) -> int:

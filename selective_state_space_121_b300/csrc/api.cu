@@ -524,7 +524,7 @@ static int ssd_impl(const void* x, const void* dt, const float* A, const void* B
                     const void* z, const float* dt_bias, int softplus, const float* h0, void* y, float* h_last,
                     int64_t batch, int64_t seqlen, int64_t nheads, int64_t headdim, int64_t ngroups, int64_t dstate,
                     int in_dtype, int out_dtype, void* workspace, size_t workspace_bytes, uint32_t wait_limit,
-                    int withhold_arrive, void* stream) {
+                    int withhold_arrive, void* stream, int64_t drop_ticket = -1) {
     if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype) || in_dtype != SSM_BF16) return SSM_ERR_DTYPE;
     if (batch < 0 || seqlen < 0 || nheads < 0 || ngroups < 0) return SSM_ERR_DIM;
     if (headdim != 64 || (dstate != 64 && dstate != 128)) return SSM_ERR_SHAPE;
@@ -566,7 +566,8 @@ static int ssd_impl(const void* x, const void* dt, const float* A, const void* B
         a.workspace = workspace;
         a.workspace_bytes = workspace_bytes;
     }
-    a.spin_limit = kSpinLimit;
+    a.spin_limit = wait_limit ? wait_limit : kSpinLimit;
+    a.drop_ticket = drop_ticket;
     return ssm::launch_ssd_scan(a, (cudaStream_t)stream) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
 
@@ -600,10 +601,21 @@ size_t ssm_ssd_workspace_size(int64_t batch, int64_t nheads, int64_t dstate) {
 
 int ssm_test_ssd_wait_fault(const void* x, const void* dt, const float* A, const void* B, const void* C,
                             void* y, int64_t batch, int64_t seqlen, int64_t nheads, int64_t ngroups, int64_t dstate,
-                            int64_t wait_limit, int withhold_arrive, void* stream) {
+                            int64_t wait_limit, int withhold_arrive, void* workspace, size_t workspace_bytes,
+                            int64_t drop_ticket, void* stream) {
     if (wait_limit < 1 || wait_limit > INT32_MAX) return SSM_ERR_DIM;
     return ssd_impl(x, dt, A, B, C, nullptr, nullptr, nullptr, 1, nullptr, y, nullptr, batch, seqlen, nheads, 64,
-                    ngroups, dstate, SSM_BF16, SSM_BF16, nullptr, 0, (uint32_t)wait_limit, withhold_arrive, stream);
+                    ngroups, dstate, SSM_BF16, SSM_BF16, workspace, workspace_bytes, (uint32_t)wait_limit,
+                    withhold_arrive, stream, drop_ticket);
+}
+
+int ssm_test_serial_handover_timeout(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                                     void* y, int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                     int in_dtype, void* workspace, size_t workspace_bytes, int64_t drop_ticket,
+                                     uint32_t spin_limit, void* stream) {
+    return scan_impl(u, delta, A, B, C, nullptr, nullptr, nullptr, 1, nullptr, y, nullptr, batch, dim, seqlen,
+                     dstate, in_dtype, in_dtype, workspace, workspace_bytes, SSM_ALGO_THREAD, stream, drop_ticket,
+                     spin_limit);
 }
 
 int64_t ssm_ssd_chunk_len(void) { return ssm::ssd_chunk_len(); }

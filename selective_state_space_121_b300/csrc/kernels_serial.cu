@@ -874,7 +874,8 @@ __global__ void __launch_bounds__(kThreads, 4) serial_scan_kernel(ScanArgs a, co
                     slots[(c * CPC + slot_ch0 + k) * N + j * NPL + i] = lane_state<N, G, K, Tin>(S, k, i);
             __threadfence();
             __syncthreads();
-            if (threadIdx.x == 0) st_release(&flags[c], 1u);
+            // (test hook: ticket drop_segment withholds its publication)
+            if (threadIdx.x == 0 && c != a.drop_segment) st_release(&flags[c], 1u);
         }
     }
 }

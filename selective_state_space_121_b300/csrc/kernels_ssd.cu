@@ -832,7 +832,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     __threadfence();
                     compute_sync();
-                    if (tid == 0) st_release_u32(bal_flags() + s_run.ticket, 1u);
+                    // (test hook: ticket drop_ticket withholds its publication)
+                    if (tid == 0 && s_run.ticket != a.drop_ticket) st_release_u32(bal_flags() + s_run.ticket, 1u);
                 }
             }
             v0 += c1 - c0;

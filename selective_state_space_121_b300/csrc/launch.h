@@ -133,6 +133,7 @@ struct SsdArgs {
     // skips its first "w o x ready" arrive, so the control warp's wait runs out)
     uint32_t wait_limit;
     int withhold_arrive;
+    int64_t drop_ticket;    // test hook: this ticket withholds its state publication (-1: none)
     // work-balanced launch: 0, or the CTA count; the CTAs split the (sequence, chunk)
     // work evenly and pass the state across each split through `workspace` (a
     // 16-byte header with the ticket counter at byte 4, one flag per CTA, one state

@@ -43,3 +43,22 @@ def test_wait_budget_is_validated(ssm):
     for bad in (0, -1, 1 << 31):
         assert ssm.run_ssd_wait_fault_test(t["x"], t["dt"], t["A"], t["B"], t["C"], y, wait_limit=bad,
                                            withhold_arrive=False) == ssm.SSM_ERR_DIM
+
+
+def test_withheld_state_handover_is_reported_and_context_survives(ssm):
+    """Work-balanced launch (160 sequences on 148 CTAs): ticket 5 withholds the state
+    it would publish for ticket 6, whose hand-over wait then runs out after the short
+    budget. The kernel records it, drains and returns; a normal balanced run on the
+    same context afterwards matches the oracle."""
+    inp = _inputs(batch=2, seqlen=300, nheads=80, ngroups=1, dstate=64)
+    t = ssd_to_torch(inp)
+    ws = torch.empty(ssm.ssd_workspace_size(2, 80, 64), dtype=torch.uint8, device=t["x"].device)
+    assert ssm.device_status(clear=True) == 0
+    y = torch.empty(t["x"].shape, dtype=torch.bfloat16, device=t["x"].device)
+    rc = ssm.run_ssd_wait_fault_test(t["x"], t["dt"], t["A"], t["B"], t["C"], y, wait_limit=1 << 16,
+                                     withhold_arrive=False, workspace=ws, drop_ticket=5)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert ssm.device_status(clear=True) == ssm.SSM_ERR_WAIT_TIMEOUT
+    yn, hl = _run(ssm, inp)
+    _check(yn, hl, _oracle(inp), torch.float32, "after the withheld hand-over")
