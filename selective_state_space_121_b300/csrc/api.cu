@@ -23,9 +23,14 @@ constexpr int64_t kSMs = 148;               // B300
 constexpr int64_t kSerialBalCtasPerSM = 8;
 // CTAs per SM the work-balanced SSD launch may use (its workspace is sized for this many)
 constexpr int64_t kSsdBalCtasPerSM = 2;
-// look-back geometry (build options): CTAs per SM aimed at, shortest segment
+// look-back geometry (build options): CTAs per SM aimed at, shortest segment.
+// Measured with 2048 against 256 steps (the look-back chooses the segment count
+// to fill the SMs; the minimum binds only on shorter sequences): (8, 192, 3136, 16)
+// 276 -> 80 us (the warp scan took 112), (1, 1536, 16384, 16) 372 -> 269 us,
+// (8, 384, 784, 16) 74 -> 61 us (warp scan 65); the long (1, 1536, 131072, 16)
+// workload's segments are longer than either.
 #ifndef SSM_LB_MIN_SEG
-#define SSM_LB_MIN_SEG 2048
+#define SSM_LB_MIN_SEG 256
 #endif
 constexpr int64_t kLookbackCtasPerSM = ssm::kLookbackCtasPerSM;
 constexpr int64_t kLookbackMinSeg = SSM_LB_MIN_SEG;

@@ -886,9 +886,10 @@ __global__ void __launch_bounds__(kThreads, 4) serial_scan_kernel(ScanArgs a, co
 // so every segment a CTA waits on belongs to a CTA that has already started.
 // A CTA (1) runs the aggregate pass over its segment from a zero state, giving
 // each state's map over the segment: decay P = exp(A * sum dt) and offset H;
-// (2) publishes (P, H) with flag AGG; (3) walks back over earlier segments,
-// composing their maps until it meets a published inclusive prefix I (the state
-// at that segment's end), which gives its carry; (4) publishes its own inclusive
+// (2) publishes (P, H) with flag AGG; (3) walks back over earlier segments until
+// it meets a published inclusive prefix I (the state at that segment's end) and
+// applies the maps of the segments in between to it, in order, which gives its
+// carry (the same operations as a serial chain, so the result is deterministic); (4) publishes its own inclusive
 // prefix with flag INCL; (5) runs the full pass from the carry. The last segment
 // publishes nothing and skips (1). Every wait is bounded: on expiry the kernel
 // records SSM_ERR_LOOKBACK_TIMEOUT in the workspace status word, continues with
@@ -1011,11 +1012,13 @@ __global__ void __launch_bounds__(kThreads, kLookbackCtasPerSM)
                 }
                 st_release(&mine->flag[j], kFlagAgg);
             }
-            // (accP, accH): composed map of the segments strictly between the one
-            // inspected and this one
-            float accP[NPL], accH[NPL];
-#pragma unroll
-            for (int i = 0; i < NPL; i++) { accP[i] = Dec::one(); accH[i] = 0.f; }
+            // Walk back to the nearest segment whose inclusive prefix (the state at its
+            // end) is published, then apply the maps of the segments after it in
+            // order, h <- P h + H: the very operations a serial chain of inclusive
+            // prefixes performs, so the carry is the same bits whichever prefix the
+            // walk meets first (composing the maps backwards instead would round in
+            // an order that depends on timing).
+            int64_t found = -1;
             bool timed_out = false;
             for (int64_t s = seg - 1; s >= 0; s--) {
                 const LbDesc<N>* pd = desc + ch[k] * a.n_seg + s;
@@ -1027,21 +1030,23 @@ __global__ void __launch_bounds__(kThreads, kLookbackCtasPerSM)
                     f = ld_acquire(&pd->flag[j]);
                 }
                 if (f == 0) {
-#pragma unroll
-                    for (int i = 0; i < NPL; i++) carry[k][i] = accH[i];
                     timed_out = true;
                     break;
                 }
                 if (f == kFlagIncl) {
-#pragma unroll
-                    for (int i = 0; i < NPL; i++)
-                        carry[k][i] = Dec::step(accP[i], __ldcg(&pd->I[j * NPL + i]), accH[i]);
+                    found = s;
                     break;
                 }
+            }
+            if (!timed_out && found >= 0) {
+                const LbDesc<N>* pf = desc + ch[k] * a.n_seg + found;
 #pragma unroll
-                for (int i = 0; i < NPL; i++) {
-                    accH[i] = Dec::step(accP[i], __ldcg(&pd->H[j * NPL + i]), accH[i]);
-                    accP[i] = Dec::mul(accP[i], __ldcg(&pd->P[j * NPL + i]));
+                for (int i = 0; i < NPL; i++) carry[k][i] = __ldcg(&pf->I[j * NPL + i]);
+                for (int64_t s = found + 1; s < seg; s++) {
+                    const LbDesc<N>* pd = desc + ch[k] * a.n_seg + s;
+#pragma unroll
+                    for (int i = 0; i < NPL; i++)
+                        carry[k][i] = Dec::step(__ldcg(&pd->P[j * NPL + i]), carry[k][i], __ldcg(&pd->H[j * NPL + i]));
                 }
             }
             if (timed_out) atomicExch(status, kErrLookbackTimeout);
