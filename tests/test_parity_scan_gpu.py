@@ -278,3 +278,20 @@ def test_balanced_serial_fp32_inputs(ssm):
     tol = tol_for(inp["cfg"].in_dtype)
     assert_y_close(to_np(y), yr, tol, False)
     assert_state_close(to_np(h), hr, tol)
+
+
+@pytest.mark.parametrize("N,shape", [(8, (5, 1000, 700)), (4, (5, 1000, 700)), (2, (10, 1000, 700))],
+                         ids=["N8", "N4", "N2"])
+def test_balanced_serial_dstate_variants(ssm, N, shape):
+    """The balanced form at the other state widths (4 lanes per channel down to one
+    state per lane; 2 lanes per channel at N = 2, 64 channels per group), on shapes
+    with more groups than SMs, ragged in L."""
+    bt, dim, L = shape
+    inp = W.make_scan_inputs(W.CONFIGS["mamba130m"], batch=bt, dim=dim, seqlen=L, dstate=N)
+    y, h = _serial(ssm, inp, True)
+    yr, hr = oracle.scan_inputs(inp)
+    tol = tol_for(inp["cfg"].in_dtype)
+    assert_y_close(to_np(y), yr, tol, False)
+    assert_state_close(to_np(h), hr, tol)
+    y2, h2 = _serial(ssm, inp, False)
+    assert torch.equal(y, y2) and torch.equal(h, h2)
