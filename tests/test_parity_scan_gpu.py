@@ -295,3 +295,16 @@ def test_balanced_serial_dstate_variants(ssm, N, shape):
     assert_state_close(to_np(h), hr, tol)
     y2, h2 = _serial(ssm, inp, False)
     assert torch.equal(y, y2) and torch.equal(h, h2)
+
+
+@pytest.mark.parametrize("shape", [(5, 1000, 33), (5, 1000, 40), (7, 2000, 70), (5, 1000, 1)],
+                         ids=["L33", "L40", "L70", "L1"])
+def test_balanced_serial_short_and_ragged(ssm, shape):
+    """Cuts that fall on one-step tail chunks, single-chunk sequences and L = 1."""
+    bt, dim, L = shape
+    inp = W.make_scan_inputs(W.CONFIGS["mamba130m"], batch=bt, dim=dim, seqlen=L)
+    y, h = _serial(ssm, inp, True)
+    yr, hr = oracle.scan_inputs(inp)
+    tol = tol_for(inp["cfg"].in_dtype)
+    assert_y_close(to_np(y), yr, tol, False)
+    assert_state_close(to_np(h), hr, tol)

@@ -200,3 +200,11 @@ def test_ssd_balanced_bitwise_equals_plain(ssm, case):
     y2, h2 = _run_ws(ssm, inp, None, torch.bfloat16)
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
     assert torch.equal(h1.view(torch.int32), h2.view(torch.int32))
+
+
+@pytest.mark.parametrize("L", [1, 129, 385], ids=["L1", "L129", "L385"])
+def test_ssd_balanced_short_and_ragged(ssm, L):
+    """The work-balanced launch with one-chunk sequences and one-step tail chunks."""
+    inp = _inputs(batch=2, seqlen=L, nheads=80, ngroups=1, dstate=64)
+    y, hl = _run_ws(ssm, inp, "auto", torch.float32)
+    _check(y, hl, _oracle(inp), torch.float32, f"balanced L={L}")
