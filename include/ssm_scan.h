@@ -260,8 +260,8 @@ SSM_API int ssm_causal_conv1d_update(float* conv_state, const void* x, const flo
  * 2 ("Discretization"), (dt A)^-1 (exp(dt A) - 1) dt B = (exp(dt A) - 1) / A * B
  * per (d, n), and dt * B where A = 0; zoh == 0 gives ssm_scan_fwd's dt * B.
  * Tensors, layouts and the remaining arguments are those of ssm_scan_fwd (no
- * workspace: the warp-scan algorithm). Errors as ssm_scan_fwd, plus
- * SSM_ERR_ORDER. */
+ * workspace: the warp-scan algorithm; ssm_scan_fwd_dir_ws below takes one).
+ * Errors as ssm_scan_fwd, plus SSM_ERR_ORDER. */
 typedef enum {
     SSM_ORDER_RASTER = 0,
     SSM_ORDER_REVERSE = 1,
@@ -274,6 +274,20 @@ SSM_API int ssm_scan_fwd_dir(const void* u, const void* delta, const float* A, c
                              const float* h0, void* y, float* h_last, int64_t batch, int64_t dim,
                              int64_t seqlen, int64_t dstate, int order, int64_t rows, int64_t cols, int zoh,
                              int in_dtype, int out_dtype, void* stream);
+
+/* ssm_scan_fwd_dir with a device workspace (ssm_scan_workspace_size() bytes,
+ * 16-byte aligned; NULL allowed). Without the exact-ZOH input matrix, the raster
+ * walk, and for bf16 inputs with 16-byte aligned rows and dstate > 1 the reversed
+ * walk, then run on the prefill's own algorithms (the time-serial scan, or the
+ * look-back when the workspace holds it; the reversed walk mirrors each bulk copy
+ * and reverses each 8-step vector); every other case is ssm_scan_fwd_dir. Results
+ * agree with ssm_scan_fwd_dir to the prefill's tolerance, not bit for bit. */
+SSM_API int ssm_scan_fwd_dir_ws(const void* u, const void* delta, const float* A, const void* B,
+                                const void* C, const float* D, const void* z, const float* delta_bias,
+                                int softplus, const float* h0, void* y, float* h_last, int64_t batch,
+                                int64_t dim, int64_t seqlen, int64_t dstate, int order, int64_t rows,
+                                int64_t cols, int zoh, int in_dtype, int out_dtype, void* workspace,
+                                size_t workspace_bytes, void* stream);
 
 /* Mamba-2 state-space-duality (SSD) scan on the tensor cores (Mamba SSM
  * complete guide (youngju.dev), section 6 "Mamba 2": a multi-head SSM with one

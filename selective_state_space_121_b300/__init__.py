@@ -78,6 +78,8 @@ _lib.ssm_ssd_chunk_len.argtypes = []
 _lib.ssm_ssd_chunk_len.restype = _I64
 _lib.ssm_scan_fwd_dir.argtypes = [_P] * 8 + [_I, _P, _P, _P] + [_I64] * 4 + [_I, _I64, _I64, _I, _I, _I, _P]
 _lib.ssm_scan_fwd_dir.restype = _I
+_lib.ssm_scan_fwd_dir_ws.argtypes = [_P] * 8 + [_I, _P, _P, _P] + [_I64] * 4 + [_I, _I64, _I64, _I, _I, _I, _P, _SZ, _P]
+_lib.ssm_scan_fwd_dir_ws.restype = _I
 _lib.ssm_device_status.argtypes = [_I, _P]
 _lib.ssm_device_status.restype = _I
 _lib.ssm_test_math.argtypes = [_I, _P, _P, _I64, _P]
@@ -102,7 +104,7 @@ EXPORTS = ("ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_size", "s
            "ssm_causal_conv1d_fwd", "ssm_causal_conv1d_update", "ssm_scan_bwd_workspace_size",
            "ssm_scan_bwd", "ssm_ssd_scan_fwd", "ssm_ssd_chunk_len", "ssm_device_status", "ssm_scan_fwd_dir",
            "ssm_test_math", "ssm_test_ssd_wait_fault", "ssm_ssd_scan_fwd_ws", "ssm_ssd_workspace_size",
-           "ssm_test_serial_handover_timeout")
+           "ssm_test_serial_handover_timeout", "ssm_scan_fwd_dir_ws")
 MATH = {"exp": 0, "log1p01": 1, "expm1": 2, "softplus": 3, "silu": 4, "softplus_sfu": 5, "silu_sfu": 6}
 
 
@@ -225,10 +227,13 @@ def scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, 
 
 def scan_fwd_dir(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, h0=None, *,
                  order="raster", rows=0, cols=0, zoh=False, out_dtype=None, return_last_state=True, y=None,
-                 h_last=None):
+                 h_last=None, workspace="auto"):
     """Selective scan along a traversal order ("raster", "reverse", "columns",
     "columns_reverse" of a rows x cols image stored in raster order), outputs in
-    raster order; zoh selects the zero-order-hold input matrix. Shapes as scan_fwd."""
+    raster order; zoh selects the zero-order-hold input matrix. Shapes as scan_fwd.
+    workspace: a uint8 device tensor, "auto" to allocate one (the raster and reversed
+    walks may then take the time-serial or look-back algorithm), or None for the
+    warp-scan form alone."""
     bt, dim, L = u.shape
     N = A.shape[1]
     in_code = _dtype_code(u.dtype)
@@ -241,10 +246,19 @@ def scan_fwd_dir(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=Tr
         h_last = torch.empty((bt, dim, N), dtype=torch.float32, device=u.device)
     _out(y, (bt, dim, L), "y", device=u.device)
     _out(h_last, (bt, dim, N), "h_last", (torch.float32,), u.device)
-    status = _lib.ssm_scan_fwd_dir(
-        _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
-        int(bool(softplus)), _ptr(h0), _ptr(y), _ptr(h_last), bt, dim, L, N, ORDERS[order] if isinstance(order, str)
-        else int(order), int(rows), int(cols), int(bool(zoh)), in_code, _dtype_code(y.dtype), _stream())
+    order_code = ORDERS[order] if isinstance(order, str) else int(order)
+    if workspace is None:
+        status = _lib.ssm_scan_fwd_dir(
+            _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+            int(bool(softplus)), _ptr(h0), _ptr(y), _ptr(h_last), bt, dim, L, N, order_code, int(rows), int(cols),
+            int(bool(zoh)), in_code, _dtype_code(y.dtype), _stream())
+    else:
+        if isinstance(workspace, str):
+            workspace = alloc_workspace(bt, dim, L, N, u.device)
+        status = _lib.ssm_scan_fwd_dir_ws(
+            _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
+            int(bool(softplus)), _ptr(h0), _ptr(y), _ptr(h_last), bt, dim, L, N, order_code, int(rows), int(cols),
+            int(bool(zoh)), in_code, _dtype_code(y.dtype), _ptr(workspace), _nbytes(workspace), _stream())
     _check(status)
     return y, h_last
 

@@ -203,8 +203,25 @@ int scan_impl(const void* u, const void* delta, const float* A, const void* B, c
     a.spin_limit = spin_limit;
     cudaStream_t s = (cudaStream_t)stream;
     if (order >= 0) {
-        a.order = order; a.rows = rows; a.cols = cols; a.zoh = zoh ? 1 : 0;
-        return ssm::launch_scan_dir(a, s) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+        // The raster walk and (for bf16 inputs with 16-byte aligned rows, on the
+        // bulk-copy path) the reversed walk, without the exact-ZOH input matrix, take
+        // the prefill's own algorithms when they apply: the time-serial one, or the
+        // look-back when the workspace holds it. Everything else takes the warp scan
+        // with its per-step position map.
+        bool direct = false;
+        if (!zoh && (order == SSM_ORDER_RASTER ||
+                     (order == SSM_ORDER_REVERSE && in_dtype == SSM_BF16 && vec && dstate > 1 &&
+                      seqlen < ((int64_t)1 << 31) && dim < ((int64_t)1 << 31)))) {
+            if (p.algo == SSM_ALGO_THREAD) direct = true;
+            if (p.algo == SSM_ALGO_LOOKBACK && workspace && aligned(workspace, 16) &&
+                workspace_bytes >= ssm::lookback_workspace_bytes(batch, dim, (int)dstate, p.n_seg))
+                direct = true;
+        }
+        if (!direct) {
+            a.order = order; a.rows = rows; a.cols = cols; a.zoh = zoh ? 1 : 0;
+            return ssm::launch_scan_dir(a, s) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+        }
+        a.reverse = order == SSM_ORDER_REVERSE ? 1 : 0;
     }
     if (p.algo == SSM_ALGO_LOOKBACK) {
         const size_t need = ssm::lookback_workspace_bytes(batch, dim, (int)dstate, p.n_seg);
@@ -641,6 +658,17 @@ int ssm_scan_fwd_dir(const void* u, const void* delta, const float* A, const voi
     return scan_impl(u, delta, A, B, C, D, z, delta_bias, softplus, h0, y, h_last, batch, dim, seqlen, dstate,
                      in_dtype, out_dtype, nullptr, 0, SSM_ALGO_WARPSCAN, stream, -1, kSpinLimit, order, rows, cols,
                      zoh);
+}
+
+int ssm_scan_fwd_dir_ws(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                        const float* D, const void* z, const float* delta_bias, int softplus, const float* h0,
+                        void* y, float* h_last, int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                        int order, int64_t rows, int64_t cols, int zoh, int in_dtype, int out_dtype,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+    if (order < 0) return SSM_ERR_ORDER;
+    return scan_impl(u, delta, A, B, C, D, z, delta_bias, softplus, h0, y, h_last, batch, dim, seqlen, dstate,
+                     in_dtype, out_dtype, workspace, workspace_bytes, SSM_ALGO_AUTO, stream, -1, kSpinLimit, order,
+                     rows, cols, zoh);
 }
 
 }  // extern "C"

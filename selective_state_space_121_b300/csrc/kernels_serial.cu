@@ -159,6 +159,12 @@ __device__ __forceinline__ uint4 load_raw(const Tin* row, int64_t t, int64_t L, 
     return r;
 }
 
+// 8 bf16 values of a 16-byte vector in reverse order
+__device__ __forceinline__ uint4 rev8(uint4 v) {
+    return make_uint4(__byte_perm(v.w, 0, 0x1032), __byte_perm(v.z, 0, 0x1032), __byte_perm(v.y, 0, 0x1032),
+                      __byte_perm(v.x, 0, 0x1032));
+}
+
 template <typename Tout, int V>
 __device__ __forceinline__ void store_steps(Tout* p, const float* v) {
     if constexpr (sizeof(Tout) == 2 && V == 8) {
@@ -259,7 +265,8 @@ using LaneStateT = LaneState<K, N / G>;
 //           registers; `phase` counts the stage mbarrier's completed phases across
 //           passes. Returns false when a copy wait ran out of budget (recorded in
 //           g_prefill_status; the outputs are then unspecified).
-template <int N, int G, int K, typename Tin, typename Tout, bool kVec, bool kFull, bool kTma = false>
+template <int N, int G, int K, typename Tin, typename Tout, bool kVec, bool kFull, bool kTma = false,
+          bool kRev = false>
 __device__ __forceinline__ bool serial_pass(const ScanArgs& a, int64_t b, int64_t d_warp0, int64_t tb,
                                             int64_t te, const A2Arr<N, G, K>& A2, LaneStateT<N, G, K>& S,
                                             const Tiles<N, G, Tin, K>& tl, uint32_t* phase = nullptr) {
@@ -293,6 +300,7 @@ __device__ __forceinline__ bool serial_pass(const ScanArgs& a, int64_t b, int64_
     const Tin* C_b = static_cast<const Tin*>(a.C) + b * N * L;
     Tout* y_base = static_cast<Tout*>(a.y);
     const bool has_z = kFull && a.z != nullptr;
+    constexpr bool rev = kTma && kRev;   // reversed walk (built for the bulk-copy path only)
     const int p = lane_grp<G, K>(lane), j = lane_sgrp<G, K>(lane);
 
     // prologue/epilogue ownership: vector q of this lane covers channel pc[q],
@@ -342,30 +350,39 @@ __device__ __forceinline__ bool serial_pass(const ScanArgs& a, int64_t b, int64_
     auto issue = [&](int64_t t0) {
         const uint32_t bytes = (uint32_t)(2 * SG::XB + (has_z ? SG::XB : 0) + (kFull ? 2 : 1) * SG::BB);
         tc::mbar_expect_tx(tl.full, bytes);
-        const int x = (int)t0, y0 = (int)tl.cta_d0, zb = (int)b;
+        // reversed walk: the chunk's steps t0 .. t0+kT-1 are positions L-1-t0 down to
+        // L-t0-kT, one box starting at L-t0-kT (a multiple of 8: L is, on this path;
+        // a negative start reads zeros)
+        const int x = rev ? (int)(L - t0 - kT) : (int)t0, y0 = (int)tl.cta_d0, zb = (int)b;
         tc::tma_load_3d(tl.stage, &tl.maps->u, x, y0, zb, tl.full);
         tc::tma_load_3d(tl.stage + SG::XB, &tl.maps->d, x, y0, zb, tl.full);
         if (has_z) tc::tma_load_3d(tl.stage + 2 * SG::XB, &tl.maps->z, x, y0, zb, tl.full);
         tc::tma_load_3d(tl.stage + 3 * SG::XB, &tl.maps->B, x, 0, zb, tl.full);
         if (kFull) tc::tma_load_3d(tl.stage + 3 * SG::XB + SG::BB, &tl.maps->C, x, 0, zb, tl.full);
     };
+    // (reversed walk: steps s .. s+V-1 of the chunk sit, in reverse order, at tile
+    // columns kT-s-V .. kT-s-1)
     auto read_stage = [&]() {
         const unsigned char* st = tl.stage;
 #pragma unroll
         for (int q = 0; q < PV; q++) {
             const int row = warp * CPW + pc[q];
-            ru[q] = *reinterpret_cast<const uint4*>(st + SG::off(row, pt[q]));
-            rd[q] = *reinterpret_cast<const uint4*>(st + SG::off(SG::CPC + row, pt[q]));
-            rz[q] = has_z ? *reinterpret_cast<const uint4*>(st + SG::off(2 * SG::CPC + row, pt[q]))
+            const int col = rev ? kT - pt[q] - V : pt[q];
+            ru[q] = *reinterpret_cast<const uint4*>(st + SG::off(row, col));
+            rd[q] = *reinterpret_cast<const uint4*>(st + SG::off(SG::CPC + row, col));
+            rz[q] = has_z ? *reinterpret_cast<const uint4*>(st + SG::off(2 * SG::CPC + row, col))
                           : make_uint4(0, 0, 0, 0);
+            if (rev) { ru[q] = rev8(ru[q]); rd[q] = rev8(rd[q]); rz[q] = rev8(rz[q]); }
         }
 #pragma unroll
         for (int r = 0; r < BCPT; r++) {
             const int v = r * kThreads + threadIdx.x;
             const int which = v / (N * VPR), rem = v % (N * VPR);
             const int n = rem / VPR, tt = (rem % VPR) * V;
-            rbc[r] = v < BCV ? *reinterpret_cast<const uint4*>(st + SG::off(3 * SG::CPC + which * N + n, tt))
+            rbc[r] = v < BCV ? *reinterpret_cast<const uint4*>(st + SG::off(3 * SG::CPC + which * N + n,
+                                                                            rev ? kT - tt - V : tt))
                              : make_uint4(0, 0, 0, 0);
+            if (rev) rbc[r] = rev8(rbc[r]);
         }
     };
 
@@ -687,7 +704,19 @@ __device__ __forceinline__ bool serial_pass(const ScanArgs& a, int64_t b, int64_
                 if (chan_ok[q]) {
                     Tout* yrow = y_base + (b * a.dim + d_warp0 + pc[q]) * L;
                     const int64_t tt = t0 + pt[q];
-                    if (kVec && tt + V <= te) {
+                    if (rev) {
+                        // steps tt .. tt+V-1 are positions L-1-tt down to L-tt-V
+                        if (tt + V <= te) {
+                            float yr[V];
+#pragma unroll
+                            for (int k = 0; k < V; k++) yr[k] = yv[V - 1 - k];
+                            store_steps<Tout, V>(yrow + (L - tt - V), yr);
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < V; k++)
+                                if (tt + k < te) yrow[L - 1 - (tt + k)] = from_f32<Tout>(yv[k]);
+                        }
+                    } else if (kVec && tt + V <= te) {
                         store_steps<Tout, V>(yrow + tt, yv);
                     } else {
 #pragma unroll
@@ -765,7 +794,7 @@ __device__ __forceinline__ float lane_state(const LaneStateT<N, G, K>& S, int k,
 //     g_prefill_status and continues from a zero state (y is then unspecified).
 //   Workspace: [4] ticket counter (zeroed by the host), flags[P] at 16, then P state
 //   slots of (channels per CTA) x N floats.
-template <int N, int G, typename Tin, typename Tout, bool kVec, bool kTma>
+template <int N, int G, typename Tin, typename Tout, bool kVec, bool kTma, bool kRev = false>
 // at most 128 registers (4 CTAs per SM): measured ~1% faster than unbounded
 __global__ void __launch_bounds__(kThreads, 4) serial_scan_kernel(ScanArgs a, const __grid_constant__ ScanMaps maps) {
     constexpr int K = 1;
@@ -855,7 +884,8 @@ __global__ void __launch_bounds__(kThreads, 4) serial_scan_kernel(ScanArgs a, co
         LaneStateT<N, G, K> S;
         lane_init<N, G, K>(a, dR, okR, j, A2, S, h0);
         const Tiles<N, G, Tin, K> tl{s_bc, s_db, s_p, s_stage, &s_full, &maps, grp * CPC};
-        if (!serial_pass<N, G, K, Tin, Tout, kVec, true, kTma>(a, b, d_warp0, tb, te, A2, S, tl, &phase)) return;
+        if (!serial_pass<N, G, K, Tin, Tout, kVec, true, kTma, kRev>(a, b, d_warp0, tb, te, A2, S, tl, &phase))
+            return;
         if (te == L && a.h_last) {
 #pragma unroll
             for (int k = 0; k < K; k++)
@@ -914,7 +944,7 @@ struct LbDesc {
 
 // kLookbackCtasPerSM CTAs per SM at least (the host plans the segments for exactly
 // that many resident CTAs: none may wait for a slot)
-template <int N, int G, typename Tin, typename Tout, bool kVec, bool kTma>
+template <int N, int G, typename Tin, typename Tout, bool kVec, bool kTma, bool kRev = false>
 __global__ void __launch_bounds__(kThreads, kLookbackCtasPerSM)
     serial_lookback_kernel(ScanArgs a, const __grid_constant__ ScanMaps maps) {
     constexpr int K = max_k<N, G, Tin>();
@@ -978,7 +1008,7 @@ __global__ void __launch_bounds__(kThreads, kLookbackCtasPerSM)
 #pragma unroll
         for (int i = 0; i < NPL; i++) { aggP[k][i] = Dec::one(); aggH[k][i] = 0.f; }
     if (!last) {
-        if (!serial_pass<N, G, K, Tin, Tout, kVec, false, kTma>(a, b, d_warp0, ts, te, A2, S, tl, &phase)) {
+        if (!serial_pass<N, G, K, Tin, Tout, kVec, false, kTma, kRev>(a, b, d_warp0, ts, te, A2, S, tl, &phase)) {
             // a failed copy wait: record it where the look-back reports, publish nothing
             // (later segments time out on their bounded waits and finish) and leave
             if (threadIdx.x == 0) atomicExch(status, kErrLookbackTimeout);
@@ -1061,7 +1091,7 @@ __global__ void __launch_bounds__(kThreads, kLookbackCtasPerSM)
     }
     // (5) the full pass from the carry
     lane_init<N, G, K>(a, dR, okR, j, A2, S, carry);
-    if (!serial_pass<N, G, K, Tin, Tout, kVec, true, kTma>(a, b, d_warp0, ts, te, A2, S, tl, &phase)) {
+    if (!serial_pass<N, G, K, Tin, Tout, kVec, true, kTma, kRev>(a, b, d_warp0, ts, te, A2, S, tl, &phase)) {
         if (threadIdx.x == 0) atomicExch(status, kErrLookbackTimeout);
         return;
     }
@@ -1138,9 +1168,14 @@ cudaError_t launch_serial(const ScanArgs& a_in, cudaStream_t s) {
     using KernelFn = void (*)(ScanArgs, ScanMaps);
     KernelFn k = nullptr;
     if constexpr (sizeof(Tin) == 2) {
-        if (make_maps<N, G, 1, Tin>(a, &maps)) k = serial_scan_kernel<N, G, Tin, Tout, true, true>;
+        if (make_maps<N, G, 1, Tin>(a, &maps))
+            k = a.reverse ? serial_scan_kernel<N, G, Tin, Tout, true, true, true>
+                          : serial_scan_kernel<N, G, Tin, Tout, true, true>;
     }
-    if (!k) k = a.vec ? serial_scan_kernel<N, G, Tin, Tout, true, false> : serial_scan_kernel<N, G, Tin, Tout, false, false>;
+    if (!k) {
+        if (a.reverse) return cudaErrorInvalidValue;   // the reversed walk needs the bulk-copy path
+        k = a.vec ? serial_scan_kernel<N, G, Tin, Tout, true, false> : serial_scan_kernel<N, G, Tin, Tout, false, false>;
+    }
     // the work-balanced form when a workspace is given and the units do not already
     // divide evenly over the SMs: a multiple of the SM count, all CTAs resident
     int64_t P = 0;
@@ -1178,13 +1213,16 @@ cudaError_t launch_lookback(const ScanArgs& a, cudaStream_t s) {
     bool launched = false;
     if constexpr (sizeof(Tin) == 2) {
         if (make_maps<N, G, K, Tin>(a, &maps)) {
-            serial_lookback_kernel<N, G, Tin, Tout, true, true><<<(unsigned)ctas, kThreads, 0, s>>>(a, maps);
+            if (a.reverse) serial_lookback_kernel<N, G, Tin, Tout, true, true, true><<<(unsigned)ctas, kThreads, 0, s>>>(a, maps);
+            else serial_lookback_kernel<N, G, Tin, Tout, true, true><<<(unsigned)ctas, kThreads, 0, s>>>(a, maps);
             launched = true;
         }
     } else {
         memset(&maps, 0, sizeof(maps));
     }
     if (launched) {
+    } else if (a.reverse) {
+        return cudaErrorInvalidValue;   // the reversed walk needs the bulk-copy path
     } else if (a.vec) serial_lookback_kernel<N, G, Tin, Tout, true, false><<<(unsigned)ctas, kThreads, 0, s>>>(a, maps);
     else serial_lookback_kernel<N, G, Tin, Tout, false, false><<<(unsigned)ctas, kThreads, 0, s>>>(a, maps);
     return cudaGetLastError();

@@ -37,6 +37,9 @@ struct ScanArgs {
     // split the (channel group, chunk) work evenly and pass the state across each
     // split point through `workspace`)
     int64_t bal_ctas;
+    // time-serial and look-back kernels, bulk-copy (TMA) path only: walk the
+    // sequence from its end (step k reads and writes position seqlen - 1 - k)
+    int reverse;
     // directional scans (launch_scan_dir only): traversal order 0 raster, 1 reversed,
     // 2 column-major of a rows x cols image, 3 reversed columns; zoh: exact
     // zero-order-hold input matrix (exp(dt A) - 1) / A * B instead of dt * B

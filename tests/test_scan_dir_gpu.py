@@ -141,3 +141,24 @@ def test_vmamba56_four_directions_sampled(ssm):
                                   order=W_ORDER[order], rows=rows, cols=cols)
             assert_y_close(to_np(y[sl]), ref[0], 2e-3, False, f"{order} ({b}, {d})")
             assert_state_close(to_np(hl[sl]), ref[1], 2e-3, f"{order} h_last ({b}, {d})")
+
+
+@pytest.mark.parametrize("order", ["raster", "reverse"])
+@pytest.mark.parametrize("shape", [(5, 1000, 25, 40), (1, 128, 100, 200)], ids=["serial", "lookback"])
+def test_dir_prefill_algorithms(ssm, order, shape):
+    """With a workspace, the raster and reversed walks of bf16 inputs with 16-byte
+    aligned rows run on the prefill's own algorithms: the time-serial scan (5,000
+    channels, work-balanced) and the look-back (128 channels, 20,000 steps, ~79
+    segments of 256 steps; the reversed walk mirrors every bulk copy). Against the
+    oracle, with h0, y in fp32."""
+    bt, dim, rows, cols = shape
+    inp = _inputs(W.BF16, bt, dim, rows, cols, 16)
+    y, hl, ref = _run(ssm, inp, order, rows, cols, False)
+    _check(y, hl, ref, 2e-3, False, f"{order} {shape}")
+    # and the same outputs as the warp-scan form, to the prefill's tolerance
+    t = scan_to_torch(inp)
+    y2, h2 = ssm.scan_fwd_dir(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], True,
+                              t["h0"], order=order, rows=rows, cols=cols, out_dtype=torch.float32, workspace=None)
+    torch.cuda.synchronize()
+    scale = y2.pow(2).mean().sqrt().item()
+    assert (y - y2).abs().max().item() <= 2e-3 * scale
