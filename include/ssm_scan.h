@@ -275,13 +275,26 @@ SSM_API int ssm_scan_fwd_dir(const void* u, const void* delta, const float* A, c
                              int64_t seqlen, int64_t dstate, int order, int64_t rows, int64_t cols, int zoh,
                              int in_dtype, int out_dtype, void* stream);
 
-/* ssm_scan_fwd_dir with a device workspace (ssm_scan_workspace_size() bytes,
- * 16-byte aligned; NULL allowed). Without the exact-ZOH input matrix, the raster
- * walk, and for bf16 inputs with 16-byte aligned rows and dstate > 1 the reversed
- * walk, then run on the prefill's own algorithms (the time-serial scan, or the
- * look-back when the workspace holds it; the reversed walk mirrors each bulk copy
- * and reverses each 8-step vector); every other case is ssm_scan_fwd_dir. Results
- * agree with ssm_scan_fwd_dir to the prefill's tolerance, not bit for bit. */
+/* Bytes of device workspace ssm_scan_fwd_dir_ws can use for these sizes and
+ * dtypes, in any order (>= 16): the prefill's own workspace plus, for the column
+ * orders, transposed copies of u, delta, z, B, C and y. */
+SSM_API size_t ssm_scan_dir_workspace_size(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                           int in_dtype, int out_dtype);
+
+/* ssm_scan_fwd_dir with a device workspace (16-byte aligned, workspace_bytes of
+ * it; ssm_scan_dir_workspace_size() bytes enable everything; NULL allowed).
+ * Without the exact-ZOH input matrix, when the prefill's plan for these sizes is
+ * the time-serial scan, or the look-back and the workspace holds it:
+ *   raster                the prefill's scan itself;
+ *   reversed              the same kernels walking from the end (bf16 inputs with
+ *                         16-byte aligned rows, dstate > 1: each bulk copy is
+ *                         mirrored and each 8-step vector reversed);
+ *   columns / reversed    the raster / reversed walk of the transposed image: u,
+ *   columns               delta, z, B, C are transposed into the workspace, the
+ *                         scan writes a transposed y there, which is transposed
+ *                         back into y (the transposed rows keep length seqlen).
+ * Every other case is ssm_scan_fwd_dir. Results agree with ssm_scan_fwd_dir to the
+ * prefill's tolerance, not bit for bit. */
 SSM_API int ssm_scan_fwd_dir_ws(const void* u, const void* delta, const float* A, const void* B,
                                 const void* C, const float* D, const void* z, const float* delta_bias,
                                 int softplus, const float* h0, void* y, float* h_last, int64_t batch,

@@ -80,6 +80,8 @@ _lib.ssm_scan_fwd_dir.argtypes = [_P] * 8 + [_I, _P, _P, _P] + [_I64] * 4 + [_I,
 _lib.ssm_scan_fwd_dir.restype = _I
 _lib.ssm_scan_fwd_dir_ws.argtypes = [_P] * 8 + [_I, _P, _P, _P] + [_I64] * 4 + [_I, _I64, _I64, _I, _I, _I, _P, _SZ, _P]
 _lib.ssm_scan_fwd_dir_ws.restype = _I
+_lib.ssm_scan_dir_workspace_size.argtypes = [_I64] * 4 + [_I, _I]
+_lib.ssm_scan_dir_workspace_size.restype = _SZ
 _lib.ssm_device_status.argtypes = [_I, _P]
 _lib.ssm_device_status.restype = _I
 _lib.ssm_test_math.argtypes = [_I, _P, _P, _I64, _P]
@@ -104,7 +106,7 @@ EXPORTS = ("ssm_abi_version", "ssm_status_string", "ssm_scan_workspace_size", "s
            "ssm_causal_conv1d_fwd", "ssm_causal_conv1d_update", "ssm_scan_bwd_workspace_size",
            "ssm_scan_bwd", "ssm_ssd_scan_fwd", "ssm_ssd_chunk_len", "ssm_device_status", "ssm_scan_fwd_dir",
            "ssm_test_math", "ssm_test_ssd_wait_fault", "ssm_ssd_scan_fwd_ws", "ssm_ssd_workspace_size",
-           "ssm_test_serial_handover_timeout", "ssm_scan_fwd_dir_ws")
+           "ssm_test_serial_handover_timeout", "ssm_scan_fwd_dir_ws", "ssm_scan_dir_workspace_size")
 MATH = {"exp": 0, "log1p01": 1, "expm1": 2, "softplus": 3, "silu": 4, "softplus_sfu": 5, "silu_sfu": 6}
 
 
@@ -231,9 +233,9 @@ def scan_fwd_dir(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=Tr
     """Selective scan along a traversal order ("raster", "reverse", "columns",
     "columns_reverse" of a rows x cols image stored in raster order), outputs in
     raster order; zoh selects the zero-order-hold input matrix. Shapes as scan_fwd.
-    workspace: a uint8 device tensor, "auto" to allocate one (the raster and reversed
-    walks may then take the time-serial or look-back algorithm), or None for the
-    warp-scan form alone."""
+    workspace: a uint8 device tensor (ssm_scan_dir_workspace_size bytes), "auto" to
+    allocate one (every walk may then take the time-serial or look-back algorithm, the
+    column orders through transposed copies), or None for the warp-scan form alone."""
     bt, dim, L = u.shape
     N = A.shape[1]
     in_code = _dtype_code(u.dtype)
@@ -254,7 +256,8 @@ def scan_fwd_dir(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=Tr
             int(bool(zoh)), in_code, _dtype_code(y.dtype), _stream())
     else:
         if isinstance(workspace, str):
-            workspace = alloc_workspace(bt, dim, L, N, u.device)
+            n = _lib.ssm_scan_dir_workspace_size(bt, dim, L, N, in_code, _dtype_code(y.dtype))
+            workspace = torch.empty(n, dtype=torch.uint8, device=u.device)
         status = _lib.ssm_scan_fwd_dir_ws(
             _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias),
             int(bool(softplus)), _ptr(h0), _ptr(y), _ptr(h_last), bt, dim, L, N, order_code, int(rows), int(cols),

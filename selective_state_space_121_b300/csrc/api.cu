@@ -141,6 +141,28 @@ size_t workspace_for(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
     return ssm::lookback_workspace_bytes(batch, dim, (int)dstate, p.n_seg);
 }
 
+// Workspace of the column-order directional walks: the scan's own part (`inner`
+// bytes), then transposed copies of u, delta, (z), B, C and y, each 256-byte aligned.
+struct DirScratch {
+    size_t inner, u, d, z, B, C, y, total;
+};
+size_t round256(size_t v) { return (v + 255) / 256 * 256; }
+DirScratch dir_scratch(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int in_dtype, int out_dtype,
+                       bool has_z, size_t inner) {
+    DirScratch r;
+    const size_t nx = (size_t)batch * (size_t)dim * (size_t)seqlen, nbc = (size_t)batch * (size_t)dstate * seqlen;
+    const size_t ei = esize(in_dtype), eo = esize(out_dtype);
+    r.inner = round256(inner);
+    r.u = r.inner;
+    r.d = r.u + round256(nx * ei);
+    r.z = r.d + round256(nx * ei);
+    r.B = r.z + (has_z ? round256(nx * ei) : 0);
+    r.C = r.B + round256(nbc * ei);
+    r.y = r.C + round256(nbc * ei);
+    r.total = r.y + round256(nx * eo);
+    return r;
+}
+
 int scan_impl(const void* u, const void* delta, const float* A, const void* B, const void* C,
               const float* D, const void* z, const float* delta_bias, int softplus,
               const float* h0, void* y, float* h_last, int64_t batch, int64_t dim,
@@ -202,47 +224,82 @@ int scan_impl(const void* u, const void* delta, const float* A, const void* B, c
     a.drop_segment = drop_segment;
     a.spin_limit = spin_limit;
     cudaStream_t s = (cudaStream_t)stream;
-    if (order >= 0) {
-        // The raster walk and (for bf16 inputs with 16-byte aligned rows, on the
-        // bulk-copy path) the reversed walk, without the exact-ZOH input matrix, take
-        // the prefill's own algorithms when they apply: the time-serial one, or the
-        // look-back when the workspace holds it. Everything else takes the warp scan
-        // with its per-step position map.
-        bool direct = false;
-        if (!zoh && (order == SSM_ORDER_RASTER ||
-                     (order == SSM_ORDER_REVERSE && in_dtype == SSM_BF16 && vec && dstate > 1 &&
-                      seqlen < ((int64_t)1 << 31) && dim < ((int64_t)1 << 31)))) {
-            if (p.algo == SSM_ALGO_THREAD) direct = true;
-            if (p.algo == SSM_ALGO_LOOKBACK && workspace && aligned(workspace, 16) &&
-                workspace_bytes >= ssm::lookback_workspace_bytes(batch, dim, (int)dstate, p.n_seg))
-                direct = true;
+    // the planned algorithm on arguments `b` with workspace (ws, ws_bytes)
+    auto run_plan = [&](ScanArgs& b, void* ws, size_t ws_bytes) -> int {
+        if (p.algo == SSM_ALGO_LOOKBACK) {
+            const size_t need = ssm::lookback_workspace_bytes(batch, dim, (int)dstate, p.n_seg);
+            if (!ws || ws_bytes < need) return SSM_ERR_WORKSPACE;
+            if (!aligned(ws, 16)) return SSM_ERR_ALIGN;
+            b.workspace = ws;
+            if (cudaMemsetAsync(ws, 0, need, s) != cudaSuccess) return SSM_ERR_LAUNCH;
+            return ssm::launch_scan_serial_lookback(b, p.lanes_per_channel, s) == cudaSuccess ? SSM_OK
+                                                                                           : SSM_ERR_LAUNCH;
         }
-        if (!direct) {
+        if (p.algo == SSM_ALGO_THREAD) {
+            // an optional workspace enables the work-balanced form of the time-serial kernel
+            if (ws && aligned(ws, 16)) {
+                b.workspace = ws;
+                b.workspace_bytes = ws_bytes;
+            }
+            const cudaError_t e = dstate == 1 ? ssm::launch_scan_scalar(b, s)
+                                              : ssm::launch_scan_thread(b, p.lanes_per_channel, s);
+            return e == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+        }
+        return ssm::launch_scan_warp(b, s) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+    };
+    if (order >= 0) {
+        // Without the exact-ZOH input matrix, the directional walks take the prefill's
+        // own algorithms when the plan is the time-serial one, or the look-back with
+        // the workspace to hold it:
+        //  - raster: directly; reversed: directly on the bulk-copy path (bf16 inputs,
+        //    16-byte aligned rows, dstate > 1: the kernels mirror each copy);
+        //  - columns / reversed columns: the raster / reversed walk of the transposed
+        //    image, through transposed copies of u, delta, z, B, C and y placed in the
+        //    workspace after the scan's own part (dir_workspace_bytes).
+        // Everything else takes the warp scan with its per-step position map.
+        const bool prefill_plan =
+            p.algo == SSM_ALGO_THREAD ||
+            (p.algo == SSM_ALGO_LOOKBACK && workspace && aligned(workspace, 16) &&
+             workspace_bytes >= ssm::lookback_workspace_bytes(batch, dim, (int)dstate, p.n_seg));
+        const bool rev_order = order == SSM_ORDER_REVERSE || order == SSM_ORDER_COLUMNS_REVERSE;
+        const bool col_order = order == SSM_ORDER_COLUMNS || order == SSM_ORDER_COLUMNS_REVERSE;
+        const bool big_ok = seqlen < ((int64_t)1 << 31) && dim < ((int64_t)1 << 31);
+        // the transposed copies keep L, so their rows are 16-byte aligned when L allows
+        const bool vec_t = col_order ? ((seqlen * (int64_t)ei) % 16 == 0 && (seqlen * (int64_t)eo) % 16 == 0) : vec;
+        const bool rev_ok = !rev_order || (in_dtype == SSM_BF16 && vec_t && dstate > 1 && big_ok);
+        bool direct = !zoh && prefill_plan && rev_ok && !col_order;
+        const DirScratch ds = dir_scratch(batch, dim, seqlen, dstate, in_dtype, out_dtype, z != nullptr,
+                                          workspace_for(batch, dim, seqlen, dstate, p.algo, in_dtype));
+        const bool transposed = !zoh && prefill_plan && rev_ok && col_order && workspace && aligned(workspace, 16) &&
+                                workspace_bytes >= ds.total && big_ok && rows <= INT32_MAX && cols <= INT32_MAX;
+        if (!direct && !transposed) {
             a.order = order; a.rows = rows; a.cols = cols; a.zoh = zoh ? 1 : 0;
             return ssm::launch_scan_dir(a, s) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
         }
-        a.reverse = order == SSM_ORDER_REVERSE ? 1 : 0;
-    }
-    if (p.algo == SSM_ALGO_LOOKBACK) {
-        const size_t need = ssm::lookback_workspace_bytes(batch, dim, (int)dstate, p.n_seg);
-        if (!workspace || workspace_bytes < need) return SSM_ERR_WORKSPACE;
-        if (!aligned(workspace, 16)) return SSM_ERR_ALIGN;
-        a.workspace = workspace;
-        if (cudaMemsetAsync(workspace, 0, need, s) != cudaSuccess) return SSM_ERR_LAUNCH;
-        return ssm::launch_scan_serial_lookback(a, p.lanes_per_channel, s) == cudaSuccess ? SSM_OK
-                                                                                       : SSM_ERR_LAUNCH;
-    }
-    if (p.algo == SSM_ALGO_THREAD) {
-        // an optional workspace enables the work-balanced form of the time-serial kernel
-        if (workspace && aligned(workspace, 16)) {
-            a.workspace = workspace;
-            a.workspace_bytes = workspace_bytes;
+        a.reverse = rev_order ? 1 : 0;
+        if (transposed) {
+            // image i (rows x cols, raster) -> (cols x rows): the column walk's step k is
+            // position k of the transposed image
+            char* w = static_cast<char*>(workspace);
+            void* uT = w + ds.u; void* dT = w + ds.d; void* zT = z ? w + ds.z : nullptr;
+            void* BT = w + ds.B; void* CT = w + ds.C; void* yT = w + ds.y;
+            const int64_t xi = batch * dim, bi = batch * dstate;
+            if (ssm::launch_transpose_images(u, uT, xi, rows, cols, (int)ei, s) != cudaSuccess ||
+                ssm::launch_transpose_images(delta, dT, xi, rows, cols, (int)ei, s) != cudaSuccess ||
+                (z && ssm::launch_transpose_images(z, zT, xi, rows, cols, (int)ei, s) != cudaSuccess) ||
+                ssm::launch_transpose_images(B, BT, bi, rows, cols, (int)ei, s) != cudaSuccess ||
+                ssm::launch_transpose_images(C, CT, bi, rows, cols, (int)ei, s) != cudaSuccess)
+                return SSM_ERR_LAUNCH;
+            ScanArgs b = a;
+            b.u = uT; b.delta = dT; b.z = zT; b.B = BT; b.C = CT; b.y = yT;
+            b.vec = vec_t;
+            const int st = run_plan(b, workspace, ds.inner);
+            if (st != SSM_OK) return st;
+            return ssm::launch_transpose_images(yT, y, xi, cols, rows, (int)eo, s) == cudaSuccess ? SSM_OK
+                                                                                                : SSM_ERR_LAUNCH;
         }
-        const cudaError_t e = dstate == 1 ? ssm::launch_scan_scalar(a, s)
-                                          : ssm::launch_scan_thread(a, p.lanes_per_channel, s);
-        return e == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
     }
-    return ssm::launch_scan_warp(a, s) == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+    return run_plan(a, workspace, workspace_bytes);
 }
 
 }  // namespace
@@ -658,6 +715,18 @@ int ssm_scan_fwd_dir(const void* u, const void* delta, const float* A, const voi
     return scan_impl(u, delta, A, B, C, D, z, delta_bias, softplus, h0, y, h_last, batch, dim, seqlen, dstate,
                      in_dtype, out_dtype, nullptr, 0, SSM_ALGO_WARPSCAN, stream, -1, kSpinLimit, order, rows, cols,
                      zoh);
+}
+
+size_t ssm_scan_dir_workspace_size(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int in_dtype,
+                                   int out_dtype) {
+    if (batch < 0 || dim < 0 || seqlen < 0 || !valid_n(dstate) || !valid_dtype(in_dtype) ||
+        !valid_dtype(out_dtype))
+        return 16;
+    if (mul(mul(batch, dim), seqlen) < 0) return 16;
+    size_t inner = 16;
+    for (int algo : {(int)SSM_ALGO_AUTO, (int)SSM_ALGO_THREAD, (int)SSM_ALGO_LOOKBACK})
+        inner = std::max(inner, workspace_for(batch, dim, seqlen, dstate, algo, in_dtype));
+    return dir_scratch(batch, dim, seqlen, dstate, in_dtype, out_dtype, true, inner).total;
 }
 
 int ssm_scan_fwd_dir_ws(const void* u, const void* delta, const float* A, const void* B, const void* C,

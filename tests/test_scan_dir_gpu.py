@@ -143,14 +143,14 @@ def test_vmamba56_four_directions_sampled(ssm):
             assert_state_close(to_np(hl[sl]), ref[1], 2e-3, f"{order} h_last ({b}, {d})")
 
 
-@pytest.mark.parametrize("order", ["raster", "reverse"])
+@pytest.mark.parametrize("order", ORDERS)
 @pytest.mark.parametrize("shape", [(5, 1000, 25, 40), (1, 128, 100, 200)], ids=["serial", "lookback"])
 def test_dir_prefill_algorithms(ssm, order, shape):
-    """With a workspace, the raster and reversed walks of bf16 inputs with 16-byte
-    aligned rows run on the prefill's own algorithms: the time-serial scan (5,000
-    channels, work-balanced) and the look-back (128 channels, 20,000 steps, ~79
-    segments of 256 steps; the reversed walk mirrors every bulk copy). Against the
-    oracle, with h0, y in fp32."""
+    """With a workspace, every walk of bf16 inputs with 16-byte aligned rows runs on
+    the prefill's own algorithms: the time-serial scan (5,000 channels, work-balanced)
+    and the look-back (128 channels, 20,000 steps, ~79 segments of 256 steps); the
+    reversed walks mirror every bulk copy, the column walks scan transposed copies.
+    Against the oracle, with h0, y in fp32."""
     bt, dim, rows, cols = shape
     inp = _inputs(W.BF16, bt, dim, rows, cols, 16)
     y, hl, ref = _run(ssm, inp, order, rows, cols, False)
