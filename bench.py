@@ -809,11 +809,15 @@ def time_case(only, config, algo, steps, warmup, dev):
         t = scan_to_torch(inp, dev)
         ys = [torch.empty((cfg.batch, cfg.dim, cfg.seqlen), dtype=torch.bfloat16, device=dev) for _ in range(4)]
         hs = [torch.empty((cfg.batch, cfg.dim, cfg.dstate), dtype=torch.float32, device=dev) for _ in range(4)]
+        # one workspace, reused by the four walks in turn (same stream)
+        dir_ws = torch.empty(ssm._lib.ssm_scan_dir_workspace_size(cfg.batch, cfg.dim, cfg.seqlen, cfg.dstate,
+                                                                 ssm.SSM_BF16, ssm.SSM_BF16),
+                             dtype=torch.uint8, device=dev)
 
         def launch():
             for k, order in enumerate(("raster", "reverse", "columns", "columns_reverse")):
                 ssm.scan_fwd_dir(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], True,
-                                 None, order=order, rows=rows, cols=cols, y=ys[k], h_last=hs[k])
+                                 None, order=order, rows=rows, cols=cols, y=ys[k], h_last=hs[k], workspace=dir_ws)
         tokch = 4 * cfg.tokens_channels
         nbytes = 4 * scan_bytes(cfg.batch, cfg.dim, cfg.seqlen, cfg.dstate, 2, 2, True, False)
         label = f"scan_dir vmamba56 ({cfg.batch},{cfg.dim},{rows}x{cols},{cfg.dstate}) x 4 directions"
