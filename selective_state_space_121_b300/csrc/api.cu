@@ -284,19 +284,22 @@ int scan_impl(const void* u, const void* delta, const float* A, const void* B, c
             void* uT = w + ds.u; void* dT = w + ds.d; void* zT = z ? w + ds.z : nullptr;
             void* BT = w + ds.B; void* CT = w + ds.C; void* yT = w + ds.y;
             const int64_t xi = batch * dim, bi = batch * dstate;
-            if (ssm::launch_transpose_images(u, uT, xi, rows, cols, (int)ei, s) != cudaSuccess ||
-                ssm::launch_transpose_images(delta, dT, xi, rows, cols, (int)ei, s) != cudaSuccess ||
-                (z && ssm::launch_transpose_images(z, zT, xi, rows, cols, (int)ei, s) != cudaSuccess) ||
-                ssm::launch_transpose_images(B, BT, bi, rows, cols, (int)ei, s) != cudaSuccess ||
-                ssm::launch_transpose_images(C, CT, bi, rows, cols, (int)ei, s) != cudaSuccess)
+            const void* xs[3] = {u, delta, z};
+            void* xd[3] = {uT, dT, zT};
+            const void* bcs[2] = {B, C};
+            void* bcd[2] = {BT, CT};
+            if (ssm::launch_transpose_images(xs, xd, z ? 3 : 2, xi, rows, cols, (int)ei, s) != cudaSuccess ||
+                ssm::launch_transpose_images(bcs, bcd, 2, bi, rows, cols, (int)ei, s) != cudaSuccess)
                 return SSM_ERR_LAUNCH;
             ScanArgs b = a;
             b.u = uT; b.delta = dT; b.z = zT; b.B = BT; b.C = CT; b.y = yT;
             b.vec = vec_t;
             const int st = run_plan(b, workspace, ds.inner);
             if (st != SSM_OK) return st;
-            return ssm::launch_transpose_images(yT, y, xi, cols, rows, (int)eo, s) == cudaSuccess ? SSM_OK
-                                                                                                : SSM_ERR_LAUNCH;
+            const void* ys[1] = {yT};
+            void* yd[1] = {y};
+            return ssm::launch_transpose_images(ys, yd, 1, xi, cols, rows, (int)eo, s) == cudaSuccess ? SSM_OK
+                                                                                                    : SSM_ERR_LAUNCH;
         }
     }
     return run_plan(a, workspace, workspace_bytes);

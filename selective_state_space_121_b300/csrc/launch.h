@@ -166,10 +166,11 @@ int conv_block_steps(int in_dtype);
 cudaError_t launch_state_update(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_scan_warp(const ScanArgs& a, cudaStream_t s);
 cudaError_t launch_scan_dir(const ScanArgs& a, cudaStream_t s);
-// transposes `images` row-major rows x cols images of esize-byte elements (2 or 4)
-// from src into dst (each becomes cols x rows)
-cudaError_t launch_transpose_images(const void* src, void* dst, int64_t images, int64_t rows, int64_t cols,
-                                    int esize, cudaStream_t s);
+// transposes, for each of n (1 .. 3) tensors of the same shape, `images` row-major
+// rows x cols images of esize-byte elements (2 or 4) from src[t] into dst[t] (each
+// becomes cols x rows), in one launch
+cudaError_t launch_transpose_images(const void* const* src, void* const* dst, int n, int64_t images, int64_t rows,
+                                    int64_t cols, int esize, cudaStream_t s);
 cudaError_t launch_scan_serial_lookback(const ScanArgs& a, int lanes_per_channel, cudaStream_t s);
 // channels one CTA of the look-back kernel covers (its segments are planned with it)
 int lookback_channels_per_cta(int dstate, int lanes_per_channel, int in_dtype);
