@@ -162,3 +162,19 @@ def test_dir_prefill_algorithms(ssm, order, shape):
     torch.cuda.synchronize()
     scale = y2.pow(2).mean().sqrt().item()
     assert (y - y2).abs().max().item() <= 2e-3 * scale
+
+
+@pytest.mark.parametrize("order", ORDERS)
+@pytest.mark.parametrize("case", [
+    dict(in_dtype=W.BF16, N=16, rows=7, cols=143, h0=True),    # L = 1001: unaligned rows, reversed walks fall back
+    dict(in_dtype=W.F32, N=16, rows=13, cols=37, h0=False),    # fp32: no bulk copies, reversed walks fall back
+    dict(in_dtype=W.BF16, N=8, rows=24, cols=40, h0=True),     # d_state 8
+], ids=["bf16_L1001", "f32", "N8"])
+def test_dir_prefill_algorithms_edges(ssm, order, case):
+    """Every order with a workspace on shapes that take the time-serial kernel (5,000
+    channels), where the prefill paths apply and where they must fall back to the
+    warp scan; against the oracle."""
+    rows, cols = case["rows"], case["cols"]
+    inp = _inputs(case["in_dtype"], 5, 1000, rows, cols, case["N"], h0=case["h0"])
+    y, hl, ref = _run(ssm, inp, order, rows, cols, False)
+    _check(y, hl, ref, 1e-5 if case["in_dtype"] == W.F32 else 2e-3, False, f"{order} {case}")
